@@ -1,0 +1,389 @@
+"""Pins of the CPU oracle to facts fixed by the P-EAGLE pages and by mathematics.
+
+Nothing here uses the CUDA path.  Each test names the passage or the closed form
+it checks.  A plausible slip in the oracle (a dropped term, a wrong sign or index,
+a transposed operand, an off-by-one causal bound, a wrong GQA head mapping)
+fails at least one of them.
+"""
+
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from pe_workload import Config, config, make_round, make_weights, f32_to_bf16, bf16_to_f32
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _tiny(**kw) -> Config:
+    base = dict(name="pin", B=2, K=3, n_layers=1, d=64, n_q=4, n_kv=2, head_dim=16, ffn=96, vocab=101,
+                dtype="f32", prefix="uniform", prefix_args=(5, 40), accepted="uniform", seed=11)
+    base.update(kw)
+    return Config(**base)
+
+
+# ----------------------------------------------------------------------------- R1: batch rebuild
+
+def _read_r1_golden(path):
+    rows, extra = [], {}
+    for line in open(path):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        parts = line.split()
+        if parts[0].isdigit():
+            rows.append([int(p) for p in parts])
+        else:
+            extra[parts[0]] = [int(p) for p in parts[1:]]
+    return np.array(rows), extra
+
+
+def test_r1_hand_written_table():
+    """The pages' batch rebuild on one sequence (K=4, a=2), checked field by field."""
+    table, extra = _read_r1_golden(os.path.join(GOLDEN, "r1_B1_K4_a2.txt"))
+    prev_tokens = np.array([[10, 11, 12, 13, 14]])
+    prev_pos = np.array([[128, 129, 130, 131, 132]])
+    bt = np.array([[0, 1, 2, 3, 4, 5, 6, 7, 9, 8]])
+    m = oracle.prepare_batch(4, 4096, prev_tokens, prev_pos, [2], [99], bt)
+    assert (m["input_ids"] == table[:, 1]).all()
+    assert (m["positions"] == table[:, 2]).all()
+    assert (m["slot_mapping"] == table[:, 3]).all()
+    assert (m["is_rejected"] == table[:, 4]).all()
+    assert (m["is_mask"] == table[:, 5]).all()
+    assert (m["hidden_map"] == table[:, 6]).all()
+    assert list(m["row_list"]) == extra["row_list"]
+    assert m["n_valid"] == extra["n_valid"][0]
+    assert list(m["draft_rows"]) == extra["draft_rows"]
+
+
+def test_r1_k1_has_no_mask_rows():
+    """K=1: only the NTP row exists (no MASK slot), so single-step EAGLE drafting remains."""
+    for a in (0, 1):
+        m = oracle.prepare_batch(1, 50, [[3, 4]], [[7, 8]], [a], [9], [[0]])
+        assert m["is_mask"].sum() == 0
+        assert m["n_valid"] == a + 1
+        ntp = a  # row a is the NTP row
+        assert m["input_ids"][ntp] == 9 and m["positions"][ntp] == 7 + a
+        assert list(m["draft_rows"]) == [a]
+
+
+@pytest.mark.parametrize("K", range(1, 9))
+def test_r1_invariants_every_a(K):
+    """For every accepted count a in 0..K: a+K valid rows; slot -1 exactly on rejected rows;
+    valid slots distinct; MASK positions contiguous after the NTP position; the MASK id on MASK
+    rows only; the hidden map follows the shift-by-one rule; K drafts per sequence."""
+    B, V, P = 3, 1000, 37
+    rng = np.random.default_rng(K)
+    for a in range(K + 1):
+        prev_tokens = rng.integers(0, V, size=(B, K + 1))
+        prev_pos = P + np.arange(K + 1)[None, :].repeat(B, 0) + 100 * np.arange(B)[:, None]
+        nacc = np.full(B, a)
+        bonus = rng.integers(0, V, size=B)
+        npages = (prev_pos[:, 0].max() + 2 * K) // 16 + 1
+        bt = rng.permutation(B * npages).reshape(B, npages)
+        m = oracle.prepare_batch(K, V, prev_tokens, prev_pos, nacc, bonus, bt)
+        S = 2 * K
+        assert m["n_valid"] == B * (a + K)
+        assert ((m["slot_mapping"] == -1) == (m["is_rejected"] == 1)).all()
+        valid_slots = m["slot_mapping"][m["row_list"]]
+        assert len(set(valid_slots.tolist())) == len(valid_slots)
+        assert ((m["input_ids"] == V) == (m["is_mask"] == 1)).all()
+        assert (m["hidden_map"][m["is_mask"] == 1] == -1).all()
+        for b in range(B):
+            rows = np.arange(b * S, (b + 1) * S)
+            pos = m["positions"][rows]
+            ntp_pos = prev_pos[b][a]
+            assert list(pos[K + 1:]) == [ntp_pos + j for j in range(1, K)]
+            for r in range(a):                  # token at p+1 with the hidden state at p
+                assert m["input_ids"][rows[r]] == prev_tokens[b][r + 1]
+                assert m["hidden_map"][rows[r]] == b * (K + 1) + r
+                assert pos[r] == prev_pos[b][r]
+            assert m["input_ids"][rows[a]] == bonus[b]
+            # valid positions of a sequence: P..P+a+K-1, each once
+            vpos = sorted(pos[m["is_rejected"][rows] == 0].tolist())
+            assert vpos == list(range(prev_pos[b][0], prev_pos[b][0] + a + K))
+        assert len(m["draft_rows"]) == B * K
+        assert (np.diff(m["row_list"]) > 0).all()
+
+
+def test_r1_rejected_positions_overlap_mask_positions():
+    """The rejected rows' copied positions P+a+1..P+K coincide with MASK positions; slot -1 is
+    what keeps them from writing over the MASK rows' cache entries."""
+    K, a = 5, 1
+    m = oracle.prepare_batch(K, 10, [[1] * (K + 1)], [[20 + j for j in range(K + 1)]], [a], [2], [[0, 1, 2]])
+    rej = set(m["positions"][m["is_rejected"] == 1].tolist())
+    mask = set(m["positions"][m["is_mask"] == 1].tolist())
+    assert rej <= mask | {20 + K}
+    assert (m["slot_mapping"][m["is_rejected"] == 1] == -1).all()
+
+
+# ----------------------------------------------------------------------------- R2: input rows
+
+def test_r2_rows_and_mask_identity():
+    """NTP row = emb(new) with h_context; MASK rows = emb(mask) with h_shared -- bit-identical
+    across every sequence; context rows = emb(token at p+1) with h(p)."""
+    cfg = _tiny(B=3, K=4, dtype="bf16")
+    w = make_weights(cfg)
+    rnd = make_round(cfg, with_cache=False)
+    m = oracle.prepare_batch(cfg.K, cfg.vocab, rnd.prev_tokens, rnd.prev_pos, rnd.num_accepted, rnd.bonus,
+                             rnd.block_table)
+    x0 = oracle.scatter_hidden(w.emb, w.h_shared, rnd.target_hidden, m["input_ids"], m["is_mask"], m["hidden_map"])
+    d = cfg.d
+    mask_rows = np.nonzero(m["is_mask"])[0]
+    assert len(mask_rows) == cfg.B * (cfg.K - 1)
+    for r in mask_rows:
+        assert (x0[r] == x0[mask_rows[0]]).all()
+        assert (x0[r, :d] == w.emb[cfg.vocab]).all() and (x0[r, d:] == w.h_shared).all()
+    S = 2 * cfg.K
+    for b in range(cfg.B):
+        a = int(rnd.num_accepted[b])
+        ntp = b * S + a
+        assert (x0[ntp, :d] == w.emb[rnd.bonus[b]]).all()
+        assert (x0[ntp, d:] == rnd.target_hidden[b * (cfg.K + 1) + a]).all()
+        for r in range(a):
+            assert (x0[b * S + r, :d] == w.emb[rnd.prev_tokens[b][r + 1]]).all()
+            assert (x0[b * S + r, d:] == rnd.target_hidden[b * (cfg.K + 1) + r]).all()
+
+
+# ----------------------------------------------------------------------------- R3: single ops
+
+def test_widen_and_bf16_rounding():
+    assert oracle.widen(np.array([0x3F80, 0xC000, 0x0000], np.uint16)).tolist() == [1.0, -2.0, 0.0]
+    # round to nearest even at the 8th fraction bit
+    x = np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -1.0 - 2 ** -9], np.float32)
+    assert bf16_to_f32(f32_to_bf16(x)).tolist() == [1.0, 1.0 + 2 ** -6, -1.0]
+
+
+def test_linear_matches_blas():
+    """Y = X W^T (nn.Linear, no bias) against numpy's BLAS product, for both storages."""
+    rng = np.random.default_rng(0)
+    X = rng.standard_normal((7, 33))
+    W32 = rng.standard_normal((19, 33)).astype(np.float32)
+    np.testing.assert_allclose(oracle.linear(X, W32), X @ W32.astype(np.float64).T, rtol=1e-12, atol=1e-12)
+    Wb = f32_to_bf16(W32)
+    np.testing.assert_allclose(oracle.linear(X, Wb), X @ bf16_to_f32(Wb).astype(np.float64).T, rtol=1e-12, atol=1e-12)
+    # orientation: a one-hot input picks a column of W
+    e = np.zeros((1, 33)); e[0, 5] = 1.0
+    assert np.array_equal(oracle.linear(e, W32)[0], W32[:, 5].astype(np.float64))
+
+
+def test_rmsnorm_closed_form():
+    g = np.ones(2, np.float32)
+    y = oracle.rmsnorm(np.array([3.0, 4.0]), g, 0.0)[0]
+    np.testing.assert_allclose(y, np.array([3.0, 4.0]) / math.sqrt(12.5), rtol=1e-15)
+    y = oracle.rmsnorm(np.array([3.0, 4.0]), np.array([2.0, 0.5], np.float32), 0.5)[0]
+    np.testing.assert_allclose(y, np.array([6.0, 2.0]) / math.sqrt(13.0), rtol=1e-15)
+    # zero row: eps keeps it finite and zero
+    assert (oracle.rmsnorm(np.zeros(4), np.ones(4, np.float32), 1e-6) == 0).all()
+    # unit gains: the output has root-mean-square 1 (eps = 0)
+    x = np.random.default_rng(1).standard_normal(100) * 7
+    y = oracle.rmsnorm(x, np.ones(100, np.float32), 0.0)[0]
+    assert abs(math.sqrt((y ** 2).mean()) - 1.0) < 1e-14
+
+
+def test_rope_rotate_half():
+    """Rotate-half RoPE: pair (i, i+hd/2), angle p * theta^(-2i/hd)."""
+    hd = 8
+    e0 = np.zeros(hd); e0[0] = 1.0
+    v = oracle.rope(e0, 1, 10000.0)
+    expect = np.zeros(hd); expect[0] = math.cos(1.0); expect[hd // 2] = math.sin(1.0)
+    np.testing.assert_allclose(v, expect, atol=1e-15)
+    # second-half unit vector rotates the other way: (x1, x2) = (0, 1) -> (-sin, cos)
+    e4 = np.zeros(hd); e4[hd // 2 + 1] = 1.0
+    ang = 3 * 10000.0 ** (-2.0 / hd)
+    v = oracle.rope(e4, 3, 10000.0)
+    assert abs(v[1] + math.sin(ang)) < 1e-15 and abs(v[hd // 2 + 1] - math.cos(ang)) < 1e-15
+    # position 0 is the identity; rotations preserve length; scores depend on p - p' only
+    rng = np.random.default_rng(2)
+    q, k = rng.standard_normal(hd), rng.standard_normal(hd)
+    assert np.array_equal(oracle.rope(q, 0, 10000.0), q)
+    assert abs(np.linalg.norm(oracle.rope(q, 1234, 10000.0)) - np.linalg.norm(q)) < 1e-12
+    s1 = oracle.rope(q, 50, 100.0) @ oracle.rope(k, 20, 100.0)
+    s2 = oracle.rope(q, 530, 100.0) @ oracle.rope(k, 500, 100.0)
+    assert abs(s1 - s2) < 1e-10
+
+
+def test_silu_closed_form():
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12 and abs(oracle.silu(-40.0)) < 1e-15
+
+
+def test_attend_closed_forms():
+    rng = np.random.default_rng(3)
+    hd = 4
+    q = rng.standard_normal(hd)
+    K1, V1 = rng.standard_normal((1, hd)), rng.standard_normal((1, hd))
+    # a single position: the output is its value row
+    np.testing.assert_allclose(oracle.attend(q, K1, V1, 0.5), V1[0], rtol=1e-15)
+    # scores 0 and ln 3 -> weights 1/4, 3/4 (scale applied to q.k)
+    q = np.array([1.0, 0, 0, 0])
+    K2 = np.array([[0.0, 0, 0, 0], [2 * math.log(3.0), 0, 0, 0]])
+    V2 = np.array([[4.0, 0, 0, 0], [8.0, 0, 0, 0]])
+    np.testing.assert_allclose(oracle.attend(q, K2, V2, 0.5), [7.0, 0, 0, 0], rtol=1e-14)
+
+
+# ----------------------------------------------------------------------------- R3: whole pass
+
+def _structured_forward(position_list, group_map_check=True):
+    """fc = 0 -> x = 0 -> q = k = 0 (uniform attention); rows write nothing (slot -1), so each
+    head averages the cache's values over positions 0..p.  Cache value of kv head g at position t
+    is (+t if g == 0 else -t); W_o copies element 0 of q-head h into feature h; the MLP adds 0."""
+    cfg = _tiny(B=1, K=2, n_q=4, n_kv=2, head_dim=8, d=16, ffn=8, vocab=5)
+    d, hd = cfg.d, cfg.head_dim
+    z = lambda *s: np.zeros(s, np.float32)
+    wo = z(d, cfg.n_q * hd)
+    for h in range(cfg.n_q):
+        wo[h, h * hd] = 1.0
+    w = type("W", (), {})()
+    w.fc, w.norm_final, w.lm_head = z(d, 2 * d), np.ones(d, np.float32), z(cfg.vocab, d)
+    w.norm_attn, w.norm_mlp = [np.ones(d, np.float32)], [np.ones(d, np.float32)]
+    w.wqkv, w.wo = [z(cfg.qkv_out, d)], [wo]
+    w.w_gate_up, w.w_down = [z(2 * cfg.ffn, d)], [z(d, cfg.ffn)]
+    npos = max(position_list) + 1
+    pages = (npos + 15) // 16
+    bt = np.arange(pages, dtype=np.int32)[None, :]
+    kc = z(pages, 16, cfg.n_kv, hd)
+    vc = z(pages, 16, cfg.n_kv, hd)
+    for t in range(pages * 16):
+        vc[t // 16, t % 16, 0, :] = t
+        vc[t // 16, t % 16, 1, :] = -t
+    n = len(position_list)
+    res = oracle.draft_forward(cfg, w, np.zeros((n, 2 * d)), position_list, [-1] * n, [0] * n, bt, [kc], [vc],
+                               [0], want_x=True)
+    return res["x"]
+
+
+def test_forward_gqa_mapping_and_causal_bound():
+    """q head h reads kv head h // (n_q/n_kv); a row at position p attends to positions 0..p."""
+    x = _structured_forward([0, 5, 30])
+    for r, p in enumerate([0, 5, 30]):
+        mean = p / 2.0                          # mean of 0..p inclusive
+        np.testing.assert_allclose(x[r, :4], [mean, mean, -mean, -mean], rtol=1e-14, atol=1e-14)
+        assert (x[r, 4:] == 0).all()
+
+
+def _c0_like():
+    return _tiny(B=3, K=4, n_layers=1, d=64, n_q=4, n_kv=2, head_dim=16, ffn=96, vocab=211)
+
+
+def test_forward_rejected_rows_change_nothing():
+    """Rows with slot -1 write no cache entry: running the pass over all padded rows (rejected ones
+    included, with any input) gives bit-identical draft logits to running it over valid rows."""
+    cfg = _c0_like()
+    w, rnd = make_weights(cfg), make_round(cfg)
+    res = oracle.run_round(cfg, w, rnd, n_threads=2)
+    meta, x0 = res["meta"], res["x0"].copy()
+    n_all = cfg.rows
+    rows_all = np.arange(n_all)
+    rej = np.nonzero(meta["is_rejected"])[0]
+    assert len(rej) > 0
+    x0[rej] = np.random.default_rng(9).standard_normal((len(rej), 2 * cfg.d)).astype(np.float32)
+    pos, sl, sq = oracle.round_rows(cfg, meta, rows_all)
+    dr_padded = meta["row_list"][meta["draft_rows"]]
+    out = oracle.draft_forward(cfg, w, x0, pos, sl, sq, rnd.block_table, rnd.k_cache, rnd.v_cache, dr_padded)
+    assert np.array_equal(out["logits"], res["logits"])
+
+
+def test_forward_page_permutation_invariance():
+    """The same logical cache under a different physical page assignment gives bit-identical logits."""
+    cfg = _c0_like()
+    w, rnd = make_weights(cfg), make_round(cfg)
+    base = oracle.run_round(cfg, w, rnd, n_threads=2)["logits"]
+    perm = np.random.default_rng(5).permutation(rnd.num_pages)    # physical page p moves to perm[p]
+    kc = [np.empty_like(k) for k in rnd.k_cache]
+    vc = [np.empty_like(v) for v in rnd.v_cache]
+    for l in range(cfg.n_layers):
+        kc[l][perm] = rnd.k_cache[l]
+        vc[l][perm] = rnd.v_cache[l]
+    bt = np.where(rnd.block_table >= 0, perm[np.maximum(rnd.block_table, 0)], -1).astype(np.int32)
+    rnd.k_cache, rnd.v_cache, rnd.block_table = kc, vc, bt
+    assert np.array_equal(oracle.run_round(cfg, w, rnd, n_threads=2)["logits"], base)
+
+
+def test_forward_identity_layer_and_mask_rows():
+    """With W_o = 0 and W_down = 0 a layer adds nothing, so logits equal the zero-layer pass
+    lm(rms(fc(X0))); in that pass all MASK rows (identical inputs) give identical logits."""
+    cfg = _c0_like()
+    w, rnd = make_weights(cfg), make_round(cfg)
+    w.wo = [np.zeros_like(x) for x in w.wo]
+    w.w_down = [np.zeros_like(x) for x in w.w_down]
+    one = oracle.run_round(cfg, w, rnd, n_threads=2)
+    cfg0 = cfg.replace(n_layers=0)
+    zero = oracle.run_round(cfg0, w, rnd, n_threads=2)
+    assert np.array_equal(one["logits"], zero["logits"])
+    lg = zero["logits"].reshape(cfg.B, cfg.K, -1)
+    for b in range(cfg.B):
+        for k in range(1, cfg.K):
+            assert np.array_equal(lg[b, k], lg[0, 1])
+
+
+def test_forward_sequences_independent():
+    """Sequences share nothing but weights: a pass over one sequence alone equals its rows of the
+    full-batch pass (bit-exact)."""
+    cfg = _c0_like()
+    w, rnd = make_weights(cfg), make_round(cfg)
+    full = oracle.run_round(cfg, w, rnd, n_threads=2)["logits"].reshape(cfg.B, cfg.K, -1)
+    for b in range(cfg.B):
+        one = oracle.run_round(cfg, w, rnd, n_threads=1, seqs=[b])["logits"]
+        assert np.array_equal(one, full[b])
+
+
+def test_forward_k1_single_step():
+    """K=1: the batch has no MASK rows; the single draft is the argmax of the NTP row's logits."""
+    cfg = _c0_like().replace(K=1)
+    w, rnd = make_weights(cfg), make_round(cfg)
+    res = oracle.run_round(cfg, w, rnd, n_threads=2)
+    assert res["meta"]["is_mask"].sum() == 0
+    assert res["drafts"].shape == (cfg.B, 1)
+    assert (res["drafts"][:, 0] == np.argmax(res["logits"], axis=1)).all()
+
+
+def test_forward_block_causal():
+    """Attention reads the cache after this round's writes and only up to the row's own position:
+    dropping a sequence's MASK rows leaves its NTP row's logits bit-identical, while the last MASK
+    row's logits depend on the NTP row's write (it sees the context rows, the NTP row and the
+    MASK rows before it)."""
+    cfg = _c0_like().replace(B=1)
+    w, rnd = make_weights(cfg), make_round(cfg)
+    res = oracle.run_round(cfg, w, rnd, n_threads=2)
+    meta, x0 = res["meta"], res["x0"]
+    rows = res["rows"]
+    a = int(rnd.num_accepted[0])
+    ntp = a                                           # compacted index of the NTP row
+    no_mask = rows[: a + 1]                           # context rows + NTP row only
+    pos, sl, sq = oracle.round_rows(cfg, meta, no_mask)
+    out = oracle.draft_forward(cfg, w, x0[no_mask], pos, sl, sq, rnd.block_table, rnd.k_cache,
+                               rnd.v_cache, [ntp])
+    assert np.array_equal(out["logits"][0], res["logits"][0])
+    # perturb the NTP row's input: every MASK row's logits move
+    x0b = x0.copy()
+    x0b[rows[ntp]] = x0[rows[0]] if a > 0 else x0[rows[-1]] * 0
+    pos, sl, sq = oracle.round_rows(cfg, meta, rows)
+    out = oracle.draft_forward(cfg, w, x0b[rows], pos, sl, sq, rnd.block_table, rnd.k_cache, rnd.v_cache,
+                               meta["draft_rows"])
+    for k in range(1, cfg.K):
+        assert not np.array_equal(out["logits"][k], res["logits"][k])
+
+
+# ----------------------------------------------------------------------------- R4: verify
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+def test_verify_brute_force(K):
+    """All draft/target pairs over vocab {0,1,2}, packed 3 sequences per batch, against the
+    longest-matching-prefix definition: a = max{j : draft[i] == target[i] for all i < j}."""
+    drafts = list(itertools.product(range(3), repeat=K))
+    targets = list(itertools.product(range(3), repeat=K + 1))
+    pairs = [(d, t) for d in drafts for t in targets]
+    for i in range(0, len(pairs), 3):
+        chunk = pairs[i:i + 3]
+        D = np.array([p[0] for p in chunk])
+        T = np.array([p[1] for p in chunk])
+        a, bonus = oracle.verify(D, T)
+        for j, (d, t) in enumerate(chunk):
+            best = max(jj for jj in range(K + 1) if all(d[x] == t[x] for x in range(jj)))
+            assert a[j] == best and bonus[j] == t[best]
