@@ -1,0 +1,613 @@
+// C ABI of the P-EAGLE drafting round: argument validation, the workspace
+// plan, TMA descriptors and the launch sequence of every stage.  Nothing here
+// allocates device memory or synchronises the stream.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "pe_internal.h"
+
+namespace pe {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+
+// Caller-created events recorded at stage boundaries (tracing).
+std::mutex g_trace_mu;
+std::vector<cudaEvent_t> g_trace;
+
+void trace(int point, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (point >= 0 && point < (int)g_trace.size()) cudaEventRecord(g_trace[point], s);
+}
+
+constexpr int kMaxRows = 1 << 16;        // B*2K
+constexpr int kAttnTargetItems = 304;    // attention work items aimed for (2 per SM)
+constexpr int kAttnMinChunk = 256;       // shortest position chunk of a work item
+constexpr int kTcSmemLimit = 232448;     // opt-in shared memory per block (227 KB)
+constexpr int kTcMaxStages = 12;
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+size_t elem_bytes(pe_dtype dt) { return dt == PE_BF16 ? 2 : 4; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ----------------------------------------------------------------------------- GEMM plan
+
+struct GemmPlan {
+  int epi = 0, bn = 16, n_t = 1, n_f = 1, k_splits = 1, kb_total = 1, stages = 2;
+  uint32_t stage_bytes = 0;
+  size_t smem = 0, partial_floats = 0;
+  int tiles = 0;
+};
+
+GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
+  GemmPlan g;
+  g.epi = epi;
+  const bool paired = (epi == EPI_SWIGLU || epi == EPI_QKV_ROPE);
+  g.n_t = (n_tok + 255) / 256;
+  g.bn = round_up((n_tok + g.n_t - 1) / g.n_t, 16);
+  g.n_f = n_f_tiles;
+  g.kb_total = (k_dim + kTcBK - 1) / kTcBK;
+  g.tiles = g.n_f * g.n_t;
+  g.stage_bytes = (paired ? 2u : 1u) * kTcBM * kTcBK * 2 + (uint32_t)g.bn * kTcBK * 2;
+  const long long avail = kTcSmemLimit - 1024 - kTcCtrlBytes - (long long)g.bn * 8;
+  g.stages = (int)std::min<long long>(kTcMaxStages, avail / g.stage_bytes);
+  if (epi != EPI_ARGMAX && g.tiles < sms) {
+    g.k_splits = std::max(1, std::min(g.kb_total / 4, sms / g.tiles));
+  }
+  g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, g.bn);
+  g.partial_floats = g.k_splits > 1 ? (size_t)g.k_splits * g.tiles * (paired ? 2 : 1) * kTcBM * g.bn : 0;
+  return g;
+}
+
+struct Plan {
+  int R = 0, T = 0, S = 0, sms = 0, max_items = 0, attn_grid = 0;
+  GemmPlan fc, qkv, o, gu, down, lm;
+  size_t max_partial = 0;
+  int max_tiles = 0;
+  // workspace offsets
+  size_t tok_pos, tok_seq, tok_slot, seq_start, seq_len, seq_maxpos, item_base, n_chunks, n_items, items;
+  size_t counters, done, keys, x, y, q, ao, u, yl, partial, part_m, part_l, part_o;
+  size_t st_ids, st_pos, st_slot, st_rej, st_mask, st_hmap, st_rows, st_nvalid, st_draft, st_x0;
+  size_t total = 0;
+};
+
+Plan make_plan(const pe_config& c) {
+  Plan p;
+  p.S = 2 * c.K;
+  p.R = c.B * p.S;
+  p.T = c.B * c.K;
+  p.sms = num_sms();
+  const int half = c.head_dim / 2;
+  const int heads = c.n_q + 2 * c.n_kv;
+  const int hpt = kTcBM / half;
+  p.fc = plan_gemm(EPI_STORE_F32, (c.d + kTcBM - 1) / kTcBM, p.R, 2 * c.d, p.sms);
+  p.qkv = plan_gemm(EPI_QKV_ROPE, (heads + hpt - 1) / hpt, p.R, c.d, p.sms);
+  p.o = plan_gemm(EPI_ADD_F32, (c.d + kTcBM - 1) / kTcBM, p.R, c.n_q * c.head_dim, p.sms);
+  p.gu = plan_gemm(EPI_SWIGLU, (c.ffn + kTcBM - 1) / kTcBM, p.R, c.d, p.sms);
+  p.down = plan_gemm(EPI_ADD_F32, (c.d + kTcBM - 1) / kTcBM, p.R, c.ffn, p.sms);
+  p.lm = plan_gemm(EPI_ARGMAX, (c.vocab + kTcBM - 1) / kTcBM, p.T, c.d, p.sms);
+  for (const GemmPlan* g : {&p.fc, &p.qkv, &p.o, &p.gu, &p.down, &p.lm}) {
+    p.max_partial = std::max(p.max_partial, g->partial_floats);
+    p.max_tiles = std::max(p.max_tiles, g->tiles);
+  }
+  p.max_items = kAttnTargetItems + c.B * c.n_kv;
+  p.attn_grid = std::min(p.max_items, 2 * p.sms);
+
+  const size_t eb = elem_bytes(c.dtype);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  p.tok_pos = take(4 * (size_t)p.R);
+  p.tok_seq = take(4 * (size_t)p.R);
+  p.tok_slot = take(8 * (size_t)p.R);
+  p.seq_start = take(4 * (size_t)c.B);
+  p.seq_len = take(4 * (size_t)c.B);
+  p.seq_maxpos = take(4 * (size_t)c.B);
+  p.item_base = take(4 * (size_t)c.B);
+  p.n_chunks = take(4 * (size_t)c.B);
+  p.n_items = take(4);
+  p.items = take(16 * (size_t)p.max_items);
+  p.counters = take(4 * (size_t)(p.max_tiles + 1));  // split-K arrival counters, then the LM-head counter
+  p.done = p.counters + 4 * (size_t)p.max_tiles;
+  p.keys = take(8 * (size_t)p.T);
+  p.x = take(4 * (size_t)p.R * c.d);
+  p.y = take(eb * (size_t)p.R * c.d);
+  p.q = take(eb * (size_t)p.R * c.n_q * c.head_dim);
+  p.ao = take(eb * (size_t)p.R * c.n_q * c.head_dim);
+  p.u = take(eb * (size_t)p.R * c.ffn);
+  p.yl = take(eb * (size_t)p.T * c.d);
+  if (c.dtype == PE_BF16) {
+    p.partial = take(4 * p.max_partial);
+    p.part_m = take(4 * (size_t)p.max_items * kAttnRows);
+    p.part_l = take(4 * (size_t)p.max_items * kAttnRows);
+    p.part_o = take(4 * (size_t)p.max_items * kAttnRows * c.head_dim);
+  } else {
+    p.partial = p.part_m = p.part_l = p.part_o = 0;
+  }
+  // pe_step: batch metadata and input rows
+  p.st_ids = take(4 * (size_t)p.R);
+  p.st_pos = take(4 * (size_t)p.R);
+  p.st_slot = take(8 * (size_t)p.R);
+  p.st_rej = take((size_t)p.R);
+  p.st_mask = take((size_t)p.R);
+  p.st_hmap = take(4 * (size_t)p.R);
+  p.st_rows = take(4 * (size_t)p.R);
+  p.st_nvalid = take(4);
+  p.st_draft = take(4 * (size_t)p.T);
+  p.st_x0 = take(eb * (size_t)p.R * 2 * c.d);
+  p.total = off;
+  return p;
+}
+
+// ----------------------------------------------------------------------------- TMA descriptors
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor of `rank` dims (dims[0] innermost), 128-byte swizzle, zero fill out of bounds.
+bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+               const uint32_t* box) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+                        reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides_bytes),
+                        reinterpret_cast<const cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// [rows][cols] row-major, box of box_rows x 64 columns
+bool tmap_matrix(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t strides[1] = {cols * 2};
+  const uint32_t box[2] = {(uint32_t)kTcBK, box_rows};
+  return make_tmap(m, base, 2, dims, strides, box);
+}
+
+// w_gate_up [2F][d] as [2][F][d]: box of 128 rows of one half
+bool tmap_gate_up(CUtensorMap* m, const void* base, uint64_t F, uint64_t d) {
+  const uint64_t dims[3] = {d, F, 2};
+  const uint64_t strides[2] = {d * 2, F * d * 2};
+  const uint32_t box[3] = {(uint32_t)kTcBK, (uint32_t)kTcBM, 1};
+  return make_tmap(m, base, 3, dims, strides, box);
+}
+
+// wqkv [heads*hd][d] as [heads][2][hd/2][d]: box = the first (or second) halves of 128/(hd/2) heads
+bool tmap_qkv(CUtensorMap* m, const void* base, uint64_t heads, uint64_t hd, uint64_t d) {
+  const uint64_t half = hd / 2;
+  const uint64_t dims[4] = {d, half, 2, heads};
+  const uint64_t strides[3] = {d * 2, half * d * 2, hd * d * 2};
+  const uint32_t box[4] = {(uint32_t)kTcBK, (uint32_t)half, 1, (uint32_t)(kTcBM / half)};
+  return make_tmap(m, base, 4, dims, strides, box);
+}
+
+// ----------------------------------------------------------------------------- validation
+
+pe_status check_cfg(const pe_config* c) {
+  if (c == nullptr) return PE_ERR_INVALID_ARG;
+  if (c->dtype != PE_F32 && c->dtype != PE_BF16) return PE_ERR_INVALID_ARG;
+  if (c->B < 1 || c->K < 1 || c->d < 8 || c->n_q < 1 || c->n_kv < 1 || c->ffn < 1 || c->vocab < 2 ||
+      c->n_layers < 1 || c->max_pages_per_seq < 1)
+    return PE_ERR_SHAPE;
+  if (c->n_q % c->n_kv != 0) return PE_ERR_SHAPE;
+  if (c->page_size != 16) return PE_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return PE_ERR_UNSUPPORTED;
+  if ((long long)c->B * 2 * c->K > kMaxRows) return PE_ERR_SHAPE;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return PE_ERR_INVALID_ARG;
+  const size_t eb = elem_bytes(c->dtype);
+  if ((c->d * eb) % 16 != 0 || c->d % 4 != 0) return PE_ERR_UNSUPPORTED;  // bulk row copies, float4 norm
+  if (c->dtype == PE_BF16) {
+    if (c->ffn % 8 != 0) return PE_ERR_UNSUPPORTED;                          // TMA row strides: 16 bytes
+    if (2 * c->K * (c->n_q / c->n_kv) > kAttnRows) return PE_ERR_UNSUPPORTED;  // one query tile per item
+  }
+  return PE_OK;
+}
+
+#define PE_TRY_CUDA(expr)                         \
+  do {                                            \
+    if ((expr) != cudaSuccess) return PE_ERR_CUDA; \
+  } while (0)
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// ----------------------------------------------------------------------------- one GEMM launch
+
+struct GemmCall {
+  int epi;
+  const GemmPlan* plan;
+  const void* W;
+  const void* X;  // [tokens][k_dim]
+  int k_dim, n_out, n_tok;
+  const int32_t* n_tok_dev;
+  // tensor-map shapes of W
+  int w_kind;  // 0: matrix [w_rows][k_dim], 1: gate/up, 2: qkv
+  uint64_t w_rows;
+};
+
+pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& call, GemmArgs a, cudaStream_t s) {
+  a.n_out = call.n_out;
+  a.k_dim = call.k_dim;
+  a.n_tok = call.n_tok;
+  a.n_tok_dev = call.n_tok_dev;
+  a.W = call.W;
+  a.X = call.X;
+  a.ldx = call.k_dim;
+  if (c.dtype == PE_F32) {
+    PE_TRY_CUDA(launch_gemm_f32(call.epi, a, s));
+    return PE_OK;
+  }
+  const GemmPlan& g = *call.plan;
+  a.bn = g.bn;
+  a.kb_total = g.kb_total;
+  a.k_splits = g.k_splits;
+  a.stages = g.stages;
+  a.stage_bytes = g.stage_bytes;
+  a.partial = at<float>(ws, p.partial);
+  a.counters = at<int32_t>(ws, p.counters);
+  CUtensorMap tw, tx;
+  bool ok;
+  if (call.w_kind == 1) ok = tmap_gate_up(&tw, call.W, (uint64_t)c.ffn, (uint64_t)c.d);
+  else if (call.w_kind == 2) ok = tmap_qkv(&tw, call.W, (uint64_t)(c.n_q + 2 * c.n_kv), (uint64_t)c.head_dim, (uint64_t)c.d);
+  else ok = tmap_matrix(&tw, call.W, call.w_rows, (uint64_t)call.k_dim, (uint32_t)kTcBM);
+  ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)g.bn);
+  if (!ok) return PE_ERR_CUDA;
+  const dim3 grid(g.n_t, g.n_f, g.k_splits);
+  PE_TRY_CUDA(launch_gemm_tc(call.epi, tw, tx, a, grid, g.smem, s));
+  return PE_OK;
+}
+
+pe_status check_weights(const pe_config& c, const pe_weights* w) {
+  if (w == nullptr || w->emb == nullptr || w->h_shared == nullptr || w->fc == nullptr || w->norm_final == nullptr ||
+      w->lm_head == nullptr || w->norm_attn == nullptr || w->wqkv == nullptr || w->wo == nullptr ||
+      w->norm_mlp == nullptr || w->w_gate_up == nullptr || w->w_down == nullptr)
+    return PE_ERR_INVALID_ARG;
+  const void* ptrs[5] = {w->emb, w->h_shared, w->fc, w->norm_final, w->lm_head};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return PE_ERR_INVALID_ARG;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const void* lp[6] = {w->norm_attn[l], w->wqkv[l], w->wo[l], w->norm_mlp[l], w->w_gate_up[l], w->w_down[l]};
+    for (const void* q : lp)
+      if (q == nullptr || !aligned16(q)) return PE_ERR_INVALID_ARG;
+  }
+  return PE_OK;
+}
+
+pe_status check_kv(const pe_config& c, const pe_kv* kv) {
+  if (kv == nullptr || kv->k_cache == nullptr || kv->v_cache == nullptr || kv->num_pages < 1) return PE_ERR_INVALID_ARG;
+  for (int l = 0; l < c.n_layers; ++l)
+    if (kv->k_cache[l] == nullptr || kv->v_cache[l] == nullptr || !aligned16(kv->k_cache[l]) ||
+        !aligned16(kv->v_cache[l]))
+      return PE_ERR_INVALID_ARG;
+  return PE_OK;
+}
+
+pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv, const int32_t* block_table,
+                       const void* x0, const int32_t* positions, const int64_t* slot_mapping,
+                       const int32_t* row_list, const int32_t* n_valid, const int32_t* draft_rows, void* ws,
+                       const Plan& p, int32_t* draft_tokens, float* logits_dbg, int32_t* err, cudaStream_t s) {
+  const bool bf16 = c.dtype == PE_BF16;
+  const int hd = c.head_dim;
+  // prologue
+  InitArgs ia{};
+  ia.B = c.B; ia.K = c.K; ia.R = p.R; ia.T = p.T; ia.n_kv = c.n_kv;
+  ia.row_list = row_list; ia.n_valid = n_valid; ia.positions = positions; ia.slot_mapping = slot_mapping;
+  ia.tok_pos = at<int32_t>(ws, p.tok_pos); ia.tok_seq = at<int32_t>(ws, p.tok_seq);
+  ia.tok_slot = at<int64_t>(ws, p.tok_slot);
+  ia.seq_start = at<int32_t>(ws, p.seq_start); ia.seq_len = at<int32_t>(ws, p.seq_len);
+  ia.seq_maxpos = at<int32_t>(ws, p.seq_maxpos);
+  ia.target_items = kAttnTargetItems; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
+  ia.items = at<int4>(ws, p.items); ia.n_items = at<int32_t>(ws, p.n_items);
+  ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
+  ia.counters = at<int32_t>(ws, p.counters); ia.n_counters = p.max_tiles + 1;
+  ia.keys = at<unsigned long long>(ws, p.keys); ia.err = err;
+  PE_TRY_CUDA(launch_forward_init(ia, s));
+  trace(3, s);
+
+  GemmArgs base{};
+  base.n_q = c.n_q; base.n_kv = c.n_kv; base.head_dim = hd; base.rope_theta = c.rope_theta;
+  base.tok_pos = ia.tok_pos; base.tok_slot = ia.tok_slot; base.err = err;
+
+  float* x = at<float>(ws, p.x);
+  void* y = at<uint8_t>(ws, p.y);
+  void* qb = at<uint8_t>(ws, p.q);
+  void* ao = at<uint8_t>(ws, p.ao);
+  void* u = at<uint8_t>(ws, p.u);
+  void* yl = at<uint8_t>(ws, p.yl);
+  const int heads = c.n_q + 2 * c.n_kv;
+
+  // fc: x = X0 . W_fc^T
+  {
+    GemmArgs a = base;
+    a.out_f32 = x; a.ld_out = c.d;
+    GemmCall call{EPI_STORE_F32, &p.fc, w->fc, x0, 2 * c.d, c.d, p.R, n_valid, 0, (uint64_t)c.d};
+    pe_status st = run_gemm(c, p, ws, call, a, s);
+    if (st != PE_OK) return st;
+  }
+  trace(4, s);
+  NormArgs na{};
+  na.x = x; na.d = c.d; na.row_map = nullptr; na.n_rows = p.R; na.n_rows_dev = n_valid; na.src_rows = p.R;
+  na.eps = c.rms_eps; na.y = y; na.err = err;
+
+  AttnArgs at_{};
+  at_.n_q = c.n_q; at_.n_kv = c.n_kv; at_.head_dim = hd; at_.max_pages = c.max_pages_per_seq;
+  at_.page_size = c.page_size; at_.num_pages = kv->num_pages; at_.scale = 1.0f / sqrtf((float)hd);
+  at_.q = qb; at_.block_table = block_table; at_.tok_pos = ia.tok_pos; at_.tok_seq = ia.tok_seq;
+  at_.seq_start = ia.seq_start; at_.seq_len = ia.seq_len; at_.n_valid = n_valid; at_.items = ia.items;
+  at_.n_items = ia.n_items; at_.item_base = ia.item_base; at_.n_chunks = ia.n_chunks;
+  at_.part_m = bf16 ? at<float>(ws, p.part_m) : nullptr;
+  at_.part_l = bf16 ? at<float>(ws, p.part_l) : nullptr;
+  at_.part_o = bf16 ? at<float>(ws, p.part_o) : nullptr;
+  at_.out = ao; at_.n_rows = p.R; at_.err = err;
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    const int tp = 5 + 7 * l;
+    na.g = w->norm_attn[l];
+    PE_TRY_CUDA(launch_rmsnorm(na, c.dtype, s));
+    trace(tp + 0, s);
+    {
+      GemmArgs a = base;
+      a.out_act = qb; a.ld_out = c.n_q * hd; a.k_cache = kv->k_cache[l]; a.v_cache = kv->v_cache[l];
+      GemmCall call{EPI_QKV_ROPE, &p.qkv, w->wqkv[l], y, c.d, heads * hd / 2, p.R, n_valid, 2, 0};
+      pe_status st = run_gemm(c, p, ws, call, a, s);
+      if (st != PE_OK) return st;
+    }
+    trace(tp + 1, s);
+    at_.k_cache = kv->k_cache[l];
+    at_.v_cache = kv->v_cache[l];
+    if (bf16) {
+      PE_TRY_CUDA(launch_attention_bf16(at_, p.attn_grid, s));
+      PE_TRY_CUDA(launch_attention_combine_bf16(at_, s));
+    } else {
+      PE_TRY_CUDA(launch_attention_f32(at_, s));
+    }
+    trace(tp + 2, s);
+    {
+      GemmArgs a = base;
+      a.out_f32 = x; a.ld_out = c.d;
+      GemmCall call{EPI_ADD_F32, &p.o, w->wo[l], ao, c.n_q * hd, c.d, p.R, n_valid, 0, (uint64_t)c.d};
+      pe_status st = run_gemm(c, p, ws, call, a, s);
+      if (st != PE_OK) return st;
+    }
+    trace(tp + 3, s);
+    na.g = w->norm_mlp[l];
+    PE_TRY_CUDA(launch_rmsnorm(na, c.dtype, s));
+    trace(tp + 4, s);
+    {
+      GemmArgs a = base;
+      a.out_act = u; a.ld_out = c.ffn;
+      GemmCall call{EPI_SWIGLU, &p.gu, w->w_gate_up[l], y, c.d, c.ffn, p.R, n_valid, 1, 0};
+      pe_status st = run_gemm(c, p, ws, call, a, s);
+      if (st != PE_OK) return st;
+    }
+    trace(tp + 5, s);
+    {
+      GemmArgs a = base;
+      a.out_f32 = x; a.ld_out = c.d;
+      GemmCall call{EPI_ADD_F32, &p.down, w->w_down[l], u, c.ffn, c.d, p.R, n_valid, 0, (uint64_t)c.d};
+      pe_status st = run_gemm(c, p, ws, call, a, s);
+      if (st != PE_OK) return st;
+    }
+    trace(tp + 6, s);
+  }
+  const int tf = 5 + 7 * c.n_layers;
+  // final norm of the draft rows (in draft order), then LM head + argmax
+  NormArgs nf = na;
+  nf.row_map = draft_rows; nf.n_rows = p.T; nf.n_rows_dev = nullptr; nf.src_rows = p.R; nf.g = w->norm_final;
+  nf.y = yl;
+  PE_TRY_CUDA(launch_rmsnorm(nf, c.dtype, s));
+  trace(tf, s);
+  {
+    GemmArgs a = base;
+    a.keys = ia.keys; a.logits_dbg = logits_dbg; a.done_counter = at<int32_t>(ws, p.done);
+    a.draft_out = draft_tokens;
+    GemmCall call{EPI_ARGMAX, &p.lm, w->lm_head, yl, c.d, c.vocab, p.T, nullptr, 0, (uint64_t)c.vocab};
+    pe_status st = run_gemm(c, p, ws, call, a, s);
+    if (st != PE_OK) return st;
+  }
+  trace(tf + 1, s);
+  return PE_OK;
+}
+
+}  // namespace
+}  // namespace pe
+
+using namespace pe;
+
+extern "C" {
+
+const char* pe_status_str(pe_status st) {
+  switch (st) {
+    case PE_OK: return "ok";
+    case PE_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer or bad value)";
+    case PE_ERR_SHAPE: return "inconsistent or out-of-range sizes";
+    case PE_ERR_UNSUPPORTED: return "configuration not supported by this build";
+    case PE_ERR_CUDA: return "CUDA launch or runtime call failed";
+    case PE_ERR_DEVICE_CHECK: return "a device-side check fired";
+    case PE_ERR_TIMEOUT: return "a bounded device wait timed out";
+  }
+  return "unknown status";
+}
+
+pe_status pe_check_config(const pe_config* cfg) { return check_cfg(cfg); }
+
+size_t pe_workspace_bytes(const pe_config* cfg) {
+  if (check_cfg(cfg) != PE_OK) return 0;
+  return make_plan(*cfg).total;
+}
+
+pe_status pe_prepare_batch(const pe_config* cfg, const int32_t* prev_tokens, const int32_t* prev_pos,
+                           const int32_t* num_accepted, const int32_t* bonus, const int32_t* block_table,
+                           int32_t num_pages, int32_t* input_ids, int32_t* positions, int64_t* slot_mapping,
+                           uint8_t* is_rejected, uint8_t* is_mask, int32_t* hidden_map, int32_t* row_list,
+                           int32_t* n_valid, int32_t* draft_rows, int32_t* err_word, pe_stream_t stream) {
+  pe_status st = check_cfg(cfg);
+  if (st != PE_OK) return st;
+  if (!prev_tokens || !prev_pos || !num_accepted || !bonus || !block_table || !input_ids || !positions ||
+      !slot_mapping || !is_rejected || !is_mask || !hidden_map || !row_list || !n_valid || !draft_rows || !err_word)
+    return PE_ERR_INVALID_ARG;
+  if (num_pages < 1) return PE_ERR_SHAPE;
+  PrepArgs a{};
+  a.B = cfg->B; a.K = cfg->K; a.vocab = cfg->vocab; a.max_pages = cfg->max_pages_per_seq; a.num_pages = num_pages;
+  a.page_size = cfg->page_size; a.prev_tokens = prev_tokens; a.prev_pos = prev_pos; a.num_accepted = num_accepted;
+  a.bonus = bonus; a.block_table = block_table; a.input_ids = input_ids; a.positions = positions;
+  a.slot_mapping = slot_mapping; a.is_rejected = is_rejected; a.is_mask = is_mask; a.hidden_map = hidden_map;
+  a.row_list = row_list; a.n_valid = n_valid; a.draft_rows = draft_rows; a.err = err_word;
+  if (launch_prepare(a, (cudaStream_t)stream) != cudaSuccess) return PE_ERR_CUDA;
+  return PE_OK;
+}
+
+pe_status pe_scatter_hidden(const pe_config* cfg, const pe_weights* w, const void* target_hidden,
+                            const int32_t* input_ids, const uint8_t* is_mask, const int32_t* hidden_map,
+                            const int32_t* row_list, const int32_t* n_valid, void* x0, int32_t* err_word,
+                            pe_stream_t stream) {
+  pe_status st = check_cfg(cfg);
+  if (st != PE_OK) return st;
+  if (w == nullptr || !w->emb || !w->h_shared || !target_hidden || !input_ids || !is_mask || !hidden_map ||
+      !row_list || !n_valid || !x0 || !err_word)
+    return PE_ERR_INVALID_ARG;
+  if (!aligned16(w->emb) || !aligned16(w->h_shared) || !aligned16(target_hidden) || !aligned16(x0))
+    return PE_ERR_INVALID_ARG;
+  ScatterArgs a{};
+  a.R = cfg->B * 2 * cfg->K; a.d = cfg->d; a.elem_bytes = (int)elem_bytes(cfg->dtype); a.vocab = cfg->vocab;
+  a.n_hidden = cfg->B * (cfg->K + 1); a.emb = w->emb; a.h_shared = w->h_shared; a.hidden = target_hidden;
+  a.input_ids = input_ids; a.is_mask = is_mask; a.hidden_map = hidden_map; a.row_list = row_list;
+  a.n_valid = n_valid; a.x0 = x0; a.err = err_word;
+  if (launch_scatter(a, (cudaStream_t)stream) != cudaSuccess) return PE_ERR_CUDA;
+  return PE_OK;
+}
+
+pe_status pe_draft_forward(const pe_config* cfg, const pe_weights* w, const pe_kv* kv, const int32_t* block_table,
+                           const void* x0, const int32_t* positions, const int64_t* slot_mapping,
+                           const int32_t* row_list, const int32_t* n_valid, const int32_t* draft_rows,
+                           void* workspace, size_t workspace_bytes, int32_t* draft_tokens, float* logits_dbg,
+                           int32_t* err_word, pe_stream_t stream) {
+  pe_status st = check_cfg(cfg);
+  if (st != PE_OK) return st;
+  if ((st = check_weights(*cfg, w)) != PE_OK) return st;
+  if ((st = check_kv(*cfg, kv)) != PE_OK) return st;
+  if (!block_table || !x0 || !positions || !slot_mapping || !row_list || !n_valid || !draft_rows || !workspace ||
+      !draft_tokens || !err_word)
+    return PE_ERR_INVALID_ARG;
+  if (!aligned16(x0) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PE_ERR_INVALID_ARG;
+  const Plan p = make_plan(*cfg);
+  if (workspace_bytes < p.total) return PE_ERR_SHAPE;
+  for (int i = 0; i < 3; ++i) trace(i, (cudaStream_t)stream);
+  return forward_impl(*cfg, w, kv, block_table, x0, positions, slot_mapping, row_list, n_valid, draft_rows,
+                      workspace, p, draft_tokens, logits_dbg, err_word, (cudaStream_t)stream);
+}
+
+pe_status pe_verify(const pe_config* cfg, const int32_t* draft_tokens, const int32_t* target_tokens,
+                    int32_t* num_accepted_out, int32_t* bonus_out, pe_stream_t stream) {
+  pe_status st = check_cfg(cfg);
+  if (st != PE_OK) return st;
+  if (!draft_tokens || !target_tokens || !num_accepted_out || !bonus_out) return PE_ERR_INVALID_ARG;
+  VerifyArgs a{};
+  a.B = cfg->B; a.K = cfg->K; a.draft = draft_tokens; a.target = target_tokens; a.acc_out = num_accepted_out;
+  a.bonus_out = bonus_out;
+  if (launch_verify(a, (cudaStream_t)stream) != cudaSuccess) return PE_ERR_CUDA;
+  return PE_OK;
+}
+
+pe_status pe_step(const pe_config* cfg, const pe_weights* w, const pe_kv* kv, const int32_t* block_table,
+                  const int32_t* prev_tokens, const int32_t* prev_pos, const int32_t* num_accepted,
+                  const int32_t* bonus, const void* target_hidden, const int32_t* target_tokens, void* workspace,
+                  size_t workspace_bytes, int32_t* draft_tokens, int32_t* num_accepted_out, int32_t* bonus_out,
+                  int32_t* next_prev_tokens, int32_t* next_prev_pos, float* logits_dbg, int32_t* err_word,
+                  pe_stream_t stream) {
+  pe_status st = check_cfg(cfg);
+  if (st != PE_OK) return st;
+  if ((st = check_weights(*cfg, w)) != PE_OK) return st;
+  if ((st = check_kv(*cfg, kv)) != PE_OK) return st;
+  if (!block_table || !prev_tokens || !prev_pos || !num_accepted || !bonus || !target_hidden || !target_tokens ||
+      !workspace || !draft_tokens || !num_accepted_out || !bonus_out || !next_prev_tokens || !next_prev_pos ||
+      !err_word)
+    return PE_ERR_INVALID_ARG;
+  if (!aligned16(target_hidden) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PE_ERR_INVALID_ARG;
+  const Plan p = make_plan(*cfg);
+  if (workspace_bytes < p.total) return PE_ERR_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* ws = workspace;
+  int32_t* ids = at<int32_t>(ws, p.st_ids);
+  int32_t* pos = at<int32_t>(ws, p.st_pos);
+  int64_t* slot = at<int64_t>(ws, p.st_slot);
+  uint8_t* rej = at<uint8_t>(ws, p.st_rej);
+  uint8_t* msk = at<uint8_t>(ws, p.st_mask);
+  int32_t* hmap = at<int32_t>(ws, p.st_hmap);
+  int32_t* rows = at<int32_t>(ws, p.st_rows);
+  int32_t* nval = at<int32_t>(ws, p.st_nvalid);
+  int32_t* drows = at<int32_t>(ws, p.st_draft);
+  void* x0 = at<uint8_t>(ws, p.st_x0);
+  trace(0, s);
+  st = pe_prepare_batch(cfg, prev_tokens, prev_pos, num_accepted, bonus, block_table, kv->num_pages, ids, pos, slot,
+                        rej, msk, hmap, rows, nval, drows, err_word, stream);
+  if (st != PE_OK) return st;
+  trace(1, s);
+  st = pe_scatter_hidden(cfg, w, target_hidden, ids, msk, hmap, rows, nval, x0, err_word, stream);
+  if (st != PE_OK) return st;
+  trace(2, s);
+  st = forward_impl(*cfg, w, kv, block_table, x0, pos, slot, rows, nval, drows, ws, p, draft_tokens, logits_dbg,
+                    err_word, s);
+  if (st != PE_OK) return st;
+  VerifyArgs va{};
+  va.B = cfg->B; va.K = cfg->K; va.draft = draft_tokens; va.target = target_tokens; va.acc_out = num_accepted_out;
+  va.bonus_out = bonus_out; va.prev_pos = prev_pos; va.num_accepted = num_accepted; va.bonus_in = bonus;
+  va.next_tokens = next_prev_tokens; va.next_pos = next_prev_pos;
+  if (launch_verify(va, s) != cudaSuccess) return PE_ERR_CUDA;
+  trace(7 + 7 * cfg->n_layers, s);
+  return PE_OK;
+}
+
+pe_status pe_set_trace_events(void* const* events, int32_t n_events) {
+  if (n_events < 0 || (n_events > 0 && events == nullptr)) return PE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace.assign(n_events, nullptr);
+  for (int i = 0; i < n_events; ++i) g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+  return PE_OK;
+}
+
+int32_t pe_trace_points(const pe_config* cfg) {
+  if (check_cfg(cfg) != PE_OK) return 0;
+  return 8 + 7 * cfg->n_layers;
+}
+
+uint64_t pe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

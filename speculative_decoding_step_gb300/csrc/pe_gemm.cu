@@ -1,0 +1,446 @@
+// Dense contractions of the drafter pass with fused epilogues:
+//   fc (2d -> d), QKV + RoPE + paged KV write, o-proj + residual,
+//   gate/up + SwiGLU, down + residual, LM head + argmax.
+//
+// bf16 configurations run on the 5th-generation tensor cores: weights stream
+// through a TMA -> shared-memory ring (128-byte swizzle) and one elected thread
+// issues tcgen05.mma with fp32 accumulators in tensor memory.  The weight
+// matrix sits on the MMA's M side (128 weight rows per tile) and the few
+// token rows on its N side, so a batch of 16..256 rows reads every weight
+// byte once.  Split-K spreads small matrices over all SMs; the last CTA of a
+// tile (arrival counter, no waiting) sums the partials in split order, so the
+// result does not depend on scheduling.  The LM head never writes logits: each
+// CTA reduces its 128 vocabulary rows to a (max, argmax) key per token and
+// folds it into a global 64-bit atomicMax; the last CTA decodes the keys.
+//
+// fp32 configurations run a CUDA-core kernel with the same epilogues.
+#include "pe_device.cuh"
+#include "pe_internal.h"
+
+namespace pe {
+
+// ============================================================================= epilogues
+
+// Rotate-half RoPE of the pair (x1, x2) = (v[i], v[i + hd/2]) at position pos.
+PE_DEV void rope_pair(float x1, float x2, int pos, float inv_freq, float& o1, float& o2) {
+  float s, c;
+  sincosf((float)pos * inv_freq, &s, &c);
+  o1 = x1 * c - x2 * s;
+  o2 = x2 * c + x1 * s;
+}
+
+// unit = head * (hd/2) + i for the pair (i, i + hd/2) of `head` in the
+// q | k | v concatenation.  q and k are rotated; q goes to the q buffer, k and
+// v to the paged cache at the token's slot (no write for slot -1).
+template <typename T>
+PE_DEV void epi_qkv(const GemmArgs& a, int unit, int t, float x1, float x2, float inv_freq) {
+  const int half = a.head_dim >> 1;
+  const int head = unit / half, i = unit - head * half;
+  if (head < a.n_q + a.n_kv) rope_pair(x1, x2, a.tok_pos[t], inv_freq, x1, x2);
+  if (head < a.n_q) {
+    T* q = static_cast<T*>(a.out_act) + (size_t)t * a.ld_out + (size_t)head * a.head_dim + i;
+    q[0] = from_float<T>(x1);
+    q[half] = from_float<T>(x2);
+    return;
+  }
+  const long long slot = a.tok_slot[t];
+  if (slot < 0) return;
+  const bool is_k = head < a.n_q + a.n_kv;
+  const int g = is_k ? head - a.n_q : head - a.n_q - a.n_kv;
+  T* c = static_cast<T*>(is_k ? a.k_cache : a.v_cache) + ((size_t)slot * a.n_kv + g) * a.head_dim + i;
+  c[0] = from_float<T>(x1);
+  c[half] = from_float<T>(x2);
+}
+
+template <int EPI, typename T>
+PE_DEV void epi_elem(const GemmArgs& a, int unit, int t, float v, float v2, float inv_freq) {
+  if (EPI == EPI_STORE_F32) {
+    a.out_f32[(size_t)t * a.ld_out + unit] = v;
+  } else if (EPI == EPI_ADD_F32) {
+    float* o = a.out_f32 + (size_t)t * a.ld_out + unit;
+    *o = *o + v;
+  } else if (EPI == EPI_SWIGLU) {
+    static_cast<T*>(a.out_act)[(size_t)t * a.ld_out + unit] = from_float<T>(silu(v) * v2);
+  } else if (EPI == EPI_QKV_ROPE) {
+    epi_qkv<T>(a, unit, t, v, v2, inv_freq);
+  }
+}
+
+PE_DEV float rope_inv_freq(const GemmArgs& a, int unit) {
+  const int half = a.head_dim >> 1;
+  const int i = unit % half;
+  return powf(a.rope_theta, -2.0f * (float)i / (float)a.head_dim);
+}
+
+// Last CTA of the LM head: turn the per-token keys into token ids.
+PE_DEV void argmax_finish(const GemmArgs& a, int n_tok, int thread, int nthreads) {
+  for (int t = thread; t < n_tok; t += nthreads) {
+    const unsigned long long k = __ldcg(a.keys + t);
+    a.draft_out[t] = argmax_key_index(k);
+  }
+}
+
+PE_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// ============================================================================= tensor-core kernel
+
+size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int bn) {
+  return 1024 /*alignment slack*/ + (size_t)stages * stage_bytes + kTcCtrlBytes + (size_t)bn * 8;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const GemmArgs a) {
+  constexpr bool PAIRED = (EPI == EPI_SWIGLU || EPI == EPI_QKV_ROPE);
+  constexpr uint32_t A_BYTES = kTcBM * kTcBK * 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_t = blockIdx.x, tile_f = blockIdx.y, split = blockIdx.z;
+  const int BN = a.bn;
+  int n_tok = a.n_tok;
+  if (a.n_tok_dev != nullptr) n_tok = min(n_tok, *a.n_tok_dev);
+  // token tile entirely past the valid rows: uniform exit (the LM head has a host-known token count and
+  // every CTA must reach its completion counter, so it never takes this exit)
+  if (EPI != EPI_ARGMAX && tile_t * BN >= n_tok) return;
+
+  uint8_t* ctrl = smem + (size_t)a.stages * a.stage_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + a.stages;
+  uint64_t* accf = empty + a.stages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(ctrl + kTcCtrlBytes);
+
+  const int kb0 = (int)((long long)split * a.kb_total / a.k_splits);
+  const int kb1 = (int)((long long)(split + 1) * a.kb_total / a.k_splits);
+  const int nkb = kb1 - kb0;
+  const int acc_cols = PAIRED ? 2 * BN : BN;
+  const uint32_t tmem_cols = acc_cols <= 32 ? 32u : acc_cols <= 64 ? 64u : acc_cols <= 128 ? 128u
+                                                 : acc_cols <= 256 ? 256u : 512u;
+  const uint32_t b_off = (PAIRED ? 2u : 1u) * A_BYTES;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    mbar_init(smem_u32(accf), 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+  }
+  if (EPI == EPI_ARGMAX)
+    for (int j = threadIdx.x; j < BN; j += blockDim.x) red[j] = 0ull;
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), tmem_cols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();  // weights: read once
+      const uint64_t pol_x = l2_policy_evict_last();   // activations: re-read by every weight tile
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % a.stages;
+        const uint32_t use = (uint32_t)(i / a.stages);
+        if (i >= a.stages && !mbar_wait(smem_u32(empty + s), (use & 1u) ^ 1u, a.err, abort_flag)) break;
+        const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
+        const uint32_t fb = smem_u32(full + s);
+        mbar_expect_tx(fb, a.stage_bytes);
+        const int kx = (kb0 + i) * kTcBK;
+        if (EPI == EPI_SWIGLU) {           // W viewed as [2][F][d]: gate rows, then up rows
+          tma_load_3d(sa, &tmW, fb, kx, tile_f * kTcBM, 0, pol_w);
+          tma_load_3d(sa + A_BYTES, &tmW, fb, kx, tile_f * kTcBM, 1, pol_w);
+        } else if (EPI == EPI_QKV_ROPE) {  // W viewed as [heads][2][hd/2][d]: first / second halves
+          const int hpt = kTcBM / (a.head_dim >> 1);
+          tma_load_4d(sa, &tmW, fb, kx, 0, 0, tile_f * hpt, pol_w);
+          tma_load_4d(sa + A_BYTES, &tmW, fb, kx, 0, 1, tile_f * hpt, pol_w);
+        } else {
+          tma_load_2d(sa, &tmW, fb, kx, tile_f * kTcBM, pol_w);
+        }
+        tma_load_2d(sa + b_off, &tmX, fb, kx, tile_t * BN, pol_x);
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        // do not leave bulk copies in flight into this CTA's shared memory
+        const int lo = issued > a.stages ? issued - a.stages : 0;
+        for (int i = lo; i < issued; ++i)
+          mbar_wait(smem_u32(full + (i % a.stages)), (uint32_t)(i / a.stages) & 1u, a.err, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kTcBM, BN);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % a.stages;
+        const uint32_t use = (uint32_t)(i / a.stages);
+        if (!mbar_wait(smem_u32(full + s), use & 1u, a.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
+        const uint64_t da = sdesc_k_sw128(sa);
+        const uint64_t da2 = sdesc_k_sw128(sa + A_BYTES);
+        const uint64_t db = sdesc_k_sw128(sa + b_off);
+#pragma unroll
+        for (int kk = 0; kk < kTcBK / 16; ++kk) {
+          const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, accum);
+          if (PAIRED) tc_mma_bf16(tmem + (uint32_t)BN, da2 + 2 * kk, db + 2 * kk, idesc, accum);
+        }
+        tc_commit(smem_u32(empty + s));
+      }
+      tc_commit(smem_u32(accf));
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;            // row of the tile = TMEM lane
+    const int unit = tile_f * kTcBM + r;
+    const int ethread = threadIdx.x - 64;   // 0..127
+    const bool ok = mbar_wait(smem_u32(accf), 0u, a.err, abort_flag);
+    tc_fence_after();
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
+    const int rows_per = PAIRED ? 2 * kTcBM : kTcBM;
+    const size_t tile_elems = (size_t)rows_per * BN;
+    const size_t tile_index = (size_t)tile_f * gridDim.x + tile_t;
+
+    bool do_epilogue = ok;
+    if (ok && a.k_splits > 1) {
+      float* P = a.partial + ((size_t)split * gridDim.y * gridDim.x + tile_index) * tile_elems;
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16];
+        tmem_load16(tl + (uint32_t)(c * 16), v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) P[(size_t)(c * 16 + j) * rows_per + r] = v[j];
+        if (PAIRED) {
+          tmem_load16(tl + (uint32_t)(BN + c * 16), v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) P[(size_t)(c * 16 + j) * rows_per + kTcBM + r] = v[j];
+        }
+      }
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (ethread == 0) {
+        const int old = atomicAdd(a.counters + tile_index, 1);
+        *last_flag = (old == a.k_splits - 1) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      do_epilogue = *last_flag != 0;
+      if (do_epilogue) __threadfence();
+    }
+
+    if (do_epilogue) {
+      const size_t split_stride = (size_t)gridDim.y * gridDim.x * tile_elems;
+      const float* P0 = a.partial + tile_index * tile_elems;
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16], v2[16];
+        if (a.k_splits == 1) {
+          tmem_load16(tl + (uint32_t)(c * 16), v);
+          if (PAIRED) tmem_load16(tl + (uint32_t)(BN + c * 16), v2);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float s1 = 0.f, s2 = 0.f;
+            for (int sp = 0; sp < a.k_splits; ++sp) {
+              const float* P = P0 + sp * split_stride + (size_t)(c * 16 + j) * rows_per;
+              s1 += __ldcg(P + r);
+              if (PAIRED) s2 += __ldcg(P + kTcBM + r);
+            }
+            v[j] = s1;
+            v2[j] = s2;
+          }
+        }
+        if (EPI == EPI_ARGMAX) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = tile_t * BN + c * 16 + j;
+            unsigned long long key = 0ull;
+            if (unit < a.n_out && t < n_tok) {
+              if (!isfinite(v[j])) set_err(a.err, PE_DEV_NONFINITE);
+              key = argmax_key(v[j], (uint32_t)unit);
+              if (a.logits_dbg != nullptr) a.logits_dbg[(size_t)t * a.n_out + unit] = v[j];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, key, o);
+              key = other > key ? other : key;
+            }
+            if (lane == 0 && key != 0ull) atomicMax(red + c * 16 + j, key);
+          }
+        } else {
+          if (unit < a.n_out) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int t = tile_t * BN + c * 16 + j;
+              if (t < n_tok) epi_elem<EPI, __nv_bfloat16>(a, unit, t, v[j], v2[j], inv_freq);
+            }
+          }
+        }
+      }
+      if (a.k_splits > 1 && ethread == 0) a.counters[tile_index] = 0;  // ready for the next launch
+    }
+
+    if (EPI == EPI_ARGMAX) {
+      named_bar_sync(1, 128);
+      if (do_epilogue)
+        for (int j = ethread; j < BN; j += 128) {
+          const int t = tile_t * BN + j;
+          if (t < n_tok && red[j] != 0ull) atomicMax(a.keys + t, red[j]);
+        }
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (ethread == 0) {
+        const int total = gridDim.x * gridDim.y * gridDim.z;
+        const int old = atomicAdd(a.done_counter, 1);
+        *last_flag = (old == total - 1) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      if (*last_flag) {
+        __threadfence();
+        argmax_finish(a, n_tok, ethread, 128);
+        if (ethread == 0) *a.done_counter = 0;
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+template <int EPI>
+static cudaError_t launch_tc_typed(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, dim3 grid,
+                                   size_t smem, cudaStream_t s) {
+  static size_t configured = 0;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  gemm_tc_kernel<EPI><<<grid, kTcThreads, smem, s>>>(tmW, tmX, a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, dim3 grid,
+                           size_t smem, cudaStream_t s) {
+  switch (epi) {
+    case EPI_STORE_F32: return launch_tc_typed<EPI_STORE_F32>(tmW, tmX, a, grid, smem, s);
+    case EPI_ADD_F32: return launch_tc_typed<EPI_ADD_F32>(tmW, tmX, a, grid, smem, s);
+    case EPI_SWIGLU: return launch_tc_typed<EPI_SWIGLU>(tmW, tmX, a, grid, smem, s);
+    case EPI_QKV_ROPE: return launch_tc_typed<EPI_QKV_ROPE>(tmW, tmX, a, grid, smem, s);
+    case EPI_ARGMAX: return launch_tc_typed<EPI_ARGMAX>(tmW, tmX, a, grid, smem, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// ============================================================================= fp32 CUDA-core kernel
+// One warp per output unit (a feature, a gate/up pair or a RoPE pair): lanes
+// split the reduction, each lane keeps partial sums for 8 tokens at a time,
+// then a butterfly reduction gives every lane the full sums.
+
+constexpr int kF32Warps = 8;
+constexpr int kF32Tok = 8;
+
+template <int EPI>
+__global__ void __launch_bounds__(kF32Warps * 32) gemm_f32_kernel(const GemmArgs a) {
+  constexpr bool PAIRED = (EPI == EPI_SWIGLU || EPI == EPI_QKV_ROPE);
+  __shared__ int last_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * kF32Warps + warp;
+  int n_tok = a.n_tok;
+  if (a.n_tok_dev != nullptr) n_tok = min(n_tok, *a.n_tok_dev);
+  const float* W = static_cast<const float*>(a.W);
+  const float* X = static_cast<const float*>(a.X);
+  if (unit < a.n_out) {
+    int row1 = unit, row2 = unit;
+    if (EPI == EPI_SWIGLU) row2 = a.n_out + unit;
+    if (EPI == EPI_QKV_ROPE) {
+      const int half = a.head_dim >> 1;
+      const int head = unit / half, i = unit - head * half;
+      row1 = head * a.head_dim + i;
+      row2 = row1 + half;
+    }
+    const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
+    const float* w1 = W + (size_t)row1 * a.k_dim;
+    const float* w2 = W + (size_t)row2 * a.k_dim;
+    for (int t0 = 0; t0 < n_tok; t0 += kF32Tok) {
+      float acc1[kF32Tok], acc2[kF32Tok];
+#pragma unroll
+      for (int j = 0; j < kF32Tok; ++j) acc1[j] = acc2[j] = 0.f;
+      for (int k = lane; k < a.k_dim; k += 32) {
+        const float wa = w1[k];
+        const float wb = PAIRED ? w2[k] : 0.f;
+#pragma unroll
+        for (int j = 0; j < kF32Tok; ++j)
+          if (t0 + j < n_tok) {
+            const float x = X[(size_t)(t0 + j) * a.ldx + k];
+            acc1[j] += wa * x;
+            if (PAIRED) acc2[j] += wb * x;
+          }
+      }
+#pragma unroll
+      for (int j = 0; j < kF32Tok; ++j)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          acc1[j] += __shfl_xor_sync(0xFFFFFFFFu, acc1[j], o);
+          if (PAIRED) acc2[j] += __shfl_xor_sync(0xFFFFFFFFu, acc2[j], o);
+        }
+#pragma unroll
+      for (int j = 0; j < kF32Tok; ++j) {
+        const int t = t0 + j;
+        if (t >= n_tok || lane != j) continue;
+        if (EPI == EPI_ARGMAX) {
+          if (!isfinite(acc1[j])) set_err(a.err, PE_DEV_NONFINITE);
+          if (a.logits_dbg != nullptr) a.logits_dbg[(size_t)t * a.n_out + unit] = acc1[j];
+          atomicMax(a.keys + t, argmax_key(acc1[j], (uint32_t)unit));
+        } else {
+          epi_elem<EPI, float>(a, unit, t, acc1[j], acc2[j], inv_freq);
+        }
+      }
+    }
+  }
+  if (EPI == EPI_ARGMAX) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last_s = (atomicAdd(a.done_counter, 1) == (int)gridDim.x - 1) ? 1 : 0;
+    __syncthreads();
+    if (last_s) {
+      __threadfence();
+      argmax_finish(a, n_tok, threadIdx.x, blockDim.x);
+      if (threadIdx.x == 0) *a.done_counter = 0;
+    }
+  }
+}
+
+cudaError_t launch_gemm_f32(int epi, const GemmArgs& a, cudaStream_t s) {
+  const int grid = (a.n_out + kF32Warps - 1) / kF32Warps;
+  const int threads = kF32Warps * 32;
+  switch (epi) {
+    case EPI_STORE_F32: gemm_f32_kernel<EPI_STORE_F32><<<grid, threads, 0, s>>>(a); break;
+    case EPI_ADD_F32: gemm_f32_kernel<EPI_ADD_F32><<<grid, threads, 0, s>>>(a); break;
+    case EPI_SWIGLU: gemm_f32_kernel<EPI_SWIGLU><<<grid, threads, 0, s>>>(a); break;
+    case EPI_QKV_ROPE: gemm_f32_kernel<EPI_QKV_ROPE><<<grid, threads, 0, s>>>(a); break;
+    case EPI_ARGMAX: gemm_f32_kernel<EPI_ARGMAX><<<grid, threads, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace pe

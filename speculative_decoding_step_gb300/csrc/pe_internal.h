@@ -1,0 +1,159 @@
+// Internal interface between the C-ABI layer (pe_api.cu) and the kernels.
+// Every struct is passed to a kernel by value; every pointer is a device pointer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pe.h"
+
+namespace pe {
+
+// Counts every kernel launch of the library (reported by pe_kernel_launches).
+void count_launch(int n = 1);
+
+// ----------------------------------------------------------------------------- batch metadata
+
+struct PrepArgs {
+  int B, K, vocab, max_pages, num_pages, page_size;
+  const int32_t *prev_tokens, *prev_pos, *num_accepted, *bonus, *block_table;
+  int32_t *input_ids, *positions;
+  int64_t* slot_mapping;
+  uint8_t *is_rejected, *is_mask;
+  int32_t *hidden_map, *row_list, *n_valid, *draft_rows, *err;
+};
+cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s);
+
+struct ScatterArgs {
+  int R, d, elem_bytes, vocab, n_hidden;
+  const void *emb, *h_shared, *hidden;
+  const int32_t* input_ids;
+  const uint8_t* is_mask;
+  const int32_t *hidden_map, *row_list, *n_valid;
+  void* x0;
+  int32_t* err;
+};
+cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
+
+struct VerifyArgs {
+  int B, K;
+  const int32_t *draft, *target;
+  int32_t *acc_out, *bonus_out;
+  // optional: next round's verify batch (pe_step)
+  const int32_t *prev_pos, *num_accepted, *bonus_in;
+  int32_t *next_tokens, *next_pos;
+};
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
+
+// Forward prologue: per compacted row metadata, per sequence ranges, the
+// attention work list, and zeroing of the pass's counters and argmax keys.
+struct InitArgs {
+  int B, K, R, T, n_kv;
+  const int32_t *row_list, *n_valid, *positions;
+  const int64_t* slot_mapping;
+  int32_t *tok_pos, *tok_seq;
+  int64_t* tok_slot;
+  int32_t *seq_start, *seq_len, *seq_maxpos;
+  int target_items, max_items, min_chunk;
+  int4* items;
+  int32_t *n_items, *item_base, *n_chunks;
+  int32_t* counters;
+  int n_counters;
+  unsigned long long* keys;
+  int32_t* err;
+};
+cudaError_t launch_forward_init(const InitArgs& a, cudaStream_t s);
+
+// ----------------------------------------------------------------------------- RMSNorm
+
+struct NormArgs {
+  const float* x;            // residual stream [rows][d] fp32
+  int d;
+  const int32_t* row_map;    // output row i reads x[row_map[i]] (nullable: identity)
+  int n_rows;                // host upper bound of output rows
+  const int32_t* n_rows_dev; // actual count (nullable)
+  int src_rows;              // bound on source rows (device check)
+  const void* g;             // gains [d], storage dtype
+  float eps;
+  void* y;                   // [rows][d], bf16 (bf16 configs) or fp32
+  int32_t* err;
+};
+cudaError_t launch_rmsnorm(const NormArgs& a, pe_dtype dt, cudaStream_t s);
+
+// ----------------------------------------------------------------------------- GEMM + fused epilogues
+
+enum Epi : int {
+  EPI_STORE_F32 = 0,  // x[t][f] = acc                 (fc)
+  EPI_ADD_F32 = 1,    // x[t][f] += acc                (o-proj, down: residual add)
+  EPI_SWIGLU = 2,     // u[t][f] = silu(gate) * up     (gate/up, paired rows)
+  EPI_QKV_ROPE = 3,   // RoPE(q,k); q -> q buffer; k,v -> paged cache at the row's slot
+  EPI_ARGMAX = 4,     // LM head: per-token max / argmax over the vocabulary
+};
+
+struct GemmArgs {
+  int n_out;             // output units: features; SwiGLU: F; QKV: (head, pair) units = heads*hd/2
+  int k_dim;             // reduction length
+  int n_tok;             // token rows (host upper bound)
+  const int32_t* n_tok_dev;  // actual token rows (nullable)
+  // tensor-core tiling (ignored by the fp32 kernel)
+  int bn;                // token columns per tile (MMA N)
+  int kb_total, k_splits, stages;
+  uint32_t stage_bytes;
+  float* partial;        // split-K partial sums
+  int32_t* counters;     // split-K arrival counters per output tile (zero between launches)
+  // fp32 kernel operands
+  const void* W;         // [rows][k_dim]
+  const void* X;         // [tokens][ldx]
+  int ldx;
+  // epilogue
+  float* out_f32;        // residual stream [tokens][ld_out]
+  void* out_act;         // SwiGLU output / q buffer (bf16 or fp32 by config)
+  int ld_out;
+  int n_q, n_kv, head_dim;
+  float rope_theta;
+  const int32_t* tok_pos;
+  const int64_t* tok_slot;
+  void *k_cache, *v_cache;
+  unsigned long long* keys;  // LM head: one key per token (zero before the launch)
+  float* logits_dbg;         // nullable [tokens][n_out]
+  int32_t* done_counter;     // LM head: CTAs finished (zero before the launch)
+  int32_t* draft_out;        // LM head: argmax per token
+  int32_t* err;
+};
+
+// Tensor-core GEMM (tcgen05 + TMA): D[f][t] = W[f][:] . X[t][:], weights on the MMA M side.
+cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, dim3 grid,
+                           size_t smem_bytes, cudaStream_t s);
+// fp32 CUDA-core GEMM for fp32 configurations (same epilogues).
+cudaError_t launch_gemm_f32(int epi, const GemmArgs& a, cudaStream_t s);
+
+constexpr int kTcThreads = 192;        // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+constexpr int kTcBM = 128;             // weight rows per tile
+constexpr int kTcBK = 64;              // k per pipeline stage (one 128-byte swizzle row)
+constexpr int kTcCtrlBytes = 1024;     // barriers + TMEM slot + flags
+size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int bn);
+
+// ----------------------------------------------------------------------------- attention
+
+struct AttnArgs {
+  int n_q, n_kv, head_dim, max_pages, page_size, num_pages;
+  float scale;               // 1/sqrt(head_dim)
+  const void* q;             // [rows][n_q*hd], post-RoPE
+  const void *k_cache, *v_cache;
+  const int32_t* block_table;
+  const int32_t *tok_pos, *tok_seq, *seq_start, *seq_len, *n_valid;
+  const int4* items;         // (b, g, c0, c1)
+  const int32_t *n_items, *item_base, *n_chunks;
+  float *part_m, *part_l, *part_o;  // [items][128], [items][128], [items][128][hd]
+  void* out;                 // [rows][n_q*hd]
+  int n_rows;                // host upper bound on rows
+  int32_t* err;
+};
+constexpr int kAttnRows = 128;    // query rows (row x GQA head) per work item
+cudaError_t launch_attention_bf16(const AttnArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_attention_combine_bf16(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attention_f32(const AttnArgs& a, cudaStream_t s);
+
+}  // namespace pe

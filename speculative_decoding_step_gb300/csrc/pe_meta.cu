@@ -1,0 +1,400 @@
+// Indexing and bandwidth stages of the P-EAGLE drafting round:
+//   prepare_batch  -- stage (a): one pass over the B*2K padded rows
+//   verify         -- stage (e): greedy verification (+ next round's verify batch)
+//   forward_init   -- per compacted row metadata and the attention work list
+//   scatter        -- stage (b): drafter input rows moved with bulk async copies
+//   rmsnorm        -- row RMSNorm of the fp32 residual stream
+#include <climits>
+
+#include "pe_device.cuh"
+#include "pe_internal.h"
+
+namespace pe {
+
+// ============================================================================= stage (a)
+// P-EAGLE: Parallel Speculative Decoding in vLLM, "vLLM implementation details":
+// one fused pass copies the previous token ids and positions, inserts the bonus
+// token, fills the parallel-draft slots with the MASK id and emits the rejected
+// mask, the MASK mask and the hidden-state map; "KV cache and CUDA Graphs":
+// rejected tokens map to PADDING_SLOT_ID (-1).  Valid rows are compacted with a
+// warp-ballot + block prefix sum so the drafter pass never touches them.
+
+constexpr int kPrepThreads = 1024;
+
+__global__ void __launch_bounds__(kPrepThreads) prepare_kernel(const PrepArgs a) {
+  __shared__ int warp_off[32];
+  __shared__ int carry_s;
+  __shared__ int chunk_total_s;
+  const int S = 2 * a.K, R = a.B * S;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  if (tid == 0) carry_s = 0;
+  __syncthreads();
+
+  for (int base = 0; base < R; base += blockDim.x) {
+    const int row = base + tid;
+    int valid = 0, draft_k = -1, b = 0;
+    if (row < R) {
+      b = row / S;
+      const int r = row % S;
+      int acc = a.num_accepted[b];
+      if (acc < 0 || acc > a.K) {
+        set_err(a.err, PE_DEV_BAD_ACCEPTED);
+        acc = acc < 0 ? 0 : a.K;
+      }
+      const int32_t* pt = a.prev_tokens + (size_t)b * (a.K + 1);
+      const int32_t* pp = a.prev_pos + (size_t)b * (a.K + 1);
+      int tok, pos, hmap, rej = 0, msk = 0;
+      if (r < acc) {                 // accepted context row: token at p+1, hidden state of p
+        tok = pt[r + 1];
+        pos = pp[r];
+        hmap = b * (a.K + 1) + r;
+      } else if (r == acc) {         // NTP row: bonus token with h_context
+        tok = a.bonus[b];
+        pos = pp[acc];
+        hmap = b * (a.K + 1) + acc;
+        draft_k = 0;
+      } else if (r <= a.K) {         // rejected draft position
+        tok = 0;
+        pos = pp[r];
+        hmap = b * (a.K + 1) + r;
+        rej = 1;
+      } else {                       // MASK slot m = r - K
+        const int m = r - a.K;
+        tok = a.vocab;
+        pos = pp[acc] + m;
+        hmap = -1;
+        msk = 1;
+        draft_k = m;
+      }
+      if (!msk && (tok < 0 || tok >= a.vocab)) set_err(a.err, PE_DEV_BAD_TOKEN);
+      long long slot = -1;
+      if (!rej) {
+        const int pi = pos / a.page_size;
+        if (pos < 0 || pi >= a.max_pages) {
+          set_err(a.err, PE_DEV_BAD_POSITION);
+        } else {
+          const int page = a.block_table[(size_t)b * a.max_pages + pi];
+          if (page < 0 || page >= a.num_pages) set_err(a.err, PE_DEV_BAD_PAGE);
+          else slot = (long long)page * a.page_size + pos % a.page_size;
+        }
+      }
+      a.input_ids[row] = tok;
+      a.positions[row] = pos;
+      a.slot_mapping[row] = slot;
+      a.is_rejected[row] = (uint8_t)rej;
+      a.is_mask[row] = (uint8_t)msk;
+      a.hidden_map[row] = hmap;
+      valid = !rej;
+    }
+    // block-wide exclusive prefix sum of `valid` (warp ballots, then a scan of warp totals)
+    const unsigned ballot = __ballot_sync(0xFFFFFFFFu, valid);
+    const int lane_prefix = __popc(ballot & ((1u << lane) - 1u));
+    if (lane == 0) warp_off[warp] = __popc(ballot);
+    __syncthreads();
+    if (warp == 0) {
+      const int v = lane < nwarps ? warp_off[lane] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (lane < nwarps) warp_off[lane] = incl - v;
+      if (lane == 31) chunk_total_s = incl;
+    }
+    __syncthreads();
+    if (valid) {
+      const int idx = carry_s + warp_off[warp] + lane_prefix;
+      a.row_list[idx] = row;
+      if (draft_k >= 0) a.draft_rows[b * a.K + draft_k] = idx;
+    }
+    __syncthreads();
+    if (tid == 0) carry_s += chunk_total_s;
+    __syncthreads();
+  }
+  for (int i = carry_s + tid; i < R; i += blockDim.x) a.row_list[i] = -1;
+  if (tid == 0) *a.n_valid = carry_s;
+}
+
+cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s) {
+  const int R = a.B * 2 * a.K;
+  const int threads = R >= kPrepThreads ? kPrepThreads : ((R + 31) / 32) * 32;
+  prepare_kernel<<<1, threads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ============================================================================= stage (e)
+// vLLM Speculators: parallel drafting for speculative decoding, "Production
+// integration in vLLM": verification preserves the target's output; greedy
+// form: accept the longest prefix of drafts equal to the target's tokens,
+// then take the target's token at the first mismatch as the bonus token.
+
+__global__ void verify_kernel(const VerifyArgs a) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= a.B) return;
+  const int32_t* d = a.draft + (size_t)b * a.K;
+  const int32_t* t = a.target + (size_t)b * (a.K + 1);
+  int acc = 0;
+  while (acc < a.K && d[acc] == t[acc]) ++acc;
+  a.acc_out[b] = acc;
+  a.bonus_out[b] = t[acc];
+  if (a.next_tokens != nullptr) {
+    // next verify batch: [bonus, t_1..t_K] at positions after the NTP position
+    int prev_a = a.num_accepted[b];
+    prev_a = prev_a < 0 ? 0 : (prev_a > a.K ? a.K : prev_a);
+    const int p0 = a.prev_pos[(size_t)b * (a.K + 1) + prev_a] + 1;
+    int32_t* nt = a.next_tokens + (size_t)b * (a.K + 1);
+    int32_t* np = a.next_pos + (size_t)b * (a.K + 1);
+    nt[0] = a.bonus_in[b];
+    for (int k = 0; k < a.K; ++k) nt[k + 1] = d[k];
+    for (int j = 0; j <= a.K; ++j) np[j] = p0 + j;
+  }
+}
+
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
+  const int threads = 128;
+  verify_kernel<<<(a.B + threads - 1) / threads, threads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ============================================================================= forward prologue
+
+constexpr int kInitThreads = 1024;
+
+__global__ void __launch_bounds__(kInitThreads) forward_init_kernel(const InitArgs a) {
+  const int tid = threadIdx.x;
+  int n = *a.n_valid;
+  if (n < 0 || n > a.R) {
+    if (tid == 0) set_err(a.err, PE_DEV_BAD_ROW);
+    n = n < 0 ? 0 : a.R;
+  }
+  const int S = 2 * a.K;
+  for (int i = tid; i < a.n_counters; i += blockDim.x) a.counters[i] = 0;
+  for (int i = tid; i < a.T; i += blockDim.x) a.keys[i] = 0ull;
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    a.seq_start[b] = INT_MAX;
+    a.seq_len[b] = 0;
+    a.seq_maxpos[b] = -1;
+  }
+  __syncthreads();
+  for (int t = tid; t < a.R; t += blockDim.x) {
+    if (t < n) {
+      const int row = a.row_list[t];
+      if (row < 0 || row >= a.R) {
+        set_err(a.err, PE_DEV_BAD_ROW);
+        a.tok_pos[t] = 0;
+        a.tok_slot[t] = -1;
+        a.tok_seq[t] = 0;
+        continue;
+      }
+      const int b = row / S;
+      const int pos = a.positions[row];
+      a.tok_pos[t] = pos;
+      a.tok_slot[t] = a.slot_mapping[row];
+      a.tok_seq[t] = b;
+      atomicMin(&a.seq_start[b], t);
+      atomicAdd(&a.seq_len[b], 1);
+      atomicMax(&a.seq_maxpos[b], pos);
+    } else {
+      a.tok_pos[t] = 0;
+      a.tok_slot[t] = -1;
+      a.tok_seq[t] = 0;
+    }
+  }
+  __syncthreads();
+  // Attention work list: every (sequence, kv head) splits its causal range
+  // 0..maxpos into equal chunks; the chunk length is set so that the whole
+  // batch yields about target_items items.
+  __shared__ int chunk_s;
+  if (tid == 0) {
+    long long total = 0;
+    for (int b = 0; b < a.B; ++b)
+      if (a.seq_len[b] > 0) total += a.seq_maxpos[b] + 1;
+    long long per = (total * a.n_kv + a.target_items - 1) / a.target_items;
+    per = ((per + 63) / 64) * 64;
+    int chunk = (int)(per < a.min_chunk ? a.min_chunk : per);
+    int it = 0;
+    for (int b = 0; b < a.B; ++b) {
+      const int L = a.seq_len[b] > 0 ? a.seq_maxpos[b] + 1 : 0;
+      const int nc = (L + chunk - 1) / chunk;
+      a.n_chunks[b] = nc;
+      a.item_base[b] = it;
+      it += nc * a.n_kv;
+    }
+    if (it > a.max_items) {   // cannot happen with the host's sizing; keep the list in bounds
+      set_err(a.err, PE_DEV_BAD_ROW);
+      it = 0;
+      for (int b = 0; b < a.B; ++b) a.n_chunks[b] = 0;
+    }
+    *a.n_items = it;
+    chunk_s = chunk;
+  }
+  __syncthreads();
+  const int chunk = chunk_s;
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    const int L = a.seq_len[b] > 0 ? a.seq_maxpos[b] + 1 : 0;
+    const int nc = a.n_chunks[b];
+    int it = a.item_base[b];
+    for (int g = 0; g < a.n_kv; ++g)
+      for (int c = 0; c < nc; ++c) {
+        const int c0 = c * chunk;
+        const int c1 = c0 + chunk < L ? c0 + chunk : L;
+        a.items[it++] = make_int4(b, g, c0, c1);
+      }
+  }
+}
+
+cudaError_t launch_forward_init(const InitArgs& a, cudaStream_t s) {
+  forward_init_kernel<<<1, kInitThreads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ============================================================================= stage (b)
+// P-EAGLE: Parallel Speculative Decoding in vLLM, step 2 "Parallel Drafting"
+// and "Hidden-state management": each valid row is concat(emb(token), hidden),
+// hidden = target hidden state (context / NTP rows) or the learned h_shared
+// (MASK rows).  Rows are moved HBM -> shared -> HBM with bulk async copies;
+// the MASK row (emb(mask), h_shared) is staged in shared memory once per CTA
+// and stored to every MASK row the CTA owns.
+
+constexpr int kScatterRowsPerCta = 4;
+
+__global__ void __launch_bounds__(32) scatter_kernel(const ScatterArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  int n = *a.n_valid;
+  n = n < 0 ? 0 : (n > a.R ? a.R : n);
+  const int i0 = blockIdx.x * kScatterRowsPerCta;
+  if (i0 >= n) return;
+  const int i1 = i0 + kScatterRowsPerCta < n ? i0 + kScatterRowsPerCta : n;
+  const uint32_t rb = (uint32_t)a.d * a.elem_bytes;  // bytes of one half row
+  const uint8_t* emb = static_cast<const uint8_t*>(a.emb);
+  const uint8_t* hid = static_cast<const uint8_t*>(a.hidden);
+  uint8_t* x0 = static_cast<uint8_t*>(a.x0);
+  const uint32_t base = smem_u32(sm);
+  const uint32_t mask_slot = base + (uint32_t)(2 * kScatterRowsPerCta) * rb;  // [emb(mask) | h_shared]
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+
+  // which rows need what
+  int kind[kScatterRowsPerCta];      // 0 skip, 1 regular, 2 MASK
+  const uint8_t* src_e[kScatterRowsPerCta];
+  const uint8_t* src_h[kScatterRowsPerCta];
+  uint32_t bytes = 0;
+  bool any_mask = false;
+  for (int i = i0; i < i1; ++i) {
+    const int k = i - i0;
+    kind[k] = 0;
+    const int row = a.row_list[i];
+    if (row < 0 || row >= a.R) { set_err(a.err, PE_DEV_BAD_ROW); continue; }
+    if (a.is_mask[row]) { kind[k] = 2; any_mask = true; continue; }
+    const int tok = a.input_ids[row];
+    const int hm = a.hidden_map[row];
+    if (tok < 0 || tok > a.vocab) { set_err(a.err, PE_DEV_BAD_TOKEN); continue; }
+    if (hm < 0 || hm >= a.n_hidden) { set_err(a.err, PE_DEV_BAD_ROW); continue; }
+    kind[k] = 1;
+    src_e[k] = emb + (size_t)tok * rb;
+    src_h[k] = hid + (size_t)hm * rb;
+    bytes += 2 * rb;
+  }
+  if (any_mask) bytes += 2 * rb;
+  if (bytes == 0) return;
+  mbar_expect_tx(b, bytes);
+  for (int k = 0; k < i1 - i0; ++k) {
+    if (kind[k] != 1) continue;
+    bulk_g2s(base + (uint32_t)(2 * k) * rb, src_e[k], rb, b);
+    bulk_g2s(base + (uint32_t)(2 * k + 1) * rb, src_h[k], rb, b);
+  }
+  if (any_mask) {
+    bulk_g2s(mask_slot, emb + (size_t)a.vocab * rb, rb, b);
+    bulk_g2s(mask_slot + rb, a.h_shared, rb, b);
+  }
+  if (!mbar_wait(b, 0, a.err, nullptr)) return;
+  fence_proxy_async_smem();
+  for (int k = 0; k < i1 - i0; ++k) {
+    uint8_t* dst = x0 + (size_t)(i0 + k) * 2 * rb;
+    if (kind[k] == 1) {
+      bulk_s2g(dst, base + (uint32_t)(2 * k) * rb, rb);
+      bulk_s2g(dst + rb, base + (uint32_t)(2 * k + 1) * rb, rb);
+    } else if (kind[k] == 2) {
+      bulk_s2g(dst, mask_slot, 2 * rb);
+    }
+  }
+  bulk_commit();
+  bulk_wait_all();
+}
+
+cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
+  const size_t smem = (size_t)(2 * kScatterRowsPerCta + 2) * a.d * a.elem_bytes;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = (a.R + kScatterRowsPerCta - 1) / kScatterRowsPerCta;
+  scatter_kernel<<<grid, 32, smem, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ============================================================================= RMSNorm
+// y = x / sqrt(mean(x^2) + eps) * g, one warp per row, fp32 math, fixed
+// reduction order (per-lane partial sums, then a butterfly).
+
+template <typename OutT, typename GT>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const NormArgs a) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  int n = a.n_rows;
+  if (a.n_rows_dev != nullptr) n = min(n, *a.n_rows_dev);
+  if (warp >= n) return;
+  int src = warp;
+  if (a.row_map != nullptr) {
+    src = a.row_map[warp];
+    if (src < 0 || src >= a.src_rows) {
+      if (lane == 0) set_err(a.err, PE_DEV_BAD_ROW);
+      return;
+    }
+  }
+  const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)src * a.d);
+  const int nv = a.d / 4;
+  float ss = 0.f;
+  for (int j = lane; j < nv; j += 32) {
+    const float4 v = xr[j];
+    ss += v.x * v.x;
+    ss += v.y * v.y;
+    ss += v.z * v.z;
+    ss += v.w * v.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  const float inv = 1.0f / sqrtf(ss / (float)a.d + a.eps);
+  const GT* g = static_cast<const GT*>(a.g);
+  OutT* y = static_cast<OutT*>(a.y) + (size_t)warp * a.d;
+  for (int j = lane; j < nv; j += 32) {
+    const float4 v = xr[j];
+    y[4 * j + 0] = from_float<OutT>(v.x * inv * to_float<GT>(g[4 * j + 0]));
+    y[4 * j + 1] = from_float<OutT>(v.y * inv * to_float<GT>(g[4 * j + 1]));
+    y[4 * j + 2] = from_float<OutT>(v.z * inv * to_float<GT>(g[4 * j + 2]));
+    y[4 * j + 3] = from_float<OutT>(v.w * inv * to_float<GT>(g[4 * j + 3]));
+  }
+}
+
+cudaError_t launch_rmsnorm(const NormArgs& a, pe_dtype dt, cudaStream_t s) {
+  const int threads = 256, rows_per_block = threads / 32;
+  const int grid = (a.n_rows + rows_per_block - 1) / rows_per_block;
+  if (grid == 0) return cudaSuccess;
+  if (dt == PE_BF16)
+    rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, threads, 0, s>>>(a);
+  else
+    rmsnorm_kernel<float, float><<<grid, threads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace pe

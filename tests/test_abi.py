@@ -1,0 +1,70 @@
+"""The C-ABI library loads, exports every symbol include/pe.h declares, and validates
+arguments on the host (no GPU needed: nothing here launches a kernel)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_step_gb300 as pe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "pe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_five_stage_calls():
+    names = _declared_functions()
+    for n in ["pe_prepare_batch", "pe_scatter_hidden", "pe_draft_forward", "pe_verify", "pe_step"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = pe.lib()
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    assert set(_declared_functions()) == set(pe.EXPORTED_SYMBOLS)
+
+
+def _cfg(**kw):
+    base = dict(B=8, K=7, d=2048, n_q=32, n_kv=4, head_dim=128, ffn=6144, vocab=151936, n_layers=1,
+                max_pages_per_seq=257, dtype="bf16")
+    base.update(kw)
+    return pe.Config.make(**base)
+
+
+def test_config_validation_codes():
+    assert pe.check_config(_cfg()) == pe.PE_OK
+    assert pe.check_config(_cfg(B=0)) == 2
+    assert pe.check_config(_cfg(n_q=30, n_kv=4)) == 2          # n_kv must divide n_q
+    assert pe.check_config(_cfg(head_dim=96)) == 3
+    assert pe.check_config(_cfg(page_size=32)) == 3
+    assert pe.check_config(_cfg(K=9, n_q=64, n_kv=8)) == 3     # 2K * (n_q/n_kv) > 128 query rows
+    assert pe.check_config(_cfg(d=2052)) == 3                  # bf16 rows must be 16-byte multiples
+    assert pe.check_config(_cfg(dtype="f32", d=2050)) == 3     # fp32 rows too
+    assert pe.check_config(_cfg(dtype="f32", d=2048)) == pe.PE_OK
+    assert pe.status_str(0) == "ok"
+
+
+def test_workspace_bytes_grow_with_batch():
+    small = pe.workspace_bytes(_cfg(B=1))
+    big = pe.workspace_bytes(_cfg(B=64, K=7, n_q=64, n_kv=8))
+    assert 0 < small < big
+    assert pe.workspace_bytes(_cfg(B=0)) == 0
+    assert pe.trace_points(_cfg(n_layers=2)) == 8 + 14
+
+
+def test_null_pointers_rejected_before_launch():
+    L = pe.lib()
+    cfg = _cfg()
+    null = ctypes.c_void_p(None)
+    st = L.pe_prepare_batch(ctypes.byref(cfg), null, null, null, null, null, 10, *([null] * 11))
+    assert st == 1
+    st = L.pe_verify(ctypes.byref(cfg), null, null, null, null, null)
+    assert st == 1
+    assert L.pe_set_trace_events(None, -1) == 1

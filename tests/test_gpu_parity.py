@@ -1,0 +1,260 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Integer work (batch metadata, compaction, verification) is bit-exact; the input
+rows are a copy, so bit-exact too; logits are within 1e-3 (fp32) / 5e-2 (bf16)
+and draft tokens equal wherever the oracle's top-1/top-2 gap exceeds 0.1.
+"""
+
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_step_gb300 as pe
+from pe_workload import Config, config, make_round, make_targets, make_weights, sweep_config
+
+from gpu_harness import (check_kv_writes, check_logits, meta_np, oracle_round, run_stages, setup,
+                         to_np_storage)
+
+pytestmark = pytest.mark.gpu
+
+
+def _small(**kw) -> Config:
+    base = dict(name="small-bf16", B=3, K=4, n_layers=1, d=256, n_q=8, n_kv=2, head_dim=64, ffn=384,
+                vocab=1000, dtype="bf16", prefix="uniform", prefix_args=(1, 300), accepted="uniform", seed=7)
+    base.update(kw)
+    return Config(**base)
+
+
+SMALL = {
+    "bf16-hd64": _small(),
+    "bf16-hd128-K8-G8": _small(B=2, K=8, n_q=16, n_kv=2, head_dim=128, d=512, ffn=640, vocab=777, seed=8),
+    "bf16-K1": _small(B=5, K=1, seed=9),
+    "bf16-L2-long": _small(B=2, K=7, n_layers=2, prefix_args=(900, 2100), vocab=3001, seed=10),
+    "f32-c0": config(0),
+    "f32-L2": _small(dtype="f32", n_layers=2, seed=11),
+}
+
+
+# ----------------------------------------------------------------------------- stage (a)
+
+def _prep_compare(cfg_np, rnd):
+    R = {k: torch.from_numpy(np.ascontiguousarray(getattr(rnd, k), dtype=np.int32)).cuda()
+         for k in ("prev_tokens", "prev_pos", "num_accepted", "bonus", "block_table")}
+    cfg = pe.Config.make(cfg_np.B, cfg_np.K, cfg_np.d, cfg_np.n_q, cfg_np.n_kv, cfg_np.head_dim, cfg_np.ffn,
+                         cfg_np.vocab, cfg_np.n_layers, rnd.block_table.shape[1], cfg_np.dtype)
+    meta = pe.alloc_batch(cfg)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pe.prepare_batch(cfg, R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"], R["block_table"],
+                     rnd.num_pages, meta, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.prepare_batch(cfg_np.K, cfg_np.vocab, rnd.prev_tokens, rnd.prev_pos, rnd.num_accepted, rnd.bonus,
+                               rnd.block_table, cfg_np.page_size)
+    got = {k: v.cpu().numpy() for k, v in meta.items()}
+    n = ref["n_valid"]
+    assert int(got["n_valid"][0]) == n
+    for k in ("input_ids", "positions", "slot_mapping", "is_rejected", "is_mask", "hidden_map"):
+        assert np.array_equal(got[k], ref[k]), k
+    assert np.array_equal(got["row_list"][:n], ref["row_list"])
+    assert (got["row_list"][n:] == -1).all()
+    assert np.array_equal(got["draft_rows"], ref["draft_rows"])
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3])
+def test_prepare_batch_bit_exact_configs(idx):
+    cfg_np = config(idx)
+    _prep_compare(cfg_np, make_round(cfg_np, with_cache=False))
+
+
+@pytest.mark.parametrize("K,a_mode", [(1, "all0"), (1, "allK"), (8, "all0"), (8, "allK"), (5, "mixed")])
+def test_prepare_batch_bit_exact_edges(K, a_mode):
+    cfg_np = sweep_config(37, K)
+    rnd = make_round(cfg_np, with_cache=False)
+    if a_mode == "all0":
+        rnd.num_accepted[:] = 0
+    elif a_mode == "allK":
+        rnd.num_accepted[:] = K
+    _prep_compare(cfg_np, rnd)
+
+
+def test_prepare_batch_large_batch_multi_chunk():
+    """B*2K > 1024: the single-CTA rebuild scans several chunks with a carry."""
+    cfg_np = sweep_config(100, 8)   # 1600 padded rows
+    _prep_compare(cfg_np, make_round(cfg_np, with_cache=False))
+
+
+# ----------------------------------------------------------------------------- stage (e)
+
+def test_verify_brute_force_and_random():
+    rows_d, rows_t = [], []
+    K = 3
+    for d in itertools.product(range(3), repeat=K):
+        for t in itertools.product(range(3), repeat=K + 1):
+            rows_d.append(d)
+            rows_t.append(t)
+    rng = np.random.default_rng(0)
+    for _ in range(500):
+        d = rng.integers(0, 4, K)
+        rows_d.append(tuple(d))
+        rows_t.append(tuple(rng.integers(0, 4, K + 1)))
+    D = np.array(rows_d, np.int32)
+    T = np.array(rows_t, np.int32)
+    cfg = pe.Config.make(len(D), K, 256, 4, 4, 64, 256, 16, 1, 4, "bf16")
+    acc = torch.empty(len(D), dtype=torch.int32, device="cuda")
+    bon = torch.empty_like(acc)
+    pe.verify(cfg, torch.from_numpy(D).cuda(), torch.from_numpy(T).cuda(), acc, bon)
+    torch.cuda.synchronize()
+    ra, rb = oracle.verify(D, T)
+    assert np.array_equal(acc.cpu().numpy(), ra)
+    assert np.array_equal(bon.cpu().numpy(), rb)
+
+
+# ----------------------------------------------------------------------------- stage (b)
+
+@pytest.mark.parametrize("name", ["f32-c0", "bf16-hd64", "bf16-K1"])
+def test_scatter_bit_exact(name):
+    c = setup(SMALL[name])
+    R = c.Rd
+    c.rd.prepare(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"])
+    c.rd.scatter(R["target_hidden"])
+    torch.cuda.synchronize()
+    assert int(c.rd.err.item()) == 0
+    m = oracle.prepare_batch(c.cfg_np.K, c.cfg_np.vocab, c.r_np.prev_tokens, c.r_np.prev_pos,
+                             c.r_np.num_accepted, c.r_np.bonus, c.r_np.block_table)
+    x0 = oracle.scatter_hidden(c.w_np.emb, c.w_np.h_shared, c.r_np.target_hidden, m["input_ids"], m["is_mask"],
+                               m["hidden_map"])
+    got = to_np_storage(c.rd.x0)[: m["n_valid"]]
+    assert np.array_equal(got, x0[m["row_list"]])
+
+
+def test_scatter_bit_exact_full_size_c3():
+    cfg_np = config(3)
+    c = setup(cfg_np)
+    R = c.Rd
+    c.rd.prepare(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"])
+    c.rd.scatter(R["target_hidden"])
+    torch.cuda.synchronize()
+    assert int(c.rd.err.item()) == 0
+    m = oracle.prepare_batch(cfg_np.K, cfg_np.vocab, c.r_np.prev_tokens, c.r_np.prev_pos, c.r_np.num_accepted,
+                             c.r_np.bonus, c.r_np.block_table)
+    x0 = oracle.scatter_hidden(c.w_np.emb, c.w_np.h_shared, c.r_np.target_hidden, m["input_ids"], m["is_mask"],
+                               m["hidden_map"])
+    assert np.array_equal(to_np_storage(c.rd.x0)[: m["n_valid"]], x0[m["row_list"]])
+
+
+# ----------------------------------------------------------------------------- stages (c)+(d)
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_small_full_oracle(name):
+    """Every sequence, every draft logit, and every cache entry, against the oracle."""
+    c = setup(SMALL[name])
+    assert run_stages(c) == 0
+    ref = oracle_round(c, want_kv=True)
+    check_logits(c, ref)
+    check_kv_writes(c, ref)
+
+
+@pytest.mark.parametrize("idx,seqs", [(1, None), (2, None), (3, "sample")])
+def test_forward_full_size(idx, seqs):
+    """The benchmark workloads at their full sizes; at B=64 the oracle checks a sample of
+    sequences (independent of one another): the shortest, the longest, and two fully rejected
+    ones where present."""
+    cfg_np = config(idx)
+    c = setup(cfg_np)
+    assert run_stages(c) == 0
+    if seqs == "sample":
+        P, a = c.r_np.prefix_len, c.r_np.num_accepted
+        seqs = sorted({int(np.argmin(P)), int(np.argmax(P))} | set(np.nonzero(a == 0)[0][:2].tolist())
+                      | {int(np.argmax(a))})
+    ref = oracle_round(c, seqs=seqs, want_kv=False)
+    check_logits(c, ref, seqs)
+
+
+def test_forward_sweep_corners():
+    """K x B sweep drafter (2 layers): corners B=1, K=1 and B=64, K=8 (sampled)."""
+    for B, K in ((1, 1), (64, 8)):
+        cfg_np = sweep_config(B, K)
+        c = setup(cfg_np)
+        assert run_stages(c) == 0
+        seqs = None if B == 1 else [0, int(np.argmax(c.r_np.prefix_len))]
+        check_logits(c, oracle_round(c, seqs=seqs), seqs)
+
+
+# ----------------------------------------------------------------------------- invariants on the GPU path
+
+def test_deterministic_and_page_permutation_invariant():
+    cfg_np = SMALL["bf16-L2-long"]
+    c = setup(cfg_np)
+    assert run_stages(c) == 0
+    lg1, d1 = c.rd.logits.clone(), c.rd.draft_tokens.clone()
+    # same inputs again (fresh cache copy): bit-identical
+    for l in range(cfg_np.n_layers):
+        c.kv.k_cache[l].copy_(c.k_before[l])
+        c.kv.v_cache[l].copy_(c.v_before[l])
+    assert run_stages(c) == 0
+    assert torch.equal(lg1, c.rd.logits) and torch.equal(d1, c.rd.draft_tokens)
+    # the same logical cache on permuted physical pages
+    rnd = c.r_np
+    perm = np.random.default_rng(1).permutation(rnd.num_pages)
+    for l in range(cfg_np.n_layers):
+        rnd.k_cache[l] = rnd.k_cache[l].copy()
+        rnd.v_cache[l] = rnd.v_cache[l].copy()
+        k2, v2 = np.empty_like(rnd.k_cache[l]), np.empty_like(rnd.v_cache[l])
+        k2[perm], v2[perm] = rnd.k_cache[l], rnd.v_cache[l]
+        rnd.k_cache[l], rnd.v_cache[l] = k2, v2
+    rnd.block_table = np.where(rnd.block_table >= 0, perm[np.maximum(rnd.block_table, 0)], -1).astype(np.int32)
+    c2 = setup(cfg_np, weights=c.w_np, rnd=rnd)
+    assert run_stages(c2) == 0
+    assert torch.equal(lg1, c2.rd.logits) and torch.equal(d1, c2.rd.draft_tokens)
+
+
+def test_step_equals_stages_and_next_batch():
+    cfg_np = SMALL["bf16-hd64"]
+    c = setup(cfg_np)
+    assert run_stages(c) == 0
+    drafts = c.rd.draft_tokens.cpu().numpy()
+    target = make_targets(drafts, c.r_np.target_u, c.r_np.target_r)
+    # fresh cache, then the whole round in one call
+    for l in range(cfg_np.n_layers):
+        c.kv.k_cache[l].copy_(c.k_before[l])
+        c.kv.v_cache[l].copy_(c.v_before[l])
+    lg_stages = c.rd.logits.clone()
+    R = c.Rd
+    c.rd.step(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"], R["target_hidden"],
+              torch.from_numpy(target).cuda(), logits=True)
+    torch.cuda.synchronize()
+    assert int(c.rd.err.item()) == 0
+    assert torch.equal(c.rd.logits, lg_stages)
+    assert np.array_equal(c.rd.draft_tokens.cpu().numpy(), drafts)
+    ra, rb = oracle.verify(drafts, target)
+    assert np.array_equal(c.rd.out["num_accepted"].cpu().numpy(), ra)
+    assert np.array_equal(c.rd.out["bonus"].cpu().numpy(), rb)
+    nt = c.rd.out["next_prev_tokens"].cpu().numpy()
+    npos = c.rd.out["next_prev_pos"].cpu().numpy()
+    for b in range(cfg_np.B):
+        a = int(c.r_np.num_accepted[b])
+        assert nt[b, 0] == c.r_np.bonus[b] and np.array_equal(nt[b, 1:], drafts[b])
+        assert np.array_equal(npos[b], c.r_np.prev_pos[b][a] + 1 + np.arange(cfg_np.K + 1))
+
+
+# ----------------------------------------------------------------------------- device-side checks
+
+def test_device_check_bad_accepted_count():
+    """An accepted count above K is flagged on the device; the rows stay in bounds."""
+    cfg_np = SMALL["bf16-hd64"]
+    rnd = make_round(cfg_np)
+    rnd.num_accepted[1] = cfg_np.K + 3
+    c = setup(cfg_np, rnd=rnd)
+    assert run_stages(c) == pe.PE_DEV_BAD_ACCEPTED
+
+
+def test_device_check_bad_page():
+    """A block-table entry outside the page pool is flagged and no cache access uses it."""
+    cfg_np = SMALL["bf16-hd64"]
+    rnd = make_round(cfg_np)
+    rnd.block_table[0, 0] = rnd.num_pages + 5
+    c = setup(cfg_np, rnd=rnd)
+    assert run_stages(c) == pe.PE_DEV_BAD_PAGE
