@@ -1,0 +1,430 @@
+"""Benchmark of one P-EAGLE parallel-drafting round (pe_step) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+Prints one JSON line.  A step is one pe_step call: batch rebuild, input-row
+scatter, drafter pass, LM head + argmax, greedy verification, over seeded
+synthetic inputs of the chosen workload (default: workload 1, the
+Qwen3-Coder-30B-shaped drafter at B=8, K=7).  Inputs are resident in HBM
+before timing; every timed step is bracketed by CUDA events on the launch
+stream and L2 is flushed (512 MiB write) between steps, outside the events.
+`e2e` repeats the measurement through the same C-ABI call with the round's
+per-step inputs copied from pinned host memory and its results copied back.
+Under torchrun each rank runs an independent replica (no collective on the
+data path); the max over ranks is reported.
+
+`--impl reference` times the CPU oracle on the host cores (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from pe_workload import config, make_round, make_targets, make_weights, sweep_config  # noqa: E402
+
+METRIC = "draft tokens/s and µs per parallel-draft round; % of HBM / tensor roofline"
+UNIT = "draft tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1, help="workload index 0..3")
+    ap.add_argument("--sweep", type=str, default=None, help="B,K of the 2-layer K x B sweep workload")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-oracle sample time")
+    return ap.parse_args()
+
+
+def workload(args):
+    if args.sweep:
+        B, K = (int(x) for x in args.sweep.split(","))
+        return sweep_config(B, K)
+    return config(args.config)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- cost model
+
+def round_cost(cfg, rnd) -> dict:
+    """Algorithmic bytes and flops of one round (counting only).  Bytes: every weight once (the
+    embedding table only for the rows the batch needs), the KV prefix once per sequence and layer,
+    the new KV entries, the valid rows' hidden states, metadata.  Flops: 2*rows*params of every
+    linear map over the valid rows, the LM head over the B*K draft rows, and q.k + p.v over each
+    valid row's causal range.  Rejected (padding) rows are not counted."""
+    eb = 2 if cfg.dtype == "bf16" else 4
+    K, B, d, hd = cfg.K, cfg.B, cfg.d, cfg.head_dim
+    a = rnd.num_accepted.astype(np.int64)
+    n_b = a + K                                   # valid rows per sequence
+    n_valid = int(n_b.sum())
+    P = rnd.prefix_len.astype(np.int64)
+    layer_params = (cfg.qkv_out * d + d * cfg.n_q * hd + 2 * cfg.ffn * d + d * cfg.ffn)
+    weights = (d * 2 * d + cfg.n_layers * (layer_params + 2 * d) + d + cfg.vocab * d) * eb
+    lm_bytes = cfg.vocab * d * eb
+    kv_read = int(cfg.n_layers * (P + n_b).sum() * cfg.n_kv * hd * 2 * eb)
+    kv_write = cfg.n_layers * n_valid * cfg.n_kv * hd * 2 * eb
+    rows = n_valid * d * eb * 2                  # embedding row + hidden row per valid row
+    meta = B * (K + 1) * 4 * 4 + B * 2 * K * 32
+    bytes_total = weights + kv_read + kv_write + rows + meta
+    ctx = 0
+    for b in range(B):
+        pos = P[b] + np.arange(n_b[b])
+        ctx += int((pos + 1).sum())
+    flops_lin = 2 * n_valid * (d * 2 * d + cfg.n_layers * layer_params)
+    flops_lm = 2 * B * K * cfg.vocab * d
+    flops_attn = cfg.n_layers * 4 * cfg.n_q * hd * ctx
+    return dict(bytes=int(bytes_total), flops=int(flops_lin + flops_lm + flops_attn), lm_bytes=int(lm_bytes),
+                lm_flops=int(flops_lm), n_valid=n_valid, weights_bytes=int(weights), kv_read_bytes=kv_read,
+                attn_flops=int(flops_attn))
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clocks and throttle reasons while the timed loop runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        fd, self.path = tempfile.mkstemp(prefix="pe_clocks_", suffix=".csv")
+        os.close(fd)
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def recorded_traffic(kernel_key: str, workload_name: str):
+    """DRAM bytes per launch from an ncu capture recorded in profiles/ncu_traffic.json, or None when
+    there is none or the kernel's source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(kernel_key, {}).get(workload_name)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+# ----------------------------------------------------------------------------- CPU oracle arms
+
+def cpu_oracle_sample(cfg, w, rnd, target_seconds: float):
+    """The oracle on whole sequences of the workload, round-robin, for about target_seconds."""
+    import oracle
+
+    oracle.build()
+    tokens, elapsed, n, i = 0, 0.0, 0, 0
+    while elapsed < target_seconds:
+        t0 = time.perf_counter()
+        oracle.run_round(cfg, w, rnd, seqs=[i % cfg.B])
+        elapsed += time.perf_counter() - t0
+        tokens += cfg.K
+        n += 1
+        i += 1
+    return dict(value=tokens / elapsed, unit=UNIT, cores=oracle.threads_used(), kind="oracle",
+                sample=f"{n} single-sequence passes (round-robin over the {cfg.B} sequences) of {cfg.name}: "
+                       f"batch rebuild, input rows, fp64 drafter pass and LM head over the sequence's draft "
+                       f"rows; {elapsed:.1f} s")
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    cfg = workload(args)
+    w, rnd = make_weights(cfg), make_round(cfg)
+    oracle.build()
+    for i in range(args.warmup):
+        oracle.run_round(cfg, w, rnd, seqs=[i % cfg.B])
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.run_round(cfg, w, rnd, seqs=[i % cfg.B])
+        times.append(time.perf_counter() - t0)
+    per = sum(times) / len(times)
+    value = cfg.K / per
+    out = dict(impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus, steps=args.steps,
+               warmup=args.warmup, ms_per_step=1e3 * per, higher_is_better=True, scaling="weak",
+               vs_baseline=None, dtype="f64", data="synthetic (seeded; shapes and value distributions of the workload)",
+               config=dict(workload=cfg.name, B=cfg.B, K=cfg.K, n_layers=cfg.n_layers,
+                           step="one sequence's share of the round (sequences round-robin)"),
+               cpu_baseline=dict(kind="oracle", cores=oracle.threads_used(), value=value, unit=UNIT,
+                                 sample=f"{args.steps} single-sequence passes of {cfg.name}"),
+               e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(out), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def stage_names(n_layers):
+    names = ["prepare", "scatter", "forward_init", "fc"]
+    for l in range(n_layers):
+        names += [f"l{l}.norm1", f"l{l}.qkv_rope_kv", f"l{l}.attention", f"l{l}.o_proj", f"l{l}.norm2",
+                  f"l{l}.gate_up_swiglu", f"l{l}.down"]
+    return names + ["final_norm", "lm_head_argmax", "verify"]
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import speculative_decoding_step_gb300 as pe
+    from pe_workload.device import round_to_device, weights_to_device
+
+    pe.build()
+    cfg_np = workload(args)
+    seed = cfg_np.seed + 1000 * rank if world > 1 else cfg_np.seed
+    w_np, rnd = make_weights(cfg_np, seed), make_round(cfg_np, seed)
+    W, R = weights_to_device(w_np, dev), round_to_device(rnd, dev)
+    cfg = pe.Config.make(cfg_np.B, cfg_np.K, cfg_np.d, cfg_np.n_q, cfg_np.n_kv, cfg_np.head_dim, cfg_np.ffn,
+                         cfg_np.vocab, cfg_np.n_layers, rnd.block_table.shape[1], cfg_np.dtype,
+                         rms_eps=cfg_np.rms_eps, rope_theta=cfg_np.rope_theta)
+    rd = pe.Round(cfg, pe.DeviceWeights(**W), pe.DeviceKV(R["k_cache"], R["v_cache"]), R["block_table"], dev)
+    stream = torch.cuda.current_stream()
+
+    # target tokens of this round's verify batch: from one untimed pass's drafts
+    rd.prepare(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"])
+    rd.scatter(R["target_hidden"])
+    rd.forward()
+    torch.cuda.synchronize()
+    target = torch.from_numpy(make_targets(rd.draft_tokens.cpu().numpy(), rnd.target_u, rnd.target_r)).to(dev)
+
+    def step():
+        rd.step(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"], R["target_hidden"], target)
+
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def timed(n, fn, traced=None):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            if traced is not None:
+                pe.set_trace_events(traced[i])
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        if traced is not None:
+            pe.set_trace_events([])
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    err = int(rd.err.item())
+
+    # ---- headline: direct pe_step launches, device-resident inputs
+    sampler = ClockSampler(torch.cuda.current_device())
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = pe.kernel_launches()
+    t_wall = time.perf_counter()
+    step_ms = timed(args.steps, step)
+    wall = time.perf_counter() - t_wall
+    launches = pe.kernel_launches() - launches0
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = sum(step_ms) / len(step_ms)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- the same call captured once in a CUDA graph and replayed
+    graph_us = None
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step()
+            g.replay()
+            torch.cuda.synchronize()
+            graph_us = 1e3 * statistics.mean(timed(args.steps, g.replay))
+        except Exception as exc:  # report the direct launches only
+            graph_us = f"unavailable: {exc}"[:200]
+
+    # ---- per-stage device times: a separate traced pass (events between kernels; not the headline)
+    npts = pe.trace_points(cfg)
+    tr = [[torch.cuda.Event(enable_timing=True) for _ in range(npts)] for _ in range(args.steps)]
+    for row in tr:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    timed(args.steps, step, traced=tr)
+    names = stage_names(cfg_np.n_layers)
+    stage_ms = [statistics.median(tr[i][j].elapsed_time(tr[i][j + 1]) for i in range(args.steps))
+                for j in range(npts - 1)]
+    stages_us = {n: round(1e3 * t, 2) for n, t in zip(names, stage_ms)}
+    lm_ms = stage_ms[names.index("lm_head_argmax")]
+
+    # ---- end to end through the same C-ABI call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: R[k].cpu().pin_memory() for k in ("prev_tokens", "prev_pos", "num_accepted", "bonus",
+                                                       "target_hidden")}
+        host_in["target"] = target.cpu().pin_memory()
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+        outs = ("draft_tokens", "num_accepted", "bonus")
+        host_out = {k: torch.empty(rd.out[k].shape, dtype=rd.out[k].dtype).pin_memory() for k in outs}
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+        def e2e_step():
+            for k in host_in:
+                dev_in[k].copy_(host_in[k], non_blocking=True)
+            rd.step(dev_in["prev_tokens"], dev_in["prev_pos"], dev_in["num_accepted"], dev_in["bonus"],
+                    dev_in["target_hidden"], dev_in["target"])
+            for k in outs:
+                host_out[k].copy_(rd.out[k], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        e_ms = statistics.mean(timed(args.steps, e2e_step))
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = dict(value=world * cfg_np.B * cfg_np.K / (e_ms * 1e-3), unit=UNIT, h2d_bytes_per_step=int(h2d),
+                   d2h_bytes_per_step=int(d2h), ms_per_step=e_ms)
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    peaks, src = load_peaks()
+    cost = round_cost(cfg_np, rnd)
+    hbm = peaks["hbm_gbs"] * 1e9
+    tc_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 1e12
+    # dominant kernel: the LM head + argmax GEMM (one launch per round)
+    lm_t = lm_ms * 1e-3
+    if cfg_np.dtype == "bf16" and cost["lm_flops"] / tc_sus > cost["lm_bytes"] / hbm:
+        roof = dict(bound="tensor", achieved=cost["lm_flops"] / lm_t / 1e12, peak=tc_sus / 1e12, unit="TFLOP/s",
+                    peak_source=f"bf16_tflops_sustained, of {src}")
+    else:
+        roof = dict(bound="hbm", achieved=cost["lm_bytes"] / lm_t / 1e9, peak=hbm / 1e9, unit="GB/s",
+                    peak_source=f"hbm_gbs, of {src}")
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic("lm_head_argmax", cfg_np.name)
+    roof.update(kernel="gemm_tc_kernel<EPI_ARGMAX> (LM head + argmax)", algorithmic_bytes_per_launch=cost["lm_bytes"],
+                algorithmic_flops_per_launch=cost["lm_flops"], avg_launch_us=lm_ms * 1e3)
+    t_round = max(cost["bytes"] / hbm, cost["flops"] / tc_sus)
+    round_roof = dict(bytes=cost["bytes"], flops=cost["flops"], roofline_us=t_round * 1e6, measured_us=ms * 1e3,
+                      frac=t_round / (ms * 1e-3),
+                      bound="hbm" if cost["bytes"] / hbm >= cost["flops"] / tc_sus else "tensor")
+    if isinstance(graph_us, float):
+        round_roof["frac_graph"] = t_round * 1e6 / graph_us
+
+    cpu = None if args.no_cpu_baseline else cpu_oracle_sample(cfg_np, w_np, rnd, args.cpu_seconds)
+    value = world * cfg_np.B * cfg_np.K / (ms * 1e-3)
+    out = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
+               ms_per_step=ms, us_per_round=ms * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
+               dtype=cfg_np.dtype, data="synthetic (seeded; shapes and value distributions of the workload)",
+               config=dict(workload=cfg_np.name, B=cfg_np.B, K=cfg_np.K, n_layers=cfg_np.n_layers, d=cfg_np.d,
+                           vocab=cfg_np.vocab, n_valid_rows=cost["n_valid"],
+                           l2="flushed between timed steps (512 MiB write outside the step events)",
+                           replicas="one independent replica per rank" if world > 1 else "single GPU"),
+               graph_us_per_round=graph_us, roofline=roof, round_roofline=round_roof, stages_us=stages_us,
+               gpu_launches=int(launches), launches_per_step=launches / args.steps, device_error_word=err,
+               wall_s_timed_loop=wall, clocks=clocks, cpu_baseline=cpu, e2e=e2e)
+    print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
