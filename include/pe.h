@@ -203,6 +203,36 @@ pe_status pe_draft_forward(const pe_config *cfg, const pe_weights *w, const pe_k
                            int32_t *draft_tokens, float *logits_dbg, int32_t *err_word, pe_stream_t stream);
 
 /*
+ * pe_draft_forward for callers that cannot allocate device memory.  The P-EAGLE
+ * pages have no counterpart of this call; it exists for deployment.
+ *
+ * Some callers have no way to obtain a workspace.  Examples are a plugin whose
+ * host framework owns all device memory through its own pool and offers
+ * plugins no allocation hook, and a latency-critical serving loop where
+ * cudaMalloc is forbidden because it can synchronise the device.  For these
+ * callers the scratch lives in one fixed array of PE_NOALLOC_SCRATCH_BYTES
+ * inside this library.  Every GPU that loads the library reserves that array
+ * until the process exits.
+ *
+ * Arguments and results are those of pe_draft_forward, without the workspace.
+ * A config whose pe_workspace_bytes(cfg) exceeds PE_NOALLOC_SCRATCH_BYTES is
+ * rejected with PE_ERR_SHAPE before any launch.  The first call on a device
+ * looks up the array's device address on the current device; make that first
+ * call before any stream capture.  This call allocates nothing and calls no
+ * allocating routine.  Every call shares the one array, and the array keeps
+ * whatever the last call left in it.  The pass zeroes every counter and
+ * accumulator it needs at its start, so leftover contents do no harm.  Two
+ * calls that overlap on the GPU (different streams, or different host threads
+ * without ordering) race on the array and corrupt each other's results.
+ */
+#define PE_NOALLOC_SCRATCH_BYTES (48u << 20)
+pe_status pe_draft_forward_noalloc(const pe_config *cfg, const pe_weights *w, const pe_kv *kv,
+                                   const int32_t *block_table, const void *x0, const int32_t *positions,
+                                   const int64_t *slot_mapping, const int32_t *row_list, const int32_t *n_valid,
+                                   const int32_t *draft_rows, int32_t *draft_tokens, float *logits_dbg,
+                                   int32_t *err_word, pe_stream_t stream);
+
+/*
  * Stage (e): greedy verification (vLLM Speculators: parallel drafting for
  * speculative decoding, "Production integration in vLLM": verification keeps
  * the target's output; greedy form).

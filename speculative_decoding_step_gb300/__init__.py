@@ -35,7 +35,10 @@ PE_DEV_TIMEOUT = 0x0106
 
 EXPORTED_SYMBOLS = ["pe_prepare_batch", "pe_scatter_hidden", "pe_draft_forward", "pe_verify", "pe_step",
                     "pe_workspace_bytes", "pe_check_config", "pe_status_str", "pe_set_trace_events",
-                    "pe_trace_points", "pe_kernel_launches"]
+                    "pe_trace_points", "pe_kernel_launches", "pe_draft_forward_noalloc"]
+
+# Size of the library-owned scratch used by pe_draft_forward_noalloc (PE_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 48 << 20
 
 
 class PeError(RuntimeError):
@@ -135,6 +138,8 @@ def lib():
         L.pe_scatter_hidden.argtypes = [cp, ctypes.POINTER(_Weights)] + [vp] * 9
         L.pe_draft_forward.argtypes = ([cp, ctypes.POINTER(_Weights), ctypes.POINTER(_KV)] + [vp] * 7 +
                                        [vp, ctypes.c_size_t, vp, vp, vp, vp])
+        L.pe_draft_forward_noalloc.argtypes = ([cp, ctypes.POINTER(_Weights), ctypes.POINTER(_KV)] + [vp] * 7 +
+                                               [vp, vp, vp, vp])
         L.pe_verify.argtypes = [cp, vp, vp, vp, vp, vp]
         L.pe_step.argtypes = ([cp, ctypes.POINTER(_Weights), ctypes.POINTER(_KV)] + [vp] * 7 +
                               [vp, ctypes.c_size_t] + [vp] * 8)
@@ -218,6 +223,18 @@ def draft_forward(cfg, weights: DeviceWeights, kv: DeviceKV, block_table, x0, me
                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _ptr(draft_tokens), _ptr(logits_dbg), _ptr(err), _stream(stream))
     _check(st, "pe_draft_forward")
+
+
+def draft_forward_noalloc(cfg, weights: DeviceWeights, kv: DeviceKV, block_table, x0, meta: dict, draft_tokens,
+                          err, logits_dbg=None, stream=None):
+    """draft_forward without a workspace: the library's own fixed scratch array is used, for callers
+    that cannot allocate device memory.  Calls that overlap on the GPU race on that array."""
+    st = lib().pe_draft_forward_noalloc(ctypes.byref(cfg), ctypes.byref(weights.struct), ctypes.byref(kv.struct),
+                                        _ptr(block_table), _ptr(x0), _ptr(meta["positions"]),
+                                        _ptr(meta["slot_mapping"]), _ptr(meta["row_list"]), _ptr(meta["n_valid"]),
+                                        _ptr(meta["draft_rows"]), _ptr(draft_tokens), _ptr(logits_dbg), _ptr(err),
+                                        _stream(stream))
+    _check(st, "pe_draft_forward_noalloc")
 
 
 def verify(cfg, draft_tokens, target_tokens, num_accepted_out, bonus_out, stream=None):

@@ -1,0 +1,50 @@
+// pe_draft_forward_noalloc: the drafter pass with its scratch in a fixed array
+// that this library owns, for callers that cannot allocate device memory
+// (a plugin whose host framework owns every device allocation, or a serving
+// loop that must never call cudaMalloc).  See include/pe.h for the contract.
+#include <mutex>
+
+#include "pe_internal.h"
+
+namespace {
+
+// The scratch array.  In host code its name is only a host-side stand-in; the
+// kernels receive the device address that cudaGetSymbolAddress returns.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[PE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_addr[kMaxDevices] = {nullptr};
+
+// Device address of the array on the current device (looked up once per device).
+pe_status scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PE_ERR_CUDA;
+    g_addr[dev] = p;
+  }
+  *out = g_addr[dev];
+  return PE_OK;
+}
+
+}  // namespace
+
+extern "C" pe_status pe_draft_forward_noalloc(const pe_config* cfg, const pe_weights* w, const pe_kv* kv,
+                                              const int32_t* block_table, const void* x0, const int32_t* positions,
+                                              const int64_t* slot_mapping, const int32_t* row_list,
+                                              const int32_t* n_valid, const int32_t* draft_rows,
+                                              int32_t* draft_tokens, float* logits_dbg, int32_t* err_word,
+                                              pe_stream_t stream) {
+  const pe_status st = pe_check_config(cfg);
+  if (st != PE_OK) return st;
+  const size_t need = pe_workspace_bytes(cfg);
+  if (need == 0 || need > (size_t)PE_NOALLOC_SCRATCH_BYTES) return PE_ERR_SHAPE;
+  void* scratch = nullptr;
+  const pe_status sa = scratch_address(&scratch);
+  if (sa != PE_OK) return sa;
+  return pe_draft_forward(cfg, w, kv, block_table, x0, positions, slot_mapping, row_list, n_valid, draft_rows,
+                          scratch, (size_t)PE_NOALLOC_SCRATCH_BYTES, draft_tokens, logits_dbg, err_word, stream);
+}
