@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -15,6 +16,14 @@ namespace pe {
 
 static std::atomic<uint64_t> g_launches{0};
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("PE_PDL");
+    return !(e != nullptr && e[0] == '0');
+  }();
+  return on;
+}
 
 namespace {
 
@@ -28,7 +37,7 @@ void trace(int point, cudaStream_t s) {
 }
 
 constexpr int kMaxRows = 1 << 16;        // B*2K
-constexpr int kAttnTargetItems = 304;    // attention work items aimed for (2 per SM)
+constexpr int kAttnItemsPerSm = 8;       // attention work items aimed for, per SM (load balance)
 constexpr int kAttnMinChunk = 256;       // shortest position chunk of a work item
 constexpr int kTcSmemLimit = 232448;     // opt-in shared memory per block (227 KB)
 constexpr int kTcMaxStages = 12;
@@ -53,12 +62,19 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ----------------------------------------------------------------------------- GEMM plan
 
 struct GemmPlan {
-  int epi = 0, bn = 16, n_t = 1, n_f = 1, k_splits = 1, kb_total = 1, stages = 2;
+  int epi = 0, bn = 16, n_t = 1, n_f = 1, k_splits = 1, kb_total = 1, stages = 2, grid = 1;
+  int nbuf = 1, acc_stride = 16;
+  uint32_t tmem_cols = 32;
   uint32_t stage_bytes = 0;
   size_t smem = 0, partial_floats = 0;
   int tiles = 0;
 };
 
+// Work decomposition of one GEMM: 128 weight rows x bn token rows per tile.
+// With fewer tiles than SMs, split K so that every SM streams weights, while
+// keeping the fp32 partial traffic (4 * splits * bn bytes per weight row) at
+// most the bf16 weight traffic (2 * k_dim bytes per weight row), and at least
+// four 64-wide k blocks per split.  The persistent grid has one CTA per SM.
 GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   GemmPlan g;
   g.epi = epi;
@@ -69,18 +85,28 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   g.kb_total = (k_dim + kTcBK - 1) / kTcBK;
   g.tiles = g.n_f * g.n_t;
   g.stage_bytes = (paired ? 2u : 1u) * kTcBM * kTcBK * 2 + (uint32_t)g.bn * kTcBK * 2;
-  const long long avail = kTcSmemLimit - 1024 - kTcCtrlBytes - (long long)g.bn * 8;
+  const int red = epi == EPI_ARGMAX ? g.n_t * g.bn : 0;
+  const long long avail = kTcSmemLimit - 1024 - kTcCtrlBytes - (long long)red * 8;
   g.stages = (int)std::min<long long>(kTcMaxStages, avail / g.stage_bytes);
   if (epi != EPI_ARGMAX && g.tiles < sms) {
-    g.k_splits = std::max(1, std::min(g.kb_total / 4, sms / g.tiles));
+    const int by_sms = sms / g.tiles;
+    const int by_depth = std::max(1, g.kb_total / 4);
+    const int by_traffic = std::max(1, k_dim / (2 * g.bn));
+    g.k_splits = std::max(1, std::min(by_sms, std::min(by_depth, by_traffic)));
   }
-  g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, g.bn);
+  const int acc_cols = (paired ? 2 : 1) * g.bn;
+  g.nbuf = 2 * acc_cols <= 512 ? 2 : 1;
+  g.acc_stride = acc_cols;
+  const int need = g.nbuf * acc_cols;
+  g.tmem_cols = need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
+  g.grid = std::min(g.tiles * g.k_splits, sms);
+  g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, red);
   g.partial_floats = g.k_splits > 1 ? (size_t)g.k_splits * g.tiles * (paired ? 2 : 1) * kTcBM * g.bn : 0;
   return g;
 }
 
 struct Plan {
-  int R = 0, T = 0, S = 0, sms = 0, max_items = 0, attn_grid = 0;
+  int R = 0, T = 0, S = 0, sms = 0, max_items = 0, attn_grid = 0, attn_target = 0;
   GemmPlan fc, qkv, o, gu, down, lm;
   size_t max_partial = 0;
   int max_tiles = 0;
@@ -110,8 +136,13 @@ Plan make_plan(const pe_config& c) {
     p.max_partial = std::max(p.max_partial, g->partial_floats);
     p.max_tiles = std::max(p.max_tiles, g->tiles);
   }
-  p.max_items = kAttnTargetItems + c.B * c.n_kv;
-  p.attn_grid = std::min(p.max_items, 2 * p.sms);
+  // attention items: the work list aims at attn_target items; rounding adds at
+  // most one per (sequence, kv head), and no (sequence, kv head) can have more
+  // chunks than its longest possible range holds minimum chunks
+  p.attn_target = kAttnItemsPerSm * p.sms;
+  const long long per_pair = ((long long)c.max_pages_per_seq * c.page_size + kAttnMinChunk - 1) / kAttnMinChunk;
+  p.max_items = (int)std::min<long long>(p.attn_target + (long long)c.B * c.n_kv, per_pair * c.B * c.n_kv);
+  p.attn_grid = std::min(p.max_items, (c.head_dim == 64 ? 2 : 1) * p.sms);
 
   const size_t eb = elem_bytes(c.dtype);
   size_t off = 0;
@@ -228,6 +259,7 @@ pe_status check_cfg(const pe_config* c) {
   if (c->page_size != 16) return PE_ERR_UNSUPPORTED;
   if (c->head_dim != 64 && c->head_dim != 128) return PE_ERR_UNSUPPORTED;
   if ((long long)c->B * 2 * c->K > kMaxRows) return PE_ERR_SHAPE;
+  if (c->d > 16384) return PE_ERR_UNSUPPORTED;  // RMSNorm keeps a row in registers
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return PE_ERR_INVALID_ARG;
   const size_t eb = elem_bytes(c->dtype);
   if ((c->d * eb) % 16 != 0 || c->d % 4 != 0) return PE_ERR_UNSUPPORTED;  // bulk row copies, float4 norm
@@ -280,6 +312,12 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   a.k_splits = g.k_splits;
   a.stages = g.stages;
   a.stage_bytes = g.stage_bytes;
+  a.n_t = g.n_t;
+  a.n_f = g.n_f;
+  a.nbuf = g.nbuf;
+  a.acc_stride = g.acc_stride;
+  a.tmem_cols = g.tmem_cols;
+  a.n_tok_min = call.n_tok_dev != nullptr ? std::min(call.n_tok, c.B * c.K) : call.n_tok;
   a.partial = at<float>(ws, p.partial);
   a.counters = at<int32_t>(ws, p.counters);
   CUtensorMap tw, tx;
@@ -289,8 +327,7 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   else ok = tmap_matrix(&tw, call.W, call.w_rows, (uint64_t)call.k_dim, (uint32_t)kTcBM);
   ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)g.bn);
   if (!ok) return PE_ERR_CUDA;
-  const dim3 grid(g.n_t, g.n_f, g.k_splits);
-  PE_TRY_CUDA(launch_gemm_tc(call.epi, tw, tx, a, grid, g.smem, s));
+  PE_TRY_CUDA(launch_gemm_tc(call.epi, tw, tx, a, g.grid, g.smem, s));
   return PE_OK;
 }
 
@@ -333,7 +370,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   ia.tok_slot = at<int64_t>(ws, p.tok_slot);
   ia.seq_start = at<int32_t>(ws, p.seq_start); ia.seq_len = at<int32_t>(ws, p.seq_len);
   ia.seq_maxpos = at<int32_t>(ws, p.seq_maxpos);
-  ia.target_items = kAttnTargetItems; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
+  ia.target_items = p.attn_target; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
   ia.items = at<int4>(ws, p.items); ia.n_items = at<int32_t>(ws, p.n_items);
   ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
   ia.counters = at<int32_t>(ws, p.counters); ia.n_counters = p.max_tiles + 1;

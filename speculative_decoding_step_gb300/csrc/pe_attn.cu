@@ -66,14 +66,16 @@ PE_DEV uint32_t swz(uint32_t base, int row, int chunk) {
 
 constexpr int kAttnBlk = 64;      // kv positions per pipeline block
 constexpr int kAttnThreads = 256; // 8 warps x 16 query rows
+constexpr int kAttnStages = 3;    // cp.async ring depth (blocks in flight)
 
 template <int HD>
-__global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, HD == 64 ? 2 : 1) attn_bf16_kernel(const AttnArgs a) {
   constexpr int CH = HD / 8;  // 16-byte chunks per row
+  constexpr int S = kAttnStages;
   extern __shared__ __align__(128) uint8_t sm[];
   const uint32_t sQ = smem_u32(sm);
   const uint32_t sK = sQ + kAttnRows * HD * 2;
-  const uint32_t sV = sK + 2 * kAttnBlk * HD * 2;
+  const uint32_t sV = sK + S * kAttnBlk * HD * 2;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.n_q / a.n_kv;
   const float scale_log2 = a.scale * 1.4426950408889634f;
@@ -81,6 +83,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(const AttnArgs 
   const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(a.k_cache);
   const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(a.v_cache);
   const int ldq = a.n_q * HD;
+  pdl_wait();
+  pdl_trigger();
   const int n_items = *a.n_items;
 
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -111,6 +115,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(const AttnArgs 
         const int pos = kb0 + r;
         bool valid = pos < c1;
         const __nv_bfloat16* src = kc;
+        if (valid && pos / a.page_size >= a.max_pages) {
+          set_err(a.err, PE_DEV_BAD_POSITION);
+          valid = false;
+        }
         if (valid) {
           const int page = a.block_table[(size_t)b * a.max_pages + pos / a.page_size];
           if (page < 0 || page >= a.num_pages) {
@@ -124,11 +132,13 @@ __global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(const AttnArgs 
         const uint32_t base = (which == 0 ? sK : sV) + (uint32_t)(buf * kAttnBlk * HD * 2);
         cp_async16(swz<HD>(base, r, ch), src, valid);
       }
-      cp_async_commit();
     };
 
     const int nblk = (c1 - c0 + kAttnBlk - 1) / kAttnBlk;
-    load_block(0, 0);
+    for (int st = 0; st < S - 1; ++st) {  // prologue: S-1 blocks in flight (empty groups keep the count)
+      if (st < nblk) load_block(st, st);
+      cp_async_commit();
+    }
     __syncthreads();  // query tile visible
 
     // ---- per-warp state: rows 16*warp + lane/4 and +8
@@ -151,14 +161,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(const AttnArgs 
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
     for (int blk = 0; blk < nblk; ++blk) {
-      const int buf = blk & 1;
-      if (blk + 1 < nblk) {
-        load_block(blk + 1, buf ^ 1);
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
-      }
-      __syncthreads();
+      const int buf = blk % S;
+      cp_async_wait<S - 2>();  // block blk has landed
+      __syncthreads();         // ... for every thread; and block blk-1's stage is free again
+      if (blk + S - 1 < nblk) load_block(blk + S - 1, (blk + S - 1) % S);
+      cp_async_commit();
       if (active) {
         const uint32_t kbase = sK + (uint32_t)(buf * kAttnBlk * HD * 2);
         const uint32_t vbase = sV + (uint32_t)(buf * kAttnBlk * HD * 2);
@@ -237,8 +244,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(const AttnArgs 
           }
         }
       }
-      __syncthreads();  // buffer free for the next prefetch
     }
+    cp_async_wait<0>();
 
     // ---- partials: row max (log2 domain), row sum, unnormalised output
     if (active) {
@@ -266,6 +273,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(const AttnArgs 
 // Merge the chunks of every (row, query head), in chunk order.
 template <int HD>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int n = min(*a.n_valid, a.n_rows);
   const int t = gw / a.n_q, h = gw - (gw / a.n_q) * a.n_q;
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
 
 template <int HD>
 static size_t attn_smem() {
-  return (size_t)kAttnRows * HD * 2 + 4 * (size_t)kAttnBlk * HD * 2;
+  return (size_t)kAttnRows * HD * 2 + 2 * (size_t)kAttnStages * kAttnBlk * HD * 2;
 }
 
 cudaError_t launch_attention_bf16(const AttnArgs& a, int grid, cudaStream_t s) {
@@ -313,7 +322,7 @@ cudaError_t launch_attention_bf16(const AttnArgs& a, int grid, cudaStream_t s) {
       if (e != cudaSuccess) return e;
       cfg = true;
     }
-    attn_bf16_kernel<64><<<grid, kAttnThreads, attn_smem<64>(), s>>>(a);
+    return launch_pdl(attn_bf16_kernel<64>, dim3(grid), dim3(kAttnThreads), attn_smem<64>(), s, a);
   } else if (a.head_dim == 128) {
     static bool cfg = false;
     if (!cfg) {
@@ -322,29 +331,26 @@ cudaError_t launch_attention_bf16(const AttnArgs& a, int grid, cudaStream_t s) {
       if (e != cudaSuccess) return e;
       cfg = true;
     }
-    attn_bf16_kernel<128><<<grid, kAttnThreads, attn_smem<128>(), s>>>(a);
-  } else {
-    return cudaErrorInvalidValue;
+    return launch_pdl(attn_bf16_kernel<128>, dim3(grid), dim3(kAttnThreads), attn_smem<128>(), s, a);
   }
-  count_launch();
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attention_combine_bf16(const AttnArgs& a, cudaStream_t s) {
   const long long warps = (long long)a.n_rows * a.n_q;
   const int grid = (int)((warps * 32 + 255) / 256);
   if (grid == 0) return cudaSuccess;
-  if (a.head_dim == 64) attn_combine_kernel<64><<<grid, 256, 0, s>>>(a);
-  else if (a.head_dim == 128) attn_combine_kernel<128><<<grid, 256, 0, s>>>(a);
-  else return cudaErrorInvalidValue;
-  count_launch();
-  return cudaGetLastError();
+  if (a.head_dim == 64) return launch_pdl(attn_combine_kernel<64>, dim3(grid), dim3(256), 0, s, a);
+  if (a.head_dim == 128) return launch_pdl(attn_combine_kernel<128>, dim3(grid), dim3(256), 0, s, a);
+  return cudaErrorInvalidValue;
 }
 
 // ============================================================================= fp32
 
 template <int HD>
 __global__ void __launch_bounds__(256) attn_f32_kernel(const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int n = min(*a.n_valid, a.n_rows);
   const int t = gw / a.n_q, h = gw - (gw / a.n_q) * a.n_q;
@@ -399,11 +405,9 @@ cudaError_t launch_attention_f32(const AttnArgs& a, cudaStream_t s) {
   const long long warps = (long long)a.n_rows * a.n_q;
   const int grid = (int)((warps * 32 + 255) / 256);
   if (grid == 0) return cudaSuccess;
-  if (a.head_dim == 64) attn_f32_kernel<64><<<grid, 256, 0, s>>>(a);
-  else if (a.head_dim == 128) attn_f32_kernel<128><<<grid, 256, 0, s>>>(a);
-  else return cudaErrorInvalidValue;
-  count_launch();
-  return cudaGetLastError();
+  if (a.head_dim == 64) return launch_pdl(attn_f32_kernel<64>, dim3(grid), dim3(256), 0, s, a);
+  if (a.head_dim == 128) return launch_pdl(attn_f32_kernel<128>, dim3(grid), dim3(256), 0, s, a);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pe

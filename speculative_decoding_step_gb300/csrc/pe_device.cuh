@@ -195,6 +195,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// ----------------------------------------------------------------------------- programmatic dependent launch
+// Kernels are launched so that the next kernel of the round may start while
+// this one drains: pdl_trigger() lets the dependent grid launch, pdl_wait()
+// blocks until every earlier grid of the stream has completed and its memory
+// is visible.  Every read of an earlier kernel's output comes after pdl_wait().
+// Both are no-ops for kernels launched without the attribute.
+
+PE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+PE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------------------- misc
 
 // 64-bit key whose unsigned maximum is the largest value, ties going to the

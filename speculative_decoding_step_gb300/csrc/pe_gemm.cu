@@ -83,9 +83,93 @@ PE_DEV void argmax_finish(const GemmArgs& a, int n_tok, int thread, int nthreads
 PE_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 // ============================================================================= tensor-core kernel
+//
+// Persistent: CTA b processes work units b, b + grid, b + 2*grid, ...; a unit is
+// (token tile, weight tile, k split).  Roles: warp 0 lane 0 issues TMA loads
+// into a ring of `stages` shared-memory stages (continuously across units),
+// warp 1 lane 0 issues tcgen05.mma into one of `nbuf` TMEM accumulators, warps
+// 2..5 run the epilogue of unit i while the MMAs of unit i+1 fill the other
+// accumulator.  Before waiting on the previous kernel (pdl_wait) the producer
+// already streams the weights of its first unit: they never depend on it.
 
-size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int bn) {
-  return 1024 /*alignment slack*/ + (size_t)stages * stage_bytes + kTcCtrlBytes + (size_t)bn * 8;
+size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int red_entries) {
+  return 1024 /*alignment slack*/ + (size_t)stages * stage_bytes + kTcCtrlBytes + (size_t)red_entries * 8;
+}
+
+// Token rows of this launch: the device count, never below the rows every
+// valid batch has (B*K), so that units whose weights were prefetched before
+// pdl_wait() are always processed.  Rows between the two hold stale data;
+// their outputs land in scratch rows and their KV slot is -1.
+PE_DEV int effective_ntok(const GemmArgs& a) {
+  int n = a.n_tok;
+  if (a.n_tok_dev != nullptr) {
+    const int d = *a.n_tok_dev;
+    if (d < a.n_tok_min) set_err(a.err, PE_DEV_BAD_ROW);
+    n = min(n, max(d, a.n_tok_min));
+  }
+  return n;
+}
+
+struct Unit {
+  int tile_t, tile_f, split, kb0, kb1;
+};
+
+PE_DEV Unit decode_unit(const GemmArgs& a, int u) {
+  Unit w;
+  w.tile_t = u % a.n_t;
+  const int r = u / a.n_t;
+  w.split = r % a.k_splits;
+  w.tile_f = r / a.k_splits;
+  w.kb0 = (int)((long long)w.split * a.kb_total / a.k_splits);
+  w.kb1 = (int)((long long)(w.split + 1) * a.kb_total / a.k_splits);
+  return w;
+}
+
+template <int EPI>
+PE_DEV void issue_w(const CUtensorMap* tmW, const GemmArgs& a, uint32_t sa, uint32_t fb, int kx, int tile_f,
+                    uint64_t pol) {
+  constexpr uint32_t A_BYTES = kTcBM * kTcBK * 2;
+  if (EPI == EPI_SWIGLU) {  // W viewed as [2][F][d]: gate rows, then up rows
+    tma_load_3d(sa, tmW, fb, kx, tile_f * kTcBM, 0, pol);
+    tma_load_3d(sa + A_BYTES, tmW, fb, kx, tile_f * kTcBM, 1, pol);
+  } else if (EPI == EPI_QKV_ROPE) {  // W viewed as [heads][2][hd/2][d]: first / second halves
+    const int hpt = kTcBM / (a.head_dim >> 1);
+    tma_load_4d(sa, tmW, fb, kx, 0, 0, tile_f * hpt, pol);
+    tma_load_4d(sa + A_BYTES, tmW, fb, kx, 0, 1, tile_f * hpt, pol);
+  } else {
+    tma_load_2d(sa, tmW, fb, kx, tile_f * kTcBM, pol);
+  }
+}
+
+template <int EPI>
+PE_DEV void apply16(const GemmArgs& a, int unit, int t0, int n_tok, const float (&v)[16], const float (&v2)[16],
+                    float inv_freq) {
+  if (unit >= a.n_out) return;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (t0 + j < n_tok) epi_elem<EPI, __nv_bfloat16>(a, unit, t0 + j, v[j], v2[j], inv_freq);
+}
+
+// Warp-level (max, argmax) of 16 token columns over the 32 rows the warp holds;
+// lane 0 folds the result into the CTA's running keys.
+PE_DEV void argmax16(const GemmArgs& a, int unit, int t0, int n_tok, const float (&v)[16],
+                     unsigned long long* red_col, int lane) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int t = t0 + j;
+    unsigned long long key = 0ull;
+    if (unit < a.n_out && t < n_tok) {
+      if (!isfinite(v[j])) set_err(a.err, PE_DEV_NONFINITE);
+      key = argmax_key(v[j], (uint32_t)unit);
+      if (a.logits_dbg != nullptr) a.logits_dbg[(size_t)t * a.n_out + unit] = v[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, key, o);
+      key = other > key ? other : key;
+    }
+    if (lane == 0 && key != 0ull) atomicMax(red_col + j, key);
+  }
 }
 
 template <int EPI>
@@ -98,214 +182,247 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_t = blockIdx.x, tile_f = blockIdx.y, split = blockIdx.z;
   const int BN = a.bn;
-  int n_tok = a.n_tok;
-  if (a.n_tok_dev != nullptr) n_tok = min(n_tok, *a.n_tok_dev);
-  // token tile entirely past the valid rows: uniform exit (the LM head has a host-known token count and
-  // every CTA must reach its completion counter, so it never takes this exit)
-  if (EPI != EPI_ARGMAX && tile_t * BN >= n_tok) return;
-
-  uint8_t* ctrl = smem + (size_t)a.stages * a.stage_bytes;
+  const int U = a.n_t * a.n_f * a.k_splits;
+  const int S = a.stages;
+  uint8_t* ctrl = smem + (size_t)S * a.stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* empty = full + a.stages;
-  uint64_t* accf = empty + a.stages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
   unsigned long long* red = reinterpret_cast<unsigned long long*>(ctrl + kTcCtrlBytes);
-
-  const int kb0 = (int)((long long)split * a.kb_total / a.k_splits);
-  const int kb1 = (int)((long long)(split + 1) * a.kb_total / a.k_splits);
-  const int nkb = kb1 - kb0;
-  const int acc_cols = PAIRED ? 2 * BN : BN;
-  const uint32_t tmem_cols = acc_cols <= 32 ? 32u : acc_cols <= 64 ? 64u : acc_cols <= 128 ? 128u
-                                                 : acc_cols <= 256 ? 256u : 512u;
   const uint32_t b_off = (PAIRED ? 2u : 1u) * A_BYTES;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
-    for (int s = 0; s < a.stages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), 1);
     }
-    mbar_init(smem_u32(accf), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(tfull + b), 1);
+      mbar_init(smem_u32(tempty + b), 4);  // one arrival per epilogue warp
+    }
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbar_init();
   }
   if (EPI == EPI_ARGMAX)
-    for (int j = threadIdx.x; j < BN; j += blockDim.x) red[j] = 0ull;
+    for (int j = threadIdx.x; j < a.n_t * BN; j += blockDim.x) red[j] = 0ull;
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), tmem_cols);
+    tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
     tmem_relinquish();
     tc_fence_before();
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();  // weights: read once
       const uint64_t pol_x = l2_policy_evict_last();   // activations: re-read by every weight tile
-      int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % a.stages;
-        const uint32_t use = (uint32_t)(i / a.stages);
-        if (i >= a.stages && !mbar_wait(smem_u32(empty + s), (use & 1u) ^ 1u, a.err, abort_flag)) break;
-        const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
-        const uint32_t fb = smem_u32(full + s);
-        mbar_expect_tx(fb, a.stage_bytes);
-        const int kx = (kb0 + i) * kTcBK;
-        if (EPI == EPI_SWIGLU) {           // W viewed as [2][F][d]: gate rows, then up rows
-          tma_load_3d(sa, &tmW, fb, kx, tile_f * kTcBM, 0, pol_w);
-          tma_load_3d(sa + A_BYTES, &tmW, fb, kx, tile_f * kTcBM, 1, pol_w);
-        } else if (EPI == EPI_QKV_ROPE) {  // W viewed as [heads][2][hd/2][d]: first / second halves
-          const int hpt = kTcBM / (a.head_dim >> 1);
-          tma_load_4d(sa, &tmW, fb, kx, 0, 0, tile_f * hpt, pol_w);
-          tma_load_4d(sa + A_BYTES, &tmW, fb, kx, 0, 1, tile_f * hpt, pol_w);
-        } else {
-          tma_load_2d(sa, &tmW, fb, kx, tile_f * kTcBM, pol_w);
+      // the weights of the first unit do not depend on earlier kernels: start them now
+      int npre = 0;
+      if ((int)blockIdx.x < U) {
+        const Unit w = decode_unit(a, blockIdx.x);
+        if (w.tile_t * BN < a.n_tok_min) {
+          npre = min(S, w.kb1 - w.kb0);
+          for (int i = 0; i < npre; ++i) {
+            const uint32_t sa = smem_u32(smem + (size_t)i * a.stage_bytes);
+            mbar_expect_tx(smem_u32(full + i), a.stage_bytes);
+            issue_w<EPI>(&tmW, a, sa, smem_u32(full + i), (w.kb0 + i) * kTcBK, w.tile_f, pol_w);
+          }
         }
-        tma_load_2d(sa + b_off, &tmX, fb, kx, tile_t * BN, pol_x);
-        issued = i + 1;
       }
-      if (*abort_flag) {
-        // do not leave bulk copies in flight into this CTA's shared memory
-        const int lo = issued > a.stages ? issued - a.stages : 0;
-        for (int i = lo; i < issued; ++i)
-          mbar_wait(smem_u32(full + (i % a.stages)), (uint32_t)(i / a.stages) & 1u, a.err, nullptr);
+      pdl_wait();
+      const int n_tok = effective_ntok(a);
+      int it = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < U && !stop; u += gridDim.x) {
+        const Unit w = decode_unit(a, u);
+        if (EPI != EPI_ARGMAX && w.tile_t * BN >= n_tok) continue;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t use = (uint32_t)(it / S);
+          const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
+          const uint32_t fb = smem_u32(full + s);
+          if (it >= npre) {
+            if (it >= S && !mbar_wait(smem_u32(empty + s), (use & 1u) ^ 1u, a.err, abort_flag)) {
+              stop = true;
+              break;
+            }
+            mbar_expect_tx(fb, a.stage_bytes);
+            issue_w<EPI>(&tmW, a, sa, fb, kb * kTcBK, w.tile_f, pol_w);
+          }
+          tma_load_2d(sa + b_off, &tmX, fb, kb * kTcBK, w.tile_t * BN, pol_x);
+        }
+      }
+      if (stop || *abort_flag) {
+        // leave no bulk copy in flight into this CTA's shared memory
+        const int lo = it > S ? it - S : 0;
+        for (int i = lo; i < it; ++i)
+          mbar_wait(smem_u32(full + (i % S)), (uint32_t)(i / S) & 1u, a.err, nullptr);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      pdl_wait();
+      const int n_tok = effective_ntok(a);
       const uint32_t idesc = idesc_bf16(kTcBM, BN);
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % a.stages;
-        const uint32_t use = (uint32_t)(i / a.stages);
-        if (!mbar_wait(smem_u32(full + s), use & 1u, a.err, abort_flag)) break;
+      int it = 0, i = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < U && !stop; u += gridDim.x) {
+        const Unit w = decode_unit(a, u);
+        if (EPI != EPI_ARGMAX && w.tile_t * BN >= n_tok) continue;
+        const int buf = i % a.nbuf;
+        if (i >= a.nbuf &&
+            !mbar_wait(smem_u32(tempty + buf), (uint32_t)((i / a.nbuf) - 1) & 1u, a.err, abort_flag))
+          break;
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
-        const uint64_t da = sdesc_k_sw128(sa);
-        const uint64_t da2 = sdesc_k_sw128(sa + A_BYTES);
-        const uint64_t db = sdesc_k_sw128(sa + b_off);
+        const uint32_t d = tmem + (uint32_t)(buf * a.acc_stride);
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t use = (uint32_t)(it / S);
+          if (!mbar_wait(smem_u32(full + s), use & 1u, a.err, abort_flag)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
+          const uint64_t da = sdesc_k_sw128(sa);
+          const uint64_t da2 = sdesc_k_sw128(sa + A_BYTES);
+          const uint64_t db = sdesc_k_sw128(sa + b_off);
 #pragma unroll
-        for (int kk = 0; kk < kTcBK / 16; ++kk) {
-          const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, accum);
-          if (PAIRED) tc_mma_bf16(tmem + (uint32_t)BN, da2 + 2 * kk, db + 2 * kk, idesc, accum);
+          for (int kk = 0; kk < kTcBK / 16; ++kk) {
+            const uint32_t accum = (kb > w.kb0 || kk > 0) ? 1u : 0u;
+            tc_mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accum);
+            if (PAIRED) tc_mma_bf16(d + (uint32_t)BN, da2 + 2 * kk, db + 2 * kk, idesc, accum);
+          }
+          tc_commit(smem_u32(empty + s));
         }
-        tc_commit(smem_u32(empty + s));
+        tc_commit(smem_u32(tfull + buf));
+        ++i;
       }
-      tc_commit(smem_u32(accf));
     }
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2..5)
-    const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;            // row of the tile = TMEM lane
-    const int unit = tile_f * kTcBM + r;
-    const int ethread = threadIdx.x - 64;   // 0..127
-    const bool ok = mbar_wait(smem_u32(accf), 0u, a.err, abort_flag);
-    tc_fence_after();
-    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-    const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
+    pdl_wait();
+    const int n_tok = effective_ntok(a);
+    const int q = warp & 3;                // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;           // row of the tile = TMEM lane
+    const int ethread = threadIdx.x - 64;  // 0..127
     const int rows_per = PAIRED ? 2 * kTcBM : kTcBM;
     const size_t tile_elems = (size_t)rows_per * BN;
-    const size_t tile_index = (size_t)tile_f * gridDim.x + tile_t;
-
-    bool do_epilogue = ok;
-    if (ok && a.k_splits > 1) {
-      float* P = a.partial + ((size_t)split * gridDim.y * gridDim.x + tile_index) * tile_elems;
-      for (int c = 0; c < BN / 16; ++c) {
-        float v[16];
-        tmem_load16(tl + (uint32_t)(c * 16), v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) P[(size_t)(c * 16 + j) * rows_per + r] = v[j];
-        if (PAIRED) {
-          tmem_load16(tl + (uint32_t)(BN + c * 16), v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) P[(size_t)(c * 16 + j) * rows_per + kTcBM + r] = v[j];
-        }
-      }
-      __threadfence();
-      named_bar_sync(1, 128);
-      if (ethread == 0) {
-        const int old = atomicAdd(a.counters + tile_index, 1);
-        *last_flag = (old == a.k_splits - 1) ? 1 : 0;
-      }
-      named_bar_sync(1, 128);
-      do_epilogue = *last_flag != 0;
-      if (do_epilogue) __threadfence();
-    }
-
-    if (do_epilogue) {
-      const size_t split_stride = (size_t)gridDim.y * gridDim.x * tile_elems;
-      const float* P0 = a.partial + tile_index * tile_elems;
-      for (int c = 0; c < BN / 16; ++c) {
-        float v[16], v2[16];
-        if (a.k_splits == 1) {
+    const size_t n_tiles = (size_t)a.n_f * a.n_t;
+    int i = 0;
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+      const Unit w = decode_unit(a, u);
+      if (EPI != EPI_ARGMAX && w.tile_t * BN >= n_tok) continue;
+      const int buf = i % a.nbuf;
+      const bool ok = mbar_wait(smem_u32(tfull + buf), (uint32_t)(i / a.nbuf) & 1u, a.err, abort_flag);
+      tc_fence_after();
+      const int unit = w.tile_f * kTcBM + r;
+      const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
+      const uint32_t tl = tmem + (uint32_t)(buf * a.acc_stride) + ((uint32_t)(q * 32) << 16);
+      const int tbase = w.tile_t * BN;
+      const size_t tile = (size_t)w.tile_f * a.n_t + w.tile_t;
+      if (ok && a.k_splits == 1) {
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16], v2[16];
           tmem_load16(tl + (uint32_t)(c * 16), v);
           if (PAIRED) tmem_load16(tl + (uint32_t)(BN + c * 16), v2);
-        } else {
+          if (EPI == EPI_ARGMAX)
+            argmax16(a, unit, tbase + c * 16, n_tok, v, red + w.tile_t * BN + c * 16, lane);
+          else
+            apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, inv_freq);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(tempty + buf));
+      } else if (ok) {
+        // split K: this split's partial sums, [row][token] fp32, then count arrivals
+        float* P = a.partial + ((size_t)w.split * n_tiles + tile) * tile_elems;
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16];
+          tmem_load16(tl + (uint32_t)(c * 16), v);
+          float4* dst = reinterpret_cast<float4*>(P + (size_t)r * BN + c * 16);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float s1 = 0.f, s2 = 0.f;
+          for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          if (PAIRED) {
+            tmem_load16(tl + (uint32_t)(BN + c * 16), v);
+            float4* dst2 = reinterpret_cast<float4*>(P + (size_t)(kTcBM + r) * BN + c * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst2[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(tempty + buf));  // accumulator free for the next unit
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (ethread == 0) {
+          const int old = atomicAdd(a.counters + tile, 1);
+          *last_flag = (old == a.k_splits - 1) ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        const bool last = *last_flag != 0;
+        named_bar_sync(1, 128);  // every thread has read the flag before a later unit rewrites it
+        if (last) {
+          // last split of this tile: sum the partials in split order, then the epilogue
+          __threadfence();
+          const float* P0 = a.partial + tile * tile_elems;
+          const size_t sstride = n_tiles * tile_elems;
+          for (int c8 = 0; c8 < BN; c8 += 8) {
+            float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0, g0 = s0, g1 = s0;
             for (int sp = 0; sp < a.k_splits; ++sp) {
-              const float* P = P0 + sp * split_stride + (size_t)(c * 16 + j) * rows_per;
-              s1 += __ldcg(P + r);
-              if (PAIRED) s2 += __ldcg(P + kTcBM + r);
+              const float4* src = reinterpret_cast<const float4*>(P0 + sp * sstride + (size_t)r * BN + c8);
+              const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+              s0.x += x0.x; s0.y += x0.y; s0.z += x0.z; s0.w += x0.w;
+              s1.x += x1.x; s1.y += x1.y; s1.z += x1.z; s1.w += x1.w;
+              if (PAIRED) {
+                const float4* src2 =
+                    reinterpret_cast<const float4*>(P0 + sp * sstride + (size_t)(kTcBM + r) * BN + c8);
+                const float4 y0 = __ldcg(src2), y1 = __ldcg(src2 + 1);
+                g0.x += y0.x; g0.y += y0.y; g0.z += y0.z; g0.w += y0.w;
+                g1.x += y1.x; g1.y += y1.y; g1.z += y1.z; g1.w += y1.w;
+              }
             }
-            v[j] = s1;
-            v2[j] = s2;
+            if (unit < a.n_out) {
+              const float vv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+              const float ww[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int t = tbase + c8 + j;
+                if (t < n_tok) epi_elem<EPI, __nv_bfloat16>(a, unit, t, vv[j], ww[j], inv_freq);
+              }
+            }
           }
+          if (ethread == 0) a.counters[tile] = 0;  // ready for the next launch
         }
-        if (EPI == EPI_ARGMAX) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = tile_t * BN + c * 16 + j;
-            unsigned long long key = 0ull;
-            if (unit < a.n_out && t < n_tok) {
-              if (!isfinite(v[j])) set_err(a.err, PE_DEV_NONFINITE);
-              key = argmax_key(v[j], (uint32_t)unit);
-              if (a.logits_dbg != nullptr) a.logits_dbg[(size_t)t * a.n_out + unit] = v[j];
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, key, o);
-              key = other > key ? other : key;
-            }
-            if (lane == 0 && key != 0ull) atomicMax(red + c * 16 + j, key);
-          }
-        } else {
-          if (unit < a.n_out) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int t = tile_t * BN + c * 16 + j;
-              if (t < n_tok) epi_elem<EPI, __nv_bfloat16>(a, unit, t, v[j], v2[j], inv_freq);
-            }
-          }
-        }
+      } else {
+        // a wait gave up: release the accumulator so the MMA role can unwind too
+        if (lane == 0) mbar_arrive(smem_u32(tempty + buf));
       }
-      if (a.k_splits > 1 && ethread == 0) a.counters[tile_index] = 0;  // ready for the next launch
+      ++i;
     }
-
     if (EPI == EPI_ARGMAX) {
       named_bar_sync(1, 128);
-      if (do_epilogue)
-        for (int j = ethread; j < BN; j += 128) {
-          const int t = tile_t * BN + j;
-          if (t < n_tok && red[j] != 0ull) atomicMax(a.keys + t, red[j]);
-        }
+      for (int j = ethread; j < a.n_t * BN; j += 128)  // key index = token = tile_t * BN + column
+        if (j < n_tok && red[j] != 0ull) atomicMax(a.keys + j, red[j]);
       __threadfence();
       named_bar_sync(1, 128);
       if (ethread == 0) {
-        const int total = gridDim.x * gridDim.y * gridDim.z;
         const int old = atomicAdd(a.done_counter, 1);
-        *last_flag = (old == total - 1) ? 1 : 0;
+        *last_flag = (old == (int)gridDim.x - 1) ? 1 : 0;
       }
       named_bar_sync(1, 128);
       if (*last_flag) {
@@ -319,12 +436,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, tmem_cols);
+    tmem_dealloc(tmem, a.tmem_cols);
   }
 }
 
 template <int EPI>
-static cudaError_t launch_tc_typed(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, dim3 grid,
+static cudaError_t launch_tc_typed(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
                                    size_t smem, cudaStream_t s) {
   static size_t configured = 0;
   if (smem > configured) {
@@ -332,12 +449,10 @@ static cudaError_t launch_tc_typed(const CUtensorMap& tmW, const CUtensorMap& tm
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  gemm_tc_kernel<EPI><<<grid, kTcThreads, smem, s>>>(tmW, tmX, a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), smem, s, tmW, tmX, a);
 }
 
-cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, dim3 grid,
+cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
                            size_t smem, cudaStream_t s) {
   switch (epi) {
     case EPI_STORE_F32: return launch_tc_typed<EPI_STORE_F32>(tmW, tmX, a, grid, smem, s);
@@ -361,6 +476,8 @@ template <int EPI>
 __global__ void __launch_bounds__(kF32Warps * 32) gemm_f32_kernel(const GemmArgs a) {
   constexpr bool PAIRED = (EPI == EPI_SWIGLU || EPI == EPI_QKV_ROPE);
   __shared__ int last_s;
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x * kF32Warps + warp;
   int n_tok = a.n_tok;
@@ -432,15 +549,13 @@ cudaError_t launch_gemm_f32(int epi, const GemmArgs& a, cudaStream_t s) {
   const int grid = (a.n_out + kF32Warps - 1) / kF32Warps;
   const int threads = kF32Warps * 32;
   switch (epi) {
-    case EPI_STORE_F32: gemm_f32_kernel<EPI_STORE_F32><<<grid, threads, 0, s>>>(a); break;
-    case EPI_ADD_F32: gemm_f32_kernel<EPI_ADD_F32><<<grid, threads, 0, s>>>(a); break;
-    case EPI_SWIGLU: gemm_f32_kernel<EPI_SWIGLU><<<grid, threads, 0, s>>>(a); break;
-    case EPI_QKV_ROPE: gemm_f32_kernel<EPI_QKV_ROPE><<<grid, threads, 0, s>>>(a); break;
-    case EPI_ARGMAX: gemm_f32_kernel<EPI_ARGMAX><<<grid, threads, 0, s>>>(a); break;
-    default: return cudaErrorInvalidValue;
+    case EPI_STORE_F32: return launch_pdl(gemm_f32_kernel<EPI_STORE_F32>, dim3(grid), dim3(threads), 0, s, a);
+    case EPI_ADD_F32: return launch_pdl(gemm_f32_kernel<EPI_ADD_F32>, dim3(grid), dim3(threads), 0, s, a);
+    case EPI_SWIGLU: return launch_pdl(gemm_f32_kernel<EPI_SWIGLU>, dim3(grid), dim3(threads), 0, s, a);
+    case EPI_QKV_ROPE: return launch_pdl(gemm_f32_kernel<EPI_QKV_ROPE>, dim3(grid), dim3(threads), 0, s, a);
+    case EPI_ARGMAX: return launch_pdl(gemm_f32_kernel<EPI_ARGMAX>, dim3(grid), dim3(threads), 0, s, a);
   }
-  count_launch();
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pe

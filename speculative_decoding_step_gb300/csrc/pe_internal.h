@@ -14,6 +14,28 @@ namespace pe {
 // Counts every kernel launch of the library (reported by pe_kernel_launches).
 void count_launch(int n = 1);
 
+// Programmatic dependent launch on (default on; PE_PDL=0 in the environment turns it off).
+bool pdl_enabled();
+
+// Launch with the programmatic-stream-serialization attribute so the kernel's
+// prologue may overlap the previous kernel's tail (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ----------------------------------------------------------------------------- batch metadata
 
 struct PrepArgs {
@@ -99,8 +121,13 @@ struct GemmArgs {
   const int32_t* n_tok_dev;  // actual token rows (nullable)
   // tensor-core tiling (ignored by the fp32 kernel)
   int bn;                // token columns per tile (MMA N)
+  int n_t, n_f;          // token tiles, weight tiles; work units = n_t * n_f * k_splits
+  int n_tok_min;         // token rows that certainly exist (every tile below it is computed)
   int kb_total, k_splits, stages;
   uint32_t stage_bytes;
+  int nbuf;              // TMEM accumulator buffers (2: epilogue overlaps the next unit's MMAs)
+  int acc_stride;        // TMEM columns per accumulator buffer
+  uint32_t tmem_cols;    // TMEM columns allocated (power of two >= 32)
   float* partial;        // split-K partial sums
   int32_t* counters;     // split-K arrival counters per output tile (zero between launches)
   // fp32 kernel operands
@@ -124,7 +151,8 @@ struct GemmArgs {
 };
 
 // Tensor-core GEMM (tcgen05 + TMA): D[f][t] = W[f][:] . X[t][:], weights on the MMA M side.
-cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, dim3 grid,
+// Persistent: `grid` CTAs (at most one per SM) stride over the work units.
+cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
                            size_t smem_bytes, cudaStream_t s);
 // fp32 CUDA-core GEMM for fp32 configurations (same epilogues).
 cudaError_t launch_gemm_f32(int epi, const GemmArgs& a, cudaStream_t s);
@@ -133,7 +161,8 @@ constexpr int kTcThreads = 192;        // warp 0: TMA, warp 1: MMA, warps 2-5: e
 constexpr int kTcBM = 128;             // weight rows per tile
 constexpr int kTcBK = 64;              // k per pipeline stage (one 128-byte swizzle row)
 constexpr int kTcCtrlBytes = 1024;     // barriers + TMEM slot + flags
-size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int bn);
+// dynamic shared memory: alignment slack + stage ring + control block + argmax keys (n_t * bn)
+size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int red_entries);
 
 // ----------------------------------------------------------------------------- attention
 

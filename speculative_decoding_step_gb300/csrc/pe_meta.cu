@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kPrepThreads) prepare_kernel(const PrepArgs a)
   __shared__ int warp_off[32];
   __shared__ int carry_s;
   __shared__ int chunk_total_s;
+  pdl_wait();
+  pdl_trigger();
   const int S = 2 * a.K, R = a.B * S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   if (tid == 0) carry_s = 0;
@@ -119,9 +121,7 @@ __global__ void __launch_bounds__(kPrepThreads) prepare_kernel(const PrepArgs a)
 cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s) {
   const int R = a.B * 2 * a.K;
   const int threads = R >= kPrepThreads ? kPrepThreads : ((R + 31) / 32) * 32;
-  prepare_kernel<<<1, threads, 0, s>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(prepare_kernel, dim3(1), dim3(threads), 0, s, a);
 }
 
 // ============================================================================= stage (e)
@@ -131,6 +131,8 @@ cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s) {
 // then take the target's token at the first mismatch as the bonus token.
 
 __global__ void verify_kernel(const VerifyArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= a.B) return;
   const int32_t* d = a.draft + (size_t)b * a.K;
@@ -154,9 +156,7 @@ __global__ void verify_kernel(const VerifyArgs a) {
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   const int threads = 128;
-  verify_kernel<<<(a.B + threads - 1) / threads, threads, 0, s>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(verify_kernel, dim3((a.B + threads - 1) / threads), dim3(threads), 0, s, a);
 }
 
 // ============================================================================= forward prologue
@@ -164,6 +164,8 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
 constexpr int kInitThreads = 1024;
 
 __global__ void __launch_bounds__(kInitThreads) forward_init_kernel(const InitArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x;
   int n = *a.n_valid;
   if (n < 0 || n > a.R) {
@@ -247,9 +249,7 @@ __global__ void __launch_bounds__(kInitThreads) forward_init_kernel(const InitAr
 }
 
 cudaError_t launch_forward_init(const InitArgs& a, cudaStream_t s) {
-  forward_init_kernel<<<1, kInitThreads, 0, s>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(forward_init_kernel, dim3(1), dim3(kInitThreads), 0, s, a);
 }
 
 // ============================================================================= stage (b)
@@ -265,6 +265,8 @@ constexpr int kScatterRowsPerCta = 4;
 __global__ void __launch_bounds__(32) scatter_kernel(const ScatterArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x != 0) return;
   int n = *a.n_valid;
   n = n < 0 ? 0 : (n > a.R ? a.R : n);
@@ -338,63 +340,97 @@ cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
     configured = true;
   }
   const int grid = (a.R + kScatterRowsPerCta - 1) / kScatterRowsPerCta;
-  scatter_kernel<<<grid, 32, smem, s>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(scatter_kernel, dim3(grid), dim3(32), smem, s, a);
 }
 
 // ============================================================================= RMSNorm
-// y = x / sqrt(mean(x^2) + eps) * g, one warp per row, fp32 math, fixed
-// reduction order (per-lane partial sums, then a butterfly).
+// y = x / sqrt(mean(x^2) + eps) * g.  One CTA per row; the row stays in
+// registers between the sum of squares and the scaling; the sum runs in a
+// fixed order (per-thread partials, warp butterflies, then warp totals in
+// warp order), so the result does not depend on scheduling.
 
-template <typename OutT, typename GT>
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const NormArgs a) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+constexpr int kNormThreads = 256;
+
+template <typename OutT>
+PE_DEV void store4(OutT* y, float a, float b, float c, float d);
+template <>
+PE_DEV void store4<float>(float* y, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(y) = make_float4(a, b, c, d);
+}
+template <>
+PE_DEV void store4<__nv_bfloat16>(__nv_bfloat16* y, float a, float b, float c, float d) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  uint2 v;
+  v.x = *reinterpret_cast<uint32_t*>(&lo);
+  v.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(y) = v;
+}
+
+template <typename OutT, typename GT, int VPT>
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a) {
+  __shared__ float warp_ss[kNormThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x, tid = threadIdx.x;
   int n = a.n_rows;
   if (a.n_rows_dev != nullptr) n = min(n, *a.n_rows_dev);
-  if (warp >= n) return;
-  int src = warp;
+  if (row >= n) return;
+  int src = row;
   if (a.row_map != nullptr) {
-    src = a.row_map[warp];
+    src = a.row_map[row];
     if (src < 0 || src >= a.src_rows) {
-      if (lane == 0) set_err(a.err, PE_DEV_BAD_ROW);
+      if (tid == 0) set_err(a.err, PE_DEV_BAD_ROW);
       return;
     }
   }
   const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)src * a.d);
   const int nv = a.d / 4;
+  float4 v[VPT];
   float ss = 0.f;
-  for (int j = lane; j < nv; j += 32) {
-    const float4 v = xr[j];
-    ss += v.x * v.x;
-    ss += v.y * v.y;
-    ss += v.z * v.z;
-    ss += v.w * v.w;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int j = tid + k * kNormThreads;
+    v[k] = j < nv ? xr[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += v[k].x * v[k].x;
+    ss += v[k].y * v[k].y;
+    ss += v[k].z * v[k].z;
+    ss += v[k].w * v[k].w;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-  const float inv = 1.0f / sqrtf(ss / (float)a.d + a.eps);
+  if ((tid & 31) == 0) warp_ss[tid >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += warp_ss[w];
+  const float inv = 1.0f / sqrtf(tot / (float)a.d + a.eps);
   const GT* g = static_cast<const GT*>(a.g);
-  OutT* y = static_cast<OutT*>(a.y) + (size_t)warp * a.d;
-  for (int j = lane; j < nv; j += 32) {
-    const float4 v = xr[j];
-    y[4 * j + 0] = from_float<OutT>(v.x * inv * to_float<GT>(g[4 * j + 0]));
-    y[4 * j + 1] = from_float<OutT>(v.y * inv * to_float<GT>(g[4 * j + 1]));
-    y[4 * j + 2] = from_float<OutT>(v.z * inv * to_float<GT>(g[4 * j + 2]));
-    y[4 * j + 3] = from_float<OutT>(v.w * inv * to_float<GT>(g[4 * j + 3]));
+  OutT* y = static_cast<OutT*>(a.y) + (size_t)row * a.d;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int j = tid + k * kNormThreads;
+    if (j < nv)
+      store4<OutT>(y + 4 * j, v[k].x * inv * to_float<GT>(g[4 * j + 0]), v[k].y * inv * to_float<GT>(g[4 * j + 1]),
+                   v[k].z * inv * to_float<GT>(g[4 * j + 2]), v[k].w * inv * to_float<GT>(g[4 * j + 3]));
   }
 }
 
+template <typename OutT, typename GT>
+static cudaError_t launch_norm_typed(const NormArgs& a, cudaStream_t s) {
+  const int per = (a.d / 4 + kNormThreads - 1) / kNormThreads;  // float4 per thread
+  const dim3 grid(a.n_rows), block(kNormThreads);
+  if (per <= 1) return launch_pdl(rmsnorm_kernel<OutT, GT, 1>, grid, block, 0, s, a);
+  if (per <= 2) return launch_pdl(rmsnorm_kernel<OutT, GT, 2>, grid, block, 0, s, a);
+  if (per <= 4) return launch_pdl(rmsnorm_kernel<OutT, GT, 4>, grid, block, 0, s, a);
+  if (per <= 8) return launch_pdl(rmsnorm_kernel<OutT, GT, 8>, grid, block, 0, s, a);
+  if (per <= 16) return launch_pdl(rmsnorm_kernel<OutT, GT, 16>, grid, block, 0, s, a);
+  return cudaErrorInvalidValue;  // d > 16384 is rejected by the config check
+}
+
 cudaError_t launch_rmsnorm(const NormArgs& a, pe_dtype dt, cudaStream_t s) {
-  const int threads = 256, rows_per_block = threads / 32;
-  const int grid = (a.n_rows + rows_per_block - 1) / rows_per_block;
-  if (grid == 0) return cudaSuccess;
-  if (dt == PE_BF16)
-    rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, threads, 0, s>>>(a);
-  else
-    rmsnorm_kernel<float, float><<<grid, threads, 0, s>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  if (a.n_rows == 0) return cudaSuccess;
+  if (dt == PE_BF16) return launch_norm_typed<__nv_bfloat16, __nv_bfloat16>(a, s);
+  return launch_norm_typed<float, float>(a, s);
 }
 
 }  // namespace pe
