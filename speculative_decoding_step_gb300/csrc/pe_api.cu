@@ -41,6 +41,7 @@ constexpr int kAttnItemsPerSm = 8;       // attention work items aimed for, per 
 constexpr int kAttnMinChunk = 256;       // shortest position chunk of a work item
 constexpr int kTcSmemLimit = 232448;     // opt-in shared memory per block (227 KB)
 constexpr int kTcMaxStages = 12;
+constexpr int kMaxClusterSplits = 8;     // portable cluster size
 
 int num_sms() {
   static int cached[64] = {0};
@@ -66,15 +67,16 @@ struct GemmPlan {
   int nbuf = 1, acc_stride = 16;
   uint32_t tmem_cols = 32;
   uint32_t stage_bytes = 0;
-  size_t smem = 0, partial_floats = 0;
+  size_t smem = 0;
   int tiles = 0;
 };
 
 // Work decomposition of one GEMM: 128 weight rows x bn token rows per tile.
-// With fewer tiles than SMs, split K so that every SM streams weights, while
-// keeping the fp32 partial traffic (4 * splits * bn bytes per weight row) at
-// most the bf16 weight traffic (2 * k_dim bytes per weight row), and at least
-// four 64-wide k blocks per split.  The persistent grid has one CTA per SM.
+// With fewer tiles than SMs, split K so that every SM streams weights: the
+// splits of a tile run as one thread-block cluster (at most 8 CTAs) and reduce
+// through distributed shared memory, so every CTA owns exactly one unit and all
+// clusters must fit on the GPU at once; each split keeps at least four 64-wide
+// k blocks, and its fp32 partial tile must fit in the idle stage ring.
 GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   GemmPlan g;
   g.epi = epi;
@@ -85,34 +87,34 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   g.kb_total = (k_dim + kTcBK - 1) / kTcBK;
   g.tiles = g.n_f * g.n_t;
   g.stage_bytes = (paired ? 2u : 1u) * kTcBM * kTcBK * 2 + (uint32_t)g.bn * kTcBK * 2;
-  const int red = epi == EPI_ARGMAX ? g.n_t * g.bn : 0;
+  const int red = epi == EPI_ARGMAX ? 4 * g.n_t * g.bn : 0;
   const long long avail = kTcSmemLimit - 1024 - kTcCtrlBytes - (long long)red * 8;
   g.stages = (int)std::min<long long>(kTcMaxStages, avail / g.stage_bytes);
-  if (epi != EPI_ARGMAX && g.tiles < sms) {
-    const int by_sms = sms / g.tiles;
-    const int by_depth = std::max(1, g.kb_total / 4);
-    const int by_traffic = std::max(1, k_dim / (2 * g.bn));
-    g.k_splits = std::max(1, std::min(by_sms, std::min(by_depth, by_traffic)));
+  g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, red);
+  const size_t partial_bytes = (size_t)(paired ? 2 : 1) * kTcBM * (g.bn + 4) * 4;
+  if (epi != EPI_ARGMAX && g.tiles < sms && partial_bytes <= (size_t)g.stages * g.stage_bytes) {
+    int s = std::min(kMaxClusterSplits, std::min(sms / g.tiles, std::max(1, g.kb_total / 4)));
+    for (; s > 1; --s) {
+      const int fit = gemm_tc_max_active_clusters(epi, g.smem, s);
+      if (fit >= g.tiles) break;
+    }
+    g.k_splits = std::max(1, s);
   }
   const int acc_cols = (paired ? 2 : 1) * g.bn;
   g.nbuf = 2 * acc_cols <= 512 ? 2 : 1;
   g.acc_stride = acc_cols;
   const int need = g.nbuf * acc_cols;
   g.tmem_cols = need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
-  g.grid = std::min(g.tiles * g.k_splits, sms);
-  g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, red);
-  g.partial_floats = g.k_splits > 1 ? (size_t)g.k_splits * g.tiles * (paired ? 2 : 1) * kTcBM * g.bn : 0;
+  g.grid = g.k_splits > 1 ? g.tiles * g.k_splits : std::min(g.tiles, sms);
   return g;
 }
 
 struct Plan {
   int R = 0, T = 0, S = 0, sms = 0, max_items = 0, attn_grid = 0, attn_target = 0;
   GemmPlan fc, qkv, o, gu, down, lm;
-  size_t max_partial = 0;
-  int max_tiles = 0;
   // workspace offsets
   size_t tok_pos, tok_seq, tok_slot, seq_start, seq_len, seq_maxpos, item_base, n_chunks, n_items, items;
-  size_t counters, done, keys, x, y, q, ao, u, yl, partial, part_m, part_l, part_o;
+  size_t done, keys, x, y, q, ao, u, yl, part_m, part_l, part_o;
   size_t st_ids, st_pos, st_slot, st_rej, st_mask, st_hmap, st_rows, st_nvalid, st_draft, st_x0;
   size_t total = 0;
 };
@@ -132,10 +134,6 @@ Plan make_plan(const pe_config& c) {
   p.gu = plan_gemm(EPI_SWIGLU, (c.ffn + kTcBM - 1) / kTcBM, p.R, c.d, p.sms);
   p.down = plan_gemm(EPI_ADD_F32, (c.d + kTcBM - 1) / kTcBM, p.R, c.ffn, p.sms);
   p.lm = plan_gemm(EPI_ARGMAX, (c.vocab + kTcBM - 1) / kTcBM, p.T, c.d, p.sms);
-  for (const GemmPlan* g : {&p.fc, &p.qkv, &p.o, &p.gu, &p.down, &p.lm}) {
-    p.max_partial = std::max(p.max_partial, g->partial_floats);
-    p.max_tiles = std::max(p.max_tiles, g->tiles);
-  }
   // attention items: the work list aims at attn_target items; rounding adds at
   // most one per (sequence, kv head), and no (sequence, kv head) can have more
   // chunks than its longest possible range holds minimum chunks
@@ -161,8 +159,7 @@ Plan make_plan(const pe_config& c) {
   p.n_chunks = take(4 * (size_t)c.B);
   p.n_items = take(4);
   p.items = take(16 * (size_t)p.max_items);
-  p.counters = take(4 * (size_t)(p.max_tiles + 1));  // split-K arrival counters, then the LM-head counter
-  p.done = p.counters + 4 * (size_t)p.max_tiles;
+  p.done = take(4);  // LM-head completion counter
   p.keys = take(8 * (size_t)p.T);
   p.x = take(4 * (size_t)p.R * c.d);
   p.y = take(eb * (size_t)p.R * c.d);
@@ -171,12 +168,11 @@ Plan make_plan(const pe_config& c) {
   p.u = take(eb * (size_t)p.R * c.ffn);
   p.yl = take(eb * (size_t)p.T * c.d);
   if (c.dtype == PE_BF16) {
-    p.partial = take(4 * p.max_partial);
     p.part_m = take(4 * (size_t)p.max_items * kAttnRows);
     p.part_l = take(4 * (size_t)p.max_items * kAttnRows);
     p.part_o = take(4 * (size_t)p.max_items * kAttnRows * c.head_dim);
   } else {
-    p.partial = p.part_m = p.part_l = p.part_o = 0;
+    p.part_m = p.part_l = p.part_o = 0;
   }
   // pe_step: batch metadata and input rows
   p.st_ids = take(4 * (size_t)p.R);
@@ -318,8 +314,6 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   a.acc_stride = g.acc_stride;
   a.tmem_cols = g.tmem_cols;
   a.n_tok_min = call.n_tok_dev != nullptr ? std::min(call.n_tok, c.B * c.K) : call.n_tok;
-  a.partial = at<float>(ws, p.partial);
-  a.counters = at<int32_t>(ws, p.counters);
   CUtensorMap tw, tx;
   bool ok;
   if (call.w_kind == 1) ok = tmap_gate_up(&tw, call.W, (uint64_t)c.ffn, (uint64_t)c.d);
@@ -327,7 +321,7 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   else ok = tmap_matrix(&tw, call.W, call.w_rows, (uint64_t)call.k_dim, (uint32_t)kTcBM);
   ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)g.bn);
   if (!ok) return PE_ERR_CUDA;
-  PE_TRY_CUDA(launch_gemm_tc(call.epi, tw, tx, a, g.grid, g.smem, s));
+  PE_TRY_CUDA(launch_gemm_tc(call.epi, tw, tx, a, g.grid, g.smem, g.k_splits, s));
   return PE_OK;
 }
 
@@ -373,7 +367,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   ia.target_items = p.attn_target; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
   ia.items = at<int4>(ws, p.items); ia.n_items = at<int32_t>(ws, p.n_items);
   ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
-  ia.counters = at<int32_t>(ws, p.counters); ia.n_counters = p.max_tiles + 1;
+  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1;
   ia.keys = at<unsigned long long>(ws, p.keys); ia.err = err;
   PE_TRY_CUDA(launch_forward_init(ia, s));
   trace(3, s);

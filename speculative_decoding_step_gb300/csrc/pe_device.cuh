@@ -195,6 +195,33 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// ----------------------------------------------------------------------------- thread-block clusters
+// Distributed shared memory: a CTA reads a peer CTA's shared memory through the
+// cluster window (mapa + ld.shared::cluster).  The cluster barrier is entered
+// by every thread of every CTA of the cluster.
+
+PE_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+PE_DEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+PE_DEV uint32_t dsmem_map(uint32_t local_smem, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
+  return r;
+}
+PE_DEV float4 dsmem_ld4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
 // ----------------------------------------------------------------------------- programmatic dependent launch
 // Kernels are launched so that the next kernel of the round may start while
 // this one drains: pdl_trigger() lets the dependent grid launch, pdl_wait()

@@ -7,13 +7,17 @@
 // issues tcgen05.mma with fp32 accumulators in tensor memory.  The weight
 // matrix sits on the MMA's M side (128 weight rows per tile) and the few
 // token rows on its N side, so a batch of 16..256 rows reads every weight
-// byte once.  Split-K spreads small matrices over all SMs; the last CTA of a
-// tile (arrival counter, no waiting) sums the partials in split order, so the
-// result does not depend on scheduling.  The LM head never writes logits: each
+// byte once.  Split-K spreads small matrices over all SMs; the splits of a
+// tile form a thread-block cluster and sum their partials through distributed
+// shared memory in rank order, so the result does not depend on scheduling.
+// The LM head never writes logits: each
 // CTA reduces its 128 vocabulary rows to a (max, argmax) key per token and
 // folds it into a global 64-bit atomicMax; the last CTA decodes the keys.
 //
 // fp32 configurations run a CUDA-core kernel with the same epilogues.
+#include <mutex>
+#include <vector>
+
 #include "pe_device.cuh"
 #include "pe_internal.h"
 
@@ -85,12 +89,19 @@ PE_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r
 // ============================================================================= tensor-core kernel
 //
 // Persistent: CTA b processes work units b, b + grid, b + 2*grid, ...; a unit is
-// (token tile, weight tile, k split).  Roles: warp 0 lane 0 issues TMA loads
+// (k split, token tile, weight tile).  Roles: warp 0 lane 0 issues TMA loads
 // into a ring of `stages` shared-memory stages (continuously across units),
 // warp 1 lane 0 issues tcgen05.mma into one of `nbuf` TMEM accumulators, warps
 // 2..5 run the epilogue of unit i while the MMAs of unit i+1 fill the other
 // accumulator.  Before waiting on the previous kernel (pdl_wait) the producer
 // already streams the weights of its first unit: they never depend on it.
+//
+// Split K: the k_splits CTAs of one tile form a thread-block cluster (one unit
+// per CTA).  Each leaves its fp32 partial tile in its own shared memory; after
+// a cluster barrier, CTA rank q sums a 1/k_splits slice of the tile's columns
+// over all ranks through distributed shared memory, in rank order, and runs
+// the epilogue on it.  No partial sums leave the chip and no CTA waits for a
+// straggler.
 
 size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int red_entries) {
   return 1024 /*alignment slack*/ + (size_t)stages * stage_bytes + kTcCtrlBytes + (size_t)red_entries * 8;
@@ -116,10 +127,10 @@ struct Unit {
 
 PE_DEV Unit decode_unit(const GemmArgs& a, int u) {
   Unit w;
-  w.tile_t = u % a.n_t;
-  const int r = u / a.n_t;
-  w.split = r % a.k_splits;
-  w.tile_f = r / a.k_splits;
+  w.split = u % a.k_splits;  // splits of a tile are consecutive: they form one cluster
+  const int r = u / a.k_splits;
+  w.tile_t = r % a.n_t;      // token tiles of a weight tile run side by side (L2 reuse)
+  w.tile_f = r / a.n_t;
   w.kb0 = (int)((long long)w.split * a.kb_total / a.k_splits);
   w.kb1 = (int)((long long)(w.split + 1) * a.kb_total / a.k_splits);
   return w;
@@ -150,10 +161,17 @@ PE_DEV void apply16(const GemmArgs& a, int unit, int t0, int n_tok, const float 
     if (t0 + j < n_tok) epi_elem<EPI, __nv_bfloat16>(a, unit, t0 + j, v[j], v2[j], inv_freq);
 }
 
-// Warp-level (max, argmax) of 16 token columns over the 32 rows the warp holds;
-// lane 0 folds the result into the CTA's running keys.
+PE_DEV unsigned long long umax64(unsigned long long x, unsigned long long y) { return x > y ? x : y; }
+
+// (max, argmax) keys of 16 token columns over the warp's 32 rows by a
+// transpose-reduce: each exchange round halves the columns a lane keeps, so
+// after 4 rounds lane l owns one column (bits 4..1 of l) and a final round
+// joins the lane pair holding it -- 16 exchanges instead of 5 per column.
+// The even lane folds its column into this warp's running keys (no atomics:
+// every address has one writer).
 PE_DEV void argmax16(const GemmArgs& a, int unit, int t0, int n_tok, const float (&v)[16],
-                     unsigned long long* red_col, int lane) {
+                     unsigned long long* red_w, int lane) {
+  unsigned long long k[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int t = t0 + j;
@@ -163,13 +181,29 @@ PE_DEV void argmax16(const GemmArgs& a, int unit, int t0, int n_tok, const float
       key = argmax_key(v[j], (uint32_t)unit);
       if (a.logits_dbg != nullptr) a.logits_dbg[(size_t)t * a.n_out + unit] = v[j];
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, key, o);
-      key = other > key ? other : key;
-    }
-    if (lane == 0 && key != 0ull) atomicMax(red_col + j, key);
+    k[j] = key;
   }
+  const bool h1 = (lane >> 4) & 1, h2 = (lane >> 3) & 1, h3 = (lane >> 2) & 1, h4 = (lane >> 1) & 1;
+  unsigned long long k8[8], k4[4], k2[2];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const unsigned long long mine = h1 ? k[8 + i] : k[i], other = h1 ? k[i] : k[8 + i];
+    k8[i] = umax64(mine, __shfl_xor_sync(0xFFFFFFFFu, other, 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const unsigned long long mine = h2 ? k8[4 + i] : k8[i], other = h2 ? k8[i] : k8[4 + i];
+    k4[i] = umax64(mine, __shfl_xor_sync(0xFFFFFFFFu, other, 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const unsigned long long mine = h3 ? k4[2 + i] : k4[i], other = h3 ? k4[i] : k4[2 + i];
+    k2[i] = umax64(mine, __shfl_xor_sync(0xFFFFFFFFu, other, 4));
+  }
+  unsigned long long k1 = umax64(h4 ? k2[1] : k2[0], __shfl_xor_sync(0xFFFFFFFFu, h4 ? k2[0] : k2[1], 2));
+  k1 = umax64(k1, __shfl_xor_sync(0xFFFFFFFFu, k1, 1));
+  const int col = (h1 ? 8 : 0) + (h2 ? 4 : 0) + (h3 ? 2 : 0) + (h4 ? 1 : 0);
+  if ((lane & 1) == 0 && k1 > red_w[col]) red_w[col] = k1;
 }
 
 template <int EPI>
@@ -185,6 +219,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int BN = a.bn;
   const int U = a.n_t * a.n_f * a.k_splits;
   const int S = a.stages;
+  const int NT = a.n_t * BN;  // argmax keys per warp
   uint8_t* ctrl = smem + (size_t)S * a.stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + S;
@@ -193,8 +228,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(ctrl + kTcCtrlBytes);
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(ctrl + kTcCtrlBytes);  // [4 warps][NT]
   const uint32_t b_off = (PAIRED ? 2u : 1u) * A_BYTES;
+  const int ldp = BN + 4;  // row stride of a split's partial tile in shared memory (floats)
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmW);
@@ -212,7 +248,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_mbar_init();
   }
   if (EPI == EPI_ARGMAX)
-    for (int j = threadIdx.x; j < a.n_t * BN; j += blockDim.x) red[j] = 0ull;
+    for (int j = threadIdx.x; j < 4 * NT; j += blockDim.x) red[j] = 0ull;
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
     tmem_relinquish();
@@ -318,10 +354,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int n_tok = effective_ntok(a);
     const int q = warp & 3;                // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;           // row of the tile = TMEM lane
-    const int ethread = threadIdx.x - 64;  // 0..127
-    const int rows_per = PAIRED ? 2 * kTcBM : kTcBM;
-    const size_t tile_elems = (size_t)rows_per * BN;
-    const size_t n_tiles = (size_t)a.n_f * a.n_t;
+    unsigned long long* red_w = red + (size_t)(warp - 2) * NT;
     int i = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
       const Unit w = decode_unit(a, u);
@@ -330,94 +363,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool ok = mbar_wait(smem_u32(tfull + buf), (uint32_t)(i / a.nbuf) & 1u, a.err, abort_flag);
       tc_fence_after();
       const int unit = w.tile_f * kTcBM + r;
-      const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
       const uint32_t tl = tmem + (uint32_t)(buf * a.acc_stride) + ((uint32_t)(q * 32) << 16);
       const int tbase = w.tile_t * BN;
-      const size_t tile = (size_t)w.tile_f * a.n_t + w.tile_t;
       if (ok && a.k_splits == 1) {
+        const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
         for (int c = 0; c < BN / 16; ++c) {
           float v[16], v2[16];
           tmem_load16(tl + (uint32_t)(c * 16), v);
           if (PAIRED) tmem_load16(tl + (uint32_t)(BN + c * 16), v2);
           if (EPI == EPI_ARGMAX)
-            argmax16(a, unit, tbase + c * 16, n_tok, v, red + w.tile_t * BN + c * 16, lane);
+            argmax16(a, unit, tbase + c * 16, n_tok, v, red_w + tbase + c * 16, lane);
           else
             apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, inv_freq);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(tempty + buf));
       } else if (ok) {
-        // split K: this split's partial sums, [row][token] fp32, then count arrivals
-        float* P = a.partial + ((size_t)w.split * n_tiles + tile) * tile_elems;
+        // split K (one unit per CTA, the stage ring is idle): leave this split's partial
+        // tile [rows][BN] fp32 in shared memory for the cluster reduction below
+        float* P = reinterpret_cast<float*>(smem);
         for (int c = 0; c < BN / 16; ++c) {
           float v[16];
           tmem_load16(tl + (uint32_t)(c * 16), v);
-          float4* dst = reinterpret_cast<float4*>(P + (size_t)r * BN + c * 16);
+          float4* dst = reinterpret_cast<float4*>(P + (size_t)r * ldp + c * 16);
 #pragma unroll
           for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           if (PAIRED) {
             tmem_load16(tl + (uint32_t)(BN + c * 16), v);
-            float4* dst2 = reinterpret_cast<float4*>(P + (size_t)(kTcBM + r) * BN + c * 16);
+            float4* dst2 = reinterpret_cast<float4*>(P + (size_t)(kTcBM + r) * ldp + c * 16);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               dst2[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(tempty + buf));  // accumulator free for the next unit
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (ethread == 0) {
-          const int old = atomicAdd(a.counters + tile, 1);
-          *last_flag = (old == a.k_splits - 1) ? 1 : 0;
-        }
-        named_bar_sync(1, 128);
-        const bool last = *last_flag != 0;
-        named_bar_sync(1, 128);  // every thread has read the flag before a later unit rewrites it
-        if (last) {
-          // last split of this tile: sum the partials in split order, then the epilogue
-          __threadfence();
-          const float* P0 = a.partial + tile * tile_elems;
-          const size_t sstride = n_tiles * tile_elems;
-          for (int c8 = 0; c8 < BN; c8 += 8) {
-            float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0, g0 = s0, g1 = s0;
-            for (int sp = 0; sp < a.k_splits; ++sp) {
-              const float4* src = reinterpret_cast<const float4*>(P0 + sp * sstride + (size_t)r * BN + c8);
-              const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
-              s0.x += x0.x; s0.y += x0.y; s0.z += x0.z; s0.w += x0.w;
-              s1.x += x1.x; s1.y += x1.y; s1.z += x1.z; s1.w += x1.w;
-              if (PAIRED) {
-                const float4* src2 =
-                    reinterpret_cast<const float4*>(P0 + sp * sstride + (size_t)(kTcBM + r) * BN + c8);
-                const float4 y0 = __ldcg(src2), y1 = __ldcg(src2 + 1);
-                g0.x += y0.x; g0.y += y0.y; g0.z += y0.z; g0.w += y0.w;
-                g1.x += y1.x; g1.y += y1.y; g1.z += y1.z; g1.w += y1.w;
-              }
-            }
-            if (unit < a.n_out) {
-              const float vv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-              const float ww[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const int t = tbase + c8 + j;
-                if (t < n_tok) epi_elem<EPI, __nv_bfloat16>(a, unit, t, vv[j], ww[j], inv_freq);
-              }
-            }
-          }
-          if (ethread == 0) a.counters[tile] = 0;  // ready for the next launch
-        }
-      } else {
-        // a wait gave up: release the accumulator so the MMA role can unwind too
-        if (lane == 0) mbar_arrive(smem_u32(tempty + buf));
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(tempty + buf));  // accumulator free for a later unit
       ++i;
     }
     if (EPI == EPI_ARGMAX) {
       named_bar_sync(1, 128);
-      for (int j = ethread; j < a.n_t * BN; j += 128)  // key index = token = tile_t * BN + column
-        if (j < n_tok && red[j] != 0ull) atomicMax(a.keys + j, red[j]);
+      const int ethread = threadIdx.x - 64;
+      for (int j = ethread; j < NT; j += 128) {  // key index = token = tile_t * BN + column
+        const unsigned long long k =
+            umax64(umax64(red[j], red[NT + j]), umax64(red[2 * NT + j], red[3 * NT + j]));
+        if (j < n_tok && k != 0ull) atomicMax(a.keys + j, k);
+      }
       __threadfence();
       named_bar_sync(1, 128);
       if (ethread == 0) {
@@ -431,7 +421,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ethread == 0) *a.done_counter = 0;
       }
     }
-    tc_fence_before();
+  }
+
+  if (EPI != EPI_ARGMAX && a.k_splits > 1) {
+    // cluster reduction of the split-K partial tiles (every thread takes part in the barriers)
+    __syncwarp();
+    cluster_sync_all();  // every rank's partial tile is in its shared memory
+    if (warp >= 2) {
+      const Unit w = decode_unit(a, blockIdx.x);
+      const int n_tok = effective_ntok(a);
+      if (w.tile_t * BN < n_tok) {
+        const int ns = a.k_splits;
+        const uint32_t rank = cluster_ctarank();
+        const int cs = (((BN + ns - 1) / ns) + 3) & ~3;
+        const int c0 = (int)rank * cs, c1 = min(BN, c0 + cs);
+        const int r = (warp & 3) * 32 + lane;
+        const int unit = w.tile_f * kTcBM + r;
+        const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
+        const uint32_t base = smem_u32(smem);
+        for (int col = c0; col < c1; col += 4) {
+          float4 s1 = make_float4(0.f, 0.f, 0.f, 0.f), s2 = s1;
+          for (int p = 0; p < ns; ++p) {  // rank order: the sum does not depend on timing
+            const float4 x = dsmem_ld4(dsmem_map(base + 4u * (uint32_t)(r * ldp + col), (uint32_t)p));
+            s1.x += x.x; s1.y += x.y; s1.z += x.z; s1.w += x.w;
+            if (PAIRED) {
+              const float4 y = dsmem_ld4(dsmem_map(base + 4u * (uint32_t)((kTcBM + r) * ldp + col), (uint32_t)p));
+              s2.x += y.x; s2.y += y.y; s2.z += y.z; s2.w += y.w;
+            }
+          }
+          if (unit < a.n_out) {
+            const float vv[4] = {s1.x, s1.y, s1.z, s1.w}, ww[4] = {s2.x, s2.y, s2.z, s2.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int t = w.tile_t * BN + col + j;
+              if (t < n_tok) epi_elem<EPI, __nv_bfloat16>(a, unit, t, vv[j], ww[j], inv_freq);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();  // peers are done reading this CTA's shared memory
   }
   __syncthreads();
   if (warp == 1) {
@@ -442,26 +472,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 template <int EPI>
 static cudaError_t launch_tc_typed(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
-                                   size_t smem, cudaStream_t s) {
+                                   size_t smem, int cluster, cudaStream_t s) {
   static size_t configured = 0;
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  return launch_pdl(gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), smem, s, tmW, tmX, a);
+  return launch_pdl_cluster(gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), smem, s, cluster, tmW, tmX, a);
 }
 
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
-                           size_t smem, cudaStream_t s) {
+                           size_t smem, int cluster, cudaStream_t s) {
   switch (epi) {
-    case EPI_STORE_F32: return launch_tc_typed<EPI_STORE_F32>(tmW, tmX, a, grid, smem, s);
-    case EPI_ADD_F32: return launch_tc_typed<EPI_ADD_F32>(tmW, tmX, a, grid, smem, s);
-    case EPI_SWIGLU: return launch_tc_typed<EPI_SWIGLU>(tmW, tmX, a, grid, smem, s);
-    case EPI_QKV_ROPE: return launch_tc_typed<EPI_QKV_ROPE>(tmW, tmX, a, grid, smem, s);
-    case EPI_ARGMAX: return launch_tc_typed<EPI_ARGMAX>(tmW, tmX, a, grid, smem, s);
+    case EPI_STORE_F32: return launch_tc_typed<EPI_STORE_F32>(tmW, tmX, a, grid, smem, cluster, s);
+    case EPI_ADD_F32: return launch_tc_typed<EPI_ADD_F32>(tmW, tmX, a, grid, smem, cluster, s);
+    case EPI_SWIGLU: return launch_tc_typed<EPI_SWIGLU>(tmW, tmX, a, grid, smem, cluster, s);
+    case EPI_QKV_ROPE: return launch_tc_typed<EPI_QKV_ROPE>(tmW, tmX, a, grid, smem, cluster, s);
+    case EPI_ARGMAX: return launch_tc_typed<EPI_ARGMAX>(tmW, tmX, a, grid, smem, cluster, s);
   }
   return cudaErrorInvalidValue;
+}
+
+template <int EPI>
+static int max_clusters_typed(size_t smem, int cluster) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster * 64);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int gemm_tc_max_active_clusters(int epi, size_t smem, int cluster) {
+  // the answer depends only on (device, variant, shared memory, cluster size): cache it
+  struct Entry {
+    int dev, epi, cluster, n;
+    size_t smem;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const Entry& e : cache)
+    if (e.dev == dev && e.epi == epi && e.cluster == cluster && e.smem == smem) return e.n;
+  int n = 0;
+  switch (epi) {
+    case EPI_STORE_F32: n = max_clusters_typed<EPI_STORE_F32>(smem, cluster); break;
+    case EPI_ADD_F32: n = max_clusters_typed<EPI_ADD_F32>(smem, cluster); break;
+    case EPI_SWIGLU: n = max_clusters_typed<EPI_SWIGLU>(smem, cluster); break;
+    case EPI_QKV_ROPE: n = max_clusters_typed<EPI_QKV_ROPE>(smem, cluster); break;
+  }
+  cache.push_back(Entry{dev, epi, cluster, n, smem});
+  return n;
 }
 
 // ============================================================================= fp32 CUDA-core kernel

@@ -36,6 +36,28 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// As launch_pdl, with thread-block clusters of `cluster` CTAs along x (1: no cluster).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster > 1 ? cluster : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ----------------------------------------------------------------------------- batch metadata
 
 struct PrepArgs {
@@ -128,8 +150,6 @@ struct GemmArgs {
   int nbuf;              // TMEM accumulator buffers (2: epilogue overlaps the next unit's MMAs)
   int acc_stride;        // TMEM columns per accumulator buffer
   uint32_t tmem_cols;    // TMEM columns allocated (power of two >= 32)
-  float* partial;        // split-K partial sums
-  int32_t* counters;     // split-K arrival counters per output tile (zero between launches)
   // fp32 kernel operands
   const void* W;         // [rows][k_dim]
   const void* X;         // [tokens][ldx]
@@ -151,9 +171,13 @@ struct GemmArgs {
 };
 
 // Tensor-core GEMM (tcgen05 + TMA): D[f][t] = W[f][:] . X[t][:], weights on the MMA M side.
-// Persistent: `grid` CTAs (at most one per SM) stride over the work units.
+// Persistent: `grid` CTAs (at most one per SM) stride over the work units.  With
+// k_splits > 1 every CTA owns exactly one unit and the splits of a tile form a
+// cluster of `cluster` (= k_splits) CTAs.
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
-                           size_t smem_bytes, cudaStream_t s);
+                           size_t smem_bytes, int cluster, cudaStream_t s);
+// Clusters of `cluster` CTAs of this GEMM variant that fit on the GPU at once (0 if unknown).
+int gemm_tc_max_active_clusters(int epi, size_t smem_bytes, int cluster);
 // fp32 CUDA-core GEMM for fp32 configurations (same epilogues).
 cudaError_t launch_gemm_f32(int epi, const GemmArgs& a, cudaStream_t s);
 
@@ -161,7 +185,7 @@ constexpr int kTcThreads = 192;        // warp 0: TMA, warp 1: MMA, warps 2-5: e
 constexpr int kTcBM = 128;             // weight rows per tile
 constexpr int kTcBK = 64;              // k per pipeline stage (one 128-byte swizzle row)
 constexpr int kTcCtrlBytes = 1024;     // barriers + TMEM slot + flags
-// dynamic shared memory: alignment slack + stage ring + control block + argmax keys (n_t * bn)
+// dynamic shared memory: alignment slack + stage ring + control block + argmax keys (4 warps * n_t * bn)
 size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int red_entries);
 
 // ----------------------------------------------------------------------------- attention
