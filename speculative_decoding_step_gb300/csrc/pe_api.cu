@@ -39,7 +39,6 @@ void trace(int point, cudaStream_t s) {
 constexpr int kMaxRows = 1 << 16;        // B*2K
 constexpr int kAttnItemsPerSm = 8;       // attention work items aimed for, per SM (load balance)
 constexpr int kAttnMinChunk = 256;       // shortest position chunk of a work item
-constexpr int kTcSmemLimit = 232448;     // opt-in shared memory per block (227 KB)
 constexpr int kTcMaxStages = 12;
 constexpr int kMaxClusterSplits = 8;     // portable cluster size
 
@@ -81,14 +80,19 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   GemmPlan g;
   g.epi = epi;
   const bool paired = (epi == EPI_SWIGLU || epi == EPI_QKV_ROPE);
-  g.n_t = (n_tok + 255) / 256;
-  g.bn = round_up((n_tok + g.n_t - 1) / g.n_t, 16);
+  if (n_tok <= 256 || epi == EPI_ARGMAX) {  // one token tile, or the LM head (vocabulary tiles are plenty)
+    g.n_t = (n_tok + 255) / 256;
+    g.bn = round_up((n_tok + g.n_t - 1) / g.n_t, 16);
+  } else {  // many rows: 128-row token tiles give enough units to fill the GPU without split K
+    g.bn = 128;
+    g.n_t = (n_tok + g.bn - 1) / g.bn;
+  }
   g.n_f = n_f_tiles;
   g.kb_total = (k_dim + kTcBK - 1) / kTcBK;
   g.tiles = g.n_f * g.n_t;
   g.stage_bytes = (paired ? 2u : 1u) * kTcBM * kTcBK * 2 + (uint32_t)g.bn * kTcBK * 2;
   const int red = epi == EPI_ARGMAX ? 4 * g.n_t * g.bn : 0;
-  const long long avail = kTcSmemLimit - 1024 - kTcCtrlBytes - (long long)red * 8;
+  const long long avail = kTcSmemOptIn - 1024 - kTcCtrlBytes - (long long)red * 8;
   g.stages = (int)std::min<long long>(kTcMaxStages, avail / g.stage_bytes);
   g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, red);
   const size_t partial_bytes = (size_t)(paired ? 2 : 1) * kTcBM * (g.bn + 4) * 4;

@@ -125,12 +125,18 @@ struct Unit {
   int tile_t, tile_f, split, kb0, kb1;
 };
 
-PE_DEV Unit decode_unit(const GemmArgs& a, int u) {
+// Token tiles holding at least one of this launch's rows.  Units are numbered
+// over these only, so the rows' padding never lands on a CTA's schedule.
+PE_DEV int live_token_tiles(const GemmArgs& a, int n_tok) {
+  return min(a.n_t, (n_tok + a.bn - 1) / a.bn);
+}
+
+PE_DEV Unit decode_unit(const GemmArgs& a, int u, int n_t_live) {
   Unit w;
   w.split = u % a.k_splits;  // splits of a tile are consecutive: they form one cluster
   const int r = u / a.k_splits;
-  w.tile_t = r % a.n_t;      // token tiles of a weight tile run side by side (L2 reuse)
-  w.tile_f = r / a.n_t;
+  w.tile_t = r % n_t_live;   // token tiles of a weight tile run side by side (L2 reuse)
+  w.tile_f = r / n_t_live;
   w.kb0 = (int)((long long)w.split * a.kb_total / a.k_splits);
   w.kb1 = (int)((long long)(w.split + 1) * a.kb_total / a.k_splits);
   return w;
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BN = a.bn;
-  const int U = a.n_t * a.n_f * a.k_splits;
+  const int U = a.n_t * a.n_f * a.k_splits;  // units of the largest row count
   const int S = a.stages;
   const int NT = a.n_t * BN;  // argmax keys per warp
   uint8_t* ctrl = smem + (size_t)S * a.stage_bytes;
@@ -266,9 +272,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t pol_x = l2_policy_evict_last();   // activations: re-read by every weight tile
       // the weights of the first unit do not depend on earlier kernels: start them now
       int npre = 0;
-      if ((int)blockIdx.x < U) {
-        const Unit w = decode_unit(a, blockIdx.x);
-        if (w.tile_t * BN < a.n_tok_min) {
+      if (a.n_t == 1 && (int)blockIdx.x < U) {  // unit numbering does not depend on the row count
+        const Unit w = decode_unit(a, blockIdx.x, 1);
+        {
           npre = min(S, w.kb1 - w.kb0);
           for (int i = 0; i < npre; ++i) {
             const uint32_t sa = smem_u32(smem + (size_t)i * a.stage_bytes);
@@ -279,11 +285,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       pdl_wait();
       const int n_tok = effective_ntok(a);
+      const int ntl = live_token_tiles(a, n_tok);
+      const int UL = ntl * a.n_f * a.k_splits;
       int it = 0;
       bool stop = false;
-      for (int u = blockIdx.x; u < U && !stop; u += gridDim.x) {
-        const Unit w = decode_unit(a, u);
-        if (EPI != EPI_ARGMAX && w.tile_t * BN >= n_tok) continue;
+      for (int u = blockIdx.x; u < UL && !stop; u += gridDim.x) {
+        const Unit w = decode_unit(a, u, ntl);
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t use = (uint32_t)(it / S);
@@ -312,12 +319,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       pdl_wait();
       const int n_tok = effective_ntok(a);
+      const int ntl = live_token_tiles(a, n_tok);
+      const int UL = ntl * a.n_f * a.k_splits;
       const uint32_t idesc = idesc_bf16(kTcBM, BN);
       int it = 0, i = 0;
       bool stop = false;
-      for (int u = blockIdx.x; u < U && !stop; u += gridDim.x) {
-        const Unit w = decode_unit(a, u);
-        if (EPI != EPI_ARGMAX && w.tile_t * BN >= n_tok) continue;
+      for (int u = blockIdx.x; u < UL && !stop; u += gridDim.x) {
+        const Unit w = decode_unit(a, u, ntl);
         const int buf = i % a.nbuf;
         if (i >= a.nbuf &&
             !mbar_wait(smem_u32(tempty + buf), (uint32_t)((i / a.nbuf) - 1) & 1u, a.err, abort_flag))
@@ -355,10 +363,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;                // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;           // row of the tile = TMEM lane
     unsigned long long* red_w = red + (size_t)(warp - 2) * NT;
+    const int ntl = live_token_tiles(a, n_tok);
+    const int UL = ntl * a.n_f * a.k_splits;
     int i = 0;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-      const Unit w = decode_unit(a, u);
-      if (EPI != EPI_ARGMAX && w.tile_t * BN >= n_tok) continue;
+    for (int u = blockIdx.x; u < UL; u += gridDim.x) {
+      const Unit w = decode_unit(a, u, ntl);
       const int buf = i % a.nbuf;
       const bool ok = mbar_wait(smem_u32(tfull + buf), (uint32_t)(i / a.nbuf) & 1u, a.err, abort_flag);
       tc_fence_after();
@@ -428,9 +437,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
     cluster_sync_all();  // every rank's partial tile is in its shared memory
     if (warp >= 2) {
-      const Unit w = decode_unit(a, blockIdx.x);
       const int n_tok = effective_ntok(a);
-      if (w.tile_t * BN < n_tok) {
+      const int ntl = live_token_tiles(a, n_tok);
+      const Unit w = decode_unit(a, blockIdx.x, ntl);
+      if ((int)blockIdx.x < ntl * a.n_f * a.k_splits) {
         const int ns = a.k_splits;
         const uint32_t rank = cluster_ctarank();
         const int cs = (((BN + ns - 1) / ns) + 3) & ~3;
@@ -470,15 +480,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
+// Opt every GEMM variant into the largest dynamic shared memory once per
+// device (an upper bound only; each launch passes its own size).
+template <int EPI>
+static cudaError_t ensure_smem_attr() {
+  static bool done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemOptIn);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
 template <int EPI>
 static cudaError_t launch_tc_typed(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
                                    size_t smem, int cluster, cudaStream_t s) {
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  const cudaError_t e = ensure_smem_attr<EPI>();
+  if (e != cudaSuccess) return e;
   return launch_pdl_cluster(gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), smem, s, cluster, tmW, tmX, a);
 }
 
@@ -496,8 +518,7 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& t
 
 template <int EPI>
 static int max_clusters_typed(size_t smem, int cluster) {
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return 0;
+  if (ensure_smem_attr<EPI>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster * 64);
   cfg.blockDim = dim3(kTcThreads);

@@ -185,6 +185,7 @@ constexpr int kTcThreads = 192;        // warp 0: TMA, warp 1: MMA, warps 2-5: e
 constexpr int kTcBM = 128;             // weight rows per tile
 constexpr int kTcBK = 64;              // k per pipeline stage (one 128-byte swizzle row)
 constexpr int kTcCtrlBytes = 1024;     // barriers + TMEM slot + flags
+constexpr int kTcSmemOptIn = 232448;   // largest dynamic shared memory per block (227 KB)
 // dynamic shared memory: alignment slack + stage ring + control block + argmax keys (4 warps * n_t * bn)
 size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int red_entries);
 
