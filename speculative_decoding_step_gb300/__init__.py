@@ -122,9 +122,12 @@ def lib():
     """Load libpe.so (building it first if needed).  Raises if it cannot be loaded."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB):
-            build()
-        L = ctypes.CDLL(LIB)
+        path = os.environ.get("PE_LIB")  # an alternative build of the same C ABI
+        if path is None:
+            if not os.path.exists(LIB):
+                build()
+            path = LIB
+        L = ctypes.CDLL(path)
         vp, i32 = ctypes.c_void_p, ctypes.c_int32
         cp = ctypes.POINTER(Config)
         for name in EXPORTED_SYMBOLS:

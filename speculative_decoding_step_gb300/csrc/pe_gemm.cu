@@ -70,6 +70,59 @@ PE_DEV void epi_elem(const GemmArgs& a, int unit, int t, float v, float v2, floa
   }
 }
 
+// Epilogue of one output unit over up to 16 consecutive tokens t0..t0+nv-1.
+// Every load the epilogue needs (residual values, token positions and slots)
+// is issued before the first store: interleaving them would make each token a
+// separate memory round trip, because the compiler cannot prove the stores and
+// the later loads disjoint.
+template <int EPI, typename T>
+PE_DEV void epi_chunk(const GemmArgs& a, int unit, int t0, int nv, const float (&v)[16], const float (&v2)[16],
+                      float inv_freq) {
+  if (EPI == EPI_STORE_F32) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < nv) a.out_f32[(size_t)(t0 + j) * a.ld_out + unit] = v[j];
+  } else if (EPI == EPI_ADD_F32) {
+    float old[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) old[j] = j < nv ? a.out_f32[(size_t)(t0 + j) * a.ld_out + unit] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < nv) a.out_f32[(size_t)(t0 + j) * a.ld_out + unit] = old[j] + v[j];
+  } else if (EPI == EPI_SWIGLU) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < nv) static_cast<T*>(a.out_act)[(size_t)(t0 + j) * a.ld_out + unit] = from_float<T>(silu(v[j]) * v2[j]);
+  } else if (EPI == EPI_QKV_ROPE) {
+    const int half = a.head_dim >> 1;
+    const int head = unit / half, i = unit - head * half;
+    const bool is_q = head < a.n_q, rotated = head < a.n_q + a.n_kv;
+    int pos[16];
+    long long slot[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      pos[j] = (j < nv && rotated) ? a.tok_pos[t0 + j] : 0;
+      slot[j] = (j < nv && !is_q) ? a.tok_slot[t0 + j] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j >= nv) continue;
+      float x1 = v[j], x2 = v2[j];
+      if (rotated) rope_pair(v[j], v2[j], pos[j], inv_freq, x1, x2);
+      if (is_q) {
+        T* q = static_cast<T*>(a.out_act) + (size_t)(t0 + j) * a.ld_out + (size_t)head * a.head_dim + i;
+        q[0] = from_float<T>(x1);
+        q[half] = from_float<T>(x2);
+      } else if (slot[j] >= 0) {
+        const int g = rotated ? head - a.n_q : head - a.n_q - a.n_kv;
+        T* c = static_cast<T*>(rotated ? a.k_cache : a.v_cache) + ((size_t)slot[j] * a.n_kv + g) * a.head_dim + i;
+        c[0] = from_float<T>(x1);
+        c[half] = from_float<T>(x2);
+      }
+    }
+  }
+}
+
 PE_DEV float rope_inv_freq(const GemmArgs& a, int unit) {
   const int half = a.head_dim >> 1;
   const int i = unit % half;
@@ -162,9 +215,7 @@ template <int EPI>
 PE_DEV void apply16(const GemmArgs& a, int unit, int t0, int n_tok, const float (&v)[16], const float (&v2)[16],
                     float inv_freq) {
   if (unit >= a.n_out) return;
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (t0 + j < n_tok) epi_elem<EPI, __nv_bfloat16>(a, unit, t0 + j, v[j], v2[j], inv_freq);
+  epi_chunk<EPI, __nv_bfloat16>(a, unit, t0, max(0, min(16, n_tok - t0)), v, v2, inv_freq);
 }
 
 PE_DEV unsigned long long umax64(unsigned long long x, unsigned long long y) { return x > y ? x : y; }
@@ -449,24 +500,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int unit = w.tile_f * kTcBM + r;
         const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
         const uint32_t base = smem_u32(smem);
-        for (int col = c0; col < c1; col += 4) {
-          float4 s1 = make_float4(0.f, 0.f, 0.f, 0.f), s2 = s1;
-          for (int p = 0; p < ns; ++p) {  // rank order: the sum does not depend on timing
-            const float4 x = dsmem_ld4(dsmem_map(base + 4u * (uint32_t)(r * ldp + col), (uint32_t)p));
-            s1.x += x.x; s1.y += x.y; s1.z += x.z; s1.w += x.w;
-            if (PAIRED) {
-              const float4 y = dsmem_ld4(dsmem_map(base + 4u * (uint32_t)((kTcBM + r) * ldp + col), (uint32_t)p));
-              s2.x += y.x; s2.y += y.y; s2.z += y.z; s2.w += y.w;
-            }
-          }
-          if (unit < a.n_out) {
-            const float vv[4] = {s1.x, s1.y, s1.z, s1.w}, ww[4] = {s2.x, s2.y, s2.z, s2.w};
+        for (int col0 = c0; col0 < c1; col0 += 16) {
+          const int ncol = min(16, c1 - col0);  // a multiple of 4
+          float v[16], v2[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int t = w.tile_t * BN + col + j;
-              if (t < n_tok) epi_elem<EPI, __nv_bfloat16>(a, unit, t, vv[j], ww[j], inv_freq);
+          for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
+          for (int p = 0; p < ns; ++p) {  // rank order: the sum does not depend on timing
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              if (4 * q4 >= ncol) continue;
+              const float4 x = dsmem_ld4(dsmem_map(base + 4u * (uint32_t)(r * ldp + col0 + 4 * q4), (uint32_t)p));
+              v[4 * q4] += x.x; v[4 * q4 + 1] += x.y; v[4 * q4 + 2] += x.z; v[4 * q4 + 3] += x.w;
+              if (PAIRED) {
+                const float4 y =
+                    dsmem_ld4(dsmem_map(base + 4u * (uint32_t)((kTcBM + r) * ldp + col0 + 4 * q4), (uint32_t)p));
+                v2[4 * q4] += y.x; v2[4 * q4 + 1] += y.y; v2[4 * q4 + 2] += y.z; v2[4 * q4 + 3] += y.w;
+              }
             }
           }
+          const int t0 = w.tile_t * BN + col0;
+          if (unit < a.n_out) epi_chunk<EPI, __nv_bfloat16>(a, unit, t0, max(0, min(ncol, n_tok - t0)), v, v2, inv_freq);
         }
       }
     }
