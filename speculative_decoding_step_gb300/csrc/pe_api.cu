@@ -37,8 +37,8 @@ void trace(int point, cudaStream_t s) {
 }
 
 constexpr int kMaxRows = 1 << 16;        // B*2K
-constexpr int kAttnItemsPerSm = 8;       // attention work items aimed for, per SM (load balance)
-constexpr int kAttnMinChunk = 256;       // shortest position chunk of a work item
+constexpr int kAttnItemsPerSlot = 4;     // attention work items aimed for, per resident CTA (load balance)
+constexpr int kAttnMinChunk = 512;       // shortest position chunk of a work item (bounds the chunks to merge)
 constexpr int kTcMaxStages = 12;
 constexpr int kMaxClusterSplits = 8;     // portable cluster size
 
@@ -141,10 +141,11 @@ Plan make_plan(const pe_config& c) {
   // attention items: the work list aims at attn_target items; rounding adds at
   // most one per (sequence, kv head), and no (sequence, kv head) can have more
   // chunks than its longest possible range holds minimum chunks
-  p.attn_target = kAttnItemsPerSm * p.sms;
+  const int attn_slots = (c.head_dim == 64 ? 2 : 1) * p.sms;  // resident attention CTAs
+  p.attn_target = kAttnItemsPerSlot * attn_slots;
   const long long per_pair = ((long long)c.max_pages_per_seq * c.page_size + kAttnMinChunk - 1) / kAttnMinChunk;
   p.max_items = (int)std::min<long long>(p.attn_target + (long long)c.B * c.n_kv, per_pair * c.B * c.n_kv);
-  p.attn_grid = std::min(p.max_items, (c.head_dim == 64 ? 2 : 1) * p.sms);
+  p.attn_grid = std::min(p.max_items, attn_slots);
 
   const size_t eb = elem_bytes(c.dtype);
   size_t off = 0;
@@ -163,7 +164,7 @@ Plan make_plan(const pe_config& c) {
   p.n_chunks = take(4 * (size_t)c.B);
   p.n_items = take(4);
   p.items = take(16 * (size_t)p.max_items);
-  p.done = take(4);  // LM-head completion counter
+  p.done = take(4 * (1 + (size_t)c.B * c.n_kv));  // LM-head completion counter, then attention chunk counters
   p.keys = take(8 * (size_t)p.T);
   p.x = take(4 * (size_t)p.R * c.d);
   p.y = take(eb * (size_t)p.R * c.d);
@@ -245,6 +246,14 @@ bool tmap_qkv(CUtensorMap* m, const void* base, uint64_t heads, uint64_t hd, uin
   const uint64_t strides[3] = {d * 2, half * d * 2, hd * d * 2};
   const uint32_t box[4] = {(uint32_t)kTcBK, (uint32_t)half, 1, (uint32_t)(kTcBM / half)};
   return make_tmap(m, base, 4, dims, strides, box);
+}
+
+// paged K or V pool [num_pages*16][n_kv][hd] as a 3-D tensor (hd innermost); box = 64 dims x 1 head x 16 positions
+bool tmap_kv(CUtensorMap* m, const void* base, const pe_config& c, int num_pages) {
+  const uint64_t dims[3] = {(uint64_t)c.head_dim, (uint64_t)c.n_kv, (uint64_t)num_pages * c.page_size};
+  const uint64_t strides[2] = {(uint64_t)c.head_dim * 2, (uint64_t)c.n_kv * c.head_dim * 2};
+  const uint32_t box[3] = {64, 1, (uint32_t)c.page_size};
+  return make_tmap(m, base, 3, dims, strides, box);
 }
 
 // ----------------------------------------------------------------------------- validation
@@ -371,7 +380,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   ia.target_items = p.attn_target; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
   ia.items = at<int4>(ws, p.items); ia.n_items = at<int32_t>(ws, p.n_items);
   ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
-  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1;
+  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1 + c.B * c.n_kv;
   ia.keys = at<unsigned long long>(ws, p.keys); ia.err = err;
   PE_TRY_CUDA(launch_forward_init(ia, s));
   trace(3, s);
@@ -411,6 +420,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   at_.part_l = bf16 ? at<float>(ws, p.part_l) : nullptr;
   at_.part_o = bf16 ? at<float>(ws, p.part_o) : nullptr;
   at_.out = ao; at_.n_rows = p.R; at_.err = err;
+  at_.counters = at<int32_t>(ws, p.done) + 1;
 
   for (int l = 0; l < c.n_layers; ++l) {
     const int tp = 5 + 7 * l;
@@ -428,8 +438,10 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     at_.k_cache = kv->k_cache[l];
     at_.v_cache = kv->v_cache[l];
     if (bf16) {
-      PE_TRY_CUDA(launch_attention_bf16(at_, p.attn_grid, s));
-      PE_TRY_CUDA(launch_attention_combine_bf16(at_, s));
+      CUtensorMap tk, tv;
+      if (!tmap_kv(&tk, kv->k_cache[l], c, kv->num_pages) || !tmap_kv(&tv, kv->v_cache[l], c, kv->num_pages))
+        return PE_ERR_CUDA;
+      PE_TRY_CUDA(launch_attention_bf16(tk, tv, at_, p.attn_grid, s));
     } else {
       PE_TRY_CUDA(launch_attention_f32(at_, s));
     }

@@ -25,6 +25,9 @@ PE_DEV void set_err(int32_t* err, int32_t code) {
 
 PE_DEV uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
+// Barrier among `n` threads (whole warps) of the CTA, on hardware barrier `id` (0 is __syncthreads).
+PE_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
 PE_DEV uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -137,7 +137,6 @@ PE_DEV void argmax_finish(const GemmArgs& a, int n_tok, int thread, int nthreads
   }
 }
 
-PE_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 // ============================================================================= tensor-core kernel
 //

@@ -201,13 +201,15 @@ struct AttnArgs {
   const int4* items;         // (b, g, c0, c1)
   const int32_t *n_items, *item_base, *n_chunks;
   float *part_m, *part_l, *part_o;  // [items][128], [items][128], [items][128][hd]
+  int32_t* counters;         // [B][n_kv] finished chunks (zero before the launch, left at zero)
   void* out;                 // [rows][n_q*hd]
   int n_rows;                // host upper bound on rows
   int32_t* err;
 };
 constexpr int kAttnRows = 128;    // query rows (row x GQA head) per work item
-cudaError_t launch_attention_bf16(const AttnArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_attention_combine_bf16(const AttnArgs& a, cudaStream_t s);
+// tmK / tmV: the layer's K and V pools as bf16 [num_pages*16][n_kv][hd], 128-byte swizzle, box 64 x 1 x 16.
+cudaError_t launch_attention_bf16(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a, int grid,
+                                  cudaStream_t s);
 cudaError_t launch_attention_f32(const AttnArgs& a, cudaStream_t s);
 
 }  // namespace pe
