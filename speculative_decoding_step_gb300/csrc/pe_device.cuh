@@ -216,12 +216,13 @@ PE_DEV uint32_t dsmem_map(uint32_t local_smem, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
   return r;
 }
+// No memory clobber: the compiler may batch these loads and schedule their
+// consumers later; volatile keeps them after the preceding cluster barrier.
 PE_DEV float4 dsmem_ld4(uint32_t cluster_addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(cluster_addr)
-               : "memory");
+               : "r"(cluster_addr));
   return v;
 }
 

@@ -505,15 +505,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
           for (int p = 0; p < ns; ++p) {  // rank order: the sum does not depend on timing
+            const uint32_t peer = dsmem_map(base, (uint32_t)p);
+            float4 x[4], y[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {  // every load of this rank first, then the adds
+              if (4 * q4 < ncol) {
+                x[q4] = dsmem_ld4(peer + 4u * (uint32_t)(r * ldp + col0 + 4 * q4));
+                if (PAIRED) y[q4] = dsmem_ld4(peer + 4u * (uint32_t)((kTcBM + r) * ldp + col0 + 4 * q4));
+              }
+            }
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-              if (4 * q4 >= ncol) continue;
-              const float4 x = dsmem_ld4(dsmem_map(base + 4u * (uint32_t)(r * ldp + col0 + 4 * q4), (uint32_t)p));
-              v[4 * q4] += x.x; v[4 * q4 + 1] += x.y; v[4 * q4 + 2] += x.z; v[4 * q4 + 3] += x.w;
-              if (PAIRED) {
-                const float4 y =
-                    dsmem_ld4(dsmem_map(base + 4u * (uint32_t)((kTcBM + r) * ldp + col0 + 4 * q4), (uint32_t)p));
-                v2[4 * q4] += y.x; v2[4 * q4 + 1] += y.y; v2[4 * q4 + 2] += y.z; v2[4 * q4 + 3] += y.w;
+              if (4 * q4 < ncol) {
+                v[4 * q4] += x[q4].x; v[4 * q4 + 1] += x[q4].y; v[4 * q4 + 2] += x[q4].z; v[4 * q4 + 3] += x[q4].w;
+                if (PAIRED) {
+                  v2[4 * q4] += y[q4].x; v2[4 * q4 + 1] += y[q4].y; v2[4 * q4 + 2] += y[q4].z; v2[4 * q4 + 3] += y[q4].w;
+                }
               }
             }
           }

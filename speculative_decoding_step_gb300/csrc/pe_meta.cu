@@ -208,33 +208,52 @@ __global__ void __launch_bounds__(kInitThreads) forward_init_kernel(const InitAr
   __syncthreads();
   // Attention work list: every (sequence, kv head) splits its causal range
   // 0..maxpos into equal chunks; the chunk length is set so that the whole
-  // batch yields about target_items items.
+  // batch yields about target_items items.  Total length by a block reduction,
+  // per-sequence item offsets by a warp scan (both in fixed order).
+  __shared__ long long red_s[kInitThreads / 32];
   __shared__ int chunk_s;
-  if (tid == 0) {
+  long long part = 0;
+  for (int b = tid; b < a.B; b += blockDim.x) part += a.seq_len[b] > 0 ? a.seq_maxpos[b] + 1 : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+  if ((tid & 31) == 0) red_s[tid >> 5] = part;
+  __syncthreads();
+  if (tid < 32) {
     long long total = 0;
-    for (int b = 0; b < a.B; ++b)
-      if (a.seq_len[b] > 0) total += a.seq_maxpos[b] + 1;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += red_s[w];
     long long per = (total * a.n_kv + a.target_items - 1) / a.target_items;
     per = ((per + 63) / 64) * 64;
-    int chunk = (int)(per < a.min_chunk ? a.min_chunk : per);
-    int it = 0;
-    for (int b = 0; b < a.B; ++b) {
-      const int L = a.seq_len[b] > 0 ? a.seq_maxpos[b] + 1 : 0;
+    const int chunk = (int)(per < a.min_chunk ? a.min_chunk : per);
+    int carry = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+      const int b = b0 + tid;
+      const int L = (b < a.B && a.seq_len[b] > 0) ? a.seq_maxpos[b] + 1 : 0;
       const int nc = (L + chunk - 1) / chunk;
-      a.n_chunks[b] = nc;
-      a.item_base[b] = it;
-      it += nc * a.n_kv;
+      const int v = nc * a.n_kv;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (tid >= o) incl += n;
+      }
+      if (b < a.B) {
+        a.n_chunks[b] = nc;
+        a.item_base[b] = carry + incl - v;
+      }
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
-    if (it > a.max_items) {   // cannot happen with the host's sizing; keep the list in bounds
-      set_err(a.err, PE_DEV_BAD_ROW);
-      it = 0;
-      for (int b = 0; b < a.B; ++b) a.n_chunks[b] = 0;
+    if (tid == 0) {
+      if (carry > a.max_items) {  // cannot happen with the host's sizing; keep the list in bounds
+        set_err(a.err, PE_DEV_BAD_ROW);
+        carry = 0;
+      }
+      *a.n_items = carry;
+      chunk_s = chunk;
     }
-    *a.n_items = it;
-    chunk_s = chunk;
   }
   __syncthreads();
   const int chunk = chunk_s;
+  if (*a.n_items == 0) return;
   for (int b = tid; b < a.B; b += blockDim.x) {
     const int L = a.seq_len[b] > 0 ? a.seq_maxpos[b] + 1 : 0;
     const int nc = a.n_chunks[b];
