@@ -95,7 +95,7 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   const long long avail = kTcSmemOptIn - 1024 - kTcCtrlBytes - (long long)red * 8;
   g.stages = (int)std::min<long long>(kTcMaxStages, avail / g.stage_bytes);
   g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, red);
-  const size_t partial_bytes = (size_t)(paired ? 2 : 1) * kTcBM * (g.bn + 4) * 4;
+  const size_t partial_bytes = (size_t)(paired ? 2 : 1) * kTcBM * g.bn * 4;
   if (epi != EPI_ARGMAX && g.tiles < sms && partial_bytes <= (size_t)g.stages * g.stage_bytes) {
     int s = std::min(kMaxClusterSplits, std::min(sms / g.tiles, std::max(1, g.kb_total / 4)));
     for (; s > 1; --s) {

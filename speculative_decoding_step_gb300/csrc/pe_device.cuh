@@ -218,11 +218,9 @@ PE_DEV uint32_t dsmem_map(uint32_t local_smem, uint32_t rank) {
 }
 // No memory clobber: the compiler may batch these loads and schedule their
 // consumers later; volatile keeps them after the preceding cluster barrier.
-PE_DEV float4 dsmem_ld4(uint32_t cluster_addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(cluster_addr));
+PE_DEV float dsmem_ld1(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
   return v;
 }
 

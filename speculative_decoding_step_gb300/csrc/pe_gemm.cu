@@ -9,7 +9,7 @@
 // token rows on its N side, so a batch of 16..256 rows reads every weight
 // byte once.  Split-K spreads small matrices over all SMs; the splits of a
 // tile form a thread-block cluster and sum their partials through distributed
-// shared memory in rank order, so the result does not depend on scheduling.
+// shared memory in a fixed order, so the result does not depend on scheduling.
 // The LM head never writes logits: each
 // CTA reduces its 128 vocabulary rows to a (max, argmax) key per token and
 // folds it into a global 64-bit atomicMax; the last CTA decodes the keys.
@@ -151,8 +151,9 @@ PE_DEV void argmax_finish(const GemmArgs& a, int n_tok, int thread, int nthreads
 // Split K: the k_splits CTAs of one tile form a thread-block cluster (one unit
 // per CTA).  Each leaves its fp32 partial tile in its own shared memory; after
 // a cluster barrier, CTA rank q sums a 1/k_splits slice of the tile's columns
-// over all ranks through distributed shared memory, in rank order, and runs
-// the epilogue on it.  No partial sums leave the chip and no CTA waits for a
+// over all ranks through distributed shared memory (starting at its own rank and
+// walking the ring, so each CTA's shared memory serves one reader at a time),
+// and runs the epilogue on it.  No partial sums leave the chip and no CTA waits for a
 // straggler.
 
 size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int red_entries) {
@@ -286,7 +287,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* last_flag = abort_flag + 1;
   unsigned long long* red = reinterpret_cast<unsigned long long*>(ctrl + kTcCtrlBytes);  // [4 warps][NT]
   const uint32_t b_off = (PAIRED ? 2u : 1u) * A_BYTES;
-  const int ldp = BN + 4;  // row stride of a split's partial tile in shared memory (floats)
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmW);
@@ -437,20 +437,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       } else if (ok) {
         // split K (one unit per CTA, the stage ring is idle): leave this split's partial
-        // tile [rows][BN] fp32 in shared memory for the cluster reduction below
+        // tile in shared memory for the cluster reduction below, column-major
+        // ([plane][token column][128 rows] fp32) so a warp's 32 rows of one column are
+        // 128 contiguous bytes: conflict-free here, one packet per remote load there
         float* P = reinterpret_cast<float*>(smem);
         for (int c = 0; c < BN / 16; ++c) {
           float v[16];
           tmem_load16(tl + (uint32_t)(c * 16), v);
-          float4* dst = reinterpret_cast<float4*>(P + (size_t)r * ldp + c * 16);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          for (int j = 0; j < 16; ++j) P[(size_t)(c * 16 + j) * kTcBM + r] = v[j];
           if (PAIRED) {
             tmem_load16(tl + (uint32_t)(BN + c * 16), v);
-            float4* dst2 = reinterpret_cast<float4*>(P + (size_t)(kTcBM + r) * ldp + c * 16);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst2[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            for (int j = 0; j < 16; ++j) P[(size_t)(BN + c * 16 + j) * kTcBM + r] = v[j];
           }
         }
       }
@@ -499,29 +498,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int unit = w.tile_f * kTcBM + r;
         const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
         const uint32_t base = smem_u32(smem);
+        // Rank p starts at its own tile and walks the ring (rank + j) % ns: at any moment
+        // every CTA's shared memory serves one reader, not the whole cluster.  The order
+        // of the sum is fixed per output column, so the result does not depend on timing.
+        // The loads of the next peer are in flight while the current one is added.
         for (int col0 = c0; col0 < c1; col0 += 16) {
           const int ncol = min(16, c1 - col0);  // a multiple of 4
           float v[16], v2[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
-          for (int p = 0; p < ns; ++p) {  // rank order: the sum does not depend on timing
-            const uint32_t peer = dsmem_map(base, (uint32_t)p);
-            float4 x[4], y[4];
+          float x[2][16], y[2][16];
+          auto load_peer = [&](int j, float* xd, float* yd) {
+            const uint32_t peer = dsmem_map(base, (rank + (uint32_t)j) % (uint32_t)ns);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {  // every load of this rank first, then the adds
-              if (4 * q4 < ncol) {
-                x[q4] = dsmem_ld4(peer + 4u * (uint32_t)(r * ldp + col0 + 4 * q4));
-                if (PAIRED) y[q4] = dsmem_ld4(peer + 4u * (uint32_t)((kTcBM + r) * ldp + col0 + 4 * q4));
+            for (int q = 0; q < 16; ++q) {
+              if (q < ncol) {
+                xd[q] = dsmem_ld1(peer + 4u * (uint32_t)((col0 + q) * kTcBM + r));
+                if (PAIRED) yd[q] = dsmem_ld1(peer + 4u * (uint32_t)((BN + col0 + q) * kTcBM + r));
               }
             }
+          };
+          auto add_peer = [&](const float* xs, const float* ys) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              if (4 * q4 < ncol) {
-                v[4 * q4] += x[q4].x; v[4 * q4 + 1] += x[q4].y; v[4 * q4 + 2] += x[q4].z; v[4 * q4 + 3] += x[q4].w;
-                if (PAIRED) {
-                  v2[4 * q4] += y[q4].x; v2[4 * q4 + 1] += y[q4].y; v2[4 * q4 + 2] += y[q4].z; v2[4 * q4 + 3] += y[q4].w;
-                }
+            for (int q = 0; q < 16; ++q) {
+              if (q < ncol) {
+                v[q] += xs[q];
+                if (PAIRED) v2[q] += ys[q];
               }
+            }
+          };
+          load_peer(0, x[0], y[0]);
+          for (int j = 0; j < ns; j += 2) {  // two peers per trip keeps the buffers in registers
+            if (j + 1 < ns) load_peer(j + 1, x[1], y[1]);
+            add_peer(x[0], y[0]);
+            if (j + 1 < ns) {
+              if (j + 2 < ns) load_peer(j + 2, x[0], y[0]);
+              add_peer(x[1], y[1]);
             }
           }
           const int t0 = w.tile_t * BN + col0;
