@@ -164,7 +164,7 @@ Plan make_plan(const pe_config& c) {
   p.n_chunks = take(4 * (size_t)c.B);
   p.n_items = take(4);
   p.items = take(16 * (size_t)p.max_items);
-  p.done = take(4 * (1 + (size_t)c.B * c.n_kv));  // LM-head completion counter, then attention chunk counters
+  p.done = take(4);  // LM-head completion counter
   p.keys = take(8 * (size_t)p.T);
   p.x = take(4 * (size_t)p.R * c.d);
   p.y = take(eb * (size_t)p.R * c.d);
@@ -380,7 +380,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   ia.target_items = p.attn_target; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
   ia.items = at<int4>(ws, p.items); ia.n_items = at<int32_t>(ws, p.n_items);
   ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
-  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1 + c.B * c.n_kv;
+  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1;
   ia.keys = at<unsigned long long>(ws, p.keys); ia.err = err;
   PE_TRY_CUDA(launch_forward_init(ia, s));
   trace(3, s);
@@ -411,7 +411,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   na.eps = c.rms_eps; na.y = y; na.err = err;
 
   AttnArgs at_{};
-  at_.n_q = c.n_q; at_.n_kv = c.n_kv; at_.head_dim = hd; at_.max_pages = c.max_pages_per_seq;
+  at_.B = c.B; at_.n_q = c.n_q; at_.n_kv = c.n_kv; at_.head_dim = hd; at_.max_pages = c.max_pages_per_seq;
   at_.page_size = c.page_size; at_.num_pages = kv->num_pages; at_.scale = 1.0f / sqrtf((float)hd);
   at_.q = qb; at_.block_table = block_table; at_.tok_pos = ia.tok_pos; at_.tok_seq = ia.tok_seq;
   at_.seq_start = ia.seq_start; at_.seq_len = ia.seq_len; at_.n_valid = n_valid; at_.items = ia.items;
@@ -420,7 +420,6 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   at_.part_l = bf16 ? at<float>(ws, p.part_l) : nullptr;
   at_.part_o = bf16 ? at<float>(ws, p.part_o) : nullptr;
   at_.out = ao; at_.n_rows = p.R; at_.err = err;
-  at_.counters = at<int32_t>(ws, p.done) + 1;
 
   for (int l = 0; l < c.n_layers; ++l) {
     const int tp = 5 + 7 * l;
@@ -441,7 +440,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
       CUtensorMap tk, tv;
       if (!tmap_kv(&tk, kv->k_cache[l], c, kv->num_pages) || !tmap_kv(&tv, kv->v_cache[l], c, kv->num_pages))
         return PE_ERR_CUDA;
-      PE_TRY_CUDA(launch_attention_bf16(tk, tv, at_, p.attn_grid, s));
+      PE_TRY_CUDA(launch_attention_bf16(tk, tv, at_, p.attn_grid, p.sms, s));
     } else {
       PE_TRY_CUDA(launch_attention_f32(at_, s));
     }

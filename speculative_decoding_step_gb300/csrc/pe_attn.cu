@@ -7,17 +7,23 @@
 // bf16: one work item = (sequence b, kv head g, position chunk [c0, c1)).
 // The query tile packs every valid row of the sequence times the n_q/n_kv
 // query heads of g (<= 128 query vectors), so each KV page is read once per
-// (sequence, kv head).  One producer warp streams the chunk's K and V pages
-// with 3-D TMA loads (one 16-position page per load, 128-byte swizzle,
-// pages past the range zero-filled) into a 4-stage mbarrier ring; eight
-// compute warps run QK^T and PV on warp-level tensor-core MMAs (m16n8k16
-// bf16, fp32 accumulate) with an online softmax, without any block-wide
-// barrier in the loop.  A range in one chunk is written directly; otherwise
-// every chunk leaves (max, sum, unnormalised output) partials and the last
-// chunk to finish merges them in chunk order (deterministic).
+// (sequence, kv head).  Warp 0 streams the chunk's K and V pages with 3-D TMA
+// loads (one 16-position page per load, 128-byte swizzle, pages past the
+// range zero-filled) into a 4-stage mbarrier ring of 64-position blocks.
+// Warp 1 issues the 5th-generation tensor-core MMAs: S = Q K^T (M = 128 query
+// vectors, N = 64 positions) into one of two TMEM buffers, and O += P V with
+// P read from TMEM and V as an MN-major operand straight from the ring.
+// Warps 2..5 own one query vector each (its TMEM lane): mask, exponentiate
+// (log2 domain) and write P as bf16 over the first half of S's columns.  A
+// row's reference maximum only moves when a block exceeds it by 2^8, and then
+// O is rescaled in TMEM, so the common block is one read of S and one write
+// of P per row.  A range in one chunk is written directly; otherwise every
+// chunk leaves (reference max, sum, unnormalised output) partials that a
+// second, GPU-wide kernel merges in chunk order (deterministic).
 //
 // fp32: one warp per (row, query head); lanes stride over positions with an
 // online softmax each, then merge.
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 
@@ -28,34 +34,26 @@ namespace pe {
 
 namespace {
 
-PE_DEV void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-PE_DEV void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-PE_DEV void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 PE_DEV uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// A wait's outcome, made the same for the whole warp (warp-collective
+// instructions follow it).
+PE_DEV bool warp_ok(bool ok) { return __all_sync(0xFFFFFFFFu, ok); }
+
 }  // namespace
 
-constexpr int kAttnBlk = 64;            // kv positions per pipeline stage (4 pages)
-constexpr int kAttnStages = 4;          // stages in flight
-constexpr int kAttnComputeWarps = 8;    // 16 query rows each
-constexpr int kAttnThreads = 32 * (kAttnComputeWarps + 1);  // + one TMA producer warp
+constexpr int kAttnBlk = 64;          // kv positions per pipeline stage (4 pages) = MMA N of S
+constexpr int kAttnStages = 4;        // stages in flight
+constexpr int kAttnThreads = 192;     // warp 0: TMA, warp 1: MMA, warps 2..5: softmax (thread = query row)
+constexpr int kAttnSoftmax = 128;     // softmax threads
+constexpr uint32_t kAttnTmemCols = 256;  // S double buffer (2 x 64 columns) + O (head_dim columns)
+constexpr uint32_t kAttnTmemO = 2 * kAttnBlk;
+// Lazy rescaling: a row keeps its reference maximum until a block's maximum
+// exceeds it by more than this (log2 units), so P <= 2^8 and O is rescaled rarely.
+constexpr float kAttnRescaleLog2 = 8.f;
 
 // Shared-memory tile [HD/64 halves][ROWS][64 bf16]: 128-byte rows with the
 // 128-byte swizzle that TMA applies (16-byte unit c of row r sits at c ^ (r % 8)).
@@ -70,8 +68,23 @@ struct AttnLayout {
   static constexpr uint32_t KV = kAttnBlk * HD * 2;      // K (or V) of one stage
   static constexpr uint32_t STAGE = 2 * KV;
   static constexpr uint32_t BARS = Q + kAttnStages * STAGE;
-  static constexpr uint32_t TOTAL = 1024 + BARS + 128;   // + alignment slack
+  static constexpr uint32_t TOTAL = 1024 + BARS + 256;   // + alignment slack
 };
+
+// Barriers and flags after the tiles.
+struct AttnCtrl {
+  uint64_t full[kAttnStages], empty[kAttnStages];
+  uint64_t q_full;      // softmax threads staged the item's query tile
+  uint64_t s_full[2];   // S of a block is in TMEM buffer (block & 1)
+  uint64_t p_full[2];   // P of a block is in TMEM (over its S), O rescaled where needed
+  uint64_t pv_done;     // one phase per PV product
+  uint64_t o_free;      // softmax threads read O of the item
+  uint64_t drain;       // every MMA issued has completed
+  uint32_t tmem;
+  int abort;
+};
+
+static_assert(sizeof(AttnCtrl) <= 256, "attention control block");
 
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, HD == 64 ? 2 : 1)
@@ -84,9 +97,8 @@ __global__ void __launch_bounds__(kAttnThreads, HD == 64 ? 2 : 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(sm);
   const uint32_t sRing = sQ + Lay::Q;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
-  uint64_t* empty = full + S;
-  volatile int* last_s = reinterpret_cast<volatile int*>(empty + S);
+  AttnCtrl* ctl = reinterpret_cast<AttnCtrl*>(sm + Lay::BARS);
+  volatile int* abort_flag = &ctl->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.n_q / a.n_kv;
 
@@ -94,79 +106,170 @@ __global__ void __launch_bounds__(kAttnThreads, HD == 64 ? 2 : 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), kAttnComputeWarps);
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
+    mbar_init(smem_u32(&ctl->q_full), kAttnSoftmax);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl->s_full[b]), 1);
+      mbar_init(smem_u32(&ctl->p_full[b]), kAttnSoftmax);
+    }
+    mbar_init(smem_u32(&ctl->pv_done), 1);
+    mbar_init(smem_u32(&ctl->o_free), kAttnSoftmax);
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
     fence_mbar_init();
   }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem), kAttnTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
   pdl_wait();
   pdl_trigger();
   const int n_items = *a.n_items;
 
-  if (warp == kAttnComputeWarps) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();  // the prefix is read once per round
-      const int oob = a.num_pages * a.page_size;     // a row past the pool: TMA fills zeros
-      int gi = 0;
-      bool stop = false;
-      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
-        const int4 item = a.items[it];
-        const int b = item.x, g = item.y, c0 = item.z, c1 = item.w;
-        const int nblk = (c1 - c0 + kAttnBlk - 1) / kAttnBlk;
-        for (int blk = 0; blk < nblk; ++blk, ++gi) {
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer (whole warp)
+    // The warp reads the page ids of 8 blocks (32 pages) at once, one per lane;
+    // lane 0 then issues the TMA loads.  Reading them one at a time would put an
+    // L2 round trip in front of every page.
+    const uint64_t pol = l2_policy_evict_first();  // the prefix is read once per round
+    const int oob = a.num_pages * a.page_size;     // a row past the pool: TMA fills zeros
+    constexpr int kPagesPerBlk = kAttnBlk / 16;
+    constexpr int kBlkPerBatch = 32 / kPagesPerBlk;
+    int gi = 0;
+    bool stop = false;
+    for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+      const int4 item = a.items[it];
+      const int b = item.x, g = item.y, c0 = item.z, c1 = item.w;
+      const int nblk = (c1 - c0 + kAttnBlk - 1) / kAttnBlk;
+      for (int blk0 = 0; blk0 < nblk && !stop; blk0 += kBlkPerBatch) {
+        const int pos0 = c0 + (blk0 * kPagesPerBlk + lane) * 16;
+        int y = oob;
+        if (pos0 < c1) {
+          const int pi = pos0 / a.page_size;
+          if (pi >= a.max_pages) {
+            set_err(a.err, PE_DEV_BAD_POSITION);
+          } else {
+            const int page = __ldg(a.block_table + (size_t)b * a.max_pages + pi);
+            if (page < 0 || page >= a.num_pages) set_err(a.err, PE_DEV_BAD_PAGE);
+            else y = page * a.page_size;
+          }
+        }
+        const int nb = min(kBlkPerBatch, nblk - blk0);
+        for (int bb = 0; bb < nb; ++bb, ++gi) {
           const int s = gi % S;
-          const uint32_t use = (uint32_t)(gi / S);
-          if (gi >= S && !mbar_wait(smem_u32(empty + s), (use & 1u) ^ 1u, a.err, nullptr)) {
+          bool ok = true;
+          if (lane == 0 && gi >= S)
+            ok = mbar_wait(smem_u32(&ctl->empty[s]), ((uint32_t)(gi / S) & 1u) ^ 1u, a.err, abort_flag);
+          if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
             stop = true;
             break;
           }
-          const uint32_t fb = smem_u32(full + s);
-          mbar_expect_tx(fb, Lay::STAGE);
+          const uint32_t fb = smem_u32(&ctl->full[s]);
           const uint32_t kdst = sRing + (uint32_t)s * Lay::STAGE;
+          if (lane == 0) mbar_expect_tx(fb, Lay::STAGE);
 #pragma unroll
-          for (int p = 0; p < kAttnBlk / 16; ++p) {
-            const int pos0 = c0 + blk * kAttnBlk + p * 16;
-            int y = oob;
-            if (pos0 < c1) {
-              const int pi = pos0 / a.page_size;
-              if (pi >= a.max_pages) {
-                set_err(a.err, PE_DEV_BAD_POSITION);
-              } else {
-                const int page = a.block_table[(size_t)b * a.max_pages + pi];
-                if (page < 0 || page >= a.num_pages) set_err(a.err, PE_DEV_BAD_PAGE);
-                else y = page * a.page_size;
+          for (int p = 0; p < kPagesPerBlk; ++p) {
+            const int yp = __shfl_sync(0xFFFFFFFFu, y, bb * kPagesPerBlk + p);
+            if (lane == 0) {
+#pragma unroll
+              for (int h = 0; h < HD / 64; ++h) {
+                const uint32_t off = (uint32_t)(h * kAttnBlk * 128 + p * 16 * 128);
+                tma_load_3d(kdst + off, &tmK, fb, h * 64, g, yp, pol);
+                tma_load_3d(kdst + Lay::KV + off, &tmV, fb, h * 64, g, yp, pol);
               }
-            }
-#pragma unroll
-            for (int h = 0; h < HD / 64; ++h) {
-              const uint32_t off = (uint32_t)(h * kAttnBlk * 128 + p * 16 * 128);
-              tma_load_3d(kdst + off, &tmK, fb, h * 64, g, y, pol);
-              tma_load_3d(kdst + Lay::KV + off, &tmV, fb, h * 64, g, y, pol);
             }
           }
         }
       }
     }
+    if (stop && lane == 0) {
+      // leave no bulk copy in flight into this CTA's shared memory
+      for (int i = (gi > S ? gi - S : 0); i < gi; ++i)
+        mbar_wait(smem_u32(&ctl->full[i % S]), (uint32_t)(i / S) & 1u, a.err, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16(kAttnRows, kAttnBlk);                 // S = Q K^T: N = positions
+      const uint32_t id_o = idesc_bf16(kAttnRows, HD) | kIdescTransposeB;   // O += P V: V is MN-major
+      int gi = 0, ii = 0;
+      bool stop = false;
+      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x, ++ii) {
+        const int4 item = a.items[it];
+        const int nblk = (item.w - item.z + kAttnBlk - 1) / kAttnBlk;
+        if (!mbar_wait(smem_u32(&ctl->q_full), (uint32_t)ii & 1u, a.err, abort_flag)) break;
+        tc_fence_after();
+        // S of block j is issued one block ahead of the PV product of block j - 1
+        for (int j = 0; j <= nblk; ++j) {
+          if (j < nblk) {
+            const int x = gi + j, s = x % S;
+            if (!mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)(x / S) & 1u, a.err, abort_flag)) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t kbase = sRing + (uint32_t)s * Lay::STAGE;
+            const uint32_t d = tmem + (uint32_t)((x & 1) * kAttnBlk);
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+              const uint64_t ad = sdesc_k_sw128(sQ + (uint32_t)((kk >> 2) * kAttnRows * 128)) + 2 * (kk & 3);
+              const uint64_t bd = sdesc_k_sw128(kbase + (uint32_t)((kk >> 2) * kAttnBlk * 128)) + 2 * (kk & 3);
+              tc_mma_bf16(d, ad, bd, id_s, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(smem_u32(&ctl->s_full[x & 1]));
+          }
+          if (j >= 1) {
+            const int x = gi + j - 1, s = x % S;
+            if (j == 1 && ii > 0 &&
+                !mbar_wait(smem_u32(&ctl->o_free), (uint32_t)(ii - 1) & 1u, a.err, abort_flag)) {
+              stop = true;
+              break;
+            }
+            if (!mbar_wait(smem_u32(&ctl->p_full[x & 1]), (uint32_t)(x >> 1) & 1u, a.err, abort_flag)) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t vbase = sRing + (uint32_t)s * Lay::STAGE + Lay::KV;
+            const uint32_t pa = tmem + (uint32_t)((x & 1) * kAttnBlk);
+#pragma unroll
+            for (int kk = 0; kk < kAttnBlk / 16; ++kk)
+              tc_mma_bf16_tmem_a(tmem + kAttnTmemO, pa + 8u * kk,
+                                 sdesc_mn_sw128(vbase + (uint32_t)kk * 2048u, kAttnBlk * 128), id_o,
+                                 (j > 1 || kk > 0) ? 1u : 0u);
+            tc_commit(smem_u32(&ctl->pv_done));
+            tc_commit(smem_u32(&ctl->empty[s]));
+          }
+        }
+        gi += nblk;
+      }
+      // TMEM is freed only after every MMA issued here has completed
+      tc_commit(smem_u32(&ctl->drain));
+      mbar_wait(smem_u32(&ctl->drain), 0, a.err, nullptr);
+    }
   } else {
-    // ------------------------------------------------------------------ compute warps
-    const float scale_log2 = a.scale * 1.4426950408889634f;
+    // ------------------------------------------------------------------ softmax + epilogue (warps 2..5)
+    const int et = tid - 64;                        // 0..127
+    const int r = (warp & 3) * 32 + lane;           // query row = TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const float sl2 = a.scale * 1.4426950408889634f;
     const __nv_bfloat16* qbuf = static_cast<const __nv_bfloat16*>(a.q);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
     const int ldq = a.n_q * HD;
-    int gi = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-      const int4 item = a.items[it];
-      const int b = item.x, g = item.y, c0 = item.z, c1 = item.w;
-      const int start = a.seq_start[b], nb = a.seq_len[b];
-      const int M = min(nb * G, kAttnRows);
-      const int nblk = (c1 - c0 + kAttnBlk - 1) / kAttnBlk;
-      const int nc = a.n_chunks[b];
 
-      // query tile: row m = (row m / G of the sequence, head g*G + m % G); zeros past the valid rows
-      named_bar_sync(1, 32 * kAttnComputeWarps);  // every warp holds its fragments of the previous tile
-      for (int idx = tid; idx < kAttnRows * CH; idx += 32 * kAttnComputeWarps) {
+    // query tile: row m = (row m / G of the sequence, head g*G + m % G); zeros past the valid rows
+    auto stage_q = [&](int it) {
+      const int4 item = a.items[it];
+      const int b = item.x, g = item.y;
+      const int start = a.seq_start[b];
+      const int M = min(a.seq_len[b] * G, kAttnRows);
+      for (int idx = et; idx < kAttnRows * CH; idx += kAttnSoftmax) {
         const int m = idx / CH, ch = idx - (idx / CH) * CH;
         uint4 val = make_uint4(0, 0, 0, 0);
         if (m < M) {
@@ -177,203 +280,151 @@ __global__ void __launch_bounds__(kAttnThreads, HD == 64 ? 2 : 1)
                      "r"(val.y), "r"(val.z), "r"(val.w)
                      : "memory");
       }
-      named_bar_sync(1, 32 * kAttnComputeWarps);
+      fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+      mbar_arrive(smem_u32(&ctl->q_full));
+    };
+    if ((int)blockIdx.x < n_items) stage_q(blockIdx.x);
 
-      const bool active = warp * 16 < M;
-      const int r0 = warp * 16 + (lane >> 2), r1 = r0 + 8;
-      const int p0 = r0 < M ? a.tok_pos[start + r0 / G] : -1;
-      const int p1 = r1 < M ? a.tok_pos[start + r1 / G] : -1;
-      // smallest causal bound of the warp's rows; rows past M bound nothing (they are discarded)
-      int pmin = min(r0 < M ? p0 : INT_MAX, r1 < M ? p1 : INT_MAX);
+    int gi = 0;
+    bool stop = false;
+    for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+      const int4 item = a.items[it];
+      const int b = item.x, g = item.y, c0 = item.z, c1 = item.w;
+      const int start = a.seq_start[b];
+      const int M = min(a.seq_len[b] * G, kAttnRows);
+      const int nblk = (c1 - c0 + kAttnBlk - 1) / kAttnBlk;
+      const int nc = a.n_chunks[b];
+      const bool valid = r < M;
+      // causal bound: positions <= lim (row's own position, clipped to the chunk)
+      const int lim = valid ? min(a.tok_pos[start + r / G], c1 - 1) : -1;
+      const bool warp_any = __any_sync(0xFFFFFFFFu, valid);
+      int wmin = valid ? lim : INT_MAX;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) pmin = min(pmin, __shfl_xor_sync(0xFFFFFFFFu, pmin, o));
-      uint32_t qf[HD / 16][4];
-      if (active) {
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          ldmatrix_x4(tile_addr<kAttnRows>(sQ, warp * 16 + (lane & 15), kk * 2 + (lane >> 4)), qf[kk][0], qf[kk][1],
-                      qf[kk][2], qf[kk][3]);
-      }
-      float o[HD / 8][4];
-#pragma unroll
-      for (int n = 0; n < HD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-      float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+      for (int o = 16; o > 0; o >>= 1) wmin = min(wmin, __shfl_xor_sync(0xFFFFFFFFu, wmin, o));
 
-      for (int blk = 0; blk < nblk; ++blk, ++gi) {
-        const int s = gi % S;
-        mbar_wait(smem_u32(full + s), (uint32_t)(gi / S) & 1u, a.err, nullptr);
-        if (active) {
-          const uint32_t kbase = sRing + (uint32_t)s * Lay::STAGE;
-          const uint32_t vbase = kbase + Lay::KV;
-#pragma unroll 1
-          for (int hb = 0; hb < kAttnBlk / 32; ++hb) {  // 32 positions at a time (bounds the score registers)
-            float sc[4][4];
+      float m_ref = -INFINITY, l = 0.f;  // reference maximum (log2 units, scaled) and row sum
+      for (int j = 0; j < nblk; ++j) {
+        const int x = gi + j;
+        if (!warp_ok(mbar_wait(smem_u32(&ctl->s_full[x & 1]), (uint32_t)(x >> 1) & 1u, a.err, abort_flag))) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sbuf = tmem + lane_base + (uint32_t)((x & 1) * kAttnBlk);
+        if (warp_any) {
+          float sc[kAttnBlk];
+          tmem_load64(sbuf, sc);
+          const int kb0 = c0 + j * kAttnBlk;
+          float bm = -INFINITY;
+          if (kb0 + kAttnBlk - 1 <= wmin) {  // no position of the block is masked for any row of the warp
 #pragma unroll
-            for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+            for (int c = 0; c < kAttnBlk; ++c) bm = fmaxf(bm, sc[c]);
+          } else {
 #pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) {
-#pragma unroll
-              for (int np = 0; np < 2; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(tile_addr<kAttnBlk>(kbase, hb * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3),
-                                                kk * 2 + ((lane >> 3) & 1)),
-                            b0, b1, b2, b3);
-                mma_bf16_16816(sc[2 * np], qf[kk], b0, b1);
-                mma_bf16_16816(sc[2 * np + 1], qf[kk], b2, b3);
-              }
+            for (int c = 0; c < kAttnBlk; ++c) {
+              sc[c] = (kb0 + c <= lim) ? sc[c] : -INFINITY;
+              bm = fmaxf(bm, sc[c]);
             }
-            // scale, causal mask (only where this half reaches the end of the range or a row's
-            // position), online softmax (log2 domain)
-            const int kb0 = c0 + blk * kAttnBlk + hb * 32;
-            float mx[2] = {-INFINITY, -INFINITY};
-            if (kb0 + 32 <= c1 && kb0 + 31 <= pmin) {
-#pragma unroll
-              for (int n = 0; n < 4; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  sc[n][e] *= scale_log2;
-                  mx[e >> 1] = fmaxf(mx[e >> 1], sc[n][e]);
-                }
+          }
+          bm *= sl2;
+          const bool fresh = (m_ref == -INFINITY);
+          const bool need = !fresh && bm > m_ref + kAttnRescaleLog2;
+          if (__any_sync(0xFFFFFFFFu, need)) {
+            // O holds the PV products of blocks before j of this item (j >= 1 since m_ref is finite)
+            if (!warp_ok(mbar_wait(smem_u32(&ctl->pv_done), (uint32_t)(x - 1) & 1u, a.err, abort_flag))) {
+              stop = true;
             } else {
+              tc_fence_after();
+              const float f = need ? exp2f(m_ref - bm) : 1.f;
+#pragma unroll 1
+              for (int c = 0; c < HD; c += 16) {
+                float ov[16];
+                tmem_load16(tmem + lane_base + kAttnTmemO + (uint32_t)c, ov);
 #pragma unroll
-              for (int n = 0; n < 4; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int pos = kb0 + n * 8 + 2 * (lane & 3) + (e & 1);
-                  const int rp = e < 2 ? p0 : p1;
-                  sc[n][e] = (pos < c1 && pos <= rp) ? sc[n][e] * scale_log2 : -INFINITY;
-                  mx[e >> 1] = fmaxf(mx[e >> 1], sc[n][e]);
-                }
-            }
-            float corr[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xFFFFFFFFu, mx[h], 1));
-              mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xFFFFFFFFu, mx[h], 2));
-              const float m_new = fmaxf(m_run[h], mx[h]);
-              corr[h] = (m_new == -INFINITY) ? 1.f : exp2f(m_run[h] - m_new);
-              m_run[h] = m_new;
-            }
-            float rs[2] = {0.f, 0.f};
-#pragma unroll
-            for (int n = 0; n < 4; ++n)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float mr = m_run[e >> 1];
-                const float pv = (mr == -INFINITY) ? 0.f : exp2f(sc[n][e] - mr);
-                sc[n][e] = pv;
-                rs[e >> 1] += pv;
+                for (int e = 0; e < 16; ++e) ov[e] *= f;
+                tmem_store16(tmem + lane_base + kAttnTmemO + (uint32_t)c, ov);
               }
-            l_run[0] = l_run[0] * corr[0] + rs[0];
-            l_run[1] = l_run[1] * corr[1] + rs[1];
-#pragma unroll
-            for (int n = 0; n < HD / 8; ++n) {
-              o[n][0] *= corr[0];
-              o[n][1] *= corr[0];
-              o[n][2] *= corr[1];
-              o[n][3] *= corr[1];
-            }
-            // O += P V over these 32 positions
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              uint32_t pa[4];
-              pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-              pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-              pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-              pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-#pragma unroll
-              for (int np = 0; np < HD / 16; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4_trans(tile_addr<kAttnBlk>(vbase, hb * 32 + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
-                                                      np * 2 + (lane >> 4)),
-                                  b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * np], pa, b0, b1);
-                mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+              if (need) {
+                l *= f;
+                m_ref = bm;
               }
             }
           }
+          if (fresh) m_ref = bm;  // first block with an unmasked position (or still -inf)
+          const float mr = m_ref;
+          uint32_t pk[kAttnBlk / 2];
+          float rs = 0.f;
+#pragma unroll
+          for (int c = 0; c < kAttnBlk / 2; ++c) {
+            const float p0 = mr == -INFINITY ? 0.f : exp2f(fmaf(sc[2 * c], sl2, -mr));
+            const float p1 = mr == -INFINITY ? 0.f : exp2f(fmaf(sc[2 * c + 1], sl2, -mr));
+            rs += p0 + p1;
+            pk[c] = pack_bf16(p0, p1);
+          }
+          l += rs;
+          tmem_store32(sbuf, pk);  // P over the first half of S's columns
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(empty + s));
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ctl->p_full[x & 1]));
+        if (stop) break;
       }
+      if (stop) break;
+      // every S product of this item has completed: the next item's query tile may go in
+      if (it + (int)gridDim.x < n_items) stage_q(it + gridDim.x);
 
-      // ---- results of this item
-      if (active) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          l_run[h] += __shfl_xor_sync(0xFFFFFFFFu, l_run[h], 1);
-          l_run[h] += __shfl_xor_sync(0xFFFFFFFFu, l_run[h], 2);
-        }
-      }
+      const int xl = gi + nblk - 1;
+      gi += nblk;
+      if (!warp_ok(mbar_wait(smem_u32(&ctl->pv_done), (uint32_t)xl & 1u, a.err, abort_flag))) break;
+      tc_fence_after();
       if (nc == 1) {
-        // the item covers the whole range: normalise and write the output rows directly
-        if (active) {
-          const float i0 = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f, i1 = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
-#pragma unroll
-          for (int n = 0; n < HD / 8; ++n) {
-            const int col = n * 8 + 2 * (lane & 3);
-            if (r0 < M)
-              *reinterpret_cast<uint32_t*>(out + (size_t)(start + r0 / G) * ldq + (size_t)(g * G + r0 % G) * HD + col) =
-                  pack_bf16(o[n][0] * i0, o[n][1] * i0);
-            if (r1 < M)
-              *reinterpret_cast<uint32_t*>(out + (size_t)(start + r1 / G) * ldq + (size_t)(g * G + r1 % G) * HD + col) =
-                  pack_bf16(o[n][2] * i1, o[n][3] * i1);
+        // the item covers the whole range: normalise and write the output row directly
+        if (warp_any) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          __nv_bfloat16* dst = out + (size_t)(start + r / G) * ldq + (size_t)(g * G + r % G) * HD;
+#pragma unroll 1
+          for (int c = 0; c < HD; c += 16) {
+            float ov[16];
+            tmem_load16(tmem + lane_base + kAttnTmemO + (uint32_t)c, ov);
+            if (valid) {
+              uint4 w0, w1;
+              w0.x = pack_bf16(ov[0] * inv, ov[1] * inv);   w0.y = pack_bf16(ov[2] * inv, ov[3] * inv);
+              w0.z = pack_bf16(ov[4] * inv, ov[5] * inv);   w0.w = pack_bf16(ov[6] * inv, ov[7] * inv);
+              w1.x = pack_bf16(ov[8] * inv, ov[9] * inv);   w1.y = pack_bf16(ov[10] * inv, ov[11] * inv);
+              w1.z = pack_bf16(ov[12] * inv, ov[13] * inv); w1.w = pack_bf16(ov[14] * inv, ov[15] * inv);
+              *reinterpret_cast<uint4*>(dst + c) = w0;
+              *reinterpret_cast<uint4*>(dst + c + 8) = w1;
+            }
           }
         }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ctl->o_free));
         continue;
       }
       const size_t ib = (size_t)it * kAttnRows;
-      if (active) {
-        if ((lane & 3) == 0) {
-          if (r0 < M) { a.part_m[ib + r0] = m_run[0]; a.part_l[ib + r0] = l_run[0]; }
-          if (r1 < M) { a.part_m[ib + r1] = m_run[1]; a.part_l[ib + r1] = l_run[1]; }
-        }
+      if (warp_any) {
+#pragma unroll 1
+        for (int c = 0; c < HD; c += 16) {
+          float ov[16];
+          tmem_load16(tmem + lane_base + kAttnTmemO + (uint32_t)c, ov);
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(a.part_o + (ib + r) * HD + c);
 #pragma unroll
-        for (int n = 0; n < HD / 8; ++n) {
-          const int col = n * 8 + 2 * (lane & 3);
-          if (r0 < M) *reinterpret_cast<float2*>(a.part_o + (ib + r0) * HD + col) = make_float2(o[n][0], o[n][1]);
-          if (r1 < M) *reinterpret_cast<float2*>(a.part_o + (ib + r1) * HD + col) = make_float2(o[n][2], o[n][3]);
-        }
-      }
-      // the last chunk of (sequence, kv head) to finish merges all chunks, in chunk order
-      __threadfence();
-      named_bar_sync(1, 32 * kAttnComputeWarps);
-      if (tid == 0) {
-        const int old = atomicAdd(a.counters + b * a.n_kv + g, 1);
-        *last_s = (old == nc - 1) ? 1 : 0;
-      }
-      named_bar_sync(1, 32 * kAttnComputeWarps);
-      if (*last_s) {
-        __threadfence();
-        const int base = a.item_base[b] + g * nc;
-        for (int idx = tid; idx < M * (HD / 4); idx += 32 * kAttnComputeWarps) {
-          const int m = idx / (HD / 4), e4 = idx - (idx / (HD / 4)) * (HD / 4);
-          // chunk statistics first (independent loads), then the weighted sum, in chunk order
-          float Mx = -INFINITY;
-#pragma unroll 4
-          for (int c = 0; c < nc; ++c) Mx = fmaxf(Mx, __ldcg(a.part_m + (size_t)(base + c) * kAttnRows + m));
-          float L = 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-          for (int c = 0; c < nc; ++c) {
-            const size_t pr = (size_t)(base + c) * kAttnRows + m;
-            const float mc = __ldcg(a.part_m + pr);
-            const float lc = __ldcg(a.part_l + pr);
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + pr * HD) + e4);
-            const float wgt = mc == -INFINITY ? 0.f : exp2f(mc - Mx);
-            L += wgt * lc;
-            acc.x += wgt * v.x; acc.y += wgt * v.y; acc.z += wgt * v.z; acc.w += wgt * v.w;
+            for (int e = 0; e < 4; ++e) dst[e] = make_float4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
           }
-          const float inv = L > 0.f ? 1.f / L : 0.f;
-          __nv_bfloat16* dst = out + (size_t)(start + m / G) * ldq + (size_t)(g * G + m % G) * HD + 4 * e4;
-          uint2 pk;
-          pk.x = pack_bf16(acc.x * inv, acc.y * inv);
-          pk.y = pack_bf16(acc.z * inv, acc.w * inv);
-          *reinterpret_cast<uint2*>(dst) = pk;
         }
-        if (tid == 0) a.counters[b * a.n_kv + g] = 0;  // ready for the next layer
+        if (valid) {
+          a.part_m[ib + r] = m_ref;
+          a.part_l[ib + r] = l;
+        }
       }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ctl->o_free));
     }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kAttnTmemCols);
   }
 }
 
@@ -393,11 +444,99 @@ static cudaError_t launch_attn_typed(const CUtensorMap& tk, const CUtensorMap& t
                     a);
 }
 
+// Merge of the chunks of every (sequence, kv head) whose range took more than
+// one chunk: one warp per (sequence, kv head, query vector), lanes over
+// head_dim.  out = sum_c w_c O_c / sum_c w_c l_c with w_c = 2^(m_c - max_c m_c);
+// the weighted sum runs in chunk order (deterministic).
+constexpr int kMergeThreads = 256;
+
+template <int HD>
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int VPL = HD / 32;  // output values per lane
+  const int G = a.n_q / a.n_kv, lane = threadIdx.x & 31;
+  const int ldq = a.n_q * HD;
+  const long long n_tasks = (long long)a.B * a.n_kv * kAttnRows;
+  const long long warps = (long long)gridDim.x * (kMergeThreads / 32);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  for (long long task = ((long long)blockIdx.x * kMergeThreads + threadIdx.x) >> 5; task < n_tasks; task += warps) {
+    const int m = (int)(task % kAttnRows);
+    const int bg = (int)(task / kAttnRows);
+    const int b = bg / a.n_kv, g = bg - (bg / a.n_kv) * a.n_kv;
+    const int nc = a.n_chunks[b];
+    if (nc <= 1 || m >= min(a.seq_len[b] * G, kAttnRows)) continue;
+    const size_t base = (size_t)(a.item_base[b] + g * nc) * kAttnRows + m;  // partial row of chunk 0
+    float mx = -INFINITY;
+    for (int c = lane; c < nc; c += 32) mx = fmaxf(mx, __ldcg(a.part_m + base + (size_t)c * kAttnRows));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    float L = 0.f;
+    for (int c = lane; c < nc; c += 32) {
+      const float mc = __ldcg(a.part_m + base + (size_t)c * kAttnRows);
+      L += (mc == -INFINITY ? 0.f : exp2f(mc - mx)) * __ldcg(a.part_l + base + (size_t)c * kAttnRows);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+    float acc[VPL];
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
+    for (int c0 = 0; c0 < nc; c0 += 8) {  // eight chunks' loads in flight, added in chunk order
+      float w[8], v[8][VPL];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (c0 + k < nc) {
+          const size_t pr = base + (size_t)(c0 + k) * kAttnRows;
+          const float mc = __ldcg(a.part_m + pr);
+          w[k] = mc == -INFINITY ? 0.f : exp2f(mc - mx);
+          const float* src = a.part_o + pr * HD + lane * VPL;
+          if constexpr (VPL == 4) {
+            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+            v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
+          } else {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+            v[k][0] = t.x; v[k][1] = t.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (c0 + k < nc) {
+#pragma unroll
+          for (int e = 0; e < VPL; ++e) acc[e] += w[k] * v[k][e];
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16* dst =
+        out + (size_t)(a.seq_start[b] + m / G) * ldq + (size_t)(g * G + m % G) * HD + (size_t)lane * VPL;
+    if constexpr (VPL == 4) {
+      uint2 pk;
+      pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+      pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(dst) = pk;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
+    }
+  }
+}
+
+template <int HD>
+static cudaError_t launch_merge_typed(const AttnArgs& a, int sms, cudaStream_t s) {
+  const long long warps = (long long)a.B * a.n_kv * kAttnRows;
+  const long long need = (warps + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
+  const int grid = (int)std::min<long long>(need, 8LL * sms);
+  if (grid <= 0) return cudaSuccess;
+  return launch_pdl(attn_merge_kernel<HD>, dim3(grid), dim3(kMergeThreads), 0, s, a);
+}
+
 cudaError_t launch_attention_bf16(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a, int grid,
-                                  cudaStream_t s) {
-  if (a.head_dim == 64) return launch_attn_typed<64>(tmK, tmV, a, grid, s);
-  if (a.head_dim == 128) return launch_attn_typed<128>(tmK, tmV, a, grid, s);
-  return cudaErrorInvalidValue;
+                                  int sms, cudaStream_t s) {
+  cudaError_t e = cudaErrorInvalidValue;
+  if (a.head_dim == 64) e = launch_attn_typed<64>(tmK, tmV, a, grid, s);
+  if (a.head_dim == 128) e = launch_attn_typed<128>(tmK, tmV, a, grid, s);
+  if (e != cudaSuccess) return e;
+  if (a.head_dim == 64) return launch_merge_typed<64>(a, sms, s);
+  return launch_merge_typed<128>(a, sms, s);
 }
 
 // ============================================================================= fp32

@@ -192,7 +192,7 @@ size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int red_entries);
 // ----------------------------------------------------------------------------- attention
 
 struct AttnArgs {
-  int n_q, n_kv, head_dim, max_pages, page_size, num_pages;
+  int B, n_q, n_kv, head_dim, max_pages, page_size, num_pages;
   float scale;               // 1/sqrt(head_dim)
   const void* q;             // [rows][n_q*hd], post-RoPE
   const void *k_cache, *v_cache;
@@ -201,15 +201,15 @@ struct AttnArgs {
   const int4* items;         // (b, g, c0, c1)
   const int32_t *n_items, *item_base, *n_chunks;
   float *part_m, *part_l, *part_o;  // [items][128], [items][128], [items][128][hd]
-  int32_t* counters;         // [B][n_kv] finished chunks (zero before the launch, left at zero)
   void* out;                 // [rows][n_q*hd]
   int n_rows;                // host upper bound on rows
   int32_t* err;
 };
 constexpr int kAttnRows = 128;    // query rows (row x GQA head) per work item
 // tmK / tmV: the layer's K and V pools as bf16 [num_pages*16][n_kv][hd], 128-byte swizzle, box 64 x 1 x 16.
+// Launches the attention kernel (`grid` CTAs) and then the chunk merge.
 cudaError_t launch_attention_bf16(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a, int grid,
-                                  cudaStream_t s);
+                                  int sms, cudaStream_t s);
 cudaError_t launch_attention_f32(const AttnArgs& a, cudaStream_t s);
 
 }  // namespace pe
