@@ -38,7 +38,7 @@ void trace(int point, cudaStream_t s) {
 
 constexpr int kMaxRows = 1 << 16;        // B*2K
 constexpr int kAttnItemsPerSlot = 4;     // attention work items aimed for, per resident CTA (load balance)
-constexpr int kAttnMinChunk = 512;       // shortest position chunk of a work item (bounds the chunks to merge)
+constexpr int kAttnMinChunk = 256;       // shortest position chunk of a work item (bounds the chunks to merge)
 constexpr int kTcMaxStages = 12;
 constexpr int kMaxClusterSplits = 8;     // portable cluster size
 
@@ -141,7 +141,7 @@ Plan make_plan(const pe_config& c) {
   // attention items: the work list aims at attn_target items; rounding adds at
   // most one per (sequence, kv head), and no (sequence, kv head) can have more
   // chunks than its longest possible range holds minimum chunks
-  const int attn_slots = (c.head_dim == 64 ? 2 : 1) * p.sms;  // resident attention CTAs
+  const int attn_slots = 2 * p.sms;  // resident attention CTAs (two per SM)
   p.attn_target = kAttnItemsPerSlot * attn_slots;
   const long long per_pair = ((long long)c.max_pages_per_seq * c.page_size + kAttnMinChunk - 1) / kAttnMinChunk;
   p.max_items = (int)std::min<long long>(p.attn_target + (long long)c.B * c.n_kv, per_pair * c.B * c.n_kv);

@@ -9,7 +9,8 @@
 // query heads of g (<= 128 query vectors), so each KV page is read once per
 // (sequence, kv head).  Warp 0 streams the chunk's K and V pages with 3-D TMA
 // loads (one 16-position page per load, 128-byte swizzle, pages past the
-// range zero-filled) into a 4-stage mbarrier ring of 64-position blocks.
+// range zero-filled) into an mbarrier ring of 64-position blocks (4 stages
+// at head_dim 64, 2 at head_dim 128: two CTAs share an SM).
 // Warp 1 issues the 5th-generation tensor-core MMAs: S = Q K^T (M = 128 query
 // vectors, N = 64 positions) into one of two TMEM buffers, and O += P V with
 // P read from TMEM and V as an MN-major operand straight from the ring.
@@ -39,6 +40,13 @@ PE_DEV uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 2^x by the hardware approximation (MUFU; subnormal results flush to zero).
+PE_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // A wait's outcome, made the same for the whole warp (warp-collective
 // instructions follow it).
 PE_DEV bool warp_ok(bool ok) { return __all_sync(0xFFFFFFFFu, ok); }
@@ -46,7 +54,10 @@ PE_DEV bool warp_ok(bool ok) { return __all_sync(0xFFFFFFFFu, ok); }
 }  // namespace
 
 constexpr int kAttnBlk = 64;          // kv positions per pipeline stage (4 pages) = MMA N of S
-constexpr int kAttnStages = 4;        // stages in flight
+// stages in flight: 4 x 16 KB (head_dim 64) or 2 x 32 KB (head_dim 128), so two CTAs fit per SM
+template <int HD>
+__host__ __device__ constexpr int attn_stages() { return HD == 64 ? 4 : 2; }
+constexpr int kAttnMaxStages = 4;
 constexpr int kAttnThreads = 192;     // warp 0: TMA, warp 1: MMA, warps 2..5: softmax (thread = query row)
 constexpr int kAttnSoftmax = 128;     // softmax threads
 constexpr uint32_t kAttnTmemCols = 256;  // S double buffer (2 x 64 columns) + O (head_dim columns)
@@ -67,13 +78,13 @@ struct AttnLayout {
   static constexpr uint32_t Q = kAttnRows * HD * 2;      // query tile
   static constexpr uint32_t KV = kAttnBlk * HD * 2;      // K (or V) of one stage
   static constexpr uint32_t STAGE = 2 * KV;
-  static constexpr uint32_t BARS = Q + kAttnStages * STAGE;
+  static constexpr uint32_t BARS = Q + attn_stages<HD>() * STAGE;
   static constexpr uint32_t TOTAL = 1024 + BARS + 256;   // + alignment slack
 };
 
 // Barriers and flags after the tiles.
 struct AttnCtrl {
-  uint64_t full[kAttnStages], empty[kAttnStages];
+  uint64_t full[kAttnMaxStages], empty[kAttnMaxStages];
   uint64_t q_full;      // softmax threads staged the item's query tile
   uint64_t s_full[2];   // S of a block is in TMEM buffer (block & 1)
   uint64_t p_full[2];   // P of a block is in TMEM (over its S), O rescaled where needed
@@ -87,12 +98,12 @@ struct AttnCtrl {
 static_assert(sizeof(AttnCtrl) <= 256, "attention control block");
 
 template <int HD>
-__global__ void __launch_bounds__(kAttnThreads, HD == 64 ? 2 : 1)
+__global__ void __launch_bounds__(kAttnThreads, 2)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const AttnArgs a) {
   using Lay = AttnLayout<HD>;
   constexpr int CH = HD / 8;  // 16-byte units per row
-  constexpr int S = kAttnStages;
+  constexpr int S = attn_stages<HD>();
   extern __shared__ uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(sm);
@@ -315,17 +326,17 @@ __global__ void __launch_bounds__(kAttnThreads, HD == 64 ? 2 : 1)
           float sc[kAttnBlk];
           tmem_load64(sbuf, sc);
           const int kb0 = c0 + j * kAttnBlk;
-          float bm = -INFINITY;
-          if (kb0 + kAttnBlk - 1 <= wmin) {  // no position of the block is masked for any row of the warp
+          if (kb0 + kAttnBlk - 1 > wmin) {  // some position of the block is masked for some row of the warp
 #pragma unroll
-            for (int c = 0; c < kAttnBlk; ++c) bm = fmaxf(bm, sc[c]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < kAttnBlk; ++c) {
-              sc[c] = (kb0 + c <= lim) ? sc[c] : -INFINITY;
-              bm = fmaxf(bm, sc[c]);
-            }
+            for (int c = 0; c < kAttnBlk; ++c) sc[c] = (kb0 + c <= lim) ? sc[c] : -INFINITY;
           }
+          float mx8[8];  // eight independent chains
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx8[e] = sc[e];
+#pragma unroll
+          for (int c = 8; c < kAttnBlk; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
+          float bm = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
           bm *= sl2;
           const bool fresh = (m_ref == -INFINITY);
           const bool need = !fresh && bm > m_ref + kAttnRescaleLog2;
@@ -335,7 +346,7 @@ __global__ void __launch_bounds__(kAttnThreads, HD == 64 ? 2 : 1)
               stop = true;
             } else {
               tc_fence_after();
-              const float f = need ? exp2f(m_ref - bm) : 1.f;
+              const float f = need ? ex2_approx(m_ref - bm) : 1.f;
 #pragma unroll 1
               for (int c = 0; c < HD; c += 16) {
                 float ov[16];
@@ -351,17 +362,21 @@ __global__ void __launch_bounds__(kAttnThreads, HD == 64 ? 2 : 1)
             }
           }
           if (fresh) m_ref = bm;  // first block with an unmasked position (or still -inf)
-          const float mr = m_ref;
+          // P = 2^(s * scale * log2e - m_ref).  Masked scores are -inf (2^-inf = 0); a row
+          // with nothing unmasked yet has m_ref = -inf and takes offset -inf, so P = 0 there too.
+          const float nmr = m_ref == -INFINITY ? -INFINITY : -m_ref;
           uint32_t pk[kAttnBlk / 2];
-          float rs = 0.f;
+          float rs8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
 #pragma unroll
           for (int c = 0; c < kAttnBlk / 2; ++c) {
-            const float p0 = mr == -INFINITY ? 0.f : exp2f(fmaf(sc[2 * c], sl2, -mr));
-            const float p1 = mr == -INFINITY ? 0.f : exp2f(fmaf(sc[2 * c + 1], sl2, -mr));
-            rs += p0 + p1;
+            const float p0 = ex2_approx(fmaf(sc[2 * c], sl2, nmr));
+            const float p1 = ex2_approx(fmaf(sc[2 * c + 1], sl2, nmr));
+            rs8[c & 7] += p0 + p1;
             pk[c] = pack_bf16(p0, p1);
           }
-          l += rs;
+          l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
           tmem_store32(sbuf, pk);  // P over the first half of S's columns
         }
         tc_fence_before();
