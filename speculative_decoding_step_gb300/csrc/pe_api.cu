@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -289,6 +290,15 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+// RoPE turn frequencies in double, stored as hi + lo floats.
+void set_rope_table(GemmArgs& g, float theta, int hd) {
+  for (int i = 0; i < 64; ++i) {
+    const double tf = i < hd / 2 ? std::pow((double)theta, -2.0 * i / hd) / (2.0 * 3.14159265358979323846) : 0.0;
+    g.rope_tf_hi[i] = (float)tf;
+    g.rope_tf_lo[i] = (float)(tf - (double)g.rope_tf_hi[i]);
+  }
+}
+
 // ----------------------------------------------------------------------------- one GEMM launch
 
 struct GemmCall {
@@ -386,7 +396,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   trace(3, s);
 
   GemmArgs base{};
-  base.n_q = c.n_q; base.n_kv = c.n_kv; base.head_dim = hd; base.rope_theta = c.rope_theta;
+  base.n_q = c.n_q; base.n_kv = c.n_kv; base.head_dim = hd; set_rope_table(base, c.rope_theta, hd);
   base.tok_pos = ia.tok_pos; base.tok_slot = ia.tok_slot; base.err = err;
 
   float* x = at<float>(ws, p.x);

@@ -280,15 +280,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       const int b = item.x, g = item.y;
       const int start = a.seq_start[b];
       const int M = min(a.seq_len[b] * G, kAttnRows);
-      for (int idx = et; idx < kAttnRows * CH; idx += kAttnSoftmax) {
+      // every load of this thread first (one round trip), then the shared-memory stores
+      constexpr int PER = kAttnRows * CH / kAttnSoftmax;
+      uint4 val[PER];
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int idx = et + k * kAttnSoftmax;
         const int m = idx / CH, ch = idx - (idx / CH) * CH;
-        uint4 val = make_uint4(0, 0, 0, 0);
+        val[k] = make_uint4(0, 0, 0, 0);
         if (m < M) {
           const int i = m / G, j = m - (m / G) * G;
-          val = *reinterpret_cast<const uint4*>(qbuf + (size_t)(start + i) * ldq + (size_t)(g * G + j) * HD + ch * 8);
+          val[k] = __ldg(reinterpret_cast<const uint4*>(qbuf + (size_t)(start + i) * ldq + (size_t)(g * G + j) * HD +
+                                                        ch * 8));
         }
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tile_addr<kAttnRows>(sQ, m, ch)), "r"(val.x),
-                     "r"(val.y), "r"(val.z), "r"(val.w)
+      }
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int idx = et + k * kAttnSoftmax;
+        const int m = idx / CH, ch = idx - (idx / CH) * CH;
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tile_addr<kAttnRows>(sQ, m, ch)), "r"(val[k].x),
+                     "r"(val[k].y), "r"(val[k].z), "r"(val[k].w)
                      : "memory");
       }
       fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core

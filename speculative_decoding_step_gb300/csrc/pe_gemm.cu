@@ -26,9 +26,17 @@ namespace pe {
 // ============================================================================= epilogues
 
 // Rotate-half RoPE of the pair (x1, x2) = (v[i], v[i + hd/2]) at position pos.
-PE_DEV void rope_pair(float x1, float x2, int pos, float inv_freq, float& o1, float& o2) {
+// tf = theta^(-2i/hd) / (2 pi) as hi + lo floats: the angle in turns, pos * tf,
+// is reduced to [-1/2, 1/2] without loss (the rounding error of pos * tf.hi is
+// recovered by an fma; subtracting the nearest integer is exact), so the
+// hardware sine / cosine only ever sees |angle| <= pi.
+PE_DEV void rope_pair(float x1, float x2, int pos, float2 tf, float& o1, float& o2) {
+  const float p = (float)pos;  // exact below 2^24
+  const float h = p * tf.x;
+  const float e = fmaf(p, tf.x, -h);
+  const float r = (h - rintf(h)) + fmaf(p, tf.y, e);
   float s, c;
-  sincosf((float)pos * inv_freq, &s, &c);
+  __sincosf(r * 6.283185307179586f, &s, &c);
   o1 = x1 * c - x2 * s;
   o2 = x2 * c + x1 * s;
 }
@@ -37,10 +45,10 @@ PE_DEV void rope_pair(float x1, float x2, int pos, float inv_freq, float& o1, fl
 // q | k | v concatenation.  q and k are rotated; q goes to the q buffer, k and
 // v to the paged cache at the token's slot (no write for slot -1).
 template <typename T>
-PE_DEV void epi_qkv(const GemmArgs& a, int unit, int t, float x1, float x2, float inv_freq) {
+PE_DEV void epi_qkv(const GemmArgs& a, int unit, int t, float x1, float x2, float2 tf) {
   const int half = a.head_dim >> 1;
   const int head = unit / half, i = unit - head * half;
-  if (head < a.n_q + a.n_kv) rope_pair(x1, x2, a.tok_pos[t], inv_freq, x1, x2);
+  if (head < a.n_q + a.n_kv) rope_pair(x1, x2, a.tok_pos[t], tf, x1, x2);
   if (head < a.n_q) {
     T* q = static_cast<T*>(a.out_act) + (size_t)t * a.ld_out + (size_t)head * a.head_dim + i;
     q[0] = from_float<T>(x1);
@@ -57,7 +65,7 @@ PE_DEV void epi_qkv(const GemmArgs& a, int unit, int t, float x1, float x2, floa
 }
 
 template <int EPI, typename T>
-PE_DEV void epi_elem(const GemmArgs& a, int unit, int t, float v, float v2, float inv_freq) {
+PE_DEV void epi_elem(const GemmArgs& a, int unit, int t, float v, float v2, float2 tf) {
   if (EPI == EPI_STORE_F32) {
     a.out_f32[(size_t)t * a.ld_out + unit] = v;
   } else if (EPI == EPI_ADD_F32) {
@@ -66,7 +74,7 @@ PE_DEV void epi_elem(const GemmArgs& a, int unit, int t, float v, float v2, floa
   } else if (EPI == EPI_SWIGLU) {
     static_cast<T*>(a.out_act)[(size_t)t * a.ld_out + unit] = from_float<T>(silu(v) * v2);
   } else if (EPI == EPI_QKV_ROPE) {
-    epi_qkv<T>(a, unit, t, v, v2, inv_freq);
+    epi_qkv<T>(a, unit, t, v, v2, tf);
   }
 }
 
@@ -74,10 +82,12 @@ PE_DEV void epi_elem(const GemmArgs& a, int unit, int t, float v, float v2, floa
 // Every load the epilogue needs (residual values, token positions and slots)
 // is issued before the first store: interleaving them would make each token a
 // separate memory round trip, because the compiler cannot prove the stores and
-// the later loads disjoint.
+// the later loads disjoint.  The RoPE and SwiGLU bodies run as rolled loops:
+// this code runs once per CTA in the split-K path, where straight-line code
+// costs an instruction fetch per line.
 template <int EPI, typename T>
 PE_DEV void epi_chunk(const GemmArgs& a, int unit, int t0, int nv, const float (&v)[16], const float (&v2)[16],
-                      float inv_freq) {
+                      float2 tf) {
   if (EPI == EPI_STORE_F32) {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
@@ -90,9 +100,9 @@ PE_DEV void epi_chunk(const GemmArgs& a, int unit, int t0, int nv, const float (
     for (int j = 0; j < 16; ++j)
       if (j < nv) a.out_f32[(size_t)(t0 + j) * a.ld_out + unit] = old[j] + v[j];
   } else if (EPI == EPI_SWIGLU) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j < nv) static_cast<T*>(a.out_act)[(size_t)(t0 + j) * a.ld_out + unit] = from_float<T>(silu(v[j]) * v2[j]);
+    T* o = static_cast<T*>(a.out_act) + (size_t)t0 * a.ld_out + unit;
+#pragma unroll 1
+    for (int j = 0; j < nv; ++j) o[(size_t)j * a.ld_out] = from_float<T>(silu(v[j]) * v2[j]);
   } else if (EPI == EPI_QKV_ROPE) {
     const int half = a.head_dim >> 1;
     const int head = unit / half, i = unit - head * half;
@@ -104,18 +114,18 @@ PE_DEV void epi_chunk(const GemmArgs& a, int unit, int t0, int nv, const float (
       pos[j] = (j < nv && rotated) ? a.tok_pos[t0 + j] : 0;
       slot[j] = (j < nv && !is_q) ? a.tok_slot[t0 + j] : -1;
     }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (j >= nv) continue;
+    T* qdst = static_cast<T*>(a.out_act) + (size_t)t0 * a.ld_out + (size_t)head * a.head_dim + i;
+    const int g = rotated ? head - a.n_q : head - a.n_q - a.n_kv;
+    T* cache = static_cast<T*>(rotated ? a.k_cache : a.v_cache) + (size_t)g * a.head_dim + i;
+#pragma unroll 1
+    for (int j = 0; j < nv; ++j) {
       float x1 = v[j], x2 = v2[j];
-      if (rotated) rope_pair(v[j], v2[j], pos[j], inv_freq, x1, x2);
+      if (rotated) rope_pair(v[j], v2[j], pos[j], tf, x1, x2);
       if (is_q) {
-        T* q = static_cast<T*>(a.out_act) + (size_t)(t0 + j) * a.ld_out + (size_t)head * a.head_dim + i;
-        q[0] = from_float<T>(x1);
-        q[half] = from_float<T>(x2);
+        qdst[(size_t)j * a.ld_out] = from_float<T>(x1);
+        qdst[(size_t)j * a.ld_out + half] = from_float<T>(x2);
       } else if (slot[j] >= 0) {
-        const int g = rotated ? head - a.n_q : head - a.n_q - a.n_kv;
-        T* c = static_cast<T*>(rotated ? a.k_cache : a.v_cache) + ((size_t)slot[j] * a.n_kv + g) * a.head_dim + i;
+        T* c = cache + (size_t)slot[j] * a.n_kv * a.head_dim;
         c[0] = from_float<T>(x1);
         c[half] = from_float<T>(x2);
       }
@@ -123,10 +133,10 @@ PE_DEV void epi_chunk(const GemmArgs& a, int unit, int t0, int nv, const float (
   }
 }
 
-PE_DEV float rope_inv_freq(const GemmArgs& a, int unit) {
-  const int half = a.head_dim >> 1;
-  const int i = unit % half;
-  return powf(a.rope_theta, -2.0f * (float)i / (float)a.head_dim);
+// RoPE turn frequency of the pair index of `unit` (hi + lo).
+PE_DEV float2 rope_tf(const GemmArgs& a, int unit) {
+  const int i = unit % (a.head_dim >> 1);
+  return make_float2(a.rope_tf_hi[i], a.rope_tf_lo[i]);
 }
 
 // Last CTA of the LM head: turn the per-token keys into token ids.
@@ -213,9 +223,9 @@ PE_DEV void issue_w(const CUtensorMap* tmW, const GemmArgs& a, uint32_t sa, uint
 
 template <int EPI>
 PE_DEV void apply16(const GemmArgs& a, int unit, int t0, int n_tok, const float (&v)[16], const float (&v2)[16],
-                    float inv_freq) {
+                    float2 tf) {
   if (unit >= a.n_out) return;
-  epi_chunk<EPI, __nv_bfloat16>(a, unit, t0, max(0, min(16, n_tok - t0)), v, v2, inv_freq);
+  epi_chunk<EPI, __nv_bfloat16>(a, unit, t0, max(0, min(16, n_tok - t0)), v, v2, tf);
 }
 
 PE_DEV unsigned long long umax64(unsigned long long x, unsigned long long y) { return x > y ? x : y; }
@@ -425,7 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t tl = tmem + (uint32_t)(buf * a.acc_stride) + ((uint32_t)(q * 32) << 16);
       const int tbase = w.tile_t * BN;
       if (ok && a.k_splits == 1) {
-        const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
+        const float2 tf = (EPI == EPI_QKV_ROPE) ? rope_tf(a, unit) : make_float2(0.f, 0.f);
         for (int c = 0; c < BN / 16; ++c) {
           float v[16], v2[16];
           tmem_load16(tl + (uint32_t)(c * 16), v);
@@ -433,7 +443,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (EPI == EPI_ARGMAX)
             argmax16(a, unit, tbase + c * 16, n_tok, v, red_w + tbase + c * 16, lane);
           else
-            apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, inv_freq);
+            apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, tf);
         }
       } else if (ok) {
         // split K (one unit per CTA, the stage ring is idle): leave this split's partial
@@ -496,7 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int c0 = (int)rank * cs, c1 = min(BN, c0 + cs);
         const int r = (warp & 3) * 32 + lane;
         const int unit = w.tile_f * kTcBM + r;
-        const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
+        const float2 tf = (EPI == EPI_QKV_ROPE) ? rope_tf(a, unit) : make_float2(0.f, 0.f);
         const uint32_t base = smem_u32(smem);
         // Rank p starts at its own tile and walks the ring (rank + j) % ns: at any moment
         // every CTA's shared memory serves one reader, not the whole cluster.  The order
@@ -537,7 +547,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
           const int t0 = w.tile_t * BN + col0;
-          if (unit < a.n_out) epi_chunk<EPI, __nv_bfloat16>(a, unit, t0, max(0, min(ncol, n_tok - t0)), v, v2, inv_freq);
+          if (unit < a.n_out) epi_chunk<EPI, __nv_bfloat16>(a, unit, t0, max(0, min(ncol, n_tok - t0)), v, v2, tf);
         }
       }
     }
@@ -662,7 +672,7 @@ __global__ void __launch_bounds__(kF32Warps * 32) gemm_f32_kernel(const GemmArgs
       row1 = head * a.head_dim + i;
       row2 = row1 + half;
     }
-    const float inv_freq = (EPI == EPI_QKV_ROPE) ? rope_inv_freq(a, unit) : 0.f;
+    const float2 tf = (EPI == EPI_QKV_ROPE) ? rope_tf(a, unit) : make_float2(0.f, 0.f);
     const float* w1 = W + (size_t)row1 * a.k_dim;
     const float* w2 = W + (size_t)row2 * a.k_dim;
     for (int t0 = 0; t0 < n_tok; t0 += kF32Tok) {
@@ -696,7 +706,7 @@ __global__ void __launch_bounds__(kF32Warps * 32) gemm_f32_kernel(const GemmArgs
           if (a.logits_dbg != nullptr) a.logits_dbg[(size_t)t * a.n_out + unit] = acc1[j];
           atomicMax(a.keys + t, argmax_key(acc1[j], (uint32_t)unit));
         } else {
-          epi_elem<EPI, float>(a, unit, t, acc1[j], acc2[j], inv_freq);
+          epi_elem<EPI, float>(a, unit, t, acc1[j], acc2[j], tf);
         }
       }
     }

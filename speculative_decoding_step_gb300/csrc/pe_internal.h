@@ -159,7 +159,9 @@ struct GemmArgs {
   void* out_act;         // SwiGLU output / q buffer (bf16 or fp32 by config)
   int ld_out;
   int n_q, n_kv, head_dim;
-  float rope_theta;
+  // RoPE: turns per position of pair index i, theta^(-2i/head_dim) / (2 pi), split into
+  // a float and the float nearest its remainder (i < head_dim / 2 <= 64)
+  float rope_tf_hi[64], rope_tf_lo[64];
   const int32_t* tok_pos;
   const int64_t* tok_slot;
   void *k_cache, *v_cache;
