@@ -41,7 +41,7 @@ constexpr int kMaxRows = 1 << 16;        // B*2K
 constexpr int kAttnItemsPerSlot = 4;     // attention work items aimed for, per resident CTA (load balance)
 constexpr int kAttnMinChunk = 256;       // shortest position chunk of a work item (bounds the chunks to merge)
 constexpr int kTcMaxStages = 12;
-constexpr int kMaxClusterSplits = 8;     // portable cluster size
+constexpr int kMaxSplits = 16;           // split-K ways per tile
 
 int num_sms() {
   static int cached[64] = {0};
@@ -72,11 +72,10 @@ struct GemmPlan {
 };
 
 // Work decomposition of one GEMM: 128 weight rows x bn token rows per tile.
-// With fewer tiles than SMs, split K so that every SM streams weights: the
-// splits of a tile run as one thread-block cluster (at most 8 CTAs) and reduce
-// through distributed shared memory, so every CTA owns exactly one unit and all
-// clusters must fit on the GPU at once; each split keeps at least four 64-wide
-// k blocks, and its fp32 partial tile must fit in the idle stage ring.
+// With fewer tiles than SMs, split K so that nearly every SM streams weights:
+// every CTA owns exactly one unit and the grid is at most one CTA per SM (the
+// splits of a tile wait for one another, so they must be resident together);
+// each split keeps at least four 64-wide k blocks.
 GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   GemmPlan g;
   g.epi = epi;
@@ -96,14 +95,16 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   const long long avail = kTcSmemOptIn - 1024 - kTcCtrlBytes - (long long)red * 8;
   g.stages = (int)std::min<long long>(kTcMaxStages, avail / g.stage_bytes);
   g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, red);
-  const size_t partial_bytes = (size_t)(paired ? 2 : 1) * kTcBM * g.bn * 4;
-  if (epi != EPI_ARGMAX && g.tiles < sms && partial_bytes <= (size_t)g.stages * g.stage_bytes) {
-    int s = std::min(kMaxClusterSplits, std::min(sms / g.tiles, std::max(1, g.kb_total / 4)));
+  if (epi != EPI_ARGMAX && g.tiles < sms) {
+    // the partial tile, and every split's slice of this rank's columns, are staged in the stage ring
+    const size_t ring = (size_t)g.stages * g.stage_bytes;
+    const int planes = paired ? 2 : 1;
+    int s = std::max(1, std::min(kMaxSplits, std::min(sms / g.tiles, g.kb_total / 4)));
     for (; s > 1; --s) {
-      const int fit = gemm_tc_max_active_clusters(epi, g.smem, s);
-      if (fit >= g.tiles) break;
+      const size_t cs = (size_t)((((g.bn + s - 1) / s) + 3) & ~3);
+      if ((size_t)planes * g.bn * kTcBM * 4 <= ring && (size_t)s * planes * cs * kTcBM * 4 <= ring) break;
     }
-    g.k_splits = std::max(1, s);
+    g.k_splits = s;
   }
   const int acc_cols = (paired ? 2 : 1) * g.bn;
   g.nbuf = 2 * acc_cols <= 512 ? 2 : 1;
@@ -119,7 +120,8 @@ struct Plan {
   GemmPlan fc, qkv, o, gu, down, lm;
   // workspace offsets
   size_t tok_pos, tok_seq, tok_slot, seq_start, seq_len, seq_maxpos, item_base, n_chunks, n_items, items;
-  size_t done, keys, x, y, q, ao, u, yl, part_m, part_l, part_o;
+  size_t done, keys, x, y, q, ao, u, yl, part_m, part_l, part_o, split_part;
+  int n_split_ctr = 0;  // split-K arrival counters after the LM-head counter
   size_t st_ids, st_pos, st_slot, st_rej, st_mask, st_hmap, st_rows, st_nvalid, st_draft, st_x0;
   size_t total = 0;
 };
@@ -165,7 +167,10 @@ Plan make_plan(const pe_config& c) {
   p.n_chunks = take(4 * (size_t)c.B);
   p.n_items = take(4);
   p.items = take(16 * (size_t)p.max_items);
-  p.done = take(4);  // LM-head completion counter
+  // LM-head completion counter, then one block of split-K arrival counters per GEMM
+  // launch (fc, then qkv, o, gate/up, down per layer), p.sms per block (tiles < SMs)
+  p.n_split_ctr = (1 + 4 * c.n_layers) * p.sms;
+  p.done = take(4 * (1 + (size_t)p.n_split_ctr));
   p.keys = take(8 * (size_t)p.T);
   p.x = take(4 * (size_t)p.R * c.d);
   p.y = take(eb * (size_t)p.R * c.d);
@@ -173,6 +178,13 @@ Plan make_plan(const pe_config& c) {
   p.ao = take(eb * (size_t)p.R * c.n_q * c.head_dim);
   p.u = take(eb * (size_t)p.R * c.ffn);
   p.yl = take(eb * (size_t)p.T * c.d);
+  size_t split_bytes = 0;  // fp32 partial tiles of the largest split-K launch
+  for (const GemmPlan* g : {&p.fc, &p.qkv, &p.o, &p.gu, &p.down})
+    if (g->k_splits > 1) {
+      const bool paired = g->epi == EPI_SWIGLU || g->epi == EPI_QKV_ROPE;
+      split_bytes = std::max(split_bytes, (size_t)g->grid * (paired ? 2 : 1) * g->bn * kTcBM * 4);
+    }
+  p.split_part = c.dtype == PE_BF16 && split_bytes > 0 ? take(split_bytes) : 0;
   if (c.dtype == PE_BF16) {
     p.part_m = take(4 * (size_t)p.max_items * kAttnRows);
     p.part_l = take(4 * (size_t)p.max_items * kAttnRows);
@@ -311,6 +323,7 @@ struct GemmCall {
   // tensor-map shapes of W
   int w_kind;  // 0: matrix [w_rows][k_dim], 1: gate/up, 2: qkv
   uint64_t w_rows;
+  int slot;    // block of split-K arrival counters (GEMM launch index in the pass)
 };
 
 pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& call, GemmArgs a, cudaStream_t s) {
@@ -337,6 +350,10 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   a.acc_stride = g.acc_stride;
   a.tmem_cols = g.tmem_cols;
   a.n_tok_min = call.n_tok_dev != nullptr ? std::min(call.n_tok, c.B * c.K) : call.n_tok;
+  if (g.k_splits > 1) {
+    a.partial = at<float>(ws, p.split_part);
+    a.tile_counters = at<int32_t>(ws, p.done) + 1 + (size_t)call.slot * p.sms;
+  }
   CUtensorMap tw, tx;
   bool ok;
   if (call.w_kind == 1) ok = tmap_gate_up(&tw, call.W, (uint64_t)c.ffn, (uint64_t)c.d);
@@ -344,7 +361,7 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   else ok = tmap_matrix(&tw, call.W, call.w_rows, (uint64_t)call.k_dim, (uint32_t)kTcBM);
   ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)g.bn);
   if (!ok) return PE_ERR_CUDA;
-  PE_TRY_CUDA(launch_gemm_tc(call.epi, tw, tx, a, g.grid, g.smem, g.k_splits, s));
+  PE_TRY_CUDA(launch_gemm_tc(call.epi, tw, tx, a, g.grid, g.smem, s));
   return PE_OK;
 }
 
@@ -390,7 +407,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   ia.target_items = p.attn_target; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
   ia.items = at<int4>(ws, p.items); ia.n_items = at<int32_t>(ws, p.n_items);
   ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
-  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1;
+  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1 + p.n_split_ctr;
   ia.keys = at<unsigned long long>(ws, p.keys); ia.err = err;
   PE_TRY_CUDA(launch_forward_init(ia, s));
   trace(3, s);
@@ -411,7 +428,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   {
     GemmArgs a = base;
     a.out_f32 = x; a.ld_out = c.d;
-    GemmCall call{EPI_STORE_F32, &p.fc, w->fc, x0, 2 * c.d, c.d, p.R, n_valid, 0, (uint64_t)c.d};
+    GemmCall call{EPI_STORE_F32, &p.fc, w->fc, x0, 2 * c.d, c.d, p.R, n_valid, 0, (uint64_t)c.d, 0};
     pe_status st = run_gemm(c, p, ws, call, a, s);
     if (st != PE_OK) return st;
   }
@@ -439,7 +456,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     {
       GemmArgs a = base;
       a.out_act = qb; a.ld_out = c.n_q * hd; a.k_cache = kv->k_cache[l]; a.v_cache = kv->v_cache[l];
-      GemmCall call{EPI_QKV_ROPE, &p.qkv, w->wqkv[l], y, c.d, heads * hd / 2, p.R, n_valid, 2, 0};
+      GemmCall call{EPI_QKV_ROPE, &p.qkv, w->wqkv[l], y, c.d, heads * hd / 2, p.R, n_valid, 2, 0, 1 + 4 * l};
       pe_status st = run_gemm(c, p, ws, call, a, s);
       if (st != PE_OK) return st;
     }
@@ -458,7 +475,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     {
       GemmArgs a = base;
       a.out_f32 = x; a.ld_out = c.d;
-      GemmCall call{EPI_ADD_F32, &p.o, w->wo[l], ao, c.n_q * hd, c.d, p.R, n_valid, 0, (uint64_t)c.d};
+      GemmCall call{EPI_ADD_F32, &p.o, w->wo[l], ao, c.n_q * hd, c.d, p.R, n_valid, 0, (uint64_t)c.d, 2 + 4 * l};
       pe_status st = run_gemm(c, p, ws, call, a, s);
       if (st != PE_OK) return st;
     }
@@ -469,7 +486,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     {
       GemmArgs a = base;
       a.out_act = u; a.ld_out = c.ffn;
-      GemmCall call{EPI_SWIGLU, &p.gu, w->w_gate_up[l], y, c.d, c.ffn, p.R, n_valid, 1, 0};
+      GemmCall call{EPI_SWIGLU, &p.gu, w->w_gate_up[l], y, c.d, c.ffn, p.R, n_valid, 1, 0, 3 + 4 * l};
       pe_status st = run_gemm(c, p, ws, call, a, s);
       if (st != PE_OK) return st;
     }
@@ -477,7 +494,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     {
       GemmArgs a = base;
       a.out_f32 = x; a.ld_out = c.d;
-      GemmCall call{EPI_ADD_F32, &p.down, w->w_down[l], u, c.ffn, c.d, p.R, n_valid, 0, (uint64_t)c.d};
+      GemmCall call{EPI_ADD_F32, &p.down, w->w_down[l], u, c.ffn, c.d, p.R, n_valid, 0, (uint64_t)c.d, 4 + 4 * l};
       pe_status st = run_gemm(c, p, ws, call, a, s);
       if (st != PE_OK) return st;
     }
@@ -494,7 +511,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     GemmArgs a = base;
     a.keys = ia.keys; a.logits_dbg = logits_dbg; a.done_counter = at<int32_t>(ws, p.done);
     a.draft_out = draft_tokens;
-    GemmCall call{EPI_ARGMAX, &p.lm, w->lm_head, yl, c.d, c.vocab, p.T, nullptr, 0, (uint64_t)c.vocab};
+    GemmCall call{EPI_ARGMAX, &p.lm, w->lm_head, yl, c.d, c.vocab, p.T, nullptr, 0, (uint64_t)c.vocab, -1};
     pe_status st = run_gemm(c, p, ws, call, a, s);
     if (st != PE_OK) return st;
   }

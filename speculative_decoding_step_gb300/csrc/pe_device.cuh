@@ -134,6 +134,7 @@ PE_DEV void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
 PE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 PE_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 PE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+PE_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // ----------------------------------------------------------------------------- tcgen05 (TMEM + MMA)
 
@@ -269,30 +270,23 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 
 constexpr uint32_t kIdescTransposeB = 1u << 16;
 
-// ----------------------------------------------------------------------------- thread-block clusters
-// Distributed shared memory: a CTA reads a peer CTA's shared memory through the
-// cluster window (mapa + ld.shared::cluster).  The cluster barrier is entered
-// by every thread of every CTA of the cluster.
+// ----------------------------------------------------------------------------- grid-wide counters
 
-PE_DEV uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-PE_DEV void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-PE_DEV uint32_t dsmem_map(uint32_t local_smem, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
-  return r;
-}
-// No memory clobber: the compiler may batch these loads and schedule their
-// consumers later; volatile keeps them after the preceding cluster barrier.
-PE_DEV float dsmem_ld1(uint32_t cluster_addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
-  return v;
+// Wait until *p >= target (acquire).  Bounded like every other wait: on expiry it
+// records PE_DEV_TIMEOUT and returns false.  Used only between CTAs that are
+// resident together (cooperative launch).
+PE_DEV bool wait_counter_geq(const int32_t* p, int target, int32_t* err) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      set_err(err, PE_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(32);
+  }
 }
 
 // ----------------------------------------------------------------------------- programmatic dependent launch

@@ -8,8 +8,9 @@
 // matrix sits on the MMA's M side (128 weight rows per tile) and the few
 // token rows on its N side, so a batch of 16..256 rows reads every weight
 // byte once.  Split-K spreads small matrices over all SMs; the splits of a
-// tile form a thread-block cluster and sum their partials through distributed
-// shared memory in a fixed order, so the result does not depend on scheduling.
+// tile leave fp32 partials in L2, meet at a per-tile arrival counter and each
+// sums a slice of the tile's columns in a fixed order, so the result does not
+// depend on scheduling.
 // The LM head never writes logits: each
 // CTA reduces its 128 vocabulary rows to a (max, argmax) key per token and
 // folds it into a global 64-bit atomicMax; the last CTA decodes the keys.
@@ -158,13 +159,17 @@ PE_DEV void argmax_finish(const GemmArgs& a, int n_tok, int thread, int nthreads
 // accumulator.  Before waiting on the previous kernel (pdl_wait) the producer
 // already streams the weights of its first unit: they never depend on it.
 //
-// Split K: the k_splits CTAs of one tile form a thread-block cluster (one unit
-// per CTA).  Each leaves its fp32 partial tile in its own shared memory; after
-// a cluster barrier, CTA rank q sums a 1/k_splits slice of the tile's columns
-// over all ranks through distributed shared memory (starting at its own rank and
-// walking the ring, so each CTA's shared memory serves one reader at a time),
-// and runs the epilogue on it.  No partial sums leave the chip and no CTA waits for a
-// straggler.
+// Split K: one unit per CTA, at most one CTA per SM, cooperative launch (the
+// splits of a tile are resident together).  Each split stages its fp32 partial
+// tile column-major in its idle stage ring (a token column's 128 rows are 512
+// contiguous bytes), bulk-stores it to the workspace, then adds one to the
+// tile's arrival counter and waits, bounded, until every split of the tile has
+// arrived.  Split q then fetches its 1/k_splits slice of the tile's token
+// columns from every split with one bulk copy each, sums them in shared memory
+// (starting at its own split and walking the ring, a fixed order per column)
+// and runs the epilogue on it.  Using every SM matters more here than the partials' round trip through
+// L2: the weight stream of a small GEMM is spread over all SMs, and each CTA's
+// ring holds nearly all of its weights before the previous kernel has finished.
 
 size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int red_entries) {
   return 1024 /*alignment slack*/ + (size_t)stages * stage_bytes + kTcCtrlBytes + (size_t)red_entries * 8;
@@ -196,7 +201,7 @@ PE_DEV int live_token_tiles(const GemmArgs& a, int n_tok) {
 
 PE_DEV Unit decode_unit(const GemmArgs& a, int u, int n_t_live) {
   Unit w;
-  w.split = u % a.k_splits;  // splits of a tile are consecutive: they form one cluster
+  w.split = u % a.k_splits;  // splits of a tile are consecutive (one arrival counter per tile)
   const int r = u / a.k_splits;
   w.tile_t = r % n_t_live;   // token tiles of a weight tile run side by side (L2 reuse)
   w.tile_f = r / n_t_live;
@@ -295,6 +300,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
+  uint64_t* rbar = reinterpret_cast<uint64_t*>(ctrl + 512);  // split K: partial slices landed
   unsigned long long* red = reinterpret_cast<unsigned long long*>(ctrl + kTcCtrlBytes);  // [4 warps][NT]
   const uint32_t b_off = (PAIRED ? 2u : 1u) * A_BYTES;
 
@@ -309,6 +315,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_u32(tfull + b), 1);
       mbar_init(smem_u32(tempty + b), 4);  // one arrival per epilogue warp
     }
+    mbar_init(smem_u32(rbar), 1);
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbar_init();
@@ -446,22 +453,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, tf);
         }
       } else if (ok) {
-        // split K (one unit per CTA, the stage ring is idle): leave this split's partial
-        // tile in shared memory for the cluster reduction below, column-major
-        // ([plane][token column][128 rows] fp32) so a warp's 32 rows of one column are
-        // 128 contiguous bytes: conflict-free here, one packet per remote load there
+        // split K (one unit per CTA; the stage ring is idle): this split's partial tile,
+        // column-major ([plane][token column][128 rows] fp32, conflict-free), into shared
+        // memory for one bulk store per plane
         float* P = reinterpret_cast<float*>(smem);
-        for (int c = 0; c < BN / 16; ++c) {
-          float v[16];
-          tmem_load16(tl + (uint32_t)(c * 16), v);
+        // (64-column TMEM loads only at 64-aligned columns, 16-column ones elsewhere)
+        const int cend = (PAIRED ? 2 : 1) * BN;
+        for (int c = 0; c < cend;) {
+          if ((c & 63) == 0 && c + 64 <= cend) {
+            float v[64];
+            tmem_load64(tl + (uint32_t)c, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) P[(size_t)(c * 16 + j) * kTcBM + r] = v[j];
-          if (PAIRED) {
-            tmem_load16(tl + (uint32_t)(BN + c * 16), v);
+            for (int j = 0; j < 64; ++j) P[(size_t)(c + j) * kTcBM + r] = v[j];
+            c += 64;
+          } else {
+            float v[16];
+            tmem_load16(tl + (uint32_t)c, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) P[(size_t)(BN + c * 16 + j) * kTcBM + r] = v[j];
+            for (int j = 0; j < 16; ++j) P[(size_t)(c + j) * kTcBM + r] = v[j];
+            c += 16;
           }
         }
+        fence_proxy_async_smem();  // the bulk store reads what these generic stores wrote
       }
       tc_fence_before();
       __syncwarp();
@@ -491,68 +504,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
-  if (EPI != EPI_ARGMAX && a.k_splits > 1) {
-    // cluster reduction of the split-K partial tiles (every thread takes part in the barriers)
-    __syncwarp();
-    cluster_sync_all();  // every rank's partial tile is in its shared memory
-    if (warp >= 2) {
-      const int n_tok = effective_ntok(a);
-      const int ntl = live_token_tiles(a, n_tok);
+  if (EPI != EPI_ARGMAX && a.k_splits > 1 && warp >= 2) {
+    // split-K reduction (epilogue warps only)
+    const int n_tok = effective_ntok(a);
+    const int ntl = live_token_tiles(a, n_tok);
+    const int ns = a.k_splits;
+    if ((int)blockIdx.x < ntl * a.n_f * ns) {
       const Unit w = decode_unit(a, blockIdx.x, ntl);
-      if ((int)blockIdx.x < ntl * a.n_f * a.k_splits) {
-        const int ns = a.k_splits;
-        const uint32_t rank = cluster_ctarank();
-        const int cs = (((BN + ns - 1) / ns) + 3) & ~3;
-        const int c0 = (int)rank * cs, c1 = min(BN, c0 + cs);
+      constexpr int PL = PAIRED ? 2 : 1;
+      const size_t tile_floats = (size_t)PL * BN * kTcBM;
+      const int rank = w.split;
+      const int cs = (((BN + ns - 1) / ns) + 3) & ~3;
+      const int c0 = rank * cs, c1 = min(BN, c0 + cs);
+      const float* part0 = a.partial + (size_t)(blockIdx.x - rank) * tile_floats;  // split 0 of the tile
+      // 1. publish: bulk store of the partial tile, then the tile's arrival counter
+      named_bar_sync(2, 128);
+      if (threadIdx.x == 64) {
+        bulk_s2g(a.partial + (size_t)blockIdx.x * tile_floats, smem_u32(smem), (uint32_t)(tile_floats * 4));
+        bulk_commit();
+        bulk_wait_all();            // the tile is in global memory
+        fence_proxy_async_global();
+        __threadfence();
+        int32_t* ctr = a.tile_counters + blockIdx.x / ns;
+        atomicAdd(ctr, 1);
+        // 2. wait for the tile's other splits, then fetch this rank's column slice of
+        //    every split (one bulk copy per split and plane) into the idle ring
+        bool ok = wait_counter_geq(ctr, ns, a.err);
+        if (ok && c1 > c0) {
+          fence_proxy_async_global();
+          const uint32_t slice = (uint32_t)(c1 - c0) * kTcBM * 4;
+          mbar_expect_tx(smem_u32(rbar), slice * PL * ns);
+          for (int j = 0; j < ns; ++j)
+            for (int pl = 0; pl < PL; ++pl)
+              bulk_g2s(smem_u32(smem) + (uint32_t)(j * PL + pl) * slice,
+                       part0 + (size_t)((rank + j) % ns) * tile_floats + (size_t)(pl * BN + c0) * kTcBM, slice,
+                       smem_u32(rbar));
+          ok = mbar_wait(smem_u32(rbar), 0, a.err, nullptr);
+        }
+        if (!ok) *abort_flag = 1;
+      }
+      named_bar_sync(2, 128);
+      // 3. sum the slices in shared memory (split `rank` first, then the ring: a fixed
+      //    order per column) and run the epilogue
+      if (!*abort_flag && c1 > c0) {
         const int r = (warp & 3) * 32 + lane;
         const int unit = w.tile_f * kTcBM + r;
         const float2 tf = (EPI == EPI_QKV_ROPE) ? rope_tf(a, unit) : make_float2(0.f, 0.f);
-        const uint32_t base = smem_u32(smem);
-        // Rank p starts at its own tile and walks the ring (rank + j) % ns: at any moment
-        // every CTA's shared memory serves one reader, not the whole cluster.  The order
-        // of the sum is fixed per output column, so the result does not depend on timing.
-        // The loads of the next peer are in flight while the current one is added.
+        const float* R = reinterpret_cast<const float*>(smem);
+        const int scols = c1 - c0;
         for (int col0 = c0; col0 < c1; col0 += 16) {
           const int ncol = min(16, c1 - col0);  // a multiple of 4
           float v[16], v2[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = v2[j] = 0.f;
-          float x[2][16], y[2][16];
-          auto load_peer = [&](int j, float* xd, float* yd) {
-            const uint32_t peer = dsmem_map(base, (rank + (uint32_t)j) % (uint32_t)ns);
+          for (int q = 0; q < 16; ++q) v[q] = v2[q] = 0.f;
+          for (int j = 0; j < ns; ++j) {
+            const float* sx = R + ((size_t)(j * PL) * scols + (col0 - c0)) * kTcBM + r;
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
+            for (int q = 0; q < 16; ++q)
               if (q < ncol) {
-                xd[q] = dsmem_ld1(peer + 4u * (uint32_t)((col0 + q) * kTcBM + r));
-                if (PAIRED) yd[q] = dsmem_ld1(peer + 4u * (uint32_t)((BN + col0 + q) * kTcBM + r));
+                v[q] += sx[(size_t)q * kTcBM];
+                if (PAIRED) v2[q] += sx[((size_t)scols + q) * kTcBM];
               }
-            }
-          };
-          auto add_peer = [&](const float* xs, const float* ys) {
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              if (q < ncol) {
-                v[q] += xs[q];
-                if (PAIRED) v2[q] += ys[q];
-              }
-            }
-          };
-          load_peer(0, x[0], y[0]);
-          for (int j = 0; j < ns; j += 2) {  // two peers per trip keeps the buffers in registers
-            if (j + 1 < ns) load_peer(j + 1, x[1], y[1]);
-            add_peer(x[0], y[0]);
-            if (j + 1 < ns) {
-              if (j + 2 < ns) load_peer(j + 2, x[0], y[0]);
-              add_peer(x[1], y[1]);
-            }
           }
           const int t0 = w.tile_t * BN + col0;
           if (unit < a.n_out) epi_chunk<EPI, __nv_bfloat16>(a, unit, t0, max(0, min(ncol, n_tok - t0)), v, v2, tf);
         }
       }
     }
-    __syncwarp();
-    cluster_sync_all();  // peers are done reading this CTA's shared memory
   }
   __syncthreads();
   if (warp == 1) {
@@ -579,68 +597,22 @@ static cudaError_t ensure_smem_attr() {
 
 template <int EPI>
 static cudaError_t launch_tc_typed(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
-                                   size_t smem, int cluster, cudaStream_t s) {
+                                   size_t smem, cudaStream_t s) {
   const cudaError_t e = ensure_smem_attr<EPI>();
   if (e != cudaSuccess) return e;
-  return launch_pdl_cluster(gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), smem, s, cluster, tmW, tmX, a);
+  return launch_pdl_coop(gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), smem, s, a.k_splits > 1, tmW, tmX, a);
 }
 
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
-                           size_t smem, int cluster, cudaStream_t s) {
+                           size_t smem, cudaStream_t s) {
   switch (epi) {
-    case EPI_STORE_F32: return launch_tc_typed<EPI_STORE_F32>(tmW, tmX, a, grid, smem, cluster, s);
-    case EPI_ADD_F32: return launch_tc_typed<EPI_ADD_F32>(tmW, tmX, a, grid, smem, cluster, s);
-    case EPI_SWIGLU: return launch_tc_typed<EPI_SWIGLU>(tmW, tmX, a, grid, smem, cluster, s);
-    case EPI_QKV_ROPE: return launch_tc_typed<EPI_QKV_ROPE>(tmW, tmX, a, grid, smem, cluster, s);
-    case EPI_ARGMAX: return launch_tc_typed<EPI_ARGMAX>(tmW, tmX, a, grid, smem, cluster, s);
+    case EPI_STORE_F32: return launch_tc_typed<EPI_STORE_F32>(tmW, tmX, a, grid, smem, s);
+    case EPI_ADD_F32: return launch_tc_typed<EPI_ADD_F32>(tmW, tmX, a, grid, smem, s);
+    case EPI_SWIGLU: return launch_tc_typed<EPI_SWIGLU>(tmW, tmX, a, grid, smem, s);
+    case EPI_QKV_ROPE: return launch_tc_typed<EPI_QKV_ROPE>(tmW, tmX, a, grid, smem, s);
+    case EPI_ARGMAX: return launch_tc_typed<EPI_ARGMAX>(tmW, tmX, a, grid, smem, s);
   }
   return cudaErrorInvalidValue;
-}
-
-template <int EPI>
-static int max_clusters_typed(size_t smem, int cluster) {
-  if (ensure_smem_attr<EPI>() != cudaSuccess) return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cluster * 64);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI>, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
-}
-
-int gemm_tc_max_active_clusters(int epi, size_t smem, int cluster) {
-  // the answer depends only on (device, variant, shared memory, cluster size): cache it
-  struct Entry {
-    int dev, epi, cluster, n;
-    size_t smem;
-  };
-  static std::mutex mu;
-  static std::vector<Entry> cache;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  std::lock_guard<std::mutex> lk(mu);
-  for (const Entry& e : cache)
-    if (e.dev == dev && e.epi == epi && e.cluster == cluster && e.smem == smem) return e.n;
-  int n = 0;
-  switch (epi) {
-    case EPI_STORE_F32: n = max_clusters_typed<EPI_STORE_F32>(smem, cluster); break;
-    case EPI_ADD_F32: n = max_clusters_typed<EPI_ADD_F32>(smem, cluster); break;
-    case EPI_SWIGLU: n = max_clusters_typed<EPI_SWIGLU>(smem, cluster); break;
-    case EPI_QKV_ROPE: n = max_clusters_typed<EPI_QKV_ROPE>(smem, cluster); break;
-  }
-  cache.push_back(Entry{dev, epi, cluster, n, smem});
-  return n;
 }
 
 // ============================================================================= fp32 CUDA-core kernel

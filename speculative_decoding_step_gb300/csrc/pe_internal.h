@@ -36,10 +36,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
-// As launch_pdl, with thread-block clusters of `cluster` CTAs along x (1: no cluster).
+// As launch_pdl; `cooperative` asks for every CTA of the grid to be resident at
+// once (for kernels whose CTAs wait for one another).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                               int cluster, Args&&... args) {
+cudaError_t launch_pdl_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            bool cooperative, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -48,10 +49,8 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = cluster > 1 ? cluster : 1;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = cooperative ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   count_launch();
@@ -168,18 +167,18 @@ struct GemmArgs {
   unsigned long long* keys;  // LM head: one key per token (zero before the launch)
   float* logits_dbg;         // nullable [tokens][n_out]
   int32_t* done_counter;     // LM head: CTAs finished (zero before the launch)
+  float* partial;            // split K: [grid][planes][bn][128] fp32 partial tiles (column-major per plane)
+  int32_t* tile_counters;    // split K: arrivals per tile (zero before the launch)
   int32_t* draft_out;        // LM head: argmax per token
   int32_t* err;
 };
 
 // Tensor-core GEMM (tcgen05 + TMA): D[f][t] = W[f][:] . X[t][:], weights on the MMA M side.
 // Persistent: `grid` CTAs (at most one per SM) stride over the work units.  With
-// k_splits > 1 every CTA owns exactly one unit and the splits of a tile form a
-// cluster of `cluster` (= k_splits) CTAs.
+// k_splits > 1 every CTA owns exactly one unit, the grid is at most one CTA per SM
+// and the launch is cooperative (the splits of a tile wait for one another).
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
-                           size_t smem_bytes, int cluster, cudaStream_t s);
-// Clusters of `cluster` CTAs of this GEMM variant that fit on the GPU at once (0 if unknown).
-int gemm_tc_max_active_clusters(int epi, size_t smem_bytes, int cluster);
+                           size_t smem_bytes, cudaStream_t s);
 // fp32 CUDA-core GEMM for fp32 configurations (same epilogues).
 cudaError_t launch_gemm_f32(int epi, const GemmArgs& a, cudaStream_t s);
 
