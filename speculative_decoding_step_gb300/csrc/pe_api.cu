@@ -41,7 +41,7 @@ constexpr int kMaxRows = 1 << 16;        // B*2K
 constexpr int kAttnItemsPerSlot = 4;     // attention work items aimed for, per resident CTA (load balance)
 constexpr int kAttnMinChunk = 256;       // shortest position chunk of a work item (bounds the chunks to merge)
 constexpr int kTcMaxStages = 12;
-constexpr int kMaxSplits = 16;           // split-K ways per tile
+constexpr int kMaxSplits = 16;           // split-K ways per tile (the RMSNorm that sums deferred partials takes up to 16)
 
 int num_sms() {
   static int cached[64] = {0};
@@ -73,9 +73,8 @@ struct GemmPlan {
 
 // Work decomposition of one GEMM: 128 weight rows x bn token rows per tile.
 // With fewer tiles than SMs, split K so that nearly every SM streams weights:
-// every CTA owns exactly one unit and the grid is at most one CTA per SM (the
-// splits of a tile wait for one another, so they must be resident together);
-// each split keeps at least four 64-wide k blocks.
+// every CTA owns exactly one unit and leaves an fp32 partial tile for the
+// consumer to sum; each split keeps at least four 64-wide k blocks.
 GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   GemmPlan g;
   g.epi = epi;
@@ -95,17 +94,8 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   const long long avail = kTcSmemOptIn - 1024 - kTcCtrlBytes - (long long)red * 8;
   g.stages = (int)std::min<long long>(kTcMaxStages, avail / g.stage_bytes);
   g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, red);
-  if (epi != EPI_ARGMAX && g.tiles < sms) {
-    // the partial tile, and every split's slice of this rank's columns, are staged in the stage ring
-    const size_t ring = (size_t)g.stages * g.stage_bytes;
-    const int planes = paired ? 2 : 1;
-    int s = std::max(1, std::min(kMaxSplits, std::min(sms / g.tiles, g.kb_total / 4)));
-    for (; s > 1; --s) {
-      const size_t cs = (size_t)((((g.bn + s - 1) / s) + 3) & ~3);
-      if ((size_t)planes * g.bn * kTcBM * 4 <= ring && (size_t)s * planes * cs * kTcBM * 4 <= ring) break;
-    }
-    g.k_splits = s;
-  }
+  if (epi != EPI_ARGMAX && g.tiles < sms)
+    g.k_splits = std::max(1, std::min(kMaxSplits, std::min(sms / g.tiles, g.kb_total / 4)));
   const int acc_cols = (paired ? 2 : 1) * g.bn;
   g.nbuf = 2 * acc_cols <= 512 ? 2 : 1;
   g.acc_stride = acc_cols;
@@ -121,7 +111,6 @@ struct Plan {
   // workspace offsets
   size_t tok_pos, tok_seq, tok_slot, seq_start, seq_len, seq_maxpos, item_base, n_chunks, n_items, items;
   size_t done, keys, x, y, q, ao, u, yl, part_m, part_l, part_o, split_part;
-  int n_split_ctr = 0;  // split-K arrival counters after the LM-head counter
   size_t st_ids, st_pos, st_slot, st_rej, st_mask, st_hmap, st_rows, st_nvalid, st_draft, st_x0;
   size_t total = 0;
 };
@@ -167,10 +156,7 @@ Plan make_plan(const pe_config& c) {
   p.n_chunks = take(4 * (size_t)c.B);
   p.n_items = take(4);
   p.items = take(16 * (size_t)p.max_items);
-  // LM-head completion counter, then one block of split-K arrival counters per GEMM
-  // launch (fc, then qkv, o, gate/up, down per layer), p.sms per block (tiles < SMs)
-  p.n_split_ctr = (1 + 4 * c.n_layers) * p.sms;
-  p.done = take(4 * (1 + (size_t)p.n_split_ctr));
+  p.done = take(4);  // LM-head completion counter
   p.keys = take(8 * (size_t)p.T);
   p.x = take(4 * (size_t)p.R * c.d);
   p.y = take(eb * (size_t)p.R * c.d);
@@ -323,7 +309,6 @@ struct GemmCall {
   // tensor-map shapes of W
   int w_kind;  // 0: matrix [w_rows][k_dim], 1: gate/up, 2: qkv
   uint64_t w_rows;
-  int slot;    // block of split-K arrival counters (GEMM launch index in the pass)
 };
 
 pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& call, GemmArgs a, cudaStream_t s) {
@@ -350,10 +335,7 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   a.acc_stride = g.acc_stride;
   a.tmem_cols = g.tmem_cols;
   a.n_tok_min = call.n_tok_dev != nullptr ? std::min(call.n_tok, c.B * c.K) : call.n_tok;
-  if (g.k_splits > 1) {
-    a.partial = at<float>(ws, p.split_part);
-    a.tile_counters = at<int32_t>(ws, p.done) + 1 + (size_t)call.slot * p.sms;
-  }
+  if (g.k_splits > 1) a.partial = at<float>(ws, p.split_part);
   CUtensorMap tw, tx;
   bool ok;
   if (call.w_kind == 1) ok = tmap_gate_up(&tw, call.W, (uint64_t)c.ffn, (uint64_t)c.d);
@@ -362,6 +344,8 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)g.bn);
   if (!ok) return PE_ERR_CUDA;
   PE_TRY_CUDA(launch_gemm_tc(call.epi, tw, tx, a, g.grid, g.smem, s));
+  if (g.k_splits > 1 && (call.epi == EPI_QKV_ROPE || call.epi == EPI_SWIGLU))
+    PE_TRY_CUDA(launch_splitk_finish(call.epi, a, p.sms, s));
   return PE_OK;
 }
 
@@ -407,7 +391,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   ia.target_items = p.attn_target; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
   ia.items = at<int4>(ws, p.items); ia.n_items = at<int32_t>(ws, p.n_items);
   ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
-  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1 + p.n_split_ctr;
+  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1;
   ia.keys = at<unsigned long long>(ws, p.keys); ia.err = err;
   PE_TRY_CUDA(launch_forward_init(ia, s));
   trace(3, s);
@@ -424,11 +408,24 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   void* yl = at<uint8_t>(ws, p.yl);
   const int heads = c.n_q + 2 * c.n_kv;
 
+  // fc, o-proj and down leave their split-K partials to the RMSNorm that follows them, which
+  // sums them (plus the residual) while it normalises (QKV and gate/up: splitk_finish_kernel)
+  auto deferred = [&](const GemmPlan& g) { return bf16 && g.k_splits > 1; };
+  auto norm_after = [&](NormArgs& n, const GemmPlan& g, bool residual, bool keep_x) {
+    if (deferred(g)) {
+      n.part = at<float>(ws, p.split_part); n.n_splits = g.k_splits; n.bn = g.bn; n.n_t = g.n_t;
+      n.g_ntok = p.R; n.g_ntok_dev = n_valid; n.g_ntok_min = std::min(p.R, c.B * c.K);
+      n.x = residual ? x : nullptr; n.x_out = keep_x ? x : nullptr;
+    } else {
+      n.part = nullptr; n.n_splits = 0; n.x = x; n.x_out = nullptr;
+    }
+  };
+
   // fc: x = X0 . W_fc^T
   {
     GemmArgs a = base;
     a.out_f32 = x; a.ld_out = c.d;
-    GemmCall call{EPI_STORE_F32, &p.fc, w->fc, x0, 2 * c.d, c.d, p.R, n_valid, 0, (uint64_t)c.d, 0};
+    GemmCall call{EPI_STORE_F32, &p.fc, w->fc, x0, 2 * c.d, c.d, p.R, n_valid, 0, (uint64_t)c.d};
     pe_status st = run_gemm(c, p, ws, call, a, s);
     if (st != PE_OK) return st;
   }
@@ -451,12 +448,14 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   for (int l = 0; l < c.n_layers; ++l) {
     const int tp = 5 + 7 * l;
     na.g = w->norm_attn[l];
+    if (l == 0) norm_after(na, p.fc, false, true);
+    else norm_after(na, p.down, true, true);
     PE_TRY_CUDA(launch_rmsnorm(na, c.dtype, s));
     trace(tp + 0, s);
     {
       GemmArgs a = base;
       a.out_act = qb; a.ld_out = c.n_q * hd; a.k_cache = kv->k_cache[l]; a.v_cache = kv->v_cache[l];
-      GemmCall call{EPI_QKV_ROPE, &p.qkv, w->wqkv[l], y, c.d, heads * hd / 2, p.R, n_valid, 2, 0, 1 + 4 * l};
+      GemmCall call{EPI_QKV_ROPE, &p.qkv, w->wqkv[l], y, c.d, heads * hd / 2, p.R, n_valid, 2, 0};
       pe_status st = run_gemm(c, p, ws, call, a, s);
       if (st != PE_OK) return st;
     }
@@ -475,18 +474,19 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     {
       GemmArgs a = base;
       a.out_f32 = x; a.ld_out = c.d;
-      GemmCall call{EPI_ADD_F32, &p.o, w->wo[l], ao, c.n_q * hd, c.d, p.R, n_valid, 0, (uint64_t)c.d, 2 + 4 * l};
+      GemmCall call{EPI_ADD_F32, &p.o, w->wo[l], ao, c.n_q * hd, c.d, p.R, n_valid, 0, (uint64_t)c.d};
       pe_status st = run_gemm(c, p, ws, call, a, s);
       if (st != PE_OK) return st;
     }
     trace(tp + 3, s);
     na.g = w->norm_mlp[l];
+    norm_after(na, p.o, true, true);
     PE_TRY_CUDA(launch_rmsnorm(na, c.dtype, s));
     trace(tp + 4, s);
     {
       GemmArgs a = base;
       a.out_act = u; a.ld_out = c.ffn;
-      GemmCall call{EPI_SWIGLU, &p.gu, w->w_gate_up[l], y, c.d, c.ffn, p.R, n_valid, 1, 0, 3 + 4 * l};
+      GemmCall call{EPI_SWIGLU, &p.gu, w->w_gate_up[l], y, c.d, c.ffn, p.R, n_valid, 1, 0};
       pe_status st = run_gemm(c, p, ws, call, a, s);
       if (st != PE_OK) return st;
     }
@@ -494,7 +494,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     {
       GemmArgs a = base;
       a.out_f32 = x; a.ld_out = c.d;
-      GemmCall call{EPI_ADD_F32, &p.down, w->w_down[l], u, c.ffn, c.d, p.R, n_valid, 0, (uint64_t)c.d, 4 + 4 * l};
+      GemmCall call{EPI_ADD_F32, &p.down, w->w_down[l], u, c.ffn, c.d, p.R, n_valid, 0, (uint64_t)c.d};
       pe_status st = run_gemm(c, p, ws, call, a, s);
       if (st != PE_OK) return st;
     }
@@ -505,13 +505,14 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   NormArgs nf = na;
   nf.row_map = draft_rows; nf.n_rows = p.T; nf.n_rows_dev = nullptr; nf.src_rows = p.R; nf.g = w->norm_final;
   nf.y = yl;
+  norm_after(nf, p.down, true, false);  // the residual after the last layer is needed only here
   PE_TRY_CUDA(launch_rmsnorm(nf, c.dtype, s));
   trace(tf, s);
   {
     GemmArgs a = base;
     a.keys = ia.keys; a.logits_dbg = logits_dbg; a.done_counter = at<int32_t>(ws, p.done);
     a.draft_out = draft_tokens;
-    GemmCall call{EPI_ARGMAX, &p.lm, w->lm_head, yl, c.d, c.vocab, p.T, nullptr, 0, (uint64_t)c.vocab, -1};
+    GemmCall call{EPI_ARGMAX, &p.lm, w->lm_head, yl, c.d, c.vocab, p.T, nullptr, 0, (uint64_t)c.vocab};
     pe_status st = run_gemm(c, p, ws, call, a, s);
     if (st != PE_OK) return st;
   }

@@ -270,25 +270,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 
 constexpr uint32_t kIdescTransposeB = 1u << 16;
 
-// ----------------------------------------------------------------------------- grid-wide counters
-
-// Wait until *p >= target (acquire).  Bounded like every other wait: on expiry it
-// records PE_DEV_TIMEOUT and returns false.  Used only between CTAs that are
-// resident together (cooperative launch).
-PE_DEV bool wait_counter_geq(const int32_t* p, int target, int32_t* err) {
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    if (v >= target) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      set_err(err, PE_DEV_TIMEOUT);
-      return false;
-    }
-    __nanosleep(32);
-  }
-}
-
 // ----------------------------------------------------------------------------- programmatic dependent launch
 // Kernels are launched so that the next kernel of the round may start while
 // this one drains: pdl_trigger() lets the dependent grid launch, pdl_wait()

@@ -7,10 +7,9 @@
 // issues tcgen05.mma with fp32 accumulators in tensor memory.  The weight
 // matrix sits on the MMA's M side (128 weight rows per tile) and the few
 // token rows on its N side, so a batch of 16..256 rows reads every weight
-// byte once.  Split-K spreads small matrices over all SMs; the splits of a
-// tile leave fp32 partials in L2, meet at a per-tile arrival counter and each
-// sums a slice of the tile's columns in a fixed order, so the result does not
-// depend on scheduling.
+// byte once.  Split-K spreads small matrices over all SMs; the splits leave
+// fp32 partials in L2 and the consuming kernel sums them in a fixed order, so
+// the result does not depend on scheduling.
 // The LM head never writes logits: each
 // CTA reduces its 128 vocabulary rows to a (max, argmax) key per token and
 // folds it into a global 64-bit atomicMax; the last CTA decodes the keys.
@@ -45,6 +44,26 @@ PE_DEV void rope_pair(float x1, float x2, int pos, float2 tf, float& o1, float& 
 // unit = head * (hd/2) + i for the pair (i, i + hd/2) of `head` in the
 // q | k | v concatenation.  q and k are rotated; q goes to the q buffer, k and
 // v to the paged cache at the token's slot (no write for slot -1).
+// As epi_qkv, with the token's position and KV slot already loaded.
+template <typename T>
+PE_DEV void qkv_store(const GemmArgs& a, int unit, int t, float x1, float x2, float2 tf, int pos, long long slot) {
+  const int half = a.head_dim >> 1;
+  const int head = unit / half, i = unit - head * half;
+  if (head < a.n_q + a.n_kv) rope_pair(x1, x2, pos, tf, x1, x2);
+  if (head < a.n_q) {
+    T* q = static_cast<T*>(a.out_act) + (size_t)t * a.ld_out + (size_t)head * a.head_dim + i;
+    q[0] = from_float<T>(x1);
+    q[half] = from_float<T>(x2);
+    return;
+  }
+  if (slot < 0) return;
+  const bool is_k = head < a.n_q + a.n_kv;
+  const int g = is_k ? head - a.n_q : head - a.n_q - a.n_kv;
+  T* c = static_cast<T*>(is_k ? a.k_cache : a.v_cache) + ((size_t)slot * a.n_kv + g) * a.head_dim + i;
+  c[0] = from_float<T>(x1);
+  c[half] = from_float<T>(x2);
+}
+
 template <typename T>
 PE_DEV void epi_qkv(const GemmArgs& a, int unit, int t, float x1, float x2, float2 tf) {
   const int half = a.head_dim >> 1;
@@ -159,17 +178,12 @@ PE_DEV void argmax_finish(const GemmArgs& a, int n_tok, int thread, int nthreads
 // accumulator.  Before waiting on the previous kernel (pdl_wait) the producer
 // already streams the weights of its first unit: they never depend on it.
 //
-// Split K: one unit per CTA, at most one CTA per SM, cooperative launch (the
-// splits of a tile are resident together).  Each split stages its fp32 partial
-// tile column-major in its idle stage ring (a token column's 128 rows are 512
-// contiguous bytes), bulk-stores it to the workspace, then adds one to the
-// tile's arrival counter and waits, bounded, until every split of the tile has
-// arrived.  Split q then fetches its 1/k_splits slice of the tile's token
-// columns from every split with one bulk copy each, sums them in shared memory
-// (starting at its own split and walking the ring, a fixed order per column)
-// and runs the epilogue on it.  Using every SM matters more here than the partials' round trip through
-// L2: the weight stream of a small GEMM is spread over all SMs, and each CTA's
-// ring holds nearly all of its weights before the previous kernel has finished.
+// Split K: one unit per CTA.  Each split writes its fp32 partial tile
+// column-major to the workspace and exits; the kernel that consumes the output
+// sums the splits in split order: the RMSNorm that follows fc, o-proj and down
+// (adding the residual), or splitk_finish_kernel for QKV (RoPE, q, KV cache)
+// and gate/up (SwiGLU).  No CTA waits for another, and the weight stream of a
+// small GEMM is spread over nearly all SMs.
 
 size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int red_entries) {
   return 1024 /*alignment slack*/ + (size_t)stages * stage_bytes + kTcCtrlBytes + (size_t)red_entries * 8;
@@ -300,7 +314,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
-  uint64_t* rbar = reinterpret_cast<uint64_t*>(ctrl + 512);  // split K: partial slices landed
   unsigned long long* red = reinterpret_cast<unsigned long long*>(ctrl + kTcCtrlBytes);  // [4 warps][NT]
   const uint32_t b_off = (PAIRED ? 2u : 1u) * A_BYTES;
 
@@ -315,7 +328,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_u32(tfull + b), 1);
       mbar_init(smem_u32(tempty + b), 4);  // one arrival per epilogue warp
     }
-    mbar_init(smem_u32(rbar), 1);
+
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbar_init();
@@ -453,28 +466,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, tf);
         }
       } else if (ok) {
-        // split K (one unit per CTA; the stage ring is idle): this split's partial tile,
-        // column-major ([plane][token column][128 rows] fp32, conflict-free), into shared
-        // memory for one bulk store per plane
-        float* P = reinterpret_cast<float*>(smem);
-        // (64-column TMEM loads only at 64-aligned columns, 16-column ones elsewhere)
+        // split K (one unit per CTA): this split's fp32 partial tile straight from TMEM to
+        // the workspace, column-major ([plane][token column][128 rows]: a warp's stores of
+        // one column are 128 contiguous bytes).  The next kernel sums the splits.
+        float* P = a.partial + (size_t)blockIdx.x * (PAIRED ? 2 : 1) * BN * kTcBM + r;
         const int cend = (PAIRED ? 2 : 1) * BN;
-        for (int c = 0; c < cend;) {
+        for (int c = 0; c < cend;) {  // 64-column TMEM loads only at 64-aligned columns
           if ((c & 63) == 0 && c + 64 <= cend) {
             float v[64];
             tmem_load64(tl + (uint32_t)c, v);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) P[(size_t)(c + j) * kTcBM + r] = v[j];
+            for (int j = 0; j < 64; ++j) P[(size_t)(c + j) * kTcBM] = v[j];
             c += 64;
           } else {
             float v[16];
             tmem_load16(tl + (uint32_t)c, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) P[(size_t)(c + j) * kTcBM + r] = v[j];
+            for (int j = 0; j < 16; ++j) P[(size_t)(c + j) * kTcBM] = v[j];
             c += 16;
           }
         }
-        fence_proxy_async_smem();  // the bulk store reads what these generic stores wrote
       }
       tc_fence_before();
       __syncwarp();
@@ -504,74 +515,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
-  if (EPI != EPI_ARGMAX && a.k_splits > 1 && warp >= 2) {
-    // split-K reduction (epilogue warps only)
-    const int n_tok = effective_ntok(a);
-    const int ntl = live_token_tiles(a, n_tok);
-    const int ns = a.k_splits;
-    if ((int)blockIdx.x < ntl * a.n_f * ns) {
-      const Unit w = decode_unit(a, blockIdx.x, ntl);
-      constexpr int PL = PAIRED ? 2 : 1;
-      const size_t tile_floats = (size_t)PL * BN * kTcBM;
-      const int rank = w.split;
-      const int cs = (((BN + ns - 1) / ns) + 3) & ~3;
-      const int c0 = rank * cs, c1 = min(BN, c0 + cs);
-      const float* part0 = a.partial + (size_t)(blockIdx.x - rank) * tile_floats;  // split 0 of the tile
-      // 1. publish: bulk store of the partial tile, then the tile's arrival counter
-      named_bar_sync(2, 128);
-      if (threadIdx.x == 64) {
-        bulk_s2g(a.partial + (size_t)blockIdx.x * tile_floats, smem_u32(smem), (uint32_t)(tile_floats * 4));
-        bulk_commit();
-        bulk_wait_all();            // the tile is in global memory
-        fence_proxy_async_global();
-        __threadfence();
-        int32_t* ctr = a.tile_counters + blockIdx.x / ns;
-        atomicAdd(ctr, 1);
-        // 2. wait for the tile's other splits, then fetch this rank's column slice of
-        //    every split (one bulk copy per split and plane) into the idle ring
-        bool ok = wait_counter_geq(ctr, ns, a.err);
-        if (ok && c1 > c0) {
-          fence_proxy_async_global();
-          const uint32_t slice = (uint32_t)(c1 - c0) * kTcBM * 4;
-          mbar_expect_tx(smem_u32(rbar), slice * PL * ns);
-          for (int j = 0; j < ns; ++j)
-            for (int pl = 0; pl < PL; ++pl)
-              bulk_g2s(smem_u32(smem) + (uint32_t)(j * PL + pl) * slice,
-                       part0 + (size_t)((rank + j) % ns) * tile_floats + (size_t)(pl * BN + c0) * kTcBM, slice,
-                       smem_u32(rbar));
-          ok = mbar_wait(smem_u32(rbar), 0, a.err, nullptr);
-        }
-        if (!ok) *abort_flag = 1;
-      }
-      named_bar_sync(2, 128);
-      // 3. sum the slices in shared memory (split `rank` first, then the ring: a fixed
-      //    order per column) and run the epilogue
-      if (!*abort_flag && c1 > c0) {
-        const int r = (warp & 3) * 32 + lane;
-        const int unit = w.tile_f * kTcBM + r;
-        const float2 tf = (EPI == EPI_QKV_ROPE) ? rope_tf(a, unit) : make_float2(0.f, 0.f);
-        const float* R = reinterpret_cast<const float*>(smem);
-        const int scols = c1 - c0;
-        for (int col0 = c0; col0 < c1; col0 += 16) {
-          const int ncol = min(16, c1 - col0);  // a multiple of 4
-          float v[16], v2[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) v[q] = v2[q] = 0.f;
-          for (int j = 0; j < ns; ++j) {
-            const float* sx = R + ((size_t)(j * PL) * scols + (col0 - c0)) * kTcBM + r;
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-              if (q < ncol) {
-                v[q] += sx[(size_t)q * kTcBM];
-                if (PAIRED) v2[q] += sx[((size_t)scols + q) * kTcBM];
-              }
-          }
-          const int t0 = w.tile_t * BN + col0;
-          if (unit < a.n_out) epi_chunk<EPI, __nv_bfloat16>(a, unit, t0, max(0, min(ncol, n_tok - t0)), v, v2, tf);
-        }
-      }
-    }
-  }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -600,7 +543,7 @@ static cudaError_t launch_tc_typed(const CUtensorMap& tmW, const CUtensorMap& tm
                                    size_t smem, cudaStream_t s) {
   const cudaError_t e = ensure_smem_attr<EPI>();
   if (e != cudaSuccess) return e;
-  return launch_pdl_coop(gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), smem, s, a.k_splits > 1, tmW, tmX, a);
+  return launch_pdl(gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), smem, s, tmW, tmX, a);
 }
 
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
@@ -612,6 +555,91 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& t
     case EPI_QKV_ROPE: return launch_tc_typed<EPI_QKV_ROPE>(tmW, tmX, a, grid, smem, s);
     case EPI_ARGMAX: return launch_tc_typed<EPI_ARGMAX>(tmW, tmX, a, grid, smem, s);
   }
+  return cudaErrorInvalidValue;
+}
+
+// ============================================================================= split-K finish
+//
+// Sum of the split-K partials of a QKV or gate/up GEMM and its epilogue, one
+// thread per output unit and kFinishTok consecutive tokens: RoPE + q + KV-cache
+// write, or SwiGLU.  A block of 128 threads covers one weight tile's 128 units;
+// every load of a thread (all splits of both planes, the tokens' positions and
+// slots) is in flight before the sums, which run in split order.
+constexpr int kFinishThreads = 128;
+constexpr int kFinishMaxSplits = 16;
+constexpr int kFinishTok = 2;
+
+template <int EPI, int MAXS>  // MAXS >= k_splits: bounds the registers holding the loads
+__global__ void __launch_bounds__(kFinishThreads) splitk_finish_kernel(const GemmArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int n_tok = effective_ntok(a);
+  const int ntl = live_token_tiles(a, n_tok);
+  const int ns = a.k_splits, BN = a.bn;
+  const size_t tile_floats = (size_t)2 * BN * kTcBM;  // both planes
+  const int r = threadIdx.x;
+  const int groups = (n_tok + kFinishTok - 1) / kFinishTok;
+  const long long items = (long long)a.n_f * groups;
+  for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+    const int tile_f = (int)(it / groups), t0 = (int)(it - (long long)tile_f * groups) * kFinishTok;
+    const int unit = tile_f * kTcBM + r;
+    if (unit >= a.n_out) continue;
+    float x1[kFinishTok][MAXS], x2[kFinishTok][MAXS];
+    int pos[kFinishTok];
+    long long slot[kFinishTok];
+#pragma unroll
+    for (int k = 0; k < kFinishTok; ++k) {
+      const int t = t0 + k;
+      if (t < n_tok) {
+        const int tile_t = t / BN, tt = t - tile_t * BN;
+        const float* p = a.partial + (size_t)(tile_f * ntl + tile_t) * ns * tile_floats + (size_t)tt * kTcBM + r;
+#pragma unroll
+        for (int sp = 0; sp < MAXS; ++sp)
+          if (sp < ns) {
+            x1[k][sp] = __ldcg(p + (size_t)sp * tile_floats);
+            x2[k][sp] = __ldcg(p + (size_t)sp * tile_floats + (size_t)BN * kTcBM);
+          }
+        if (EPI == EPI_QKV_ROPE) {
+          pos[k] = a.tok_pos[t];
+          slot[k] = a.tok_slot[t];
+        }
+      }
+    }
+    const float2 tf = (EPI == EPI_QKV_ROPE) ? rope_tf(a, unit) : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kFinishTok; ++k) {
+      const int t = t0 + k;
+      if (t >= n_tok) break;
+      float v = 0.f, v2 = 0.f;
+#pragma unroll
+      for (int sp = 0; sp < MAXS; ++sp)
+        if (sp < ns) {
+          v += x1[k][sp];
+          v2 += x2[k][sp];
+        }
+      if (EPI == EPI_SWIGLU) {
+        static_cast<__nv_bfloat16*>(a.out_act)[(size_t)t * a.ld_out + unit] = __float2bfloat16_rn(silu(v) * v2);
+      } else {
+        qkv_store<__nv_bfloat16>(a, unit, t, v, v2, tf, pos[k], slot[k]);
+      }
+    }
+  }
+}
+
+template <int EPI>
+static cudaError_t launch_finish_typed(const GemmArgs& a, int grid, cudaStream_t s) {
+  if (a.k_splits <= 4) return launch_pdl(splitk_finish_kernel<EPI, 4>, dim3(grid), dim3(kFinishThreads), 0, s, a);
+  if (a.k_splits <= 8) return launch_pdl(splitk_finish_kernel<EPI, 8>, dim3(grid), dim3(kFinishThreads), 0, s, a);
+  return launch_pdl(splitk_finish_kernel<EPI, kFinishMaxSplits>, dim3(grid), dim3(kFinishThreads), 0, s, a);
+}
+
+cudaError_t launch_splitk_finish(int epi, const GemmArgs& a, int sms, cudaStream_t s) {
+  if (a.k_splits > kFinishMaxSplits) return cudaErrorInvalidValue;
+  const long long items = (long long)a.n_f * ((a.n_tok + kFinishTok - 1) / kFinishTok);
+  const int grid = (int)std::min<long long>(items, 16LL * sms);
+  if (grid <= 0) return cudaSuccess;
+  if (epi == EPI_QKV_ROPE) return launch_finish_typed<EPI_QKV_ROPE>(a, grid, s);
+  if (epi == EPI_SWIGLU) return launch_finish_typed<EPI_SWIGLU>(a, grid, s);
   return cudaErrorInvalidValue;
 }
 

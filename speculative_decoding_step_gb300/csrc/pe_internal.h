@@ -36,27 +36,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
-// As launch_pdl; `cooperative` asks for every CTA of the grid to be resident at
-// once (for kernels whose CTAs wait for one another).
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                            bool cooperative, Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = cooperative ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  count_launch();
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
-}
-
 // ----------------------------------------------------------------------------- batch metadata
 
 struct PrepArgs {
@@ -112,7 +91,7 @@ cudaError_t launch_forward_init(const InitArgs& a, cudaStream_t s);
 // ----------------------------------------------------------------------------- RMSNorm
 
 struct NormArgs {
-  const float* x;            // residual stream [rows][d] fp32
+  const float* x;            // residual stream [rows][d] fp32 (nullable when partials carry the whole value)
   int d;
   const int32_t* row_map;    // output row i reads x[row_map[i]] (nullable: identity)
   int n_rows;                // host upper bound of output rows
@@ -121,6 +100,13 @@ struct NormArgs {
   const void* g;             // gains [d], storage dtype
   float eps;
   void* y;                   // [rows][d], bf16 (bf16 configs) or fp32
+  // Split-K partials of the GEMM that produced (or adds to) x, reduced here instead of in the
+  // GEMM: x_new = x + sum of n_splits partials, in split order.  n_splits = 0: x as it is.
+  const float* part;         // [units][bn][128] fp32, units numbered as the GEMM's (tile_f, tile_t, split)
+  int n_splits, bn, n_t;     // the GEMM's splits, token tile and token tiles
+  int g_ntok, g_ntok_min;    // the GEMM's token rows: host bound, rows that certainly exist
+  const int32_t* g_ntok_dev; // the GEMM's device row count (nullable)
+  float* x_out;              // nullable: where x_new is written ([rows][d], may alias x)
   int32_t* err;
 };
 cudaError_t launch_rmsnorm(const NormArgs& a, pe_dtype dt, cudaStream_t s);
@@ -168,17 +154,18 @@ struct GemmArgs {
   float* logits_dbg;         // nullable [tokens][n_out]
   int32_t* done_counter;     // LM head: CTAs finished (zero before the launch)
   float* partial;            // split K: [grid][planes][bn][128] fp32 partial tiles (column-major per plane)
-  int32_t* tile_counters;    // split K: arrivals per tile (zero before the launch)
   int32_t* draft_out;        // LM head: argmax per token
   int32_t* err;
 };
 
 // Tensor-core GEMM (tcgen05 + TMA): D[f][t] = W[f][:] . X[t][:], weights on the MMA M side.
 // Persistent: `grid` CTAs (at most one per SM) stride over the work units.  With
-// k_splits > 1 every CTA owns exactly one unit, the grid is at most one CTA per SM
-// and the launch is cooperative (the splits of a tile wait for one another).
+// k_splits > 1 every CTA owns exactly one unit and writes its fp32 partial tile to
+// `partial`; the consumer sums the splits (RMSNorm, or launch_splitk_finish).
 cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
                            size_t smem_bytes, cudaStream_t s);
+// Sum of a split-K QKV or gate/up GEMM's partials and its epilogue (the same GemmArgs).
+cudaError_t launch_splitk_finish(int epi, const GemmArgs& a, int sms, cudaStream_t s);
 // fp32 CUDA-core GEMM for fp32 configurations (same epilogues).
 cudaError_t launch_gemm_f32(int epi, const GemmArgs& a, cudaStream_t s);
 

@@ -385,31 +385,87 @@ PE_DEV void store4<__nv_bfloat16>(__nv_bfloat16* y, float a, float b, float c, f
   *reinterpret_cast<uint2*>(y) = v;
 }
 
+constexpr int kNormMaxSplits = 16;  // split-K ways a GEMM may leave to the norm
+
 template <typename OutT, typename GT, int VPT>
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a) {
   __shared__ float warp_ss[kNormThreads / 32];
-  pdl_wait();
-  pdl_trigger();
   const int row = blockIdx.x, tid = threadIdx.x;
-  int n = a.n_rows;
-  if (a.n_rows_dev != nullptr) n = min(n, *a.n_rows_dev);
-  if (row >= n) return;
-  int src = row;
-  if (a.row_map != nullptr) {
-    src = a.row_map[row];
-    if (src < 0 || src >= a.src_rows) {
-      if (tid == 0) set_err(a.err, PE_DEV_BAD_ROW);
-      return;
-    }
-  }
-  const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)src * a.d);
   const int nv = a.d / 4;
-  float4 v[VPT];
-  float ss = 0.f;
+  // the gains are weights: load them before waiting for the previous kernel
+  float gn[VPT][4];
+  const GT* g = static_cast<const GT*>(a.g);
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int j = tid + k * kNormThreads;
-    v[k] = j < nv ? xr[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) gn[k][e] = j < nv ? to_float<GT>(g[4 * j + e]) : 0.f;
+  }
+  pdl_wait();
+  pdl_trigger();
+  // every count / index this row needs, in one round trip
+  const int dev_n = a.n_rows_dev != nullptr ? *a.n_rows_dev : a.n_rows;
+  const int dev_g = a.n_splits == 0 ? 0
+                    : (a.g_ntok_dev == nullptr ? a.g_ntok
+                       : (a.g_ntok_dev == a.n_rows_dev ? dev_n : *a.g_ntok_dev));
+  const int mapped = a.row_map != nullptr ? a.row_map[row] : row;
+  const int n = min(a.n_rows, dev_n);
+  if (row >= n) return;
+  const int src = mapped;
+  if (a.row_map != nullptr && (src < 0 || src >= a.src_rows)) {
+    if (tid == 0) set_err(a.err, PE_DEV_BAD_ROW);
+    return;
+  }
+  float4 v[VPT];
+  float ss = 0.f;
+  if (a.n_splits > 0) {
+    // x_new = x + the producing GEMM's split-K partials (split order).  Units are numbered
+    // as the GEMM numbers them over its live token tiles: ((tile_f * ntl + tile_t) * splits + split).
+    const int n_eff = min(a.g_ntok, max(dev_g, a.g_ntok_min));
+    const int ntl = min(a.n_t, (n_eff + a.bn - 1) / a.bn);
+    const int tile_t = src / a.bn, tt = src - tile_t * a.bn;
+    const size_t tile_floats = (size_t)a.bn * 128;
+    constexpr int KC = VPT < 2 ? VPT : 2;  // groups of four features whose loads are in flight together
+#pragma unroll
+    for (int k0 = 0; k0 < VPT; k0 += KC) {
+      float4 q[KC][kNormMaxSplits];
+#pragma unroll
+      for (int kc = 0; kc < KC; ++kc) {
+        const int k = k0 + kc, j = tid + k * kNormThreads;
+        v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < nv) {
+          if (a.x != nullptr) v[k] = reinterpret_cast<const float4*>(a.x + (size_t)src * a.d)[j];
+          const int f = 4 * j, tile_f = f >> 7;
+          const float* p = a.part + ((size_t)(tile_f * ntl + tile_t) * a.n_splits) * tile_floats +
+                           (size_t)tt * 128 + (f & 127);
+#pragma unroll
+          for (int sp = 0; sp < kNormMaxSplits; ++sp)
+            if (sp < a.n_splits) q[kc][sp] = __ldcg(reinterpret_cast<const float4*>(p + (size_t)sp * tile_floats));
+        }
+      }
+#pragma unroll
+      for (int kc = 0; kc < KC; ++kc) {
+        const int k = k0 + kc, j = tid + k * kNormThreads;
+        if (j < nv) {
+#pragma unroll
+          for (int sp = 0; sp < kNormMaxSplits; ++sp)  // split order
+            if (sp < a.n_splits) {
+              v[k].x += q[kc][sp].x; v[k].y += q[kc][sp].y; v[k].z += q[kc][sp].z; v[k].w += q[kc][sp].w;
+            }
+          if (a.x_out != nullptr) reinterpret_cast<float4*>(a.x_out + (size_t)src * a.d)[j] = v[k];
+        }
+      }
+    }
+  } else {
+    const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)src * a.d);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * kNormThreads;
+      v[k] = j < nv ? xr[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
     ss += v[k].x * v[k].x;
     ss += v[k].y * v[k].y;
     ss += v[k].z * v[k].z;
@@ -423,14 +479,13 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
 #pragma unroll
   for (int w = 0; w < kNormThreads / 32; ++w) tot += warp_ss[w];
   const float inv = 1.0f / sqrtf(tot / (float)a.d + a.eps);
-  const GT* g = static_cast<const GT*>(a.g);
   OutT* y = static_cast<OutT*>(a.y) + (size_t)row * a.d;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int j = tid + k * kNormThreads;
     if (j < nv)
-      store4<OutT>(y + 4 * j, v[k].x * inv * to_float<GT>(g[4 * j + 0]), v[k].y * inv * to_float<GT>(g[4 * j + 1]),
-                   v[k].z * inv * to_float<GT>(g[4 * j + 2]), v[k].w * inv * to_float<GT>(g[4 * j + 3]));
+      store4<OutT>(y + 4 * j, v[k].x * inv * gn[k][0], v[k].y * inv * gn[k][1], v[k].z * inv * gn[k][2],
+                   v[k].w * inv * gn[k][3]);
   }
 }
 
