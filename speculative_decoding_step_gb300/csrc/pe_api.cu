@@ -374,13 +374,33 @@ pe_status check_kv(const pe_config& c, const pe_kv* kv) {
   return PE_OK;
 }
 
-pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv, const int32_t* block_table,
-                       const void* x0, const int32_t* positions, const int64_t* slot_mapping,
-                       const int32_t* row_list, const int32_t* n_valid, const int32_t* draft_rows, void* ws,
-                       const Plan& p, int32_t* draft_tokens, float* logits_dbg, int32_t* err, cudaStream_t s) {
-  const bool bf16 = c.dtype == PE_BF16;
-  const int hd = c.head_dim;
-  // prologue
+PrepArgs make_prep_args(const pe_config& c, const int32_t* prev_tokens, const int32_t* prev_pos,
+                        const int32_t* num_accepted, const int32_t* bonus, const int32_t* block_table, int32_t num_pages,
+                        int32_t* input_ids, int32_t* positions, int64_t* slot_mapping, uint8_t* is_rejected,
+                        uint8_t* is_mask, int32_t* hidden_map, int32_t* row_list, int32_t* n_valid, int32_t* draft_rows,
+                        int32_t* err) {
+  PrepArgs a{};
+  a.B = c.B; a.K = c.K; a.vocab = c.vocab; a.max_pages = c.max_pages_per_seq; a.num_pages = num_pages;
+  a.page_size = c.page_size; a.prev_tokens = prev_tokens; a.prev_pos = prev_pos; a.num_accepted = num_accepted;
+  a.bonus = bonus; a.block_table = block_table; a.input_ids = input_ids; a.positions = positions;
+  a.slot_mapping = slot_mapping; a.is_rejected = is_rejected; a.is_mask = is_mask; a.hidden_map = hidden_map;
+  a.row_list = row_list; a.n_valid = n_valid; a.draft_rows = draft_rows; a.err = err;
+  return a;
+}
+
+ScatterArgs make_scatter_args(const pe_config& c, const pe_weights* w, const void* target_hidden,
+                              const int32_t* input_ids, const uint8_t* is_mask, const int32_t* hidden_map,
+                              const int32_t* row_list, const int32_t* n_valid, void* x0, int32_t* err) {
+  ScatterArgs a{};
+  a.R = c.B * 2 * c.K; a.d = c.d; a.elem_bytes = (int)elem_bytes(c.dtype); a.vocab = c.vocab;
+  a.n_hidden = c.B * (c.K + 1); a.emb = w->emb; a.h_shared = w->h_shared; a.hidden = target_hidden;
+  a.input_ids = input_ids; a.is_mask = is_mask; a.hidden_map = hidden_map; a.row_list = row_list;
+  a.n_valid = n_valid; a.x0 = x0; a.err = err;
+  return a;
+}
+
+InitArgs make_init_args(const pe_config& c, const Plan& p, void* ws, const int32_t* row_list, const int32_t* n_valid,
+                        const int32_t* positions, const int64_t* slot_mapping, int32_t* err) {
   InitArgs ia{};
   ia.B = c.B; ia.K = c.K; ia.R = p.R; ia.T = p.T; ia.n_kv = c.n_kv;
   ia.row_list = row_list; ia.n_valid = n_valid; ia.positions = positions; ia.slot_mapping = slot_mapping;
@@ -393,8 +413,21 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
   ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1;
   ia.keys = at<unsigned long long>(ws, p.keys); ia.err = err;
-  PE_TRY_CUDA(launch_forward_init(ia, s));
+  return ia;
+}
+
+pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv, const int32_t* block_table,
+                       const void* x0, const int32_t* positions, const int64_t* slot_mapping,
+                       const int32_t* row_list, const int32_t* n_valid, const int32_t* draft_rows, void* ws,
+                       const Plan& p, int32_t* draft_tokens, float* logits_dbg, int32_t* err, cudaStream_t s,
+                       bool init_done = false, const VerifyArgs* verify = nullptr) {
+  const bool bf16 = c.dtype == PE_BF16;
+  const int hd = c.head_dim;
+  // prologue (already run by pe_step's fused batch-rebuild kernel when init_done)
+  const InitArgs ia = make_init_args(c, p, ws, row_list, n_valid, positions, slot_mapping, err);
+  if (!init_done) PE_TRY_CUDA(launch_forward_init(ia, s));
   trace(3, s);
+
 
   GemmArgs base{};
   base.n_q = c.n_q; base.n_kv = c.n_kv; base.head_dim = hd; set_rope_table(base, c.rope_theta, hd);
@@ -512,6 +545,10 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     GemmArgs a = base;
     a.keys = ia.keys; a.logits_dbg = logits_dbg; a.done_counter = at<int32_t>(ws, p.done);
     a.draft_out = draft_tokens;
+    if (verify != nullptr) {
+      a.verify = *verify;
+      a.has_verify = 1;
+    }
     GemmCall call{EPI_ARGMAX, &p.lm, w->lm_head, yl, c.d, c.vocab, p.T, nullptr, 0, (uint64_t)c.vocab};
     pe_status st = run_gemm(c, p, ws, call, a, s);
     if (st != PE_OK) return st;
@@ -558,12 +595,9 @@ pe_status pe_prepare_batch(const pe_config* cfg, const int32_t* prev_tokens, con
       !slot_mapping || !is_rejected || !is_mask || !hidden_map || !row_list || !n_valid || !draft_rows || !err_word)
     return PE_ERR_INVALID_ARG;
   if (num_pages < 1) return PE_ERR_SHAPE;
-  PrepArgs a{};
-  a.B = cfg->B; a.K = cfg->K; a.vocab = cfg->vocab; a.max_pages = cfg->max_pages_per_seq; a.num_pages = num_pages;
-  a.page_size = cfg->page_size; a.prev_tokens = prev_tokens; a.prev_pos = prev_pos; a.num_accepted = num_accepted;
-  a.bonus = bonus; a.block_table = block_table; a.input_ids = input_ids; a.positions = positions;
-  a.slot_mapping = slot_mapping; a.is_rejected = is_rejected; a.is_mask = is_mask; a.hidden_map = hidden_map;
-  a.row_list = row_list; a.n_valid = n_valid; a.draft_rows = draft_rows; a.err = err_word;
+  const PrepArgs a = make_prep_args(*cfg, prev_tokens, prev_pos, num_accepted, bonus, block_table, num_pages, input_ids,
+                                    positions, slot_mapping, is_rejected, is_mask, hidden_map, row_list, n_valid,
+                                    draft_rows, err_word);
   if (launch_prepare(a, (cudaStream_t)stream) != cudaSuccess) return PE_ERR_CUDA;
   return PE_OK;
 }
@@ -579,11 +613,8 @@ pe_status pe_scatter_hidden(const pe_config* cfg, const pe_weights* w, const voi
     return PE_ERR_INVALID_ARG;
   if (!aligned16(w->emb) || !aligned16(w->h_shared) || !aligned16(target_hidden) || !aligned16(x0))
     return PE_ERR_INVALID_ARG;
-  ScatterArgs a{};
-  a.R = cfg->B * 2 * cfg->K; a.d = cfg->d; a.elem_bytes = (int)elem_bytes(cfg->dtype); a.vocab = cfg->vocab;
-  a.n_hidden = cfg->B * (cfg->K + 1); a.emb = w->emb; a.h_shared = w->h_shared; a.hidden = target_hidden;
-  a.input_ids = input_ids; a.is_mask = is_mask; a.hidden_map = hidden_map; a.row_list = row_list;
-  a.n_valid = n_valid; a.x0 = x0; a.err = err_word;
+  const ScatterArgs a =
+      make_scatter_args(*cfg, w, target_hidden, input_ids, is_mask, hidden_map, row_list, n_valid, x0, err_word);
   if (launch_scatter(a, (cudaStream_t)stream) != cudaSuccess) return PE_ERR_CUDA;
   return PE_OK;
 }
@@ -654,17 +685,21 @@ pe_status pe_step(const pe_config* cfg, const pe_weights* w, const pe_kv* kv, co
                         rej, msk, hmap, rows, nval, drows, err_word, stream);
   if (st != PE_OK) return st;
   trace(1, s);
-  st = pe_scatter_hidden(cfg, w, target_hidden, ids, msk, hmap, rows, nval, x0, err_word, stream);
-  if (st != PE_OK) return st;
+  // input rows and the forward prologue in one launch (both read only the rebuild's outputs)
+  if (!w->emb || !w->h_shared || !aligned16(w->emb) || !aligned16(w->h_shared)) return PE_ERR_INVALID_ARG;
+  const ScatterArgs sa = make_scatter_args(*cfg, w, target_hidden, ids, msk, hmap, rows, nval, x0, err_word);
+  const InitArgs ia = make_init_args(*cfg, p, ws, rows, nval, pos, slot, err_word);
+  PE_TRY_CUDA(launch_scatter_init(sa, ia, s));
   trace(2, s);
-  st = forward_impl(*cfg, w, kv, block_table, x0, pos, slot, rows, nval, drows, ws, p, draft_tokens, logits_dbg,
-                    err_word, s);
-  if (st != PE_OK) return st;
   VerifyArgs va{};
   va.B = cfg->B; va.K = cfg->K; va.draft = draft_tokens; va.target = target_tokens; va.acc_out = num_accepted_out;
   va.bonus_out = bonus_out; va.prev_pos = prev_pos; va.num_accepted = num_accepted; va.bonus_in = bonus;
   va.next_tokens = next_prev_tokens; va.next_pos = next_prev_pos;
-  if (launch_verify(va, s) != cudaSuccess) return PE_ERR_CUDA;
+  const bool bf16 = cfg->dtype == PE_BF16;  // the tensor-core LM head verifies in its finishing CTA
+  st = forward_impl(*cfg, w, kv, block_table, x0, pos, slot, rows, nval, drows, ws, p, draft_tokens, logits_dbg,
+                    err_word, s, true, bf16 ? &va : nullptr);
+  if (st != PE_OK) return st;
+  if (!bf16 && launch_verify(va, s) != cudaSuccess) return PE_ERR_CUDA;
   trace(7 + 7 * cfg->n_layers, s);
   return PE_OK;
 }

@@ -511,6 +511,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __threadfence();
         argmax_finish(a, n_tok, ethread, 128);
         if (ethread == 0) *a.done_counter = 0;
+        if (a.has_verify) {  // every draft token is known: verify them here
+          named_bar_sync(1, 128);
+          for (int b = ethread; b < a.verify.B; b += 128) verify_seq(a.verify, b);
+        }
       }
     }
   }

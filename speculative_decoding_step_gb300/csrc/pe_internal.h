@@ -69,6 +69,30 @@ struct VerifyArgs {
 };
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
 
+// Greedy verification of sequence b (vLLM Speculators: parallel drafting for
+// speculative decoding, "Production integration in vLLM": the target's output is
+// preserved): the longest prefix of drafts equal to the target's tokens, then the
+// target's token at the first mismatch as the bonus; optionally the next round's
+// verify batch [bonus, drafts] at the positions after the NTP position.
+__device__ __forceinline__ void verify_seq(const VerifyArgs& a, int b) {
+  const int32_t* d = a.draft + (size_t)b * a.K;
+  const int32_t* t = a.target + (size_t)b * (a.K + 1);
+  int acc = 0;
+  while (acc < a.K && d[acc] == t[acc]) ++acc;
+  a.acc_out[b] = acc;
+  a.bonus_out[b] = t[acc];
+  if (a.next_tokens != nullptr) {
+    int prev_a = a.num_accepted[b];
+    prev_a = prev_a < 0 ? 0 : (prev_a > a.K ? a.K : prev_a);
+    const int p0 = a.prev_pos[(size_t)b * (a.K + 1) + prev_a] + 1;
+    int32_t* nt = a.next_tokens + (size_t)b * (a.K + 1);
+    int32_t* np = a.next_pos + (size_t)b * (a.K + 1);
+    nt[0] = a.bonus_in[b];
+    for (int k = 0; k < a.K; ++k) nt[k + 1] = d[k];
+    for (int j = 0; j <= a.K; ++j) np[j] = p0 + j;
+  }
+}
+
 // Forward prologue: per compacted row metadata, per sequence ranges, the
 // attention work list, and zeroing of the pass's counters and argmax keys.
 struct InitArgs {
@@ -87,6 +111,8 @@ struct InitArgs {
   int32_t* err;
 };
 cudaError_t launch_forward_init(const InitArgs& a, cudaStream_t s);
+// Input rows (ScatterArgs) and the forward prologue (InitArgs) in one launch.
+cudaError_t launch_scatter_init(const ScatterArgs& sa, const InitArgs& ia, cudaStream_t s);
 
 // ----------------------------------------------------------------------------- RMSNorm
 
@@ -155,6 +181,8 @@ struct GemmArgs {
   int32_t* done_counter;     // LM head: CTAs finished (zero before the launch)
   float* partial;            // split K: [grid][planes][bn][128] fp32 partial tiles (column-major per plane)
   int32_t* draft_out;        // LM head: argmax per token
+  VerifyArgs verify;         // LM head: greedy verification of the drafts by the finishing CTA
+  int has_verify;            //   (pe_step); 0: none
   int32_t* err;
 };
 

@@ -21,12 +21,10 @@ namespace pe {
 
 constexpr int kPrepThreads = 1024;
 
-__global__ void __launch_bounds__(kPrepThreads) prepare_kernel(const PrepArgs a) {
+PE_DEV void prepare_body(const PrepArgs& a) {
   __shared__ int warp_off[32];
   __shared__ int carry_s;
   __shared__ int chunk_total_s;
-  pdl_wait();
-  pdl_trigger();
   const int S = 2 * a.K, R = a.B * S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   if (tid == 0) carry_s = 0;
@@ -118,6 +116,12 @@ __global__ void __launch_bounds__(kPrepThreads) prepare_kernel(const PrepArgs a)
   if (tid == 0) *a.n_valid = carry_s;
 }
 
+__global__ void __launch_bounds__(kPrepThreads) prepare_kernel(const PrepArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  prepare_body(a);
+}
+
 cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s) {
   const int R = a.B * 2 * a.K;
   const int threads = R >= kPrepThreads ? kPrepThreads : ((R + 31) / 32) * 32;
@@ -134,26 +138,8 @@ __global__ void verify_kernel(const VerifyArgs a) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= a.B) return;
-  const int32_t* d = a.draft + (size_t)b * a.K;
-  const int32_t* t = a.target + (size_t)b * (a.K + 1);
-  int acc = 0;
-  while (acc < a.K && d[acc] == t[acc]) ++acc;
-  a.acc_out[b] = acc;
-  a.bonus_out[b] = t[acc];
-  if (a.next_tokens != nullptr) {
-    // next verify batch: [bonus, t_1..t_K] at positions after the NTP position
-    int prev_a = a.num_accepted[b];
-    prev_a = prev_a < 0 ? 0 : (prev_a > a.K ? a.K : prev_a);
-    const int p0 = a.prev_pos[(size_t)b * (a.K + 1) + prev_a] + 1;
-    int32_t* nt = a.next_tokens + (size_t)b * (a.K + 1);
-    int32_t* np = a.next_pos + (size_t)b * (a.K + 1);
-    nt[0] = a.bonus_in[b];
-    for (int k = 0; k < a.K; ++k) nt[k + 1] = d[k];
-    for (int j = 0; j <= a.K; ++j) np[j] = p0 + j;
-  }
+  if (b < a.B) verify_seq(a, b);
 }
-
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   const int threads = 128;
   return launch_pdl(verify_kernel, dim3((a.B + threads - 1) / threads), dim3(threads), 0, s, a);
@@ -163,9 +149,7 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
 
 constexpr int kInitThreads = 1024;
 
-__global__ void __launch_bounds__(kInitThreads) forward_init_kernel(const InitArgs a) {
-  pdl_wait();
-  pdl_trigger();
+PE_DEV void init_body(const InitArgs& a) {
   const int tid = threadIdx.x;
   int n = *a.n_valid;
   if (n < 0 || n > a.R) {
@@ -267,6 +251,12 @@ __global__ void __launch_bounds__(kInitThreads) forward_init_kernel(const InitAr
   }
 }
 
+__global__ void __launch_bounds__(kInitThreads) forward_init_kernel(const InitArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  init_body(a);
+}
+
 cudaError_t launch_forward_init(const InitArgs& a, cudaStream_t s) {
   return launch_pdl(forward_init_kernel, dim3(1), dim3(kInitThreads), 0, s, a);
 }
@@ -281,15 +271,13 @@ cudaError_t launch_forward_init(const InitArgs& a, cudaStream_t s) {
 
 constexpr int kScatterRowsPerCta = 4;
 
-__global__ void __launch_bounds__(32) scatter_kernel(const ScatterArgs a) {
+// One CTA's rows (thread 0 issues every copy).
+PE_DEV void scatter_body(const ScatterArgs& a, int cta) {
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar;
-  pdl_wait();
-  pdl_trigger();
-  if (threadIdx.x != 0) return;
   int n = *a.n_valid;
   n = n < 0 ? 0 : (n > a.R ? a.R : n);
-  const int i0 = blockIdx.x * kScatterRowsPerCta;
+  const int i0 = cta * kScatterRowsPerCta;
   if (i0 >= n) return;
   const int i1 = i0 + kScatterRowsPerCta < n ? i0 + kScatterRowsPerCta : n;
   const uint32_t rb = (uint32_t)a.d * a.elem_bytes;  // bytes of one half row
@@ -350,6 +338,12 @@ __global__ void __launch_bounds__(32) scatter_kernel(const ScatterArgs a) {
   bulk_wait_all();
 }
 
+__global__ void __launch_bounds__(32) scatter_kernel(const ScatterArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) scatter_body(a, blockIdx.x);
+}
+
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
   const size_t smem = (size_t)(2 * kScatterRowsPerCta + 2) * a.d * a.elem_bytes;
   static bool configured = false;
@@ -360,6 +354,30 @@ cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
   }
   const int grid = (a.R + kScatterRowsPerCta - 1) / kScatterRowsPerCta;
   return launch_pdl(scatter_kernel, dim3(grid), dim3(32), smem, s, a);
+}
+
+// Input rows and the forward prologue in one launch (pe_step): both read only the
+// batch rebuild's outputs, so the last CTA runs the prologue while the others copy.
+constexpr int kScatterInitThreads = 256;
+
+__global__ void __launch_bounds__(kScatterInitThreads) scatter_init_kernel(const ScatterArgs sa, const InitArgs ia) {
+  pdl_wait();
+  pdl_trigger();
+  if (blockIdx.x == gridDim.x - 1) init_body(ia);
+  else if (threadIdx.x == 0) scatter_body(sa, blockIdx.x);
+}
+
+cudaError_t launch_scatter_init(const ScatterArgs& sa, const InitArgs& ia, cudaStream_t s) {
+  const size_t smem = (size_t)(2 * kScatterRowsPerCta + 2) * sa.d * sa.elem_bytes;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(scatter_init_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = (sa.R + kScatterRowsPerCta - 1) / kScatterRowsPerCta + 1;
+  return launch_pdl(scatter_init_kernel, dim3(grid), dim3(kScatterInitThreads), smem, s, sa, ia);
 }
 
 // ============================================================================= RMSNorm
