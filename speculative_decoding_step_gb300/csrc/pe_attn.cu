@@ -481,6 +481,7 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnArg
   pdl_wait();
   pdl_trigger();
   constexpr int VPL = HD / 32;  // output values per lane
+  constexpr int CB = 8;         // chunks whose outputs are in flight together
   const int G = a.n_q / a.n_kv, lane = threadIdx.x & 31;
   const int ldq = a.n_q * HD;
   const long long n_tasks = (long long)a.B * a.n_kv * kAttnRows;
@@ -490,15 +491,36 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnArg
     const int m = (int)(task % kAttnRows);
     const int bg = (int)(task / kAttnRows);
     const int b = bg / a.n_kv, g = bg - (bg / a.n_kv) * a.n_kv;
-    const int nc = a.n_chunks[b];
-    if (nc <= 1 || m >= min(a.seq_len[b] * G, kAttnRows)) continue;
-    const size_t base = (size_t)(a.item_base[b] + g * nc) * kAttnRows + m;  // partial row of chunk 0
-    float mx = -INFINITY;
-    for (int c = lane; c < nc; c += 32) mx = fmaxf(mx, __ldcg(a.part_m + base + (size_t)c * kAttnRows));
+    // the sequence's metadata in one round trip
+    const int nc = a.n_chunks[b], len = a.seq_len[b], ibase = a.item_base[b], start = a.seq_start[b];
+    if (nc <= 1 || m >= min(len * G, kAttnRows)) continue;
+    const size_t base = (size_t)(ibase + g * nc) * kAttnRows + m;  // partial row of chunk 0
+    // chunk statistics (one chunk per lane) and the first CB chunks' outputs, all in flight together
+    float mc_l = -INFINITY, lc_l = 0.f;
+    if (lane < nc) {
+      mc_l = __ldcg(a.part_m + base + (size_t)lane * kAttnRows);
+      lc_l = __ldcg(a.part_l + base + (size_t)lane * kAttnRows);
+    }
+    float v[CB][VPL];
+#pragma unroll
+    for (int k = 0; k < CB; ++k)
+      if (k < nc) {
+        const float* src = a.part_o + (base + (size_t)k * kAttnRows) * HD + lane * VPL;
+        if constexpr (VPL == 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+          v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
+        } else {
+          const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+          v[k][0] = t.x; v[k][1] = t.y;
+        }
+      }
+    float mx = mc_l;
+    for (int c = 32 + lane; c < nc; c += 32) mx = fmaxf(mx, __ldcg(a.part_m + base + (size_t)c * kAttnRows));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    float L = 0.f;
-    for (int c = lane; c < nc; c += 32) {
+    const float w_l = mc_l == -INFINITY ? 0.f : exp2f(mc_l - mx);  // weight of chunk `lane`
+    float L = w_l * lc_l;
+    for (int c = 32 + lane; c < nc; c += 32) {
       const float mc = __ldcg(a.part_m + base + (size_t)c * kAttnRows);
       L += (mc == -INFINITY ? 0.f : exp2f(mc - mx)) * __ldcg(a.part_l + base + (size_t)c * kAttnRows);
     }
@@ -507,34 +529,24 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnArg
     float acc[VPL];
 #pragma unroll
     for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
-    for (int c0 = 0; c0 < nc; c0 += 8) {  // eight chunks' loads in flight, added in chunk order
-      float w[8], v[8][VPL];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (c0 + k < nc) {
-          const size_t pr = base + (size_t)(c0 + k) * kAttnRows;
-          const float mc = __ldcg(a.part_m + pr);
-          w[k] = mc == -INFINITY ? 0.f : exp2f(mc - mx);
-          const float* src = a.part_o + pr * HD + lane * VPL;
-          if constexpr (VPL == 4) {
-            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-            v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
-          } else {
-            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-            v[k][0] = t.x; v[k][1] = t.y;
-          }
-        }
+    for (int k = 0; k < CB; ++k) {  // chunk order
+      const float wk = __shfl_sync(0xFFFFFFFFu, w_l, k);
+      if (k < nc) {
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) acc[e] += wk * v[k][e];
       }
+    }
+    for (int c = CB; c < nc; ++c) {  // long ranges: the rest, one chunk at a time
+      const size_t pr = base + (size_t)c * kAttnRows;
+      const float mc = __ldcg(a.part_m + pr);
+      const float wk = mc == -INFINITY ? 0.f : exp2f(mc - mx);
+      const float* src = a.part_o + pr * HD + lane * VPL;
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (c0 + k < nc) {
-#pragma unroll
-          for (int e = 0; e < VPL; ++e) acc[e] += w[k] * v[k][e];
-        }
+      for (int e = 0; e < VPL; ++e) acc[e] += wk * __ldcg(src + e);
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    __nv_bfloat16* dst =
-        out + (size_t)(a.seq_start[b] + m / G) * ldq + (size_t)(g * G + m % G) * HD + (size_t)lane * VPL;
+    __nv_bfloat16* dst = out + (size_t)(start + m / G) * ldq + (size_t)(g * G + m % G) * HD + (size_t)lane * VPL;
     if constexpr (VPL == 4) {
       uint2 pk;
       pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
