@@ -156,7 +156,7 @@ Plan make_plan(const pe_config& c) {
   p.n_chunks = take(4 * (size_t)c.B);
   p.n_items = take(4);
   p.items = take(16 * (size_t)p.max_items);
-  p.done = take(4);  // LM-head completion counter
+  p.done = take(4 * (1 + (size_t)c.n_layers));  // LM-head completion counter, then one attention work counter per layer
   p.keys = take(8 * (size_t)p.T);
   p.x = take(4 * (size_t)p.R * c.d);
   p.y = take(eb * (size_t)p.R * c.d);
@@ -411,7 +411,7 @@ InitArgs make_init_args(const pe_config& c, const Plan& p, void* ws, const int32
   ia.target_items = p.attn_target; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
   ia.items = at<int4>(ws, p.items); ia.n_items = at<int32_t>(ws, p.n_items);
   ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
-  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1;
+  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1 + c.n_layers;
   ia.keys = at<unsigned long long>(ws, p.keys); ia.err = err;
   return ia;
 }
@@ -495,6 +495,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     trace(tp + 1, s);
     at_.k_cache = kv->k_cache[l];
     at_.v_cache = kv->v_cache[l];
+    at_.work_counter = at<int32_t>(ws, p.done) + 1 + l;
     if (bf16) {
       CUtensorMap tk, tv;
       if (!tmap_kv(&tk, kv->k_cache[l], c, kv->num_pages) || !tmap_kv(&tv, kv->v_cache[l], c, kv->num_pages))

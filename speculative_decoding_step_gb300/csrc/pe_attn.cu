@@ -62,6 +62,7 @@ constexpr int kAttnThreads = 192;     // warp 0: TMA, warp 1: MMA, warps 2..5: s
 constexpr int kAttnSoftmax = 128;     // softmax threads
 constexpr uint32_t kAttnTmemCols = 256;  // S double buffer (2 x 64 columns) + O (head_dim columns)
 constexpr uint32_t kAttnTmemO = 2 * kAttnBlk;
+constexpr int kAttnItemRing = 4;      // item indices the producer may publish ahead
 // Lazy rescaling: a row keeps its reference maximum until a block's maximum
 // exceeds it by more than this (log2 units), so P <= 2^8 and O is rescaled rarely.
 constexpr float kAttnRescaleLog2 = 8.f;
@@ -91,11 +92,24 @@ struct AttnCtrl {
   uint64_t pv_done;     // one phase per PV product
   uint64_t o_free;      // softmax threads read O of the item
   uint64_t drain;       // every MMA issued has completed
+  uint64_t item_full[kAttnItemRing];   // the producer published the next item index
+  uint64_t item_empty[kAttnItemRing];  // the MMA thread and every softmax thread read it
+  int item[kAttnItemRing];  // item index, -1: no more work
   uint32_t tmem;
   int abort;
 };
 
 static_assert(sizeof(AttnCtrl) <= 256, "attention control block");
+
+// Consumer side of the item ring: the index of this CTA's ii-th item (-1: done),
+// or -2 when the wait gave up (the kernel is unwinding).
+PE_DEV int attn_next_item(AttnCtrl* ctl, int ii, int32_t* err, volatile int* abort_flag) {
+  const int k = ii % kAttnItemRing;
+  if (!mbar_wait(smem_u32(&ctl->item_full[k]), (uint32_t)(ii / kAttnItemRing) & 1u, err, abort_flag)) return -2;
+  const int it = *reinterpret_cast<volatile int*>(&ctl->item[k]);
+  mbar_arrive(smem_u32(&ctl->item_empty[k]));
+  return it;
+}
 
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 2)
@@ -128,6 +142,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     mbar_init(smem_u32(&ctl->pv_done), 1);
     mbar_init(smem_u32(&ctl->o_free), kAttnSoftmax);
     mbar_init(smem_u32(&ctl->drain), 1);
+    for (int k = 0; k < kAttnItemRing; ++k) {
+      mbar_init(smem_u32(&ctl->item_full[k]), 1);
+      mbar_init(smem_u32(&ctl->item_empty[k]), 1 + kAttnSoftmax);
+    }
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -154,7 +172,29 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     constexpr int kBlkPerBatch = 32 / kPagesPerBlk;
     int gi = 0;
     bool stop = false;
-    for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+    for (int ii = 0; !stop; ++ii) {
+      // the next item for this CTA (dynamic: long and short ranges even out across SMs),
+      // published to the MMA and softmax warps through the item ring
+      int it = 0;
+      if (lane == 0) {
+        it = atomicAdd(a.work_counter, 1);
+        if (it >= n_items) it = -1;
+        const int k = ii % kAttnItemRing;
+        bool ok = true;
+        if (ii >= kAttnItemRing)
+          ok = mbar_wait(smem_u32(&ctl->item_empty[k]), ((uint32_t)(ii / kAttnItemRing) & 1u) ^ 1u, a.err,
+                         abort_flag);
+        if (!ok) it = -2;
+        else {
+          ctl->item[k] = it;
+          mbar_arrive(smem_u32(&ctl->item_full[k]));  // release: the index is visible to the waiters
+        }
+      }
+      it = __shfl_sync(0xFFFFFFFFu, it, 0);
+      if (it < 0) {
+        stop = it == -2;
+        break;
+      }
       const int4 item = a.items[it];
       const int b = item.x, g = item.y, c0 = item.z, c1 = item.w;
       const int nblk = (c1 - c0 + kAttnBlk - 1) / kAttnBlk;
@@ -211,7 +251,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       const uint32_t id_o = idesc_bf16(kAttnRows, HD) | kIdescTransposeB;   // O += P V: V is MN-major
       int gi = 0, ii = 0;
       bool stop = false;
-      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x, ++ii) {
+      for (;; ++ii) {
+        const int it = attn_next_item(ctl, ii, a.err, abort_flag);
+        if (it < 0) break;
         const int4 item = a.items[it];
         const int nblk = (item.w - item.z + kAttnBlk - 1) / kAttnBlk;
         if (!mbar_wait(smem_u32(&ctl->q_full), (uint32_t)ii & 1u, a.err, abort_flag)) break;
@@ -305,11 +347,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
       mbar_arrive(smem_u32(&ctl->q_full));
     };
-    if ((int)blockIdx.x < n_items) stage_q(blockIdx.x);
-
-    int gi = 0;
+    int gi = 0, ii = 0;
     bool stop = false;
-    for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+    int it = attn_next_item(ctl, 0, a.err, abort_flag), it_next = -1;
+    if (it >= 0) stage_q(it);
+    for (; it >= 0 && !stop; it = it_next, ++ii) {
+      it_next = -1;
       const int4 item = a.items[it];
       const int b = item.x, g = item.y, c0 = item.z, c1 = item.w;
       const int start = a.seq_start[b];
@@ -396,7 +439,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       }
       if (stop) break;
       // every S product of this item has completed: the next item's query tile may go in
-      if (it + (int)gridDim.x < n_items) stage_q(it + gridDim.x);
+      it_next = attn_next_item(ctl, ii + 1, a.err, abort_flag);
+      if (it_next == -2) break;
+      if (it_next >= 0) stage_q(it_next);
 
       const int xl = gi + nblk - 1;
       gi += nblk;

@@ -217,6 +217,7 @@ struct AttnArgs {
   const int4* items;         // (b, g, c0, c1)
   const int32_t *n_items, *item_base, *n_chunks;
   float *part_m, *part_l, *part_o;  // [items][128], [items][128], [items][128][hd]
+  int32_t* work_counter;     // items handed out so far (zero before the launch)
   void* out;                 // [rows][n_q*hd]
   int n_rows;                // host upper bound on rows
   int32_t* err;
