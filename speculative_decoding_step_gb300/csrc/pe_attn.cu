@@ -607,7 +607,7 @@ template <int HD>
 static cudaError_t launch_merge_typed(const AttnArgs& a, int sms, cudaStream_t s) {
   const long long warps = (long long)a.B * a.n_kv * kAttnRows;
   const long long need = (warps + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
-  const int grid = (int)std::min<long long>(need, 8LL * sms);
+  const int grid = (int)std::min<long long>(need, 64LL * sms);  // about one task per warp: two round trips each
   if (grid <= 0) return cudaSuccess;
   return launch_pdl(attn_merge_kernel<HD>, dim3(grid), dim3(kMergeThreads), 0, s, a);
 }
