@@ -160,6 +160,27 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def replica_seed(base_seed: int, rank: int, world: int) -> int:
+    """Seed of one rank's replica: every rank draws its own batch (weak scaling)."""
+    return base_seed + 1000 * rank if world > 1 else base_seed
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise max of per-rank timings (the slowest rank sets the job's time)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(world: int, B: int, K: int, ms: float) -> float:
+    """Draft tokens per second of all ranks together: each rank drafts B*K tokens per round."""
+    return world * B * K / (ms * 1e-3)
+
+
 def dist_env():
     return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -259,7 +280,7 @@ def run_ours(args):
 
     pe.build()
     cfg_np = workload(args)
-    seed = cfg_np.seed + 1000 * rank if world > 1 else cfg_np.seed
+    seed = replica_seed(cfg_np.seed, rank, world)
     w_np, rnd = make_weights(cfg_np, seed), make_round(cfg_np, seed)
     W, R = weights_to_device(w_np, dev), round_to_device(rnd, dev)
     cfg = pe.Config.make(cfg_np.B, cfg_np.K, cfg_np.d, cfg_np.n_q, cfg_np.n_kv, cfg_np.head_dim, cfg_np.ffn,
@@ -335,10 +356,7 @@ def run_ours(args):
         dist.barrier()
     clocks = sampler.stop()
     ms = sum(step_ms) / len(step_ms)
-    if dist is not None:
-        t = torch.tensor([ms, direct_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, direct_ms = float(t[0].item()), float(t[1].item())
+    ms, direct_ms = max_over_ranks([ms, direct_ms], dist, dev)
     launches = launches_per_step * args.steps  # kernels of ours per round x timed rounds
 
     # ---- per-stage device times: a separate traced pass (events between kernels; not the headline)
@@ -378,11 +396,8 @@ def run_ours(args):
         for _ in range(3):
             e2e_step()
         e_ms = statistics.mean(timed(args.steps, e2e_step))
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = dict(value=world * cfg_np.B * cfg_np.K / (e_ms * 1e-3), unit=UNIT, h2d_bytes_per_step=int(h2d),
+        (e_ms,) = max_over_ranks([e_ms], dist, dev)
+        e2e = dict(value=whole_job_rate(world, cfg_np.B, cfg_np.K, e_ms), unit=UNIT, h2d_bytes_per_step=int(h2d),
                    d2h_bytes_per_step=int(d2h), ms_per_step=e_ms)
 
     if rank != 0:
@@ -412,7 +427,7 @@ def run_ours(args):
     round_roof["frac_direct_launches"] = t_round / (direct_ms * 1e-3)
 
     cpu = None if args.no_cpu_baseline else cpu_oracle_sample(cfg_np, w_np, rnd, args.cpu_seconds)
-    value = world * cfg_np.B * cfg_np.K / (ms * 1e-3)
+    value = whole_job_rate(world, cfg_np.B, cfg_np.K, ms)
     out = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
                ms_per_step=ms, us_per_round=ms * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
                dtype=cfg_np.dtype, data="synthetic (seeded; shapes and value distributions of the workload)",
