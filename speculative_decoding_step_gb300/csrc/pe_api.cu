@@ -65,6 +65,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct GemmPlan {
   int epi = 0, bn = 16, n_t = 1, n_f = 1, k_splits = 1, kb_total = 1, stages = 2, grid = 1;
   int nbuf = 1, acc_stride = 16;
+  int balanced = 0;
   uint32_t tmem_cols = 32;
   uint32_t stage_bytes = 0;
   size_t smem = 0;
@@ -102,11 +103,19 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   const int need = g.nbuf * acc_cols;
   g.tmem_cols = need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
   g.grid = g.k_splits > 1 ? g.tiles * g.k_splits : std::min(g.tiles, sms);
+  // LM head with one token tile: equal k-block ranges per CTA when the last wave of
+  // vocabulary tiles is at most three quarters full (a range then spans more than a
+  // tile).  One SM streams at most about 53 GB/s (measured), little above its
+  // 1/152 share of HBM bandwidth, so a last wave of n CTAs runs at about n/152 of
+  // the HBM rate; a nearly full last wave costs less than exchanging the partial
+  // sums of the cut tiles.
+  const int last_wave = g.tiles % sms;
+  if (epi == EPI_ARGMAX && g.n_t == 1 && g.tiles > sms && last_wave != 0 && 4 * last_wave <= 3 * sms) g.balanced = 1;
   return g;
 }
 
 struct Plan {
-  int R = 0, T = 0, S = 0, sms = 0, max_items = 0, attn_grid = 0, attn_target = 0;
+  int R = 0, T = 0, S = 0, sms = 0, max_items = 0, attn_grid = 0, attn_target = 0, n_counters = 0;
   GemmPlan fc, qkv, o, gu, down, lm;
   // workspace offsets
   size_t tok_pos, tok_seq, tok_slot, seq_start, seq_len, seq_maxpos, item_base, n_chunks, n_items, items;
@@ -156,7 +165,10 @@ Plan make_plan(const pe_config& c) {
   p.n_chunks = take(4 * (size_t)c.B);
   p.n_items = take(4);
   p.items = take(16 * (size_t)p.max_items);
-  p.done = take(4 * (1 + (size_t)c.n_layers));  // LM-head completion counter, then one attention work counter per layer
+  // LM-head completion counter, one attention work counter per layer, then the
+  // balanced LM head's arrival counters (4 per CTA)
+  p.n_counters = 1 + c.n_layers + 4 * p.sms;
+  p.done = take(4 * (size_t)p.n_counters);
   p.keys = take(8 * (size_t)p.T);
   p.x = take(4 * (size_t)p.R * c.d);
   p.y = take(eb * (size_t)p.R * c.d);
@@ -170,6 +182,7 @@ Plan make_plan(const pe_config& c) {
       const bool paired = g->epi == EPI_SWIGLU || g->epi == EPI_QKV_ROPE;
       split_bytes = std::max(split_bytes, (size_t)g->grid * (paired ? 2 : 1) * g->bn * kTcBM * 4);
     }
+  if (p.lm.balanced) split_bytes = std::max(split_bytes, (size_t)p.lm.grid * 2 * p.lm.bn * kTcBM * 4);
   p.split_part = c.dtype == PE_BF16 && split_bytes > 0 ? take(split_bytes) : 0;
   if (c.dtype == PE_BF16) {
     p.part_m = take(4 * (size_t)p.max_items * kAttnRows);
@@ -335,7 +348,8 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   a.acc_stride = g.acc_stride;
   a.tmem_cols = g.tmem_cols;
   a.n_tok_min = call.n_tok_dev != nullptr ? std::min(call.n_tok, c.B * c.K) : call.n_tok;
-  if (g.k_splits > 1) a.partial = at<float>(ws, p.split_part);
+  if (g.k_splits > 1 || g.balanced) a.partial = at<float>(ws, p.split_part);
+  if (g.balanced) a.tile_cnt = at<int32_t>(ws, p.done) + 1 + c.n_layers;
   CUtensorMap tw, tx;
   bool ok;
   if (call.w_kind == 1) ok = tmap_gate_up(&tw, call.W, (uint64_t)c.ffn, (uint64_t)c.d);
@@ -343,7 +357,7 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   else ok = tmap_matrix(&tw, call.W, call.w_rows, (uint64_t)call.k_dim, (uint32_t)kTcBM);
   ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)g.bn);
   if (!ok) return PE_ERR_CUDA;
-  PE_TRY_CUDA(launch_gemm_tc(call.epi, tw, tx, a, g.grid, g.smem, s));
+  PE_TRY_CUDA(launch_gemm_tc(g.balanced ? EPI_ARGMAX_BAL : call.epi, tw, tx, a, g.grid, g.smem, s));
   if (g.k_splits > 1 && (call.epi == EPI_QKV_ROPE || call.epi == EPI_SWIGLU))
     PE_TRY_CUDA(launch_splitk_finish(call.epi, a, p.sms, s));
   return PE_OK;
@@ -411,7 +425,7 @@ InitArgs make_init_args(const pe_config& c, const Plan& p, void* ws, const int32
   ia.target_items = p.attn_target; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
   ia.items = at<int4>(ws, p.items); ia.n_items = at<int32_t>(ws, p.n_items);
   ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
-  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = 1 + c.n_layers;
+  ia.counters = at<int32_t>(ws, p.done); ia.n_counters = p.n_counters;
   ia.keys = at<unsigned long long>(ws, p.keys); ia.err = err;
   return ia;
 }

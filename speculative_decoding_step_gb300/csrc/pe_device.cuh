@@ -28,6 +28,17 @@ PE_DEV uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_ge
 // Barrier among `n` threads (whole warps) of the CTA, on hardware barrier `id` (0 is __syncthreads).
 PE_DEV void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
+// True in exactly one lane of the (converged) warp: the lowest active lane.
+PE_DEV bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(r));
+  return r != 0;
+}
+
 PE_DEV uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

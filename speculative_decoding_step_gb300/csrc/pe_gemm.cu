@@ -176,7 +176,8 @@ PE_DEV void argmax_finish(const GemmArgs& a, int n_tok, int thread, int nthreads
 // warp 1 lane 0 issues tcgen05.mma into one of `nbuf` TMEM accumulators, warps
 // 2..5 run the epilogue of unit i while the MMAs of unit i+1 fill the other
 // accumulator.  Before waiting on the previous kernel (pdl_wait) the producer
-// already streams the weights of its first unit: they never depend on it.
+// already streams the weights of its first unit (balanced LM head: its first
+// stages, across pieces): they never depend on it.
 //
 // Split K: one unit per CTA.  Each split writes its fp32 partial tile
 // column-major to the workspace and exits; the kernel that consumes the output
@@ -205,6 +206,7 @@ PE_DEV int effective_ntok(const GemmArgs& a) {
 
 struct Unit {
   int tile_t, tile_f, split, kb0, kb1;
+  int bnd, side;  // balanced LM head: schedule boundary cutting this tile (-1: none), piece 0 / 1
 };
 
 // Token tiles holding at least one of this launch's rows.  Units are numbered
@@ -221,7 +223,55 @@ PE_DEV Unit decode_unit(const GemmArgs& a, int u, int n_t_live) {
   w.tile_f = r / n_t_live;
   w.kb0 = (int)((long long)w.split * a.kb_total / a.k_splits);
   w.kb1 = (int)((long long)(w.split + 1) * a.kb_total / a.k_splits);
+  w.bnd = -1;
+  w.side = 0;
   return w;
+}
+
+// A CTA's work.  Default: units blockIdx.x, blockIdx.x + gridDim.x, ...
+// Balanced LM head (EPI_ARGMAX_BAL: one token tile, more vocabulary tiles than
+// CTAs): the n_f * kb_total k blocks, tile after tile, are cut into gridDim.x
+// contiguous ranges of equal length, so every CTA streams the same number of
+// weight bytes instead of some CTAs taking one whole tile more than the rest.  A
+// range is at least a tile long, so a tile is cut by at most one range boundary,
+// into two pieces (side 0: its first k blocks, side 1: the rest).
+struct Sched {
+  int cur, end;
+};
+
+template <int EPI>
+PE_DEV Sched sched_begin(const GemmArgs& a, int n_t_live) {
+  Sched sc;
+  if (EPI == EPI_ARGMAX_BAL) {
+    const long long W = (long long)a.n_f * a.kb_total;
+    sc.cur = (int)(W * blockIdx.x / gridDim.x);
+    sc.end = (int)(W * (blockIdx.x + 1) / gridDim.x);
+  } else {
+    sc.cur = blockIdx.x;
+    sc.end = n_t_live * a.n_f * a.k_splits;
+  }
+  return sc;
+}
+
+template <int EPI>
+PE_DEV bool sched_next(const GemmArgs& a, Sched& sc, int n_t_live, Unit& w) {
+  if (sc.cur >= sc.end) return false;
+  if (EPI == EPI_ARGMAX_BAL) {
+    const int KB = a.kb_total;
+    w.tile_t = 0;
+    w.split = 0;
+    w.tile_f = sc.cur / KB;
+    w.kb0 = sc.cur - w.tile_f * KB;
+    w.kb1 = min(KB, w.kb0 + (sc.end - sc.cur));
+    // boundary b lies between the ranges of CTAs b - 1 and b
+    w.bnd = w.kb0 > 0 ? (int)blockIdx.x : (w.kb1 < KB ? (int)blockIdx.x + 1 : -1);
+    w.side = w.kb0 > 0 ? 1 : 0;
+    sc.cur += w.kb1 - w.kb0;
+  } else {
+    w = decode_unit(a, sc.cur, n_t_live);
+    sc.cur += gridDim.x;
+  }
+  return true;
 }
 
 template <int EPI>
@@ -292,11 +342,50 @@ PE_DEV void argmax16(const GemmArgs& a, int unit, int t0, int n_tok, const float
   if ((lane & 1) == 0 && k1 > red_w[col]) red_w[col] = k1;
 }
 
+// Epilogue of one piece of a vocabulary tile cut by a schedule boundary (balanced
+// LM head).  Each epilogue warp stores its 32 rows of the piece's fp32
+// accumulator ([boundary][side][token column][128 rows]); the warp whose piece
+// arrives second adds the other piece and takes the argmax of the full sums.
+// fp32 addition is commutative, so the sum is the same whichever piece is first.
+PE_DEV void argmax_piece(const GemmArgs& a, const Unit& w, uint32_t tl, int unit, int n_tok,
+                         unsigned long long* red_w, int r, int lane) {
+  const int BN = a.bn;
+  const size_t plane = (size_t)BN * kTcBM;
+  float* mine = a.partial + (size_t)(2 * w.bnd + w.side) * plane + r;
+  const float* other = a.partial + (size_t)(2 * w.bnd + 1 - w.side) * plane + r;
+  for (int c = 0; c < BN / 16; ++c) {
+    float v[16];
+    tmem_load16(tl + (uint32_t)(c * 16), v);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) mine[(size_t)(c * 16 + j) * kTcBM] = v[j];
+  }
+  __threadfence();
+  __syncwarp();
+  int* cnt = a.tile_cnt + 4 * w.bnd + (r >> 5);
+  int old = 0;
+  if (lane == 0) old = atomicAdd(cnt, 1);
+  old = __shfl_sync(0xFFFFFFFFu, old, 0);
+  if (old == 0) return;  // the other piece finishes this tile
+  __threadfence();
+  for (int c = 0; c < BN / 16; ++c) {
+    float v[16], o[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j] = __ldcg(other + (size_t)(c * 16 + j) * kTcBM);
+    tmem_load16(tl + (uint32_t)(c * 16), v);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] += o[j];
+    argmax16(a, unit, c * 16, n_tok, v, red_w + c * 16, lane);
+  }
+  if (lane == 0) *cnt = 0;
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmArgs a) {
   constexpr bool PAIRED = (EPI == EPI_SWIGLU || EPI == EPI_QKV_ROPE);
+  constexpr bool ARGMAX = (EPI == EPI_ARGMAX || EPI == EPI_ARGMAX_BAL);
+  constexpr bool BAL = (EPI == EPI_ARGMAX_BAL);
   constexpr uint32_t A_BYTES = kTcBM * kTcBK * 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -333,7 +422,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     *last_flag = 0;
     fence_mbar_init();
   }
-  if (EPI == EPI_ARGMAX)
+  if (ARGMAX)
     for (int j = threadIdx.x; j < 4 * NT; j += blockDim.x) red[j] = 0ull;
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
@@ -347,79 +436,101 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();  // weights: read once
-      const uint64_t pol_x = l2_policy_evict_last();   // activations: re-read by every weight tile
-      // the weights of the first unit do not depend on earlier kernels: start them now
-      int npre = 0;
-      if (a.n_t == 1 && (int)blockIdx.x < U) {  // unit numbering does not depend on the row count
-        const Unit w = decode_unit(a, blockIdx.x, 1);
-        {
-          npre = min(S, w.kb1 - w.kb0);
-          for (int i = 0; i < npre; ++i) {
-            const uint32_t sa = smem_u32(smem + (size_t)i * a.stage_bytes);
-            mbar_expect_tx(smem_u32(full + i), a.stage_bytes);
-            issue_w<EPI>(&tmW, a, sa, smem_u32(full + i), (w.kb0 + i) * kTcBK, w.tile_f, pol_w);
+    // The whole warp runs the loop (converged) and waits on the barriers; one
+    // elected lane arms the barriers and issues the copies.  Stage index and
+    // phase advance incrementally: no division per k block.
+    const uint64_t pol_w = l2_policy_evict_first();  // weights: read once
+    const uint64_t pol_x = l2_policy_evict_last();   // activations: re-read by every weight tile
+    // the weights do not depend on earlier kernels: start the first stages now
+    int npre = 0;
+    if (BAL) {  // the first S k blocks of the range, across pieces
+      Sched s0 = sched_begin<EPI>(a, 1);
+      Unit w;
+      while (npre < S && sched_next<EPI>(a, s0, 1, w))
+        for (int kb = w.kb0; kb < w.kb1 && npre < S; ++kb, ++npre)
+          if (elect_one()) {
+            const uint32_t sa = smem_u32(smem + (size_t)npre * a.stage_bytes);
+            mbar_expect_tx(smem_u32(full + npre), a.stage_bytes);
+            issue_w<EPI>(&tmW, a, sa, smem_u32(full + npre), kb * kTcBK, w.tile_f, pol_w);
+          }
+    } else if (a.n_t == 1 && (int)blockIdx.x < U) {  // unit numbering does not depend on the row count
+      const Unit w = decode_unit(a, blockIdx.x, 1);
+      npre = min(S, w.kb1 - w.kb0);
+      if (elect_one())
+        for (int i = 0; i < npre; ++i) {
+          const uint32_t sa = smem_u32(smem + (size_t)i * a.stage_bytes);
+          mbar_expect_tx(smem_u32(full + i), a.stage_bytes);
+          issue_w<EPI>(&tmW, a, sa, smem_u32(full + i), (w.kb0 + i) * kTcBK, w.tile_f, pol_w);
+        }
+    }
+    __syncwarp();
+    pdl_wait();
+    const int n_tok = effective_ntok(a);
+    const int ntl = live_token_tiles(a, n_tok);
+    int it = 0, s = 0;
+    uint32_t ph = 0;  // (it / S) & 1
+    bool stop = false;
+    Sched sc = sched_begin<EPI>(a, ntl);
+    Unit w;
+    while (!stop && sched_next<EPI>(a, sc, ntl, w)) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+        const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
+        const uint32_t fb = smem_u32(full + s);
+        if (it >= npre && it >= S) {
+          const bool ok = mbar_wait(smem_u32(empty + s), ph ^ 1u, a.err, abort_flag);
+          if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+            stop = true;
+            break;
           }
         }
-      }
-      pdl_wait();
-      const int n_tok = effective_ntok(a);
-      const int ntl = live_token_tiles(a, n_tok);
-      const int UL = ntl * a.n_f * a.k_splits;
-      int it = 0;
-      bool stop = false;
-      for (int u = blockIdx.x; u < UL && !stop; u += gridDim.x) {
-        const Unit w = decode_unit(a, u, ntl);
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int s = it % S;
-          const uint32_t use = (uint32_t)(it / S);
-          const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
-          const uint32_t fb = smem_u32(full + s);
+        if (elect_one()) {
           if (it >= npre) {
-            if (it >= S && !mbar_wait(smem_u32(empty + s), (use & 1u) ^ 1u, a.err, abort_flag)) {
-              stop = true;
-              break;
-            }
             mbar_expect_tx(fb, a.stage_bytes);
             issue_w<EPI>(&tmW, a, sa, fb, kb * kTcBK, w.tile_f, pol_w);
           }
           tma_load_2d(sa + b_off, &tmX, fb, kb * kTcBK, w.tile_t * BN, pol_x);
         }
+        __syncwarp();
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
-      if (stop || *abort_flag) {
-        // leave no bulk copy in flight into this CTA's shared memory
-        const int lo = it > S ? it - S : 0;
-        for (int i = lo; i < it; ++i)
-          mbar_wait(smem_u32(full + (i % S)), (uint32_t)(i / S) & 1u, a.err, nullptr);
-      }
+    }
+    if (stop || *abort_flag) {
+      // leave no bulk copy in flight into this CTA's shared memory
+      const int lo = it > S ? it - S : 0;
+      for (int i = lo; i < it; ++i)
+        mbar_wait(smem_u32(full + (i % S)), (uint32_t)(i / S) & 1u, a.err, nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      pdl_wait();
-      const int n_tok = effective_ntok(a);
-      const int ntl = live_token_tiles(a, n_tok);
-      const int UL = ntl * a.n_f * a.k_splits;
-      const uint32_t idesc = idesc_bf16(kTcBM, BN);
-      int it = 0, i = 0;
-      bool stop = false;
-      for (int u = blockIdx.x; u < UL && !stop; u += gridDim.x) {
-        const Unit w = decode_unit(a, u, ntl);
-        const int buf = i % a.nbuf;
-        if (i >= a.nbuf &&
-            !mbar_wait(smem_u32(tempty + buf), (uint32_t)((i / a.nbuf) - 1) & 1u, a.err, abort_flag))
+    // Converged warp; the elected lane issues every MMA and commit.
+    pdl_wait();
+    const int n_tok = effective_ntok(a);
+    const int ntl = live_token_tiles(a, n_tok);
+    const uint32_t idesc = idesc_bf16(kTcBM, BN);
+    int i = 0, s = 0;
+    uint32_t ph = 0;  // (it / S) & 1 over this CTA's k blocks
+    bool stop = false;
+    Sched sc = sched_begin<EPI>(a, ntl);
+    Unit w;
+    while (!stop && sched_next<EPI>(a, sc, ntl, w)) {
+      const int buf = i % a.nbuf;
+      if (i >= a.nbuf) {
+        const bool ok = mbar_wait(smem_u32(tempty + buf), (uint32_t)((i / a.nbuf) - 1) & 1u, a.err, abort_flag);
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)(buf * a.acc_stride);
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        const bool ok = mbar_wait(smem_u32(full + s), ph, a.err, abort_flag);
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+          stop = true;
           break;
+        }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * a.acc_stride);
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int s = it % S;
-          const uint32_t use = (uint32_t)(it / S);
-          if (!mbar_wait(smem_u32(full + s), use & 1u, a.err, abort_flag)) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
+        if (elect_one()) {
           const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
           const uint64_t da = sdesc_k_sw128(sa);
           const uint64_t da2 = sdesc_k_sw128(sa + A_BYTES);
@@ -432,9 +543,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_commit(smem_u32(empty + s));
         }
-        tc_commit(smem_u32(tfull + buf));
-        ++i;
+        __syncwarp();
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
+      if (elect_one()) tc_commit(smem_u32(tfull + buf));
+      __syncwarp();
+      ++i;
     }
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2..5)
@@ -444,23 +561,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int r = q * 32 + lane;           // row of the tile = TMEM lane
     unsigned long long* red_w = red + (size_t)(warp - 2) * NT;
     const int ntl = live_token_tiles(a, n_tok);
-    const int UL = ntl * a.n_f * a.k_splits;
     int i = 0;
-    for (int u = blockIdx.x; u < UL; u += gridDim.x) {
-      const Unit w = decode_unit(a, u, ntl);
+    Sched sc = sched_begin<EPI>(a, ntl);
+    Unit w;
+    while (sched_next<EPI>(a, sc, ntl, w)) {
       const int buf = i % a.nbuf;
       const bool ok = mbar_wait(smem_u32(tfull + buf), (uint32_t)(i / a.nbuf) & 1u, a.err, abort_flag);
       tc_fence_after();
       const int unit = w.tile_f * kTcBM + r;
       const uint32_t tl = tmem + (uint32_t)(buf * a.acc_stride) + ((uint32_t)(q * 32) << 16);
       const int tbase = w.tile_t * BN;
-      if (ok && a.k_splits == 1) {
+      if (BAL && ok && w.bnd >= 0) {
+        argmax_piece(a, w, tl, unit, n_tok, red_w, r, lane);
+      } else if (ok && a.k_splits == 1) {
         const float2 tf = (EPI == EPI_QKV_ROPE) ? rope_tf(a, unit) : make_float2(0.f, 0.f);
         for (int c = 0; c < BN / 16; ++c) {
           float v[16], v2[16];
           tmem_load16(tl + (uint32_t)(c * 16), v);
           if (PAIRED) tmem_load16(tl + (uint32_t)(BN + c * 16), v2);
-          if (EPI == EPI_ARGMAX)
+          if (ARGMAX)
             argmax16(a, unit, tbase + c * 16, n_tok, v, red_w + tbase + c * 16, lane);
           else
             apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, tf);
@@ -492,7 +611,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(tempty + buf));  // accumulator free for a later unit
       ++i;
     }
-    if (EPI == EPI_ARGMAX) {
+    if (ARGMAX) {
       named_bar_sync(1, 128);
       const int ethread = threadIdx.x - 64;
       for (int j = ethread; j < NT; j += 128) {  // key index = token = tile_t * BN + column
@@ -558,6 +677,7 @@ cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& t
     case EPI_SWIGLU: return launch_tc_typed<EPI_SWIGLU>(tmW, tmX, a, grid, smem, s);
     case EPI_QKV_ROPE: return launch_tc_typed<EPI_QKV_ROPE>(tmW, tmX, a, grid, smem, s);
     case EPI_ARGMAX: return launch_tc_typed<EPI_ARGMAX>(tmW, tmX, a, grid, smem, s);
+    case EPI_ARGMAX_BAL: return launch_tc_typed<EPI_ARGMAX_BAL>(tmW, tmX, a, grid, smem, s);
   }
   return cudaErrorInvalidValue;
 }

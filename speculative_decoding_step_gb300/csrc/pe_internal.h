@@ -145,6 +145,7 @@ enum Epi : int {
   EPI_SWIGLU = 2,     // u[t][f] = silu(gate) * up     (gate/up, paired rows)
   EPI_QKV_ROPE = 3,   // RoPE(q,k); q -> q buffer; k,v -> paged cache at the row's slot
   EPI_ARGMAX = 4,     // LM head: per-token max / argmax over the vocabulary
+  EPI_ARGMAX_BAL = 5, // the same with equal k-block ranges per CTA (tensor-core kernel only)
 };
 
 struct GemmArgs {
@@ -180,6 +181,8 @@ struct GemmArgs {
   float* logits_dbg;         // nullable [tokens][n_out]
   int32_t* done_counter;     // LM head: CTAs finished (zero before the launch)
   float* partial;            // split K: [grid][planes][bn][128] fp32 partial tiles (column-major per plane)
+  int32_t* tile_cnt;         // EPI_ARGMAX_BAL: [grid][4] arrivals per cut tile and epilogue warp (zero
+                             //   before the launch); the pieces' partials go to `partial` as [grid][2][bn][128]
   int32_t* draft_out;        // LM head: argmax per token
   VerifyArgs verify;         // LM head: greedy verification of the drafts by the finishing CTA
   int has_verify;            //   (pe_step); 0: none

@@ -33,6 +33,9 @@ SMALL = {
     "bf16-hd128-K8-G8": _small(B=2, K=8, n_q=16, n_kv=2, head_dim=128, d=512, ffn=640, vocab=777, seed=8),
     "bf16-K1": _small(B=5, K=1, seed=9),
     "bf16-L2-long": _small(B=2, K=7, n_layers=2, prefix_args=(900, 2100), vocab=3001, seed=10),
+    # more vocabulary tiles (161, the last one ragged) than SMs with a short last wave:
+    # the LM head cuts tiles at CTA range boundaries and sums the two pieces
+    "bf16-lm-balanced": _small(B=4, K=8, vocab=160 * 128 + 37, seed=12),
     "f32-c0": config(0),
     "f32-L2": _small(dtype="f32", n_layers=2, seed=11),
 }
