@@ -89,7 +89,8 @@ struct AttnCtrl {
   uint64_t q_full;      // softmax threads staged the item's query tile
   uint64_t s_full[2];   // S of a block is in TMEM buffer (block & 1)
   uint64_t p_full[2];   // P of a block is in TMEM (over its S), O rescaled where needed
-  uint64_t pv_done;     // one phase per PV product
+  uint64_t pv_done;     // one phase per PV product (waited on only while the next PV cannot start)
+  uint64_t pv_item;     // one phase per item: its last PV product has completed
   uint64_t o_free;      // softmax threads read O of the item
   uint64_t drain;       // every MMA issued has completed
   uint64_t item_full[kAttnItemRing];   // the producer published the next item index
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       mbar_init(smem_u32(&ctl->p_full[b]), kAttnSoftmax);
     }
     mbar_init(smem_u32(&ctl->pv_done), 1);
+    mbar_init(smem_u32(&ctl->pv_item), 1);
     mbar_init(smem_u32(&ctl->o_free), kAttnSoftmax);
     mbar_init(smem_u32(&ctl->drain), 1);
     for (int k = 0; k < kAttnItemRing; ++k) {
@@ -246,27 +248,35 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t id_s = idesc_bf16(kAttnRows, kAttnBlk);                 // S = Q K^T: N = positions
-      const uint32_t id_o = idesc_bf16(kAttnRows, HD) | kIdescTransposeB;   // O += P V: V is MN-major
-      int gi = 0, ii = 0;
-      bool stop = false;
-      for (;; ++ii) {
-        const int it = attn_next_item(ctl, ii, a.err, abort_flag);
-        if (it < 0) break;
-        const int4 item = a.items[it];
-        const int nblk = (item.w - item.z + kAttnBlk - 1) / kAttnBlk;
-        if (!mbar_wait(smem_u32(&ctl->q_full), (uint32_t)ii & 1u, a.err, abort_flag)) break;
-        tc_fence_after();
-        // S of block j is issued one block ahead of the PV product of block j - 1
-        for (int j = 0; j <= nblk; ++j) {
-          if (j < nblk) {
-            const int x = gi + j, s = x % S;
-            if (!mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)(x / S) & 1u, a.err, abort_flag)) {
-              stop = true;
-              break;
-            }
-            tc_fence_after();
+    // Converged warp: every lane waits on the barriers; the elected lane takes the
+    // items and issues every MMA and commit (a lone lane looping is far slower).
+    const uint32_t id_s = idesc_bf16(kAttnRows, kAttnBlk);                 // S = Q K^T: N = positions
+    const uint32_t id_o = idesc_bf16(kAttnRows, HD) | kIdescTransposeB;   // O += P V: V is MN-major
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      const bool ok = mbar_wait(bar, parity, a.err, abort_flag);
+      return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+    };
+    int gi = 0, ii = 0;
+    bool stop = false;
+    for (;; ++ii) {
+      int it = 0;
+      if (elect_one()) it = attn_next_item(ctl, ii, a.err, abort_flag);
+      it = __shfl_sync(0xFFFFFFFFu, it, 0);
+      if (it < 0) break;
+      const int4 item = a.items[it];
+      const int nblk = (item.w - item.z + kAttnBlk - 1) / kAttnBlk;
+      if (!wait_all(smem_u32(&ctl->q_full), (uint32_t)ii & 1u)) break;
+      tc_fence_after();
+      // S of block j is issued one block ahead of the PV product of block j - 1
+      for (int j = 0; j <= nblk; ++j) {
+        if (j < nblk) {
+          const int x = gi + j, s = x % S;
+          if (!wait_all(smem_u32(&ctl->full[s]), (uint32_t)(x / S) & 1u)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
             const uint32_t kbase = sRing + (uint32_t)s * Lay::STAGE;
             const uint32_t d = tmem + (uint32_t)((x & 1) * kAttnBlk);
 #pragma unroll
@@ -277,18 +287,20 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             }
             tc_commit(smem_u32(&ctl->s_full[x & 1]));
           }
-          if (j >= 1) {
-            const int x = gi + j - 1, s = x % S;
-            if (j == 1 && ii > 0 &&
-                !mbar_wait(smem_u32(&ctl->o_free), (uint32_t)(ii - 1) & 1u, a.err, abort_flag)) {
-              stop = true;
-              break;
-            }
-            if (!mbar_wait(smem_u32(&ctl->p_full[x & 1]), (uint32_t)(x >> 1) & 1u, a.err, abort_flag)) {
-              stop = true;
-              break;
-            }
-            tc_fence_after();
+          __syncwarp();
+        }
+        if (j >= 1) {
+          const int x = gi + j - 1, s = x % S;
+          if (j == 1 && ii > 0 && !wait_all(smem_u32(&ctl->o_free), (uint32_t)(ii - 1) & 1u)) {
+            stop = true;
+            break;
+          }
+          if (!wait_all(smem_u32(&ctl->p_full[x & 1]), (uint32_t)(x >> 1) & 1u)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
             const uint32_t vbase = sRing + (uint32_t)s * Lay::STAGE + Lay::KV;
             const uint32_t pa = tmem + (uint32_t)((x & 1) * kAttnBlk);
 #pragma unroll
@@ -297,15 +309,19 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                                  sdesc_mn_sw128(vbase + (uint32_t)kk * 2048u, kAttnBlk * 128), id_o,
                                  (j > 1 || kk > 0) ? 1u : 0u);
             tc_commit(smem_u32(&ctl->pv_done));
+            if (j == nblk) tc_commit(smem_u32(&ctl->pv_item));
             tc_commit(smem_u32(&ctl->empty[s]));
           }
+          __syncwarp();
         }
-        gi += nblk;
       }
-      // TMEM is freed only after every MMA issued here has completed
-      tc_commit(smem_u32(&ctl->drain));
-      mbar_wait(smem_u32(&ctl->drain), 0, a.err, nullptr);
+      if (stop) break;
+      gi += nblk;
     }
+    // TMEM is freed only after every MMA issued here has completed
+    if (elect_one()) tc_commit(smem_u32(&ctl->drain));
+    __syncwarp();
+    mbar_wait(smem_u32(&ctl->drain), 0, a.err, nullptr);
   } else {
     // ------------------------------------------------------------------ softmax + epilogue (warps 2..5)
     const int et = tid - 64;                        // 0..127
@@ -443,9 +459,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       if (it_next == -2) break;
       if (it_next >= 0) stage_q(it_next);
 
-      const int xl = gi + nblk - 1;
       gi += nblk;
-      if (!warp_ok(mbar_wait(smem_u32(&ctl->pv_done), (uint32_t)xl & 1u, a.err, abort_flag))) break;
+      // The item's PV products are complete.  (Not pv_done at the last block's parity:
+      // the PV of the block before it is issued after the last S product, so pv_done
+      // may still be a phase short of that block, and a parity wait cannot tell a
+      // barrier two phases behind from one that is done.)
+      if (!warp_ok(mbar_wait(smem_u32(&ctl->pv_item), (uint32_t)ii & 1u, a.err, abort_flag))) break;
       tc_fence_after();
       if (nc == 1) {
         // the item covers the whole range: normalise and write the output row directly
