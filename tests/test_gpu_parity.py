@@ -214,6 +214,24 @@ def test_deterministic_and_page_permutation_invariant():
     assert torch.equal(lg1, c2.rd.logits) and torch.equal(d1, c2.rd.draft_tokens)
 
 
+@pytest.mark.parametrize("idx", [1, 2])
+def test_repeat_runs_bit_identical_full_size(idx):
+    """The full-size workloads run repeatedly give bit-identical logits and drafts: a
+    synchronisation race between the pipelines' warps (a stage or accumulator read before
+    its producer finished) shows up as run-to-run differences."""
+    cfg_np = config(idx)
+    c = setup(cfg_np)
+    assert run_stages(c) == 0
+    lg1, d1 = c.rd.logits.clone(), c.rd.draft_tokens.clone()
+    for _ in range(6):
+        for l in range(cfg_np.n_layers):
+            c.kv.k_cache[l].copy_(c.k_before[l])
+            c.kv.v_cache[l].copy_(c.v_before[l])
+        assert run_stages(c) == 0
+        assert torch.equal(d1, c.rd.draft_tokens)
+        assert torch.equal(lg1, c.rd.logits)
+
+
 def test_step_equals_stages_and_next_batch():
     cfg_np = SMALL["bf16-hd64"]
     c = setup(cfg_np)
