@@ -275,46 +275,62 @@ constexpr int kScatterRowsPerCta = 4;
 PE_DEV void scatter_body(const ScatterArgs& a, int cta) {
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar;
+  constexpr int RPC = kScatterRowsPerCta;
+  const int i0 = cta * RPC;
+  // the row count and this CTA's rows in one round trip (rows past the count are -1
+  // padding), then every row's metadata in a second one
   int n = *a.n_valid;
+  int rows[RPC];
+#pragma unroll
+  for (int k = 0; k < RPC; ++k) rows[k] = i0 + k < a.R ? a.row_list[i0 + k] : -1;
   n = n < 0 ? 0 : (n > a.R ? a.R : n);
-  const int i0 = cta * kScatterRowsPerCta;
   if (i0 >= n) return;
-  const int i1 = i0 + kScatterRowsPerCta < n ? i0 + kScatterRowsPerCta : n;
+  const int i1 = i0 + RPC < n ? i0 + RPC : n;
+  int msk[RPC], tok[RPC], hmp[RPC];
+#pragma unroll
+  for (int k = 0; k < RPC; ++k) {
+    const int row = rows[k];
+    const bool ok = i0 + k < i1 && row >= 0 && row < a.R;
+    msk[k] = ok ? a.is_mask[row] : 0;
+    tok[k] = ok ? a.input_ids[row] : 0;
+    hmp[k] = ok ? a.hidden_map[row] : 0;
+  }
   const uint32_t rb = (uint32_t)a.d * a.elem_bytes;  // bytes of one half row
   const uint8_t* emb = static_cast<const uint8_t*>(a.emb);
   const uint8_t* hid = static_cast<const uint8_t*>(a.hidden);
   uint8_t* x0 = static_cast<uint8_t*>(a.x0);
   const uint32_t base = smem_u32(sm);
-  const uint32_t mask_slot = base + (uint32_t)(2 * kScatterRowsPerCta) * rb;  // [emb(mask) | h_shared]
+  const uint32_t mask_slot = base + (uint32_t)(2 * RPC) * rb;  // [emb(mask) | h_shared]
   const uint32_t b = smem_u32(&bar);
   mbar_init(b, 1);
   fence_mbar_init();
 
   // which rows need what
-  int kind[kScatterRowsPerCta];      // 0 skip, 1 regular, 2 MASK
-  const uint8_t* src_e[kScatterRowsPerCta];
-  const uint8_t* src_h[kScatterRowsPerCta];
+  int kind[RPC];      // 0 skip, 1 regular, 2 MASK
+  const uint8_t* src_e[RPC];
+  const uint8_t* src_h[RPC];
   uint32_t bytes = 0;
   bool any_mask = false;
-  for (int i = i0; i < i1; ++i) {
-    const int k = i - i0;
+#pragma unroll
+  for (int k = 0; k < RPC; ++k) {
     kind[k] = 0;
-    const int row = a.row_list[i];
+    src_e[k] = src_h[k] = nullptr;
+    if (i0 + k >= i1) continue;
+    const int row = rows[k];
     if (row < 0 || row >= a.R) { set_err(a.err, PE_DEV_BAD_ROW); continue; }
-    if (a.is_mask[row]) { kind[k] = 2; any_mask = true; continue; }
-    const int tok = a.input_ids[row];
-    const int hm = a.hidden_map[row];
-    if (tok < 0 || tok > a.vocab) { set_err(a.err, PE_DEV_BAD_TOKEN); continue; }
-    if (hm < 0 || hm >= a.n_hidden) { set_err(a.err, PE_DEV_BAD_ROW); continue; }
+    if (msk[k]) { kind[k] = 2; any_mask = true; continue; }
+    if (tok[k] < 0 || tok[k] > a.vocab) { set_err(a.err, PE_DEV_BAD_TOKEN); continue; }
+    if (hmp[k] < 0 || hmp[k] >= a.n_hidden) { set_err(a.err, PE_DEV_BAD_ROW); continue; }
     kind[k] = 1;
-    src_e[k] = emb + (size_t)tok * rb;
-    src_h[k] = hid + (size_t)hm * rb;
+    src_e[k] = emb + (size_t)tok[k] * rb;
+    src_h[k] = hid + (size_t)hmp[k] * rb;
     bytes += 2 * rb;
   }
   if (any_mask) bytes += 2 * rb;
   if (bytes == 0) return;
   mbar_expect_tx(b, bytes);
-  for (int k = 0; k < i1 - i0; ++k) {
+#pragma unroll
+  for (int k = 0; k < RPC; ++k) {  // kind is 0 past this CTA's rows
     if (kind[k] != 1) continue;
     bulk_g2s(base + (uint32_t)(2 * k) * rb, src_e[k], rb, b);
     bulk_g2s(base + (uint32_t)(2 * k + 1) * rb, src_h[k], rb, b);
@@ -325,7 +341,8 @@ PE_DEV void scatter_body(const ScatterArgs& a, int cta) {
   }
   if (!mbar_wait(b, 0, a.err, nullptr)) return;
   fence_proxy_async_smem();
-  for (int k = 0; k < i1 - i0; ++k) {
+#pragma unroll
+  for (int k = 0; k < RPC; ++k) {
     uint8_t* dst = x0 + (size_t)(i0 + k) * 2 * rb;
     if (kind[k] == 1) {
       bulk_s2g(dst, base + (uint32_t)(2 * k) * rb, rb);
