@@ -9,7 +9,7 @@
 // query heads of g (<= 128 query vectors), so each KV page is read once per
 // (sequence, kv head).  Warp 0 streams the chunk's K and V pages with 3-D TMA
 // loads (one 16-position page per load, 128-byte swizzle, pages past the
-// range zero-filled) into an mbarrier ring of 64-position blocks (4 stages
+// range zero-filled) into an mbarrier ring of 64-position blocks (5 stages
 // at head_dim 64, 2 at head_dim 128: two CTAs share an SM).
 // Warp 1 issues the 5th-generation tensor-core MMAs: S = Q K^T (M = 128 query
 // vectors, N = 64 positions) into one of two TMEM buffers, and O += P V with
@@ -54,10 +54,10 @@ PE_DEV bool warp_ok(bool ok) { return __all_sync(0xFFFFFFFFu, ok); }
 }  // namespace
 
 constexpr int kAttnBlk = 64;          // kv positions per pipeline stage (4 pages) = MMA N of S
-// stages in flight: 4 x 16 KB (head_dim 64) or 2 x 32 KB (head_dim 128), so two CTAs fit per SM
+// stages in flight: 5 x 16 KB (head_dim 64) or 2 x 32 KB (head_dim 128), so two CTAs fit per SM
 template <int HD>
-__host__ __device__ constexpr int attn_stages() { return HD == 64 ? 4 : 2; }
-constexpr int kAttnMaxStages = 4;
+__host__ __device__ constexpr int attn_stages() { return HD == 64 ? 5 : 2; }
+constexpr int kAttnMaxStages = 5;
 constexpr int kAttnThreads = 192;     // warp 0: TMA, warp 1: MMA, warps 2..5: softmax (thread = query row)
 constexpr int kAttnSoftmax = 128;     // softmax threads
 constexpr uint32_t kAttnTmemCols = 256;  // S double buffer (2 x 64 columns) + O (head_dim columns)
