@@ -41,6 +41,7 @@ constexpr int kMaxRows = 1 << 16;        // B*2K
 constexpr int kAttnItemsPerSlot = 4;     // attention work items aimed for, per resident CTA (load balance)
 constexpr int kAttnMinChunk = 256;       // shortest position chunk of a work item (bounds the chunks to merge)
 constexpr int kTcMaxStages = 12;
+constexpr int kMinStagesKa2 = 3;        // ring depth below which a stage keeps one k atom
 constexpr int kMaxSplits = 16;           // split-K ways per tile (the RMSNorm that sums deferred partials takes up to 16)
 
 int num_sms() {
@@ -66,6 +67,7 @@ struct GemmPlan {
   int epi = 0, bn = 16, n_t = 1, n_f = 1, k_splits = 1, kb_total = 1, stages = 2, grid = 1;
   int nbuf = 1, acc_stride = 16;
   int balanced = 0;
+  int ka = 1;  // 64-wide k atoms per stage
   uint32_t tmem_cols = 32;
   uint32_t stage_bytes = 0;
   size_t smem = 0;
@@ -88,15 +90,22 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
     g.n_t = (n_tok + g.bn - 1) / g.bn;
   }
   g.n_f = n_f_tiles;
-  g.kb_total = (k_dim + kTcBK - 1) / kTcBK;
   g.tiles = g.n_f * g.n_t;
-  g.stage_bytes = (paired ? 2u : 1u) * kTcBM * kTcBK * 2 + (uint32_t)g.bn * kTcBK * 2;
   const int red = epi == EPI_ARGMAX ? 4 * g.n_t * g.bn : 0;
   const long long avail = kTcSmemOptIn - 1024 - kTcCtrlBytes - (long long)red * 8;
+  // Two k atoms per stage (one TMA box of both per operand: half the boxes per byte, half
+  // the barrier round trips per MMA) while the ring still holds kMinStagesKa2 stages.
+  auto stage_bytes = [&](int ka) {
+    return (uint32_t)ka * ((paired ? 2u : 1u) * kTcBM * kTcBK * 2 + (uint32_t)g.bn * kTcBK * 2);
+  };
+  g.ka = avail / stage_bytes(2) >= kMinStagesKa2 ? 2 : 1;
+  const int atoms = (k_dim + kTcBK - 1) / kTcBK;
+  g.kb_total = (atoms + g.ka - 1) / g.ka;  // the last stage's second atom may lie past K: zeros
+  g.stage_bytes = stage_bytes(g.ka);
   g.stages = (int)std::min<long long>(kTcMaxStages, avail / g.stage_bytes);
   g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, red);
   if (epi != EPI_ARGMAX && g.tiles < sms)
-    g.k_splits = std::max(1, std::min(kMaxSplits, std::min(sms / g.tiles, g.kb_total / 4)));
+    g.k_splits = std::max(1, std::min(kMaxSplits, std::min(sms / g.tiles, g.kb_total * g.ka / 4)));
   const int acc_cols = (paired ? 2 : 1) * g.bn;
   g.nbuf = 2 * acc_cols <= 512 ? 2 : 1;
   g.acc_stride = acc_cols;
@@ -236,28 +245,33 @@ bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
 }
 
 // [rows][cols] row-major, box of box_rows x 64 columns
-bool tmap_matrix(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  const uint64_t dims[2] = {cols, rows};
-  const uint64_t strides[1] = {cols * 2};
-  const uint32_t box[2] = {(uint32_t)kTcBK, box_rows};
-  return make_tmap(m, base, 2, dims, strides, box);
-}
+// GEMM operands view K as [K/64][64] (K a multiple of 64): a box of `ka` atoms lands as
+// ka consecutive [box rows][64] tiles, each 128-byte swizzled.
 
-// w_gate_up [2F][d] as [2][F][d]: box of 128 rows of one half
-bool tmap_gate_up(CUtensorMap* m, const void* base, uint64_t F, uint64_t d) {
-  const uint64_t dims[3] = {d, F, 2};
-  const uint64_t strides[2] = {d * 2, F * d * 2};
-  const uint32_t box[3] = {(uint32_t)kTcBK, (uint32_t)kTcBM, 1};
+// [rows][cols] as [cols/64][rows][64]: box of box_rows rows x ka atoms
+bool tmap_matrix(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, int ka) {
+  const uint64_t dims[3] = {(uint64_t)kTcBK, rows, cols / kTcBK};
+  const uint64_t strides[2] = {cols * 2, (uint64_t)kTcBK * 2};
+  const uint32_t box[3] = {(uint32_t)kTcBK, box_rows, (uint32_t)ka};
   return make_tmap(m, base, 3, dims, strides, box);
 }
 
-// wqkv [heads*hd][d] as [heads][2][hd/2][d]: box = the first (or second) halves of 128/(hd/2) heads
-bool tmap_qkv(CUtensorMap* m, const void* base, uint64_t heads, uint64_t hd, uint64_t d) {
-  const uint64_t half = hd / 2;
-  const uint64_t dims[4] = {d, half, 2, heads};
-  const uint64_t strides[3] = {d * 2, half * d * 2, hd * d * 2};
-  const uint32_t box[4] = {(uint32_t)kTcBK, (uint32_t)half, 1, (uint32_t)(kTcBM / half)};
+// w_gate_up [2F][d] as [d/64][2][F][64]: box of 128 rows of one half x ka atoms
+bool tmap_gate_up(CUtensorMap* m, const void* base, uint64_t F, uint64_t d, int ka) {
+  const uint64_t dims[4] = {(uint64_t)kTcBK, F, 2, d / kTcBK};
+  const uint64_t strides[3] = {d * 2, F * d * 2, (uint64_t)kTcBK * 2};
+  const uint32_t box[4] = {(uint32_t)kTcBK, (uint32_t)kTcBM, 1, (uint32_t)ka};
   return make_tmap(m, base, 4, dims, strides, box);
+}
+
+// wqkv [heads*hd][d] as [d/64][heads][2][hd/2][64]: box = the first (or second) halves of
+// 128/(hd/2) heads x ka atoms
+bool tmap_qkv(CUtensorMap* m, const void* base, uint64_t heads, uint64_t hd, uint64_t d, int ka) {
+  const uint64_t half = hd / 2;
+  const uint64_t dims[5] = {(uint64_t)kTcBK, half, 2, heads, d / kTcBK};
+  const uint64_t strides[4] = {d * 2, half * d * 2, hd * d * 2, (uint64_t)kTcBK * 2};
+  const uint32_t box[5] = {(uint32_t)kTcBK, (uint32_t)half, 1, (uint32_t)(kTcBM / half), (uint32_t)ka};
+  return make_tmap(m, base, 5, dims, strides, box);
 }
 
 // paged K or V pool [num_pages*16][n_kv][hd] as a 3-D tensor (hd innermost); box = 64 dims x 1 head x 16 positions
@@ -285,7 +299,9 @@ pe_status check_cfg(const pe_config* c) {
   const size_t eb = elem_bytes(c->dtype);
   if ((c->d * eb) % 16 != 0 || c->d % 4 != 0) return PE_ERR_UNSUPPORTED;  // bulk row copies, float4 norm
   if (c->dtype == PE_BF16) {
-    if (c->ffn % 8 != 0) return PE_ERR_UNSUPPORTED;                          // TMA row strides: 16 bytes
+    // tensor-core GEMM operands are tiled in 64-wide k atoms along every contraction
+    // (d, 2d, ffn, n_q * head_dim; head_dim is 64 or 128)
+    if (c->d % 64 != 0 || c->ffn % 64 != 0) return PE_ERR_UNSUPPORTED;
     if (2 * c->K * (c->n_q / c->n_kv) > kAttnRows) return PE_ERR_UNSUPPORTED;  // one query tile per item
   }
   return PE_OK;
@@ -339,6 +355,7 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   const GemmPlan& g = *call.plan;
   a.bn = g.bn;
   a.kb_total = g.kb_total;
+  a.ka = g.ka;
   a.k_splits = g.k_splits;
   a.stages = g.stages;
   a.stage_bytes = g.stage_bytes;
@@ -352,10 +369,11 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   if (g.balanced) a.tile_cnt = at<int32_t>(ws, p.done) + 1 + c.n_layers;
   CUtensorMap tw, tx;
   bool ok;
-  if (call.w_kind == 1) ok = tmap_gate_up(&tw, call.W, (uint64_t)c.ffn, (uint64_t)c.d);
-  else if (call.w_kind == 2) ok = tmap_qkv(&tw, call.W, (uint64_t)(c.n_q + 2 * c.n_kv), (uint64_t)c.head_dim, (uint64_t)c.d);
-  else ok = tmap_matrix(&tw, call.W, call.w_rows, (uint64_t)call.k_dim, (uint32_t)kTcBM);
-  ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)g.bn);
+  if (call.w_kind == 1) ok = tmap_gate_up(&tw, call.W, (uint64_t)c.ffn, (uint64_t)c.d, g.ka);
+  else if (call.w_kind == 2)
+    ok = tmap_qkv(&tw, call.W, (uint64_t)(c.n_q + 2 * c.n_kv), (uint64_t)c.head_dim, (uint64_t)c.d, g.ka);
+  else ok = tmap_matrix(&tw, call.W, call.w_rows, (uint64_t)call.k_dim, (uint32_t)kTcBM, g.ka);
+  ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)g.bn, g.ka);
   if (!ok) return PE_ERR_CUDA;
   PE_TRY_CUDA(launch_gemm_tc(g.balanced ? EPI_ARGMAX_BAL : call.epi, tw, tx, a, g.grid, g.smem, s));
   if (g.k_splits > 1 && (call.epi == EPI_QKV_ROPE || call.epi == EPI_SWIGLU))

@@ -274,19 +274,24 @@ PE_DEV bool sched_next(const GemmArgs& a, Sched& sc, int n_t_live, Unit& w) {
   return true;
 }
 
+// One stage of weights: a.ka 64-wide k atoms from atom `ka0` on, in one TMA box per
+// operand (the tensor maps view K as [K/64][64], so a box of ka atoms lands as ka
+// consecutive 128-byte-swizzled [128 rows][64] tiles).  One large box instead of ka
+// small ones: a single SM's TMA throughput is set by the number of boxes (measured:
+// 46 GB/s with 16 KB boxes, 95 GB/s with 32 KB boxes).
 template <int EPI>
-PE_DEV void issue_w(const CUtensorMap* tmW, const GemmArgs& a, uint32_t sa, uint32_t fb, int kx, int tile_f,
+PE_DEV void issue_w(const CUtensorMap* tmW, const GemmArgs& a, uint32_t sa, uint32_t fb, int ka0, int tile_f,
                     uint64_t pol) {
-  constexpr uint32_t A_BYTES = kTcBM * kTcBK * 2;
-  if (EPI == EPI_SWIGLU) {  // W viewed as [2][F][d]: gate rows, then up rows
-    tma_load_3d(sa, tmW, fb, kx, tile_f * kTcBM, 0, pol);
-    tma_load_3d(sa + A_BYTES, tmW, fb, kx, tile_f * kTcBM, 1, pol);
-  } else if (EPI == EPI_QKV_ROPE) {  // W viewed as [heads][2][hd/2][d]: first / second halves
+  const uint32_t A_OP = (uint32_t)a.ka * (kTcBM * kTcBK * 2);  // one operand's bytes per stage
+  if (EPI == EPI_SWIGLU) {  // W viewed as [K/64][2][F][64]: gate rows, then up rows
+    tma_load_4d(sa, tmW, fb, 0, tile_f * kTcBM, 0, ka0, pol);
+    tma_load_4d(sa + A_OP, tmW, fb, 0, tile_f * kTcBM, 1, ka0, pol);
+  } else if (EPI == EPI_QKV_ROPE) {  // W viewed as [K/64][heads][2][hd/2][64]: first / second halves
     const int hpt = kTcBM / (a.head_dim >> 1);
-    tma_load_4d(sa, tmW, fb, kx, 0, 0, tile_f * hpt, pol);
-    tma_load_4d(sa + A_BYTES, tmW, fb, kx, 0, 1, tile_f * hpt, pol);
+    tma_load_5d(sa, tmW, fb, 0, 0, 0, tile_f * hpt, ka0, pol);
+    tma_load_5d(sa + A_OP, tmW, fb, 0, 0, 1, tile_f * hpt, ka0, pol);
   } else {
-    tma_load_2d(sa, tmW, fb, kx, tile_f * kTcBM, pol);
+    tma_load_3d(sa, tmW, fb, 0, tile_f * kTcBM, ka0, pol);
   }
 }
 
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr bool PAIRED = (EPI == EPI_SWIGLU || EPI == EPI_QKV_ROPE);
   constexpr bool ARGMAX = (EPI == EPI_ARGMAX || EPI == EPI_ARGMAX_BAL);
   constexpr bool BAL = (EPI == EPI_ARGMAX_BAL);
-  constexpr uint32_t A_BYTES = kTcBM * kTcBK * 2;
+  constexpr uint32_t A_ATOM = kTcBM * kTcBK * 2;  // one 64-wide k atom of 128 weight rows
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -404,7 +409,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
   unsigned long long* red = reinterpret_cast<unsigned long long*>(ctrl + kTcCtrlBytes);  // [4 warps][NT]
-  const uint32_t b_off = (PAIRED ? 2u : 1u) * A_BYTES;
+  const uint32_t A_OP = (uint32_t)a.ka * A_ATOM;  // one weight operand per stage
+  const uint32_t b_off = (PAIRED ? 2u : 1u) * A_OP;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmW);
@@ -451,7 +457,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (elect_one()) {
             const uint32_t sa = smem_u32(smem + (size_t)npre * a.stage_bytes);
             mbar_expect_tx(smem_u32(full + npre), a.stage_bytes);
-            issue_w<EPI>(&tmW, a, sa, smem_u32(full + npre), kb * kTcBK, w.tile_f, pol_w);
+            issue_w<EPI>(&tmW, a, sa, smem_u32(full + npre), kb * a.ka, w.tile_f, pol_w);
           }
     } else if (a.n_t == 1 && (int)blockIdx.x < U) {  // unit numbering does not depend on the row count
       const Unit w = decode_unit(a, blockIdx.x, 1);
@@ -460,7 +466,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < npre; ++i) {
           const uint32_t sa = smem_u32(smem + (size_t)i * a.stage_bytes);
           mbar_expect_tx(smem_u32(full + i), a.stage_bytes);
-          issue_w<EPI>(&tmW, a, sa, smem_u32(full + i), (w.kb0 + i) * kTcBK, w.tile_f, pol_w);
+          issue_w<EPI>(&tmW, a, sa, smem_u32(full + i), (w.kb0 + i) * a.ka, w.tile_f, pol_w);
         }
     }
     __syncwarp();
@@ -486,9 +492,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (elect_one()) {
           if (it >= npre) {
             mbar_expect_tx(fb, a.stage_bytes);
-            issue_w<EPI>(&tmW, a, sa, fb, kb * kTcBK, w.tile_f, pol_w);
+            issue_w<EPI>(&tmW, a, sa, fb, kb * a.ka, w.tile_f, pol_w);
           }
-          tma_load_2d(sa + b_off, &tmX, fb, kb * kTcBK, w.tile_t * BN, pol_x);
+          tma_load_3d(sa + b_off, &tmX, fb, 0, w.tile_t * BN, kb * a.ka, pol_x);
         }
         __syncwarp();
         if (++s == S) {
@@ -532,14 +538,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         if (elect_one()) {
           const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
-          const uint64_t da = sdesc_k_sw128(sa);
-          const uint64_t da2 = sdesc_k_sw128(sa + A_BYTES);
-          const uint64_t db = sdesc_k_sw128(sa + b_off);
 #pragma unroll
-          for (int kk = 0; kk < kTcBK / 16; ++kk) {
-            const uint32_t accum = (kb > w.kb0 || kk > 0) ? 1u : 0u;
-            tc_mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accum);
-            if (PAIRED) tc_mma_bf16(d + (uint32_t)BN, da2 + 2 * kk, db + 2 * kk, idesc, accum);
+          for (int at = 0; at < 2; ++at) {  // the stage's k atoms (a.ka of them)
+            if (at < a.ka) {
+              const uint64_t da = sdesc_k_sw128(sa + (uint32_t)at * A_ATOM);
+              const uint64_t da2 = sdesc_k_sw128(sa + A_OP + (uint32_t)at * A_ATOM);
+              const uint64_t db = sdesc_k_sw128(sa + b_off + (uint32_t)(at * BN * kTcBK * 2));
+#pragma unroll
+              for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                const uint32_t accum = (kb > w.kb0 || at > 0 || kk > 0) ? 1u : 0u;
+                tc_mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accum);
+                if (PAIRED) tc_mma_bf16(d + (uint32_t)BN, da2 + 2 * kk, db + 2 * kk, idesc, accum);
+              }
+            }
           }
           tc_commit(smem_u32(empty + s));
         }

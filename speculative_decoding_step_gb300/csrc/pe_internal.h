@@ -157,7 +157,8 @@ struct GemmArgs {
   int bn;                // token columns per tile (MMA N)
   int n_t, n_f;          // token tiles, weight tiles; work units = n_t * n_f * k_splits
   int n_tok_min;         // token rows that certainly exist (every tile below it is computed)
-  int kb_total, k_splits, stages;
+  int kb_total, k_splits, stages;  // k stages over the whole K (each ka 64-wide atoms)
+  int ka;                          // 64-wide k atoms per pipeline stage (1 or 2)
   uint32_t stage_bytes;
   int nbuf;              // TMEM accumulator buffers (2: epilogue overlaps the next unit's MMAs)
   int acc_stride;        // TMEM columns per accumulator buffer
@@ -202,7 +203,7 @@ cudaError_t launch_gemm_f32(int epi, const GemmArgs& a, cudaStream_t s);
 
 constexpr int kTcThreads = 192;        // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
 constexpr int kTcBM = 128;             // weight rows per tile
-constexpr int kTcBK = 64;              // k per pipeline stage (one 128-byte swizzle row)
+constexpr int kTcBK = 64;              // k per atom (one 128-byte swizzle row); a stage holds 1 or 2 atoms
 constexpr int kTcCtrlBytes = 1024;     // barriers + TMEM slot + flags
 constexpr int kTcSmemOptIn = 232448;   // largest dynamic shared memory per block (227 KB)
 // dynamic shared memory: alignment slack + stage ring + control block + argmax keys (4 warps * n_t * bn)
