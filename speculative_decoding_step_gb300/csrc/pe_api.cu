@@ -256,21 +256,23 @@ bool tmap_matrix(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
   return make_tmap(m, base, 3, dims, strides, box);
 }
 
-// w_gate_up [2F][d] as [d/64][2][F][64]: box of 128 rows of one half x ka atoms
+// w_gate_up [2F][d] as [d/64][2][F][64]: one box = 128 rows of both halves x ka atoms,
+// landing per atom as the gate tile then the up tile
 bool tmap_gate_up(CUtensorMap* m, const void* base, uint64_t F, uint64_t d, int ka) {
   const uint64_t dims[4] = {(uint64_t)kTcBK, F, 2, d / kTcBK};
   const uint64_t strides[3] = {d * 2, F * d * 2, (uint64_t)kTcBK * 2};
-  const uint32_t box[4] = {(uint32_t)kTcBK, (uint32_t)kTcBM, 1, (uint32_t)ka};
+  const uint32_t box[4] = {(uint32_t)kTcBK, (uint32_t)kTcBM, 2, (uint32_t)ka};
   return make_tmap(m, base, 4, dims, strides, box);
 }
 
-// wqkv [heads*hd][d] as [d/64][heads][2][hd/2][64]: box = the first (or second) halves of
-// 128/(hd/2) heads x ka atoms
+// wqkv [heads*hd][d] as [d/64][2][heads][hd/2][64] (the half index outside the heads):
+// one box = both halves of 128/(hd/2) heads x ka atoms, landing per atom as the tile of
+// the heads' first halves then the tile of their second halves
 bool tmap_qkv(CUtensorMap* m, const void* base, uint64_t heads, uint64_t hd, uint64_t d, int ka) {
   const uint64_t half = hd / 2;
-  const uint64_t dims[5] = {(uint64_t)kTcBK, half, 2, heads, d / kTcBK};
-  const uint64_t strides[4] = {d * 2, half * d * 2, hd * d * 2, (uint64_t)kTcBK * 2};
-  const uint32_t box[5] = {(uint32_t)kTcBK, (uint32_t)half, 1, (uint32_t)(kTcBM / half), (uint32_t)ka};
+  const uint64_t dims[5] = {(uint64_t)kTcBK, half, heads, 2, d / kTcBK};
+  const uint64_t strides[4] = {d * 2, hd * d * 2, half * d * 2, (uint64_t)kTcBK * 2};
+  const uint32_t box[5] = {(uint32_t)kTcBK, (uint32_t)half, (uint32_t)(kTcBM / half), 2, (uint32_t)ka};
   return make_tmap(m, base, 5, dims, strides, box);
 }
 

@@ -279,17 +279,16 @@ PE_DEV bool sched_next(const GemmArgs& a, Sched& sc, int n_t_live, Unit& w) {
 // consecutive 128-byte-swizzled [128 rows][64] tiles).  One large box instead of ka
 // small ones: a single SM's TMA throughput is set by the number of boxes (measured:
 // 46 GB/s with 16 KB boxes, 95 GB/s with 32 KB boxes).
+// Paired operands (gate/up, the heads' first/second halves) come in the same box and
+// land per atom as two consecutive 128-row tiles: [ka][2][128][64].
 template <int EPI>
 PE_DEV void issue_w(const CUtensorMap* tmW, const GemmArgs& a, uint32_t sa, uint32_t fb, int ka0, int tile_f,
                     uint64_t pol) {
-  const uint32_t A_OP = (uint32_t)a.ka * (kTcBM * kTcBK * 2);  // one operand's bytes per stage
-  if (EPI == EPI_SWIGLU) {  // W viewed as [K/64][2][F][64]: gate rows, then up rows
+  if (EPI == EPI_SWIGLU) {  // W viewed as [K/64][2][F][64]
     tma_load_4d(sa, tmW, fb, 0, tile_f * kTcBM, 0, ka0, pol);
-    tma_load_4d(sa + A_OP, tmW, fb, 0, tile_f * kTcBM, 1, ka0, pol);
-  } else if (EPI == EPI_QKV_ROPE) {  // W viewed as [K/64][heads][2][hd/2][64]: first / second halves
+  } else if (EPI == EPI_QKV_ROPE) {  // W viewed as [K/64][2][heads][hd/2][64]
     const int hpt = kTcBM / (a.head_dim >> 1);
-    tma_load_5d(sa, tmW, fb, 0, 0, 0, tile_f * hpt, ka0, pol);
-    tma_load_5d(sa + A_OP, tmW, fb, 0, 0, 1, tile_f * hpt, ka0, pol);
+    tma_load_5d(sa, tmW, fb, 0, 0, tile_f * hpt, 0, ka0, pol);
   } else {
     tma_load_3d(sa, tmW, fb, 0, tile_f * kTcBM, ka0, pol);
   }
@@ -409,8 +408,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
   unsigned long long* red = reinterpret_cast<unsigned long long*>(ctrl + kTcCtrlBytes);  // [4 warps][NT]
-  const uint32_t A_OP = (uint32_t)a.ka * A_ATOM;  // one weight operand per stage
-  const uint32_t b_off = (PAIRED ? 2u : 1u) * A_OP;
+  const uint32_t b_off = (PAIRED ? 2u : 1u) * (uint32_t)a.ka * A_ATOM;  // weights: [ka][PAIRED ? 2 : 1][128][64]
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmW);
@@ -541,8 +539,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int at = 0; at < 2; ++at) {  // the stage's k atoms (a.ka of them)
             if (at < a.ka) {
-              const uint64_t da = sdesc_k_sw128(sa + (uint32_t)at * A_ATOM);
-              const uint64_t da2 = sdesc_k_sw128(sa + A_OP + (uint32_t)at * A_ATOM);
+              const uint64_t da = sdesc_k_sw128(sa + (uint32_t)(PAIRED ? 2 * at : at) * A_ATOM);
+              const uint64_t da2 = sdesc_k_sw128(sa + (uint32_t)(2 * at + 1) * A_ATOM);
               const uint64_t db = sdesc_k_sw128(sa + b_off + (uint32_t)(at * BN * kTcBK * 2));
 #pragma unroll
               for (int kk = 0; kk < kTcBK / 16; ++kk) {
