@@ -329,6 +329,8 @@ PE_DEV float from_float<float>(float v) { return v; }
 template <>
 PE_DEV __nv_bfloat16 from_float<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
-PE_DEV float silu(float x) { return x / (1.0f + expf(-x)); }
+// x * sigmoid(x) with the fast exponential and division intrinsics (the result is
+// rounded to bf16 next); -x large: exp overflows to inf and the quotient is 0.
+PE_DEV float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 }  // namespace pe
