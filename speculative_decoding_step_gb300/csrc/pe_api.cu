@@ -91,7 +91,9 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   }
   g.n_f = n_f_tiles;
   g.tiles = g.n_f * g.n_t;
-  const int red = epi == EPI_ARGMAX ? 4 * g.n_t * g.bn : 0;
+  // epilogue scratch after the ring, in 8-byte words: the LM head's per-warp keys, or the
+  // QKV epilogue's token positions and slots (two buffers of bn x 12 bytes)
+  const int red = epi == EPI_ARGMAX ? 4 * g.n_t * g.bn : (epi == EPI_QKV_ROPE ? 3 * g.bn : 0);
   const long long avail = kTcSmemOptIn - 1024 - kTcCtrlBytes - (long long)red * 8;
   // Two k atoms per stage (one TMA box of both per operand: half the boxes per byte, half
   // the barrier round trips per MMA) while the ring still holds kMinStagesKa2 stages.

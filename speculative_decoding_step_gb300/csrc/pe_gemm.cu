@@ -108,7 +108,7 @@ PE_DEV void epi_elem(const GemmArgs& a, int unit, int t, float v, float v2, floa
 // 128 x 128 SwiGLU unit).
 template <int EPI, typename T>
 PE_DEV void epi_chunk(const GemmArgs& a, int unit, int t0, int nv, const float (&v)[16], const float (&v2)[16],
-                      float2 tf) {
+                      float2 tf, const int* pos_s, const long long* slot_s) {
   if (EPI == EPI_STORE_F32) {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
@@ -132,9 +132,9 @@ PE_DEV void epi_chunk(const GemmArgs& a, int unit, int t0, int nv, const float (
     int pos[16];
     long long slot[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      pos[j] = (j < nv && rotated) ? a.tok_pos[t0 + j] : 0;
-      slot[j] = (j < nv && !is_q) ? a.tok_slot[t0 + j] : -1;
+    for (int j = 0; j < 16; ++j) {  // this chunk's tokens, staged in shared memory per unit
+      pos[j] = (j < nv && rotated) ? pos_s[j] : 0;
+      slot[j] = (j < nv && !is_q) ? slot_s[j] : -1;
     }
     T* qdst = static_cast<T*>(a.out_act) + (size_t)t0 * a.ld_out + (size_t)head * a.head_dim + i;
     const int g = rotated ? head - a.n_q : head - a.n_q - a.n_kv;
@@ -299,9 +299,9 @@ PE_DEV void issue_w(const CUtensorMap* tmW, const GemmArgs& a, uint32_t sa, uint
 
 template <int EPI>
 PE_DEV void apply16(const GemmArgs& a, int unit, int t0, int n_tok, const float (&v)[16], const float (&v2)[16],
-                    float2 tf) {
+                    float2 tf, const int* pos_s, const long long* slot_s) {
   if (unit >= a.n_out) return;
-  epi_chunk<EPI, __nv_bfloat16>(a, unit, t0, max(0, min(16, n_tok - t0)), v, v2, tf);
+  epi_chunk<EPI, __nv_bfloat16>(a, unit, t0, max(0, min(16, n_tok - t0)), v, v2, tf, pos_s, slot_s);
 }
 
 PE_DEV unsigned long long umax64(unsigned long long x, unsigned long long y) { return x > y ? x : y; }
@@ -588,6 +588,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int unit = w.tile_f * kTcBM + r;
       const uint32_t tl = tmem + (uint32_t)(buf * a.acc_stride) + ((uint32_t)(q * 32) << 16);
       const int tbase = w.tile_t * BN;
+      // QKV: the tile's token positions and KV slots, loaded once per unit by the four
+      // epilogue warps into shared memory (two buffers by unit parity, so the next unit's
+      // loads never overwrite a buffer still being read) instead of a round trip per chunk.
+      // Every epilogue warp passes the barrier once per unit, whatever its wait returned.
+      int* pos_s = nullptr;
+      long long* slot_s = nullptr;
+      if (EPI == EPI_QKV_ROPE && a.k_splits == 1) {
+        slot_s = reinterpret_cast<long long*>(red) + (size_t)(i & 1) * BN;
+        pos_s = reinterpret_cast<int*>(reinterpret_cast<long long*>(red) + 2 * (size_t)BN) + (size_t)(i & 1) * BN;
+        for (int t = threadIdx.x - 64; t < BN; t += 128) {
+          const int tok = tbase + t;
+          pos_s[t] = tok < n_tok ? a.tok_pos[tok] : 0;
+          slot_s[t] = tok < n_tok ? a.tok_slot[tok] : -1;
+        }
+        named_bar_sync(1, 128);
+      }
       if (BAL && ok && w.bnd >= 0) {
         argmax_piece(a, w, tl, unit, n_tok, red_w, r, lane);
       } else if (ok && a.k_splits == 1) {
@@ -599,7 +615,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (ARGMAX)
             argmax16(a, unit, tbase + c * 16, n_tok, v, red_w + tbase + c * 16, lane);
           else
-            apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, tf);
+            apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, tf, pos_s + c * 16, slot_s + c * 16);
         }
       } else if (ok) {
         // split K (one unit per CTA): this split's fp32 partial tile straight from TMEM to
