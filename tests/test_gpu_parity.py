@@ -36,6 +36,10 @@ SMALL = {
     # more vocabulary tiles (161, the last one ragged) than SMs with a short last wave:
     # the LM head cuts tiles at CTA range boundaries and sums the two pieces
     "bf16-lm-balanced": _small(B=4, K=8, vocab=160 * 128 + 37, seed=12),
+    # odd numbers of 64-wide k atoms in every contraction (d 320 = 5, 2d = 10, ffn 448 = 7,
+    # n_q*hd 512 = 8): two-atom pipeline stages end on a half stage whose second atom is
+    # past K and zero-filled
+    "bf16-odd-atoms": _small(B=3, K=5, d=320, ffn=448, seed=13),
     "f32-c0": config(0),
     "f32-L2": _small(dtype="f32", n_layers=2, seed=11),
 }
