@@ -75,6 +75,10 @@ def load_peaks():
 
 # ----------------------------------------------------------------------------- cost model
 
+NOMINAL_HBM_BPS = 7.9e12       # GB300 HBM3e, nominal
+NOMINAL_BF16_FLOPS = 2.25e15   # GB300 dense bf16 tensor, nominal
+
+
 def round_cost(cfg, rnd) -> dict:
     """Algorithmic bytes and flops of one round (counting only).  Bytes: every weight once (the
     embedding table only for the rows the batch needs), the KV prefix once per sequence and layer,
@@ -425,6 +429,10 @@ def run_ours(args):
                       frac=t_round / (ms * 1e-3),
                       bound="hbm" if cost["bytes"] / hbm >= cost["flops"] / tc_sus else "tensor")
     round_roof["frac_direct_launches"] = t_round / (direct_ms * 1e-3)
+    # the same round against the part's nominal peaks (HBM3e 7.9 TB/s, dense bf16 2.25 PFLOP/s)
+    t_nominal = max(cost["bytes"] / NOMINAL_HBM_BPS, cost["flops"] / NOMINAL_BF16_FLOPS)
+    round_roof["nominal"] = dict(hbm_gbs=NOMINAL_HBM_BPS / 1e9, bf16_tflops=NOMINAL_BF16_FLOPS / 1e12,
+                                 roofline_us=t_nominal * 1e6, frac=t_nominal / (ms * 1e-3))
 
     cpu = None if args.no_cpu_baseline else cpu_oracle_sample(cfg_np, w_np, rnd, args.cpu_seconds)
     value = whole_job_rate(world, cfg_np.B, cfg_np.K, ms)
