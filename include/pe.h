@@ -91,10 +91,10 @@ typedef enum { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
 typedef struct {
     int32_t B;                 /* sequences in the batch, >= 1 */
     int32_t K;                 /* draft depth (num_speculative_tokens), >= 1 */
-    int32_t d;                 /* drafter width */
+    int32_t d;                 /* drafter width (bf16: a multiple of 64) */
     int32_t n_q, n_kv;         /* query / key-value heads; n_kv divides n_q */
     int32_t head_dim;          /* 64 or 128 */
-    int32_t ffn;               /* SwiGLU width F */
+    int32_t ffn;               /* SwiGLU width F (bf16: a multiple of 64) */
     int32_t vocab;             /* V; the MASK token id is V (row V of emb) */
     int32_t n_layers;          /* L >= 1 */
     int32_t page_size;         /* KV page size; must be 16 */
@@ -283,7 +283,13 @@ uint64_t pe_kernel_launches(void);
 /* Workspace bytes needed by pe_draft_forward and pe_step for this config (0 if invalid). */
 size_t pe_workspace_bytes(const pe_config *cfg);
 
-/* Validate a config without launching anything. */
+/*
+ * Validate a config without launching anything.  PE_ERR_SHAPE: a size out of range
+ * (B*2K > 65536, n_kv not dividing n_q, ...); PE_ERR_UNSUPPORTED: a valid shape this
+ * build has no kernel for: page_size other than 16, head_dim other than 64 or 128,
+ * d > 16384, or for bf16 d or ffn not a multiple of 64 (the tensor-core GEMMs tile every
+ * contraction in 64-wide k atoms) or more than 128 query vectors per (sequence, kv head).
+ */
 pe_status pe_check_config(const pe_config *cfg);
 
 /* Static description of a status code. */

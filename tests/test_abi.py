@@ -48,6 +48,9 @@ def test_config_validation_codes():
     assert pe.check_config(_cfg(d=2052)) == 3                  # bf16 rows must be 16-byte multiples
     assert pe.check_config(_cfg(dtype="f32", d=2050)) == 3     # fp32 rows too
     assert pe.check_config(_cfg(dtype="f32", d=2048)) == pe.PE_OK
+    assert pe.check_config(_cfg(d=2080)) == 3                  # bf16 contractions tile in 64-wide k atoms
+    assert pe.check_config(_cfg(ffn=6176)) == 3
+    assert pe.check_config(_cfg(dtype="f32", d=2080, ffn=6176)) == pe.PE_OK
     assert pe.status_str(0) == "ok"
 
 
