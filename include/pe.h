@@ -287,7 +287,8 @@ size_t pe_workspace_bytes(const pe_config *cfg);
  * Validate a config without launching anything.  PE_ERR_SHAPE: a size out of range
  * (B*2K > 65536, n_kv not dividing n_q, ...); PE_ERR_UNSUPPORTED: a valid shape this
  * build has no kernel for: page_size other than 16, head_dim other than 64 or 128,
- * d > 16384, or for bf16 d or ffn not a multiple of 64 (the tensor-core GEMMs tile every
+ * d > 10240 in bf16 or 5120 in fp32 (the input-row copy stages ten d-wide row halves in
+ * shared memory), or for bf16 d or ffn not a multiple of 64 (the tensor-core GEMMs tile every
  * contraction in 64-wide k atoms) or more than 128 query vectors per (sequence, kv head).
  */
 pe_status pe_check_config(const pe_config *cfg);

@@ -299,6 +299,7 @@ pe_status check_cfg(const pe_config* c) {
   if (c->head_dim != 64 && c->head_dim != 128) return PE_ERR_UNSUPPORTED;
   if ((long long)c->B * 2 * c->K > kMaxRows) return PE_ERR_SHAPE;
   if (c->d > 16384) return PE_ERR_UNSUPPORTED;  // RMSNorm keeps a row in registers
+  if (scatter_smem_bytes(c->d, (int)elem_bytes(c->dtype)) > kScatterSmemMax) return PE_ERR_UNSUPPORTED;  // staged rows
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return PE_ERR_INVALID_ARG;
   const size_t eb = elem_bytes(c->dtype);
   if ((c->d * eb) % 16 != 0 || c->d % 4 != 0) return PE_ERR_UNSUPPORTED;  // bulk row copies, float4 norm

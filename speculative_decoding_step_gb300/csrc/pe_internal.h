@@ -58,6 +58,10 @@ struct ScatterArgs {
   int32_t* err;
 };
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
+// Shared memory of one input-row CTA (its rows' embedding and hidden halves plus the
+// MASK row); a config whose rows need more than kScatterSmemMax is rejected up front.
+constexpr size_t kScatterSmemMax = 200 * 1024;
+size_t scatter_smem_bytes(int d, int elem_bytes);
 
 struct VerifyArgs {
   int B, K;

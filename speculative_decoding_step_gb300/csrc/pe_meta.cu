@@ -361,13 +361,20 @@ __global__ void __launch_bounds__(32) scatter_kernel(const ScatterArgs a) {
   if (threadIdx.x == 0) scatter_body(a, blockIdx.x);
 }
 
+size_t scatter_smem_bytes(int d, int elem_bytes) {
+  return (size_t)(2 * kScatterRowsPerCta + 2) * (size_t)d * (size_t)elem_bytes;
+}
+
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
-  const size_t smem = (size_t)(2 * kScatterRowsPerCta + 2) * a.d * a.elem_bytes;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  const size_t smem = scatter_smem_bytes(a.d, a.elem_bytes);
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kScatterSmemMax);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   const int grid = (a.R + kScatterRowsPerCta - 1) / kScatterRowsPerCta;
   return launch_pdl(scatter_kernel, dim3(grid), dim3(32), smem, s, a);
@@ -385,13 +392,15 @@ __global__ void __launch_bounds__(kScatterInitThreads) scatter_init_kernel(const
 }
 
 cudaError_t launch_scatter_init(const ScatterArgs& sa, const InitArgs& ia, cudaStream_t s) {
-  const size_t smem = (size_t)(2 * kScatterRowsPerCta + 2) * sa.d * sa.elem_bytes;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(scatter_init_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  const size_t smem = scatter_smem_bytes(sa.d, sa.elem_bytes);
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(scatter_init_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kScatterSmemMax);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   const int grid = (sa.R + kScatterRowsPerCta - 1) / kScatterRowsPerCta + 1;
   return launch_pdl(scatter_init_kernel, dim3(grid), dim3(kScatterInitThreads), smem, s, sa, ia);

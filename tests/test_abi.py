@@ -51,6 +51,9 @@ def test_config_validation_codes():
     assert pe.check_config(_cfg(d=2080)) == 3                  # bf16 contractions tile in 64-wide k atoms
     assert pe.check_config(_cfg(ffn=6176)) == 3
     assert pe.check_config(_cfg(dtype="f32", d=2080, ffn=6176)) == pe.PE_OK
+    assert pe.check_config(_cfg(d=10240)) == pe.PE_OK
+    assert pe.check_config(_cfg(d=10304)) == 3                 # input rows staged in shared memory
+    assert pe.check_config(_cfg(dtype="f32", d=5184)) == 3
     assert pe.status_str(0) == "ok"
 
 
