@@ -251,7 +251,17 @@ pe_status pe_verify(const pe_config *cfg, const int32_t *draft_tokens, const int
  * prev_pos[b][num_accepted[b]] + 1 + j (both [B][K+1]).  target_tokens are
  * the target's tokens for that verify batch (the target model is outside this
  * library).  Batch metadata and x0 live in the workspace
- * (>= pe_workspace_bytes(cfg)).  Outputs must not alias inputs.
+ * (>= pe_workspace_bytes(cfg)).
+ *
+ * In-place state.  The round's state arrays are read only by the batch rebuild
+ * (the first launch), so the next state may overwrite them: next_prev_tokens may
+ * be prev_tokens, next_prev_pos may be prev_pos, num_accepted_out may be
+ * num_accepted and bonus_out may be bonus (each pair exactly the same pointer).
+ * With all four in place, one call -- or a CUDA graph captured from it -- run
+ * again after the caller refills target_hidden and target_tokens is the next
+ * round (the multi-round drafting loop; the prefix grows by num_accepted + 1
+ * positions per round, which the block table must cover).  No other output may
+ * alias an input.
  */
 pe_status pe_step(const pe_config *cfg, const pe_weights *w, const pe_kv *kv, const int32_t *block_table,
                   const int32_t *prev_tokens, const int32_t *prev_pos, const int32_t *num_accepted,

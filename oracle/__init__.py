@@ -22,6 +22,8 @@ Functions (each a plain restatement; pure Python loops where sizes are small):
 * ``scatter_hidden`` (R2) drafter input rows concat(emb(token), hidden).
 * ``draft_forward``  (R3) drafter pass + LM head, fp64, in ``pe_oracle.c``.
 * ``verify``         (R4) greedy verification.
+* ``next_verify_batch`` the verify batch the target checks after a round (the
+  next round's previous batch): the bonus token, then the K drafts.
 
 Parity status: the pages print no numeric example, so every function is
 pinned by closed forms, brute force and invariants in the tests rather than by
@@ -318,6 +320,26 @@ def verify(draft_tokens, target_tokens) -> tuple[np.ndarray, np.ndarray]:
         acc[b] = a
         bon[b] = target_tokens[b][a]
     return acc, bon
+
+
+def next_verify_batch(prev_pos, num_accepted, bonus, drafts) -> tuple[np.ndarray, np.ndarray]:
+    """The verify batch after a round: sequence b's NTP row sat at position prev_pos[b][a]
+    (a = its accepted count) and carried the bonus token, which belongs one position further
+    on; the target then checks [bonus, t_1..t_K] at consecutive positions from there.  This
+    batch is what the next round's rebuild copies token ids and positions from (P-EAGLE
+    pages, "vLLM implementation details", fused batch-metadata kernel)."""
+    drafts = np.asarray(drafts, dtype=np.int32)
+    B, K = drafts.shape
+    tokens = np.zeros((B, K + 1), np.int32)
+    positions = np.zeros((B, K + 1), np.int32)
+    for b in range(B):
+        p0 = int(prev_pos[b][int(num_accepted[b])]) + 1
+        tokens[b][0] = bonus[b]
+        for k in range(K):
+            tokens[b][k + 1] = drafts[b][k]
+        for j in range(K + 1):
+            positions[b][j] = p0 + j
+    return tokens, positions
 
 
 # ----------------------------------------------------------------------------- composition

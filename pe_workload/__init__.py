@@ -40,7 +40,7 @@ import numpy as np
 
 __all__ = [
     "Config", "config", "sweep_config", "Weights", "RoundInputs",
-    "make_weights", "make_round", "make_targets", "bf16_to_f32", "f32_to_bf16",
+    "make_weights", "make_round", "make_targets", "loop_round_draws", "bf16_to_f32", "f32_to_bf16",
     "LOGNORMAL_MEDIAN", "LOGNORMAL_SIGMA", "PREFIX_CAP",
 ]
 
@@ -257,8 +257,11 @@ def _accepted(cfg: Config, rng: np.random.Generator) -> np.ndarray:
     raise ValueError(cfg.accepted)
 
 
-def make_round(cfg: Config, seed: int | None = None, with_cache: bool = True) -> RoundInputs:
-    """Inputs of one drafting round.  The KV prefix is N(0,1) on every cache slot."""
+def make_round(cfg: Config, seed: int | None = None, with_cache: bool = True,
+               extra_positions: int = 0) -> RoundInputs:
+    """Inputs of one drafting round.  The KV prefix is N(0,1) on every cache slot.
+    ``extra_positions`` gives every sequence pages for that many more positions (rounds run
+    back to back grow the prefix by up to K + 1 positions each)."""
     s = cfg.seed if seed is None else seed
     rng = _stream(s, "round-metadata", 0)
     B, K, ps = cfg.B, cfg.K, cfg.page_size
@@ -267,7 +270,7 @@ def make_round(cfg: Config, seed: int | None = None, with_cache: bool = True) ->
     prev_tokens = rng.integers(0, cfg.vocab, size=(B, K + 1)).astype(np.int32)
     prev_pos = (P[:, None] + np.arange(K + 1, dtype=np.int32)[None, :]).astype(np.int32)
     bonus = rng.integers(0, cfg.vocab, size=B).astype(np.int32)
-    pages_per_seq = (P + 2 * K + ps - 1) // ps
+    pages_per_seq = (P + 2 * K + extra_positions + ps - 1) // ps
     num_pages = int(pages_per_seq.sum())
     perm = rng.permutation(num_pages).astype(np.int32)
     max_pages = int(pages_per_seq.max())
@@ -290,6 +293,18 @@ def make_round(cfg: Config, seed: int | None = None, with_cache: bool = True) ->
                        block_table=block_table, num_pages=num_pages, prefix_len=P,
                        target_hidden=hidden, k_cache=kc, v_cache=vc,
                        target_u=target_u, target_r=target_r)
+
+
+def loop_round_draws(cfg: Config, r: int, seed: int | None = None):
+    """Fresh inputs of round r >= 1 of rounds run back to back: the target hidden states of
+    the new verify batch ~ N(0, 1) and the target-token draws (uniforms and uniform tokens)
+    that ``make_targets`` turns into that batch's target tokens."""
+    s = cfg.seed if seed is None else seed
+    rng = _stream(s, f"loop-round{r}", 0)
+    target_u = rng.random(size=(cfg.B, cfg.K))
+    target_r = rng.integers(0, cfg.vocab, size=(cfg.B, cfg.K + 1)).astype(np.int32)
+    hidden = _normal(s, f"target_hidden/round{r}", (cfg.B * (cfg.K + 1), cfg.d), 1.0, cfg.dtype)
+    return hidden, target_u, target_r
 
 
 def make_targets(drafts: np.ndarray, u: np.ndarray, r: np.ndarray, p_match: float = 0.6) -> np.ndarray:

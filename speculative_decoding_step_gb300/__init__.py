@@ -326,3 +326,21 @@ class Round:
              stream=None):
         step(self.cfg, self.weights, self.kv, self.block_table, prev_tokens, prev_pos, num_accepted, bonus,
              target_hidden, target_tokens, self.workspace, self.out, self.err, self._logits(logits), stream)
+
+    def step_inplace(self, state: dict, target_hidden, target_tokens, stream=None):
+        """One round whose next verify batch, accepted counts and bonus tokens overwrite ``state``
+        (prev_tokens, prev_pos, num_accepted, bonus): the same call, or a CUDA graph of it, is
+        the next round once the caller has refilled ``target_hidden`` and ``target_tokens``."""
+        out = dict(draft_tokens=self.draft_tokens, num_accepted=state["num_accepted"], bonus=state["bonus"],
+                   next_prev_tokens=state["prev_tokens"], next_prev_pos=state["prev_pos"])
+        step(self.cfg, self.weights, self.kv, self.block_table, state["prev_tokens"], state["prev_pos"],
+             state["num_accepted"], state["bonus"], target_hidden, target_tokens, self.workspace, out, self.err,
+             None, stream)
+
+    def capture_loop(self, state: dict, target_hidden, target_tokens) -> torch.cuda.CUDAGraph:
+        """CUDA graph of ``step_inplace`` on these buffers; every replay runs the next round.
+        Run one round directly first (launch attributes are set on a kernel's first use)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step_inplace(state, target_hidden, target_tokens)
+        return g

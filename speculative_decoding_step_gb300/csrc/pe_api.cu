@@ -731,7 +731,7 @@ pe_status pe_step(const pe_config* cfg, const pe_weights* w, const pe_kv* kv, co
   trace(2, s);
   VerifyArgs va{};
   va.B = cfg->B; va.K = cfg->K; va.draft = draft_tokens; va.target = target_tokens; va.acc_out = num_accepted_out;
-  va.bonus_out = bonus_out; va.prev_pos = prev_pos; va.num_accepted = num_accepted; va.bonus_in = bonus;
+  va.bonus_out = bonus_out; va.row_list = rows; va.draft_rows = drows; va.positions = pos; va.input_ids = ids;
   va.next_tokens = next_prev_tokens; va.next_pos = next_prev_pos;
   const bool bf16 = cfg->dtype == PE_BF16;  // the tensor-core LM head verifies in its finishing CTA
   st = forward_impl(*cfg, w, kv, block_table, x0, pos, slot, rows, nval, drows, ws, p, draft_tokens, logits_dbg,

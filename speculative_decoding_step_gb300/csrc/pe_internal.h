@@ -67,8 +67,10 @@ struct VerifyArgs {
   int B, K;
   const int32_t *draft, *target;
   int32_t *acc_out, *bonus_out;
-  // optional: next round's verify batch (pe_step)
-  const int32_t *prev_pos, *num_accepted, *bonus_in;
+  // optional: next round's verify batch (pe_step), built from the rebuilt batch of this
+  // round (compacted row list, draft-row list, row positions and token ids) so that the
+  // outputs may overwrite the caller's state arrays that the rebuild read
+  const int32_t *row_list, *draft_rows, *positions, *input_ids;
   int32_t *next_tokens, *next_pos;
 };
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
@@ -77,24 +79,25 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
 // speculative decoding, "Production integration in vLLM": the target's output is
 // preserved): the longest prefix of drafts equal to the target's tokens, then the
 // target's token at the first mismatch as the bonus; optionally the next round's
-// verify batch [bonus, drafts] at the positions after the NTP position.
+// verify batch [bonus, drafts] at the positions after the NTP position.  The NTP
+// row (the first draft row: the bonus token at the last accepted position) is read
+// from the rebuilt batch, never from the previous round's state arrays.
 __device__ __forceinline__ void verify_seq(const VerifyArgs& a, int b) {
   const int32_t* d = a.draft + (size_t)b * a.K;
   const int32_t* t = a.target + (size_t)b * (a.K + 1);
   int acc = 0;
   while (acc < a.K && d[acc] == t[acc]) ++acc;
-  a.acc_out[b] = acc;
-  a.bonus_out[b] = t[acc];
   if (a.next_tokens != nullptr) {
-    int prev_a = a.num_accepted[b];
-    prev_a = prev_a < 0 ? 0 : (prev_a > a.K ? a.K : prev_a);
-    const int p0 = a.prev_pos[(size_t)b * (a.K + 1) + prev_a] + 1;
+    const int ntp = a.row_list[a.draft_rows[(size_t)b * a.K]];  // padded NTP row of sequence b
+    const int p0 = a.positions[ntp] + 1;
     int32_t* nt = a.next_tokens + (size_t)b * (a.K + 1);
     int32_t* np = a.next_pos + (size_t)b * (a.K + 1);
-    nt[0] = a.bonus_in[b];
+    nt[0] = a.input_ids[ntp];
     for (int k = 0; k < a.K; ++k) nt[k + 1] = d[k];
     for (int j = 0; j <= a.K; ++j) np[j] = p0 + j;
   }
+  a.acc_out[b] = acc;
+  a.bonus_out[b] = t[acc];
 }
 
 // Forward prologue: per compacted row metadata, per sequence ranges, the

@@ -5,6 +5,7 @@ rows are a copy, so bit-exact too; logits are within 1e-3 (fp32) / 5e-2 (bf16)
 and draft tokens equal wherever the oracle's top-1/top-2 gap exceeds 0.1.
 """
 
+import dataclasses
 import itertools
 
 import numpy as np
@@ -13,10 +14,12 @@ import torch
 
 import oracle
 import speculative_decoding_step_gb300 as pe
-from pe_workload import Config, config, make_round, make_targets, make_weights, sweep_config
+from pe_workload import (Config, config, f32_to_bf16, loop_round_draws, make_round, make_targets, make_weights,
+                         sweep_config)
+from pe_workload.device import to_torch
 
-from gpu_harness import (check_kv_writes, check_logits, meta_np, oracle_round, run_stages, setup,
-                         to_np_storage)
+from gpu_harness import (GAP, KV_TOL, LOGIT_TOL, check_kv_writes, check_logits, meta_np, oracle_round, run_stages,
+                         setup, to_np_storage)
 
 pytestmark = pytest.mark.gpu
 
@@ -263,6 +266,80 @@ def test_step_equals_stages_and_next_batch():
         a = int(c.r_np.num_accepted[b])
         assert nt[b, 0] == c.r_np.bonus[b] and np.array_equal(nt[b, 1:], drafts[b])
         assert np.array_equal(npos[b], c.r_np.prev_pos[b][a] + 1 + np.arange(cfg_np.K + 1))
+
+
+# ----------------------------------------------------------------------------- rounds back to back
+
+@pytest.mark.parametrize("name", ["f32-L2", "bf16-hd64", "bf16-L2-long"])
+def test_multi_round_loop_in_place_graph(name):
+    """Rounds back to back with the round state updated in place: round 0 through a direct
+    pe_step call, then replays of one captured CUDA graph, the caller refilling the target's
+    hidden states and tokens in between.  The oracle runs every round from the same state:
+    the drafts agree (exactly where the oracle's top-1/top-2 gap is clear, otherwise the
+    picked token's oracle logit is within twice the logit tolerance of the top one); accepted
+    counts, bonus tokens and the next verify batch are bit-exact; and after the last round the
+    caches hold the oracle's writes of every round, a later round's write winning where a
+    position was written twice (a MASK row's speculative entry overwritten by the next round's
+    accepted row at that position)."""
+    n_rounds = 4
+    cfg_np = SMALL[name]
+    B, K, L = cfg_np.B, cfg_np.K, cfg_np.n_layers
+    kvd = cfg_np.n_kv * cfg_np.head_dim
+    rnd = make_round(cfg_np, extra_positions=n_rounds * (K + 1))
+    c = setup(cfg_np, rnd=rnd)
+    storage = (lambda x: f32_to_bf16(x)) if cfg_np.dtype == "bf16" else (lambda x: x.astype(np.float32))
+    ok, ov = [x.copy() for x in rnd.k_cache], [x.copy() for x in rnd.v_cache]
+    written = np.zeros(ok[0].shape[0] * ok[0].shape[1], dtype=bool)
+    st = dict(prev_tokens=rnd.prev_tokens.copy(), prev_pos=rnd.prev_pos.copy(),
+              num_accepted=rnd.num_accepted.copy(), bonus=rnd.bonus.copy())
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    state = {k: i32(v) for k, v in st.items()}
+    th = c.Rd["target_hidden"].clone()
+    tt = torch.zeros((B, K + 1), dtype=torch.int32, device="cuda")
+    tol = LOGIT_TOL[cfg_np.dtype]
+    graph, total_accepted = None, 0
+    for r in range(n_rounds):
+        hidden, u, tr = (rnd.target_hidden, rnd.target_u, rnd.target_r) if r == 0 else loop_round_draws(cfg_np, r)
+        ref = oracle.run_round(cfg_np, c.w_np, dataclasses.replace(rnd, target_hidden=hidden, k_cache=ok,
+                                                                    v_cache=ov, **st), want_kv=True)
+        target = make_targets(ref["drafts"], u, tr)
+        th.copy_(to_torch(hidden))
+        tt.copy_(i32(target))
+        if r == 0:
+            c.rd.step_inplace(state, th, tt)
+        else:
+            if graph is None:
+                graph = c.rd.capture_loop(state, th, tt)
+            graph.replay()
+        torch.cuda.synchronize()
+        assert int(c.rd.err.item()) == 0, f"round {r}"
+        drafts = c.rd.draft_tokens.cpu().numpy()
+        lg = ref["logits"].reshape(B, K, -1)
+        picked = np.take_along_axis(lg, drafts[..., None].astype(np.int64), axis=2)[..., 0]
+        assert (picked >= lg.max(axis=2) - 2 * tol).all(), f"round {r}"
+        sure = (oracle.top2_gap(ref["logits"]) > GAP).reshape(B, K)
+        assert np.array_equal(drafts[sure], ref["drafts"][sure]), f"round {r}"
+        acc, bon = oracle.verify(drafts, target)
+        nt, npos = oracle.next_verify_batch(st["prev_pos"], st["num_accepted"], st["bonus"], drafts)
+        got = {k: v.cpu().numpy() for k, v in state.items()}
+        assert np.array_equal(got["num_accepted"], acc) and np.array_equal(got["bonus"], bon), f"round {r}"
+        assert np.array_equal(got["prev_tokens"], nt) and np.array_equal(got["prev_pos"], npos), f"round {r}"
+        slots = ref["meta"]["slot_mapping"][ref["rows"]]
+        for l in range(L):
+            ok[l].reshape(-1, kvd)[slots] = storage(ref["new_k"][l])
+            ov[l].reshape(-1, kvd)[slots] = storage(ref["new_v"][l])
+        written[slots] = True
+        st = dict(prev_tokens=nt, prev_pos=npos, num_accepted=acc, bonus=bon)
+        total_accepted += int(acc.sum())
+    assert total_accepted > 0  # the loop went past the first verify batch
+    for l in range(L):
+        for nm, dev, want in (("k", c.kv.k_cache[l], ok[l]), ("v", c.kv.v_cache[l], ov[l])):
+            g_bits = to_np_storage(dev).reshape(-1, kvd)
+            w_bits = want.reshape(-1, kvd)
+            assert np.array_equal(g_bits[~written], w_bits[~written]), f"{nm} cache layer {l}: stray write"
+            g, w = oracle.widen(g_bits[written]), oracle.widen(w_bits[written])
+            diff = np.abs(g - w) / np.maximum(1.0, np.abs(w))
+            assert diff.max() <= KV_TOL[cfg_np.dtype], f"{nm} cache layer {l}: rel diff {diff.max():.3g}"
 
 
 # ----------------------------------------------------------------------------- device-side checks

@@ -387,3 +387,48 @@ def test_verify_brute_force(K):
         for j, (d, t) in enumerate(chunk):
             best = max(jj for jj in range(K + 1) if all(d[x] == t[x] for x in range(jj)))
             assert a[j] == best and bonus[j] == t[best]
+
+
+# ----------------------------------------------------------------------------- the next verify batch
+
+def test_next_verify_batch_hand_example():
+    """Sequence at P = 100 with K = 3: a = 2 accepted, so the NTP row sat at 102 and the
+    bonus token belongs at 103; the drafts follow at 104..106.  a = 0: bonus at 101."""
+    prev_pos = np.array([[100, 101, 102, 103], [40, 41, 42, 43]])
+    drafts = np.array([[5, 6, 8], [9, 10, 11]])
+    tok, pos = oracle.next_verify_batch(prev_pos, [2, 0], [7, 3], drafts)
+    assert tok.tolist() == [[7, 5, 6, 8], [3, 9, 10, 11]]
+    assert pos.tolist() == [[103, 104, 105, 106], [41, 42, 43, 44]]
+
+
+@pytest.mark.parametrize("K", [1, 2, 5, 8])
+def test_next_verify_batch_consistent_with_rebuild(K):
+    """Against the rebuild's positions (a row at position p carries the token at p + 1 and
+    predicts the one at p + 2): the bonus token, carried by the NTP row, lands one position
+    after it; draft t_k, predicted by the k-th draft row, lands two positions after that row;
+    and the next rebuild's copy slots continue without a gap."""
+    rng = np.random.default_rng(K)
+    B, V = 6, 50
+    P = rng.integers(0, 200, size=B)
+    prev_pos = P[:, None] + np.arange(K + 1)[None, :]
+    prev_tokens = rng.integers(0, V, size=(B, K + 1))
+    acc = np.array([b % (K + 1) for b in range(B)])
+    bonus = rng.integers(0, V, size=B)
+    bt = np.arange(B * 40).reshape(B, 40)
+    meta = oracle.prepare_batch(K, V, prev_tokens, prev_pos, acc, bonus, bt)
+    drafts = rng.integers(0, V, size=(B, K))
+    tok, pos = oracle.next_verify_batch(prev_pos, acc, bonus, drafts)
+    dr = meta["row_list"][meta["draft_rows"]].reshape(B, K)
+    for b in range(B):
+        ntp = dr[b][0]
+        assert tok[b][0] == meta["input_ids"][ntp] == bonus[b]
+        assert pos[b][0] == meta["positions"][ntp] + 1
+        for k in range(K):
+            assert tok[b][k + 1] == drafts[b][k]
+            assert pos[b][k + 1] == meta["positions"][dr[b][k]] + 2
+    # the next round: its accepted rows and NTP row sit at consecutive positions from pos[b][0]
+    acc2 = np.array([(b * 3) % (K + 1) for b in range(B)])
+    meta2 = oracle.prepare_batch(K, V, tok, pos, acc2, bonus, bt)
+    for b in range(B):
+        rows = [b * 2 * K + r for r in range(acc2[b] + 1)]
+        assert [meta2["positions"][r] for r in rows] == list(range(pos[b][0], pos[b][0] + acc2[b] + 1))
