@@ -24,6 +24,15 @@ Functions (each a plain restatement; pure Python loops where sizes are small):
 * ``verify``         (R4) greedy verification.
 * ``next_verify_batch`` the verify batch the target checks after a round (the
   next round's previous batch): the bonus token, then the K drafts.
+* ``inverse_cdf``, ``drafter_distribution``, ``sample_drafts``,
+  ``verify_sampled`` (R5) non-greedy drafting and verification by rejection
+  sampling (speculative sampling): drafts drawn from the drafter's
+  temperature softmax, each accepted with probability min(1, p/q), the first
+  rejected one replaced by a draw from the normalised residual max(0, p - q),
+  a bonus drawn from the target when every draft is accepted.  The pages
+  state only that verification uses rejection sampling to keep the target's
+  output distribution; the steps are the standard speculative-sampling
+  scheme that does so.
 
 Parity status: the pages print no numeric example, so every function is
 pinned by closed forms, brute force and invariants in the tests rather than by
@@ -340,6 +349,80 @@ def next_verify_batch(prev_pos, num_accepted, bonus, drafts) -> tuple[np.ndarray
         for j in range(K + 1):
             positions[b][j] = p0 + j
     return tokens, positions
+
+
+# ----------------------------------------------------------------------------- R5: sampled drafting and verification
+# vLLM Speculators: parallel drafting for speculative decoding, closing paragraph of
+# "Production integration in vLLM": verification by rejection sampling keeps the target
+# model's output distribution.  Every random number is an input (one uniform in [0, 1)
+# per draw), so both sides draw the same sample.
+
+def inverse_cdf(w, u: float) -> int:
+    """One draw from the non-negative weights ``w`` (not all zero) with the uniform ``u``:
+    the smallest index whose running sum of weights exceeds u times the total.  A
+    zero-weight index is never drawn."""
+    c = np.cumsum(np.asarray(w, dtype=np.float64))
+    v = int(np.searchsorted(c, u * c[-1], side="right"))
+    return min(v, len(c) - 1)
+
+
+def drafter_distribution(logits_row, temperature: float) -> tuple[np.ndarray, float]:
+    """The drafter's distribution q = softmax(logits / temperature) and its natural-log
+    normaliser lse (q[v] = exp(logits[v] / temperature - lse))."""
+    z = np.asarray(logits_row, dtype=np.float64) / temperature
+    m = z.max()
+    e = np.exp(z - m)
+    tot = e.sum()
+    return e / tot, float(m + np.log(tot))
+
+
+def sample_drafts(logits, u_draft, temperature: float) -> tuple[np.ndarray, np.ndarray]:
+    """Non-greedy drafting: draft row (b, k) (logits row b*K + k) draws its token from its own
+    q with the uniform u_draft[b][k].  Returns the drafts [B][K] and each row's lse [B][K]."""
+    u_draft = np.asarray(u_draft, dtype=np.float64)
+    B, K = u_draft.shape
+    lg = np.asarray(logits).reshape(B * K, -1)
+    drafts = np.zeros((B, K), np.int32)
+    lse = np.zeros((B, K))
+    for b in range(B):
+        for k in range(K):
+            q, lse[b][k] = drafter_distribution(lg[b * K + k], temperature)
+            drafts[b][k] = inverse_cdf(q, u_draft[b][k])
+    return drafts, lse
+
+
+def verify_sampled(drafts, logits, temperature: float, target_probs, u_accept, u_resample):
+    """Rejection-sampling verification of sequence b's drafts t_1..t_K (``drafts[b]``).
+
+    target_probs[b][k] is the target's distribution p_k for the position of draft k
+    (after the verify batch's element k; p_K follows the last draft), q_k the drafter's
+    distribution of draft row k.  For k = 0, 1, ...: draft x = drafts[b][k] is accepted
+    when u_accept[b][k] * q_k(x) < p_k(x) (probability min(1, p_k(x) / q_k(x))).  At the
+    first rejection the accepted count is k and the bonus token is drawn with
+    u_resample[b] from max(0, p_k - q_k) (from p_k itself if that residual is all zero);
+    when all K are accepted the bonus is drawn from p_K.  Returns (accepted, bonus)."""
+    drafts = np.asarray(drafts)
+    B, K = drafts.shape
+    lg = np.asarray(logits).reshape(B * K, -1)
+    P = np.asarray(target_probs, dtype=np.float64)
+    acc = np.zeros(B, np.int32)
+    bonus = np.zeros(B, np.int32)
+    for b in range(B):
+        a = K
+        for k in range(K):
+            q, _ = drafter_distribution(lg[b * K + k], temperature)
+            x = int(drafts[b][k])
+            if not (u_accept[b][k] * q[x] < P[b][k][x]):
+                a = k
+                break
+        acc[b] = a
+        if a < K:
+            q, _ = drafter_distribution(lg[b * K + a], temperature)
+            res = np.maximum(0.0, P[b][a] - q)
+            bonus[b] = inverse_cdf(res if res.sum() > 0 else P[b][a], u_resample[b])
+        else:
+            bonus[b] = inverse_cdf(P[b][K], u_resample[b])
+    return acc, bonus
 
 
 # ----------------------------------------------------------------------------- composition

@@ -43,6 +43,8 @@ SMALL = {
     # n_q*hd 512 = 8): two-atom pipeline stages end on a half stage whose second atom is
     # past K and zero-filled
     "bf16-odd-atoms": _small(B=3, K=5, d=320, ffn=448, seed=13),
+    # a deeper drafter: four layers, each its own weights and KV cache
+    "bf16-L4": _small(B=2, K=6, n_layers=4, prefix_args=(100, 700), seed=14),
     "f32-c0": config(0),
     "f32-L2": _small(dtype="f32", n_layers=2, seed=11),
 }

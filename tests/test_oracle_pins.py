@@ -432,3 +432,82 @@ def test_next_verify_batch_consistent_with_rebuild(K):
     for b in range(B):
         rows = [b * 2 * K + r for r in range(acc2[b] + 1)]
         assert [meta2["positions"][r] for r in rows] == list(range(pos[b][0], pos[b][0] + acc2[b] + 1))
+
+
+# ----------------------------------------------------------------------------- R5: sampled drafting + verification
+
+def test_inverse_cdf_hand_cases():
+    """Weights [1, 2, 3, 4] (total 10): the draw changes index where u * 10 reaches the
+    running sums 1, 3, 6 (a boundary itself goes to the next index); zero weights are
+    skipped."""
+    w = [1.0, 2.0, 3.0, 4.0]
+    cases = {0.0: 0, 0.05: 0, 0.0999: 0, 0.1: 1, 0.29: 1, 0.3: 2, 0.59: 2, 0.6: 3, 0.999999: 3}
+    for u, v in cases.items():
+        assert oracle.inverse_cdf(w, u) == v, u
+    assert [oracle.inverse_cdf([0, 0, 5, 0, 5, 0], u) for u in (0.0, 0.49, 0.5, 0.99)] == [2, 2, 4, 4]
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5, 2.0])
+def test_sample_drafts_frequencies_and_normaliser(T):
+    """Logits log(1), log(2), log(3): q is proportional to [1, 2, 3]^(1/T).  Uniforms on an
+    even midpoint grid land on each token in proportion to its probability (exactly, up to
+    one grid step), and lse is the log of the sum of exp(logits / T)."""
+    lg = np.log(np.array([1.0, 2.0, 3.0]))
+    q_closed = np.array([1.0, 2.0, 3.0]) ** (1 / T)
+    q_closed /= q_closed.sum()
+    N = 30000
+    u = ((np.arange(N) + 0.5) / N).reshape(N, 1)
+    drafts, lse = oracle.sample_drafts(np.tile(lg, (N, 1)), u, T)
+    freq = np.bincount(drafts.reshape(-1), minlength=3) / N
+    assert np.abs(freq - q_closed).max() <= 1.0 / N + 1e-12
+    assert np.allclose(lse, math.log(np.sum(np.array([1.0, 2.0, 3.0]) ** (1 / T))), atol=1e-12)
+
+
+def test_verify_sampled_closed_forms():
+    """q == p: every draft is accepted (u * q < p for u < 1) and the bonus is drawn from
+    p_K.  A one-hot target at token y: a draft equal to y is accepted, any other draft is
+    rejected, and the residual max(0, p - q) is concentrated on y, so the bonus is y."""
+    rng = np.random.default_rng(5)
+    B, K, V = 6, 3, 7
+    lg = rng.normal(0, 1.5, size=(B * K, V))
+    q = np.array([oracle.drafter_distribution(r, 1.0)[0] for r in lg]).reshape(B, K, V)
+    pK = rng.dirichlet(np.ones(V), size=B)
+    P = np.concatenate([q, pK[:, None, :]], axis=1)
+    drafts = rng.integers(0, V, size=(B, K))
+    u_res = rng.random(B)
+    a, bonus = oracle.verify_sampled(drafts, lg, 1.0, P, rng.random((B, K)) * 0.999999, u_res)
+    assert (a == K).all()
+    assert [int(x) for x in bonus] == [oracle.inverse_cdf(pK[b], u_res[b]) for b in range(B)]
+    y = 4
+    P1 = np.zeros((B, K + 1, V))
+    P1[:, :, y] = 1.0
+    drafts = np.full((B, K), y)
+    drafts[:, 1] = [0, 1, 2, 3, 5, 6]  # the second draft is never y
+    a, bonus = oracle.verify_sampled(drafts, lg, 1.0, P1, rng.random((B, K)), rng.random(B))
+    assert (a == 1).all() and (bonus == y).all()
+
+
+def test_verify_sampled_preserves_target_distribution():
+    """The defining property of the scheme: whatever the drafter proposes, the token emitted
+    at a position (the accepted draft, else the bonus) follows the target's distribution
+    there.  Monte Carlo over 40000 sequences with V = 4, K = 2 and q far from p: the first
+    emitted token follows p_0, and among sequences that accepted the first draft, the second
+    follows p_1 (5-sigma bounds)."""
+    rng = np.random.default_rng(11)
+    B, K, V = 40000, 2, 4
+    lg_rows = np.log(np.array([[0.55, 0.25, 0.15, 0.05], [0.1, 0.2, 0.3, 0.4]]))
+    lg = np.tile(lg_rows, (B, 1))
+    p = np.array([[0.1, 0.2, 0.3, 0.4], [0.4, 0.4, 0.1, 0.1], [0.25, 0.25, 0.25, 0.25]])
+    P = np.broadcast_to(p, (B, K + 1, V))
+    drafts, _ = oracle.sample_drafts(lg, rng.random((B, K)), 1.0)
+    a, bonus = oracle.verify_sampled(drafts, lg, 1.0, P, rng.random((B, K)), rng.random(B))
+    first = np.where(a >= 1, drafts[:, 0], bonus)
+    f0 = np.bincount(first, minlength=V) / B
+    assert np.abs(f0 - p[0]).max() <= 5 * np.sqrt(p[0] * (1 - p[0]) / B).max()
+    sel = a >= 1
+    second = np.where(a[sel] >= 2, drafts[sel, 1], bonus[sel])
+    n = int(sel.sum())
+    f1 = np.bincount(second, minlength=V) / n
+    assert np.abs(f1 - p[1]).max() <= 5 * np.sqrt(p[1] * (1 - p[1]) / n).max()
+    # acceptance rate of the first draft: sum_v min(p_0, q_0)
+    assert abs(sel.mean() - np.minimum(p[0], np.exp(lg_rows[0])).sum()) <= 5 * 0.0025
