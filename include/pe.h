@@ -12,6 +12,12 @@
  *   pe_verify          greedy verification -> acceptance length, bonus token
  *   pe_step            all of the above on one stream
  *
+ * Non-greedy drafting and verification (from the forward pass's logits):
+ *
+ *   pe_sample_drafts   draw the drafts from the drafter's temperature softmax
+ *   pe_verify_sampled  rejection-sampling verification against the target's
+ *                      distributions
+ *
  * Conventions shared by every entry point:
  *
  * - Memory.  Unless stated otherwise a pointer argument is a DEVICE pointer to
@@ -243,6 +249,49 @@ pe_status pe_draft_forward_noalloc(const pe_config *cfg, const pe_weights *w, co
  */
 pe_status pe_verify(const pe_config *cfg, const int32_t *draft_tokens, const int32_t *target_tokens,
                     int32_t *num_accepted_out, int32_t *bonus_out, pe_stream_t stream);
+
+/*
+ * Non-greedy drafting (vLLM Speculators: parallel drafting for speculative
+ * decoding, "Production integration in vLLM": verification by rejection
+ * sampling keeps the target's output distribution).  Draft row r = b*K + k
+ * draws its token from the drafter's distribution
+ *   q_r(v) = exp(logits[r][v] / temperature - lse[r]),
+ *   lse[r] = log sum_v exp(logits[r][v] / temperature)       (natural log)
+ * with the uniform u_draft[r] in [0, 1): the first v at which the running sum
+ * of q_r exceeds u_draft[r] (inverse CDF; the sum runs in a fixed order, so the
+ * draw is deterministic).  logits [B*K][V] fp32 are pe_draft_forward's
+ * logits_dbg output; draft_tokens [B][K] and lse [B*K] are written.  workspace:
+ * 256-byte aligned, >= pe_workspace_bytes(cfg) bytes (the same workspace as
+ * pe_draft_forward may be passed; its contents are scratch).  Two launches:
+ * statistics of every 128-entry step of every row, then one warp per row for the
+ * draw.  A non-finite logit sets PE_DEV_NONFINITE (token 0, lse NaN).
+ * temperature must be positive and finite (else PE_ERR_INVALID_ARG).
+ */
+pe_status pe_sample_drafts(const pe_config *cfg, const float *logits, const float *u_draft, float temperature,
+                           void *workspace, size_t workspace_bytes, int32_t *draft_tokens, float *lse,
+                           int32_t *err_word, pe_stream_t stream);
+
+/*
+ * Verification by rejection sampling (speculative sampling) of drafts drawn by
+ * pe_sample_drafts from the same logits, lse and temperature.
+ * target_probs [B][K+1][V] fp32: p_k = target_probs[b][k] is the target's
+ * distribution for the position of draft k (after element k of the verify
+ * batch [bonus, t_1..t_K]); p_K follows the last draft.  For k = 0, 1, ...:
+ * draft x = draft_tokens[b][k] is accepted when u_accept[b][k] * q(x) < p_k(x),
+ * i.e. with probability min(1, p_k(x) / q(x)).  At the first rejection
+ * num_accepted_out[b] = k and bonus_out[b] is drawn with u_resample[b] (inverse
+ * CDF, as above) from the residual max(0, p_k - q), or from p_k when that
+ * residual is all zero; with every draft accepted, num_accepted_out[b] = K and
+ * the bonus is drawn from p_K.  u_accept [B][K], u_resample [B] in [0, 1).
+ * workspace as for pe_sample_drafts.  A draft outside [0, V) sets
+ * PE_DEV_BAD_TOKEN (and
+ * counts as rejected); a target row with no positive finite mass sets
+ * PE_DEV_NONFINITE (bonus 0).
+ */
+pe_status pe_verify_sampled(const pe_config *cfg, const int32_t *draft_tokens, const float *logits, const float *lse,
+                            float temperature, const float *target_probs, const float *u_accept,
+                            const float *u_resample, void *workspace, size_t workspace_bytes,
+                            int32_t *num_accepted_out, int32_t *bonus_out, int32_t *err_word, pe_stream_t stream);
 
 /*
  * One whole round on one stream: pe_prepare_batch -> pe_scatter_hidden ->

@@ -34,6 +34,7 @@ PE_DEV_BAD_ROW = 0x0605
 PE_DEV_TIMEOUT = 0x0106
 
 EXPORTED_SYMBOLS = ["pe_prepare_batch", "pe_scatter_hidden", "pe_draft_forward", "pe_verify", "pe_step",
+                    "pe_sample_drafts", "pe_verify_sampled",
                     "pe_workspace_bytes", "pe_check_config", "pe_status_str", "pe_set_trace_events",
                     "pe_trace_points", "pe_kernel_launches", "pe_draft_forward_noalloc"]
 
@@ -132,6 +133,9 @@ def lib():
         cp = ctypes.POINTER(Config)
         for name in EXPORTED_SYMBOLS:
             getattr(L, name)
+        L.pe_sample_drafts.argtypes = [cp, vp, vp, ctypes.c_float, vp, ctypes.c_size_t, vp, vp, vp, vp]
+        L.pe_verify_sampled.argtypes = [cp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, ctypes.c_size_t, vp, vp, vp,
+                                        vp]
         L.pe_status_str.restype = ctypes.c_char_p
         L.pe_status_str.argtypes = [ctypes.c_int]
         L.pe_workspace_bytes.restype = ctypes.c_size_t
@@ -247,6 +251,24 @@ def verify(cfg, draft_tokens, target_tokens, num_accepted_out, bonus_out, stream
     _check(st, "pe_verify")
 
 
+def sample_drafts(cfg, logits, u_draft, temperature, workspace, draft_tokens, lse, err, stream=None):
+    """Non-greedy drafting: draft tokens drawn from softmax(logits / temperature)."""
+    st = lib().pe_sample_drafts(ctypes.byref(cfg), _ptr(logits), _ptr(u_draft), ctypes.c_float(temperature),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(draft_tokens),
+                                _ptr(lse), _ptr(err), _stream(stream))
+    _check(st, "pe_sample_drafts")
+
+
+def verify_sampled(cfg, draft_tokens, logits, lse, temperature, target_probs, u_accept, u_resample, workspace,
+                   num_accepted_out, bonus_out, err, stream=None):
+    """Verification by rejection sampling against the target's distributions."""
+    st = lib().pe_verify_sampled(ctypes.byref(cfg), _ptr(draft_tokens), _ptr(logits), _ptr(lse),
+                                 ctypes.c_float(temperature), _ptr(target_probs), _ptr(u_accept), _ptr(u_resample),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _ptr(num_accepted_out), _ptr(bonus_out), _ptr(err), _stream(stream))
+    _check(st, "pe_verify_sampled")
+
+
 def step(cfg, weights: DeviceWeights, kv: DeviceKV, block_table, prev_tokens, prev_pos, num_accepted, bonus,
          target_hidden, target_tokens, workspace, out: dict, err, logits_dbg=None, stream=None):
     """One whole round.  ``out`` holds draft_tokens, num_accepted, bonus, next_prev_tokens, next_prev_pos."""
@@ -299,6 +321,7 @@ class Round:
                         bonus=torch.empty(cfg.B, **i32), next_prev_tokens=torch.empty((cfg.B, cfg.K + 1), **i32),
                         next_prev_pos=torch.empty((cfg.B, cfg.K + 1), **i32))
         self.logits = None
+        self.lse = None
 
     def _logits(self, want: bool):
         if not want:
@@ -326,6 +349,21 @@ class Round:
              stream=None):
         step(self.cfg, self.weights, self.kv, self.block_table, prev_tokens, prev_pos, num_accepted, bonus,
              target_hidden, target_tokens, self.workspace, self.out, self.err, self._logits(logits), stream)
+
+    def sample(self, u_draft, temperature: float = 1.0, stream=None):
+        """Non-greedy drafting from the logits of the last ``forward(logits=True)``: overwrites
+        draft_tokens with draws from softmax(logits / temperature) and fills ``lse``."""
+        if self.logits is None:
+            raise RuntimeError("sample() needs the logits of forward(logits=True)")
+        if self.lse is None:
+            self.lse = torch.empty(self.cfg.B * self.cfg.K, dtype=torch.float32, device=self.x0.device)
+        sample_drafts(self.cfg, self.logits, u_draft, temperature, self.workspace, self.draft_tokens, self.lse,
+                      self.err, stream)
+
+    def verify_sampled(self, target_probs, u_accept, u_resample, temperature: float = 1.0, stream=None):
+        """Rejection-sampling verification of the drafts of the last ``sample``."""
+        verify_sampled(self.cfg, self.draft_tokens, self.logits, self.lse, temperature, target_probs, u_accept,
+                       u_resample, self.workspace, self.out["num_accepted"], self.out["bonus"], self.err, stream)
 
     def step_inplace(self, state: dict, target_hidden, target_tokens, stream=None):
         """One round whose next verify batch, accepted counts and bonus tokens overwrite ``state``

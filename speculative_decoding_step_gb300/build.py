@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpe.so")
-SOURCES = ["pe_api.cu", "pe_meta.cu", "pe_gemm.cu", "pe_attn.cu", "pe_noalloc.cu"]
+SOURCES = ["pe_api.cu", "pe_meta.cu", "pe_gemm.cu", "pe_attn.cu", "pe_noalloc.cu", "pe_sample.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

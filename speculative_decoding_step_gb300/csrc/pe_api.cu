@@ -132,6 +132,7 @@ struct Plan {
   size_t tok_pos, tok_seq, tok_slot, seq_start, seq_len, seq_maxpos, item_base, n_chunks, n_items, items;
   size_t done, keys, x, y, q, ao, u, yl, part_m, part_l, part_o, split_part;
   size_t st_ids, st_pos, st_slot, st_rej, st_mask, st_hmap, st_rows, st_nvalid, st_draft, st_x0;
+  size_t samp;
   size_t total = 0;
 };
 
@@ -213,6 +214,7 @@ Plan make_plan(const pe_config& c) {
   p.st_nvalid = take(4);
   p.st_draft = take(4 * (size_t)p.T);
   p.st_x0 = take(eb * (size_t)p.R * 2 * c.d);
+  p.samp = take(sample_stats_bytes(p.T, c.vocab));  // pe_sample_drafts / pe_verify_sampled
   p.total = off;
   return p;
 }
@@ -739,6 +741,48 @@ pe_status pe_step(const pe_config* cfg, const pe_weights* w, const pe_kv* kv, co
   if (st != PE_OK) return st;
   if (!bf16 && launch_verify(va, s) != cudaSuccess) return PE_ERR_CUDA;
   trace(7 + 7 * cfg->n_layers, s);
+  return PE_OK;
+}
+
+pe_status pe_sample_drafts(const pe_config* cfg, const float* logits, const float* u_draft, float temperature,
+                           void* workspace, size_t workspace_bytes, int32_t* draft_tokens, float* lse,
+                           int32_t* err_word, pe_stream_t stream) {
+  pe_status st = check_cfg(cfg);
+  if (st != PE_OK) return st;
+  if (!logits || !u_draft || !workspace || !draft_tokens || !lse || !err_word) return PE_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return PE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PE_ERR_INVALID_ARG;
+  const Plan p = make_plan(*cfg);
+  if (workspace_bytes < p.total) return PE_ERR_SHAPE;
+  SampleArgs a{};
+  a.B = cfg->B; a.K = cfg->K; a.V = cfg->vocab;
+  a.logits = logits; a.u = u_draft; a.inv_t2 = (float)(1.4426950408889634 / (double)temperature);
+  a.stats = at<float2>(workspace, p.samp);
+  a.drafts = draft_tokens; a.lse = lse; a.err = err_word;
+  PE_TRY_CUDA(launch_sample_drafts(a, p.sms, (cudaStream_t)stream));
+  return PE_OK;
+}
+
+pe_status pe_verify_sampled(const pe_config* cfg, const int32_t* draft_tokens, const float* logits, const float* lse,
+                            float temperature, const float* target_probs, const float* u_accept,
+                            const float* u_resample, void* workspace, size_t workspace_bytes,
+                            int32_t* num_accepted_out, int32_t* bonus_out, int32_t* err_word, pe_stream_t stream) {
+  pe_status st = check_cfg(cfg);
+  if (st != PE_OK) return st;
+  if (!draft_tokens || !logits || !lse || !target_probs || !u_accept || !u_resample || !workspace ||
+      !num_accepted_out || !bonus_out || !err_word)
+    return PE_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return PE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PE_ERR_INVALID_ARG;
+  const Plan p = make_plan(*cfg);
+  if (workspace_bytes < p.total) return PE_ERR_SHAPE;
+  VerifySampledArgs a{};
+  a.B = cfg->B; a.K = cfg->K; a.V = cfg->vocab;
+  a.drafts = draft_tokens; a.logits = logits; a.lse = lse; a.inv_t2 = (float)(1.4426950408889634 / (double)temperature);
+  a.target_probs = target_probs; a.u_accept = u_accept; a.u_resample = u_resample;
+  a.stats = at<float2>(workspace, p.samp);
+  a.acc_out = num_accepted_out; a.bonus_out = bonus_out; a.err = err_word;
+  PE_TRY_CUDA(launch_verify_sampled(a, p.sms, (cudaStream_t)stream));
   return PE_OK;
 }
 

@@ -100,6 +100,35 @@ __device__ __forceinline__ void verify_seq(const VerifyArgs& a, int b) {
   a.bonus_out[b] = t[acc];
 }
 
+// Non-greedy drafting and rejection-sampling verification; see pe_sample.cu.  Each
+// draw over a vocabulary row keeps one statistic pair per 128 entries in the
+// workspace (sample_stats_bytes).
+struct SampleArgs {
+  int B, K, V;
+  const float* logits;  // [B*K][V]
+  const float* u;       // [B*K] uniforms in [0, 1)
+  float inv_t2;         // log2(e) / temperature
+  float2* stats;        // workspace: [B*K][ceil(V / 128)]
+  int32_t* drafts;      // [B*K]
+  float* lse;           // [B*K]
+  int32_t* err;
+};
+cudaError_t launch_sample_drafts(const SampleArgs& a, int sms, cudaStream_t s);
+
+struct VerifySampledArgs {
+  int B, K, V;
+  const int32_t* drafts;      // [B*K]
+  const float *logits, *lse;  // [B*K][V], [B*K] (natural log)
+  float inv_t2;               // log2(e) / temperature
+  const float* target_probs;  // [B][K+1][V]
+  const float *u_accept, *u_resample;  // [B*K], [B]
+  float2* stats;              // workspace: [B][ceil(V / 128)]
+  int32_t *acc_out, *bonus_out;
+  int32_t* err;
+};
+cudaError_t launch_verify_sampled(const VerifySampledArgs& a, int sms, cudaStream_t s);
+size_t sample_stats_bytes(int rows, int vocab);
+
 // Forward prologue: per compacted row metadata, per sequence ranges, the
 // attention work list, and zeroing of the pass's counters and argmax keys.
 struct InitArgs {
