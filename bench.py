@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--sweep", type=str, default=None, help="B,K of the 2-layer K x B sweep workload")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sampled", action="store_true", help="skip the non-greedy drafting / verification timing")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of a graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-oracle sample time")
@@ -404,6 +405,38 @@ def run_ours(args):
         e2e = dict(value=whole_job_rate(world, cfg_np.B, cfg_np.K, e_ms), unit=UNIT, h2d_bytes_per_step=int(h2d),
                    d2h_bytes_per_step=int(d2h), ms_per_step=e_ms)
 
+    # ---- non-greedy drafting and rejection-sampling verification (not the headline): the
+    # round with fp32 logits written, drafts drawn from the drafter's softmax and verified
+    # against target distributions (synthetic: softmax of N(0, 2) draws), direct launches
+    sampled = None
+    if not args.no_sampled:
+        gen = torch.Generator(device=dev).manual_seed(1234 + rank)
+        BK = (cfg_np.B, cfg_np.K)
+        u_d = torch.rand(BK, device=dev, generator=gen)
+        u_a = torch.rand(BK, device=dev, generator=gen)
+        u_r = torch.rand(cfg_np.B, device=dev, generator=gen)
+        P = torch.softmax(2 * torch.randn(cfg_np.B, cfg_np.K + 1, cfg_np.vocab, device=dev, generator=gen), dim=2)
+
+        def sampled_round():
+            rd.prepare(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"])
+            rd.scatter(R["target_hidden"])
+            rd.forward(logits=True)
+            rd.sample(u_d)
+            rd.verify_sampled(P, u_a, u_r)
+
+        for _ in range(3):
+            sampled_round()
+        torch.cuda.synchronize()
+        t_round = statistics.mean(timed(args.steps, sampled_round))
+        t_s = statistics.mean(timed(args.steps, lambda: rd.sample(u_d)))
+        t_v = statistics.mean(timed(args.steps, lambda: rd.verify_sampled(P, u_a, u_r)))
+        lbytes = cfg_np.B * cfg_np.K * cfg_np.vocab * 4
+        sampled = dict(round_us=t_round * 1e3, sample_us=t_s * 1e3, verify_sampled_us=t_v * 1e3,
+                       logits_bytes=lbytes, sample_gbs=lbytes / (t_s * 1e-3) / 1e9, temperature=1.0,
+                       device_error_word=int(rd.err.item()),
+                       timed_as="direct launches; L2 flushed before each (logits and target rows read from HBM)")
+        del P
+
     if rank != 0:
         dist.destroy_process_group()
         return
@@ -446,7 +479,7 @@ def run_ours(args):
                timed_as=mode, direct_us_per_round=direct_ms * 1e3, roofline=roof, round_roofline=round_roof,
                stages_us=stages_us, gpu_launches=int(launches), launches_per_step=launches_per_step,
                device_error_word=err,
-               wall_s_timed_loop=wall, clocks=clocks, cpu_baseline=cpu, e2e=e2e)
+               wall_s_timed_loop=wall, clocks=clocks, cpu_baseline=cpu, e2e=e2e, sampled=sampled)
     print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()
