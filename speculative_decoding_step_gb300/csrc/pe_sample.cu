@@ -9,15 +9,15 @@
 // when every draft is accepted.  Every random number is a caller-supplied uniform.
 //
 // A draw over a vocabulary row runs in two launches:
-//   phase A  many CTAs per row, each over a contiguous range of 128-entry steps: one
+//   phase A  many CTAs per row, each over a contiguous range of 512-entry steps: one
 //            statistic pair per step into the workspace (drafting: the step's
 //            maximum of z = logit / T and its sum of exp(z - that maximum), in base
 //            2; verification: the step's sums of residual weights and of target
 //            probabilities)
 //   phase B  one warp per row: the row total from the step statistics in a fixed
 //            order, the step where the running sum passes u times the total, and the
-//            entry within that step (one reload of 128 entries)
-// Draws are deterministic: every sum runs in a fixed order (a step: each lane's four
+//            entry within that step (one reload of 512 entries)
+// Draws are deterministic: every sum runs in a fixed order (a step: each lane's 16
 // consecutive entries in order, then a butterfly over the lanes; the steps: each lane
 // of the phase B warp adds a contiguous range of steps in order, then the lane totals
 // are added in lane order).  The draw is the first entry at which that running sum
@@ -32,9 +32,11 @@
 
 namespace pe {
 
-constexpr int kSampStep = 128;     // vocabulary entries per step: four consecutive per lane
-constexpr int kSampBatch = 8;      // steps whose loads a warp keeps in flight together
+constexpr int kSampPerLane = 16;   // consecutive vocabulary entries of a lane in a step
+constexpr int kSampStep = 32 * kSampPerLane;  // entries per step
+constexpr int kSampBatch = 2;      // steps whose loads a warp keeps in flight together
 constexpr int kSampAThreads = 256;
+constexpr int kSampCtasPerSm = 4;  // phase A CTAs resident per SM (256 threads, <= 64 registers)
 constexpr int kSampBWarps = 4;     // phase B rows per CTA (one warp each)
 
 PE_DEV float samp_warp_sum(float v) {  // every lane gets the same value
@@ -57,19 +59,38 @@ PE_DEV float samp_warp_scan(float v) {  // inclusive, lane order
   return v;
 }
 
-// Four consecutive values of a row from v0 (a multiple of 4); zeros past n.  `vec`:
-// the row is 16-byte aligned and n a multiple of 4, so one vector load serves.
-PE_DEV float4 ld4(const float* row, int v0, int n, bool vec) {
-  if (vec && v0 < n) return __ldg(reinterpret_cast<const float4*>(row + v0));
-  float4 r;
-  r.x = v0 < n ? __ldg(row + v0) : 0.f;
-  r.y = v0 + 1 < n ? __ldg(row + v0 + 1) : 0.f;
-  r.z = v0 + 2 < n ? __ldg(row + v0 + 2) : 0.f;
-  r.w = v0 + 3 < n ? __ldg(row + v0 + 3) : 0.f;
+// A lane's 16 consecutive values of a row from v0 (a multiple of 16); zeros past n.
+// `vec`: the row is 16-byte aligned and n a multiple of 4, so vector loads serve.
+struct Lane16 {
+  float v[kSampPerLane];
+};
+PE_DEV Lane16 ld16(const float* row, int v0, int n, bool vec) {
+  Lane16 r;
+#pragma unroll
+  for (int q = 0; q < kSampPerLane; q += 4) {
+    if (vec && v0 + q < n) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(row + v0 + q));
+      r.v[q] = x.x; r.v[q + 1] = x.y; r.v[q + 2] = x.z; r.v[q + 3] = x.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) r.v[q + e] = v0 + q + e < n ? __ldg(row + v0 + q + e) : 0.f;
+    }
+  }
+  return r;
+}
+PE_DEV Lane16 zero16() {
+  Lane16 r;
+#pragma unroll
+  for (int q = 0; q < kSampPerLane; ++q) r.v[q] = 0.f;
   return r;
 }
 PE_DEV bool vec_ok(const float* p, int n) { return (n & 3) == 0 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-PE_DEV float sum4(const float4& w) { return ((w.x + w.y) + w.z) + w.w; }
+PE_DEV float sum16(const Lane16& w) {  // in index order
+  float t = 0.f;
+#pragma unroll
+  for (int q = 0; q < kSampPerLane; ++q) t += w.v[q];
+  return t;
+}
 
 // Exponentials run in base 2: z2 = logit * (log2(e) / T), weights 2^(z2 - m2) with the
 // hardware approximation (relative error a few units in the last place, far below the
@@ -79,22 +100,19 @@ PE_DEV float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// 2^(z2 - m2) of four logits (zero past n)
-PE_DEV float4 exp4(const float4& x, int v0, int n, float inv_t2, float m2) {
-  float4 r;
-  r.x = v0 < n ? ex2(x.x * inv_t2 - m2) : 0.f;
-  r.y = v0 + 1 < n ? ex2(x.y * inv_t2 - m2) : 0.f;
-  r.z = v0 + 2 < n ? ex2(x.z * inv_t2 - m2) : 0.f;
-  r.w = v0 + 3 < n ? ex2(x.w * inv_t2 - m2) : 0.f;
+// 2^(z2 - m2) of a lane's logits (zero past n)
+PE_DEV Lane16 exp16(const Lane16& x, int v0, int n, float inv_t2, float m2) {
+  Lane16 r;
+#pragma unroll
+  for (int q = 0; q < kSampPerLane; ++q) r.v[q] = v0 + q < n ? ex2(x.v[q] * inv_t2 - m2) : 0.f;
   return r;
 }
-// max(0, p - q) of four entries (zero past n), q = 2^(z2 - lse2)
-PE_DEV float4 resid4(const float4& p, const float4& x, int v0, int n, float inv_t2, float lse2) {
-  float4 r;
-  r.x = v0 < n ? fmaxf(0.f, p.x - ex2(x.x * inv_t2 - lse2)) : 0.f;
-  r.y = v0 + 1 < n ? fmaxf(0.f, p.y - ex2(x.y * inv_t2 - lse2)) : 0.f;
-  r.z = v0 + 2 < n ? fmaxf(0.f, p.z - ex2(x.z * inv_t2 - lse2)) : 0.f;
-  r.w = v0 + 3 < n ? fmaxf(0.f, p.w - ex2(x.w * inv_t2 - lse2)) : 0.f;
+// max(0, p - q) of a lane's entries (zero past n), q = 2^(z2 - lse2)
+PE_DEV Lane16 resid16(const Lane16& p, const Lane16& x, int v0, int n, float inv_t2, float lse2) {
+  Lane16 r;
+#pragma unroll
+  for (int q = 0; q < kSampPerLane; ++q)
+    r.v[q] = v0 + q < n ? fmaxf(0.f, p.v[q] - ex2(x.v[q] * inv_t2 - lse2)) : 0.f;
   return r;
 }
 constexpr float kLog2e = 1.4426950408889634f;
@@ -138,7 +156,7 @@ PE_DEV void step_range(int steps, int g, int G, int& s_lo, int& s_hi) {
   s_hi = min(c_hi, s_lo + per_w);
 }
 
-__global__ void __launch_bounds__(kSampAThreads) sample_stats_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kSampAThreads, kSampCtasPerSm) sample_stats_kernel(const SampleArgs a) {
   pdl_wait();
   pdl_trigger();
   const int row = blockIdx.y, lane = threadIdx.x & 31;
@@ -150,26 +168,25 @@ __global__ void __launch_bounds__(kSampAThreads) sample_stats_kernel(const Sampl
   step_range(steps, blockIdx.x, gridDim.x, s_lo, s_hi);
   bool bad = false;
   for (int s0 = s_lo; s0 < s_hi; s0 += kSampBatch) {
-    float4 x[kSampBatch];
+    Lane16 x[kSampBatch];
 #pragma unroll
     for (int j = 0; j < kSampBatch; ++j)
-      x[j] = s0 + j < s_hi ? ld4(l, (s0 + j) * kSampStep + 4 * lane, V, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[j] = s0 + j < s_hi ? ld16(l, (s0 + j) * kSampStep + kSampPerLane * lane, V, vec) : zero16();
 #pragma unroll
     for (int j = 0; j < kSampBatch; ++j) {
       if (s0 + j < s_hi) {
-        const int v0 = (s0 + j) * kSampStep + 4 * lane;
-        const float e[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+        const int v0 = (s0 + j) * kSampStep + kSampPerLane * lane;
         float lm = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kSampPerLane; ++q) {
           if (v0 + q < V) {
-            const float z = e[q] * a.inv_t2;
+            const float z = x[j].v[q] * a.inv_t2;
             bad |= !isfinite(z);
             lm = fmaxf(lm, z);
           }
         }
         const float m = samp_warp_max(lm);
-        const float sm = samp_warp_sum(sum4(exp4(x[j], v0, V, a.inv_t2, m)));
+        const float sm = samp_warp_sum(sum16(exp16(x[j], v0, V, a.inv_t2, m)));
         if (lane == 0) st[s0 + j] = make_float2(m, sm);
       }
     }
@@ -177,7 +194,7 @@ __global__ void __launch_bounds__(kSampAThreads) sample_stats_kernel(const Sampl
   if (bad) set_err(a.err, PE_DEV_NONFINITE);
 }
 
-__global__ void __launch_bounds__(kSampAThreads) verify_stats_kernel(const VerifySampledArgs a) {
+__global__ void __launch_bounds__(kSampAThreads, kSampCtasPerSm) verify_stats_kernel(const VerifySampledArgs a) {
   __shared__ int s_acc;
   pdl_wait();
   pdl_trigger();
@@ -198,21 +215,23 @@ __global__ void __launch_bounds__(kSampAThreads) verify_stats_kernel(const Verif
   float2* st = a.stats + (size_t)b * steps;
   int s_lo, s_hi;
   step_range(steps, blockIdx.x, gridDim.x, s_lo, s_hi);
-  for (int s0 = s_lo; s0 < s_hi; s0 += kSampBatch) {
-    float4 pp[kSampBatch], x[kSampBatch];
+  // one step of both rows in flight (as many bytes as two steps of one row)
+  constexpr int kVB = kSampBatch / 2;
+  for (int s0 = s_lo; s0 < s_hi; s0 += kVB) {
+    Lane16 pp[kVB], x[kVB];
 #pragma unroll
-    for (int j = 0; j < kSampBatch; ++j) {
-      const int v0 = (s0 + j) * kSampStep + 4 * lane;
+    for (int j = 0; j < kVB; ++j) {
+      const int v0 = (s0 + j) * kSampStep + kSampPerLane * lane;
       const bool live = s0 + j < s_hi;
-      pp[j] = live ? ld4(p, v0, V, pvec) : make_float4(0.f, 0.f, 0.f, 0.f);
-      x[j] = live && res ? ld4(l, v0, V, lvec) : make_float4(0.f, 0.f, 0.f, 0.f);
+      pp[j] = live ? ld16(p, v0, V, pvec) : zero16();
+      x[j] = live && res ? ld16(l, v0, V, lvec) : zero16();
     }
 #pragma unroll
-    for (int j = 0; j < kSampBatch; ++j) {
+    for (int j = 0; j < kVB; ++j) {
       if (s0 + j < s_hi) {
-        const int v0 = (s0 + j) * kSampStep + 4 * lane;
-        const float sp = samp_warp_sum(sum4(pp[j]));
-        const float sr = res ? samp_warp_sum(sum4(resid4(pp[j], x[j], v0, V, a.inv_t2, ls2))) : sp;
+        const int v0 = (s0 + j) * kSampStep + kSampPerLane * lane;
+        const float sp = samp_warp_sum(sum16(pp[j]));
+        const float sr = res ? samp_warp_sum(sum16(resid16(pp[j], x[j], v0, V, a.inv_t2, ls2))) : sp;
         if (lane == 0) st[s0 + j] = make_float2(sr, sp);
       }
     }
@@ -221,7 +240,7 @@ __global__ void __launch_bounds__(kSampAThreads) verify_stats_kernel(const Verif
 
 // Phase B body shared by both draws: the warp of one row finds the step where the running
 // sum of step weights sw(s) passes u times their total, then the entry within that step
-// from its entry weights ew(v0) (float4 of v0..v0+3).  Returns the entry (-1 when the
+// from its entry weights ew(v0) (a lane's 16 weights from v0).  Returns the entry (-1 when the
 // total is not positive and finite); *total gets the total.
 template <typename SW, typename EW>
 PE_DEV int warp_draw(int steps, float u, const SW& sw, const EW& ew, float* total) {
@@ -266,18 +285,17 @@ PE_DEV int warp_draw(int steps, float u, const SW& sw, const EW& ew, float* tota
   }
   const bool in_step = sc >= 0;
   if (!in_step) sc = last_s;  // lane L's range has weight, so last_s >= 0
-  const float4 x = ew(sc * kSampStep + 4 * lane);
-  const float lt = sum4(x);
+  const Lane16 x = ew(sc * kSampStep + kSampPerLane * lane);
+  const float lt = sum16(x);
   const float inc = samp_warp_scan(lt);
-  const float e[4] = {x.x, x.y, x.z, x.w};
   float c = r + (inc - lt);
   int first = -1, last = -1;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    c += e[q];
-    if (e[q] > 0.f) {
-      last = 4 * lane + q;
-      if (first < 0 && in_step && c > t) first = 4 * lane + q;
+  for (int q = 0; q < kSampPerLane; ++q) {
+    c += x.v[q];
+    if (x.v[q] > 0.f) {
+      last = kSampPerLane * lane + q;
+      if (first < 0 && in_step && c > t) first = kSampPerLane * lane + q;
     }
   }
   const unsigned hit = __ballot_sync(0xFFFFFFFFu, first >= 0);
@@ -304,7 +322,7 @@ __global__ void __launch_bounds__(32 * kSampBWarps) sample_draw_kernel(const Sam
   if (isfinite(m))
     x = warp_draw(
         steps, a.u[row], [&](int s) { const float2 v = st[s]; return v.y * ex2(v.x - m); },
-        [&](int v0) { return exp4(ld4(l, v0, V, vec), v0, V, a.inv_t2, m); }, &tot);
+        [&](int v0) { return exp16(ld16(l, v0, V, vec), v0, V, a.inv_t2, m); }, &tot);
   if (lane == 0) {
     if (x < 0) {
       set_err(a.err, PE_DEV_NONFINITE);
@@ -337,11 +355,11 @@ __global__ void __launch_bounds__(32 * kSampBWarps) verify_draw_kernel(const Ver
     const float ls2 = a.lse[b * K + acc] * kLog2e;
     x = warp_draw(
         steps, a.u_resample[b], [&](int s) { return st[s].x; },
-        [&](int v0) { return resid4(ld4(p, v0, V, pvec), ld4(l, v0, V, lvec), v0, V, a.inv_t2, ls2); }, &tot);
+        [&](int v0) { return resid16(ld16(p, v0, V, pvec), ld16(l, v0, V, lvec), v0, V, a.inv_t2, ls2); }, &tot);
   }
   if (x < 0)  // every draft accepted, or an empty residual: the target's distribution itself
     x = warp_draw(
-        steps, a.u_resample[b], [&](int s) { return st[s].y; }, [&](int v0) { return ld4(p, v0, V, pvec); },
+        steps, a.u_resample[b], [&](int s) { return st[s].y; }, [&](int v0) { return ld16(p, v0, V, pvec); },
         &tot);
   if (lane == 0) {
     if (x < 0) {
@@ -353,10 +371,10 @@ __global__ void __launch_bounds__(32 * kSampBWarps) verify_draw_kernel(const Ver
   }
 }
 
-// CTAs per row in phase A: about four per SM over all rows, at least a batch of steps
-// per warp.
+// CTAs per row in phase A: as many as fit on the GPU at once over all rows (one wave),
+// at least a batch of steps per warp.
 static int phase_a_ctas(int rows, int steps, int sms) {
-  const int by_sm = (4 * sms + rows - 1) / rows;
+  const int by_sm = kSampCtasPerSm * sms / rows;
   const int by_steps = std::max(1, steps / (kSampBatch * (kSampAThreads / 32)));
   return std::max(1, std::min(by_sm, by_steps));
 }

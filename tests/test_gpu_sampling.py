@@ -4,11 +4,11 @@ The draws are integers decided by floating point: the GPU sums the weights in fp
 fixed blocked order, the oracle in fp64 in index order.  A draw therefore equals the
 oracle's except where the uniform lies within the fp32 error of a cumulative-sum boundary;
 there the GPU's token is checked to be a valid draw: the oracle's normalised cumulative
-sums around it bracket the uniform to within that error.  Error bound for the sums: at
-most 5 tree levels within a 32-element step, about V/1024 steps within a segment and 32
-segments, each addition off by at most 2^-24 of the running total, plus a few ulp per
-exponential (base 2, hardware approximation): below 2e-5 of the total for V <= 2^18; the
-checks use 5e-5.
+sums around it bracket the uniform to within that error.  Error bound for the sums: 16
+sequential additions within a lane, 5 tree levels within a 512-entry step, about V/16384
+steps per lane of the drawing warp and 32 lane totals, each addition off by at most 2^-24
+of the running total, plus a few ulp per exponential (base 2, hardware approximation):
+below 2e-5 of the total for V <= 2^18; the checks use 5e-5.
 """
 
 import numpy as np
