@@ -74,3 +74,24 @@ def test_null_pointers_rejected_before_launch():
     st = L.pe_verify(ctypes.byref(cfg), null, null, null, null, null)
     assert st == 1
     assert L.pe_set_trace_events(None, -1) == 1
+
+
+def test_sampling_calls_validate_before_launch():
+    """The non-greedy drafting and verification calls reject null pointers and a temperature
+    that is not positive and finite, before anything is launched."""
+    L = pe.lib()
+    cfg = _cfg()
+    null = ctypes.c_void_p(None)
+    some = ctypes.c_void_p(256)  # never dereferenced: validation fails first
+    st = L.pe_sample_drafts(ctypes.byref(cfg), null, null, ctypes.c_float(1.0), null, 0, null, null, null, null)
+    assert st == 1
+    for T in (0.0, -1.0, float("inf"), float("nan")):
+        st = L.pe_sample_drafts(ctypes.byref(cfg), some, some, ctypes.c_float(T), some, 1 << 30, some, some, some,
+                                null)
+        assert st == 1, T
+        st = L.pe_verify_sampled(ctypes.byref(cfg), some, some, some, ctypes.c_float(T), some, some, some, some,
+                                 1 << 30, some, some, some, null)
+        assert st == 1, T
+    st = L.pe_verify_sampled(ctypes.byref(cfg), null, null, null, ctypes.c_float(1.0), null, null, null, null, 0,
+                             null, null, null, null)
+    assert st == 1
