@@ -132,7 +132,7 @@ struct Plan {
   size_t tok_pos, tok_seq, tok_slot, seq_start, seq_len, seq_maxpos, item_base, n_chunks, n_items, items;
   size_t done, keys, x, y, q, ao, u, yl, part_m, part_l, part_o, split_part;
   size_t st_ids, st_pos, st_slot, st_rej, st_mask, st_hmap, st_rows, st_nvalid, st_draft, st_x0;
-  size_t samp;
+  size_t samp, samp_acc;
   size_t total = 0;
 };
 
@@ -215,6 +215,7 @@ Plan make_plan(const pe_config& c) {
   p.st_draft = take(4 * (size_t)p.T);
   p.st_x0 = take(eb * (size_t)p.R * 2 * c.d);
   p.samp = take(sample_stats_bytes(p.T, c.vocab));  // pe_sample_drafts / pe_verify_sampled
+  p.samp_acc = take(4 * (size_t)c.B);
   p.total = off;
   return p;
 }
@@ -781,6 +782,7 @@ pe_status pe_verify_sampled(const pe_config* cfg, const int32_t* draft_tokens, c
   a.drafts = draft_tokens; a.logits = logits; a.lse = lse; a.inv_t2 = (float)(1.4426950408889634 / (double)temperature);
   a.target_probs = target_probs; a.u_accept = u_accept; a.u_resample = u_resample;
   a.stats = at<float2>(workspace, p.samp);
+  a.acc_ws = at<int32_t>(workspace, p.samp_acc);
   a.acc_out = num_accepted_out; a.bonus_out = bonus_out; a.err = err_word;
   PE_TRY_CUDA(launch_verify_sampled(a, p.sms, (cudaStream_t)stream));
   return PE_OK;

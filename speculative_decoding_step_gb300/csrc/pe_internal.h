@@ -101,14 +101,14 @@ __device__ __forceinline__ void verify_seq(const VerifyArgs& a, int b) {
 }
 
 // Non-greedy drafting and rejection-sampling verification; see pe_sample.cu.  Each
-// draw over a vocabulary row keeps one statistic pair per 128 entries in the
+// draw over a vocabulary row keeps one statistic pair per 512 entries in the
 // workspace (sample_stats_bytes).
 struct SampleArgs {
   int B, K, V;
   const float* logits;  // [B*K][V]
   const float* u;       // [B*K] uniforms in [0, 1)
   float inv_t2;         // log2(e) / temperature
-  float2* stats;        // workspace: [B*K][ceil(V / 128)]
+  float2* stats;        // workspace: [B*K][steps], one per 512 vocabulary entries
   int32_t* drafts;      // [B*K]
   float* lse;           // [B*K]
   int32_t* err;
@@ -122,7 +122,8 @@ struct VerifySampledArgs {
   float inv_t2;               // log2(e) / temperature
   const float* target_probs;  // [B][K+1][V]
   const float *u_accept, *u_resample;  // [B*K], [B]
-  float2* stats;              // workspace: [B][ceil(V / 128)]
+  float2* stats;              // workspace: [B][steps]
+  int32_t* acc_ws;            // workspace: [B] accepted counts (statistics launch -> draw launch)
   int32_t *acc_out, *bonus_out;
   int32_t* err;
 };

@@ -202,7 +202,13 @@ __global__ void __launch_bounds__(kSampAThreads, kSampCtasPerSm) verify_stats_ke
   const int V = a.V, K = a.K, steps = (V + kSampStep - 1) / kSampStep;
   if (threadIdx.x < 32) {
     const int c = accept_count(a, b);
-    if (threadIdx.x == 0) s_acc = c < 0 ? -1 - c : c;
+    if (threadIdx.x == 0) {
+      s_acc = c < 0 ? -1 - c : c;
+      if (blockIdx.x == 0) {  // the draw launch takes the count from here, not a recomputation
+        a.acc_ws[b] = s_acc;
+        if (c < 0) set_err(a.err, PE_DEV_BAD_TOKEN);
+      }
+    }
   }
   __syncthreads();
   const int acc = s_acc;
@@ -341,9 +347,7 @@ __global__ void __launch_bounds__(32 * kSampBWarps) verify_draw_kernel(const Ver
   const int b = blockIdx.x * kSampBWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (b >= a.B) return;
   const int V = a.V, K = a.K, steps = (V + kSampStep - 1) / kSampStep;
-  const int c = accept_count(a, b);
-  if (c < 0 && lane == 0) set_err(a.err, PE_DEV_BAD_TOKEN);
-  const int acc = c < 0 ? -1 - c : c;
+  const int acc = a.acc_ws[b];  // decided once, by the statistics launch
   const float2* st = a.stats + (size_t)b * steps;
   const float* p = a.target_probs + ((size_t)b * (K + 1) + acc) * V;
   const bool pvec = vec_ok(p, V);
