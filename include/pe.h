@@ -263,7 +263,7 @@ pe_status pe_verify(const pe_config *cfg, const int32_t *draft_tokens, const int
  * logits_dbg output; draft_tokens [B][K] and lse [B*K] are written.  workspace:
  * 256-byte aligned, >= pe_workspace_bytes(cfg) bytes (the same workspace as
  * pe_draft_forward may be passed; its contents are scratch).  Two launches:
- * statistics of every 128-entry step of every row, then one warp per row for the
+ * statistics of every 512-entry step of every row, then one warp per row for the
  * draw.  A non-finite logit sets PE_DEV_NONFINITE (token 0, lse NaN).
  * temperature must be positive and finite (else PE_ERR_INVALID_ARG).
  */
