@@ -264,8 +264,10 @@ pe_status pe_verify(const pe_config *cfg, const int32_t *draft_tokens, const int
  * 256-byte aligned, >= pe_workspace_bytes(cfg) bytes (the same workspace as
  * pe_draft_forward may be passed; its contents are scratch).  Two launches:
  * statistics of every 512-entry step of every row, then one warp per row for the
- * draw.  A non-finite logit sets PE_DEV_NONFINITE (token 0, lse NaN).
- * temperature must be positive and finite (else PE_ERR_INVALID_ARG).
+ * draw.  A non-finite logit sets PE_DEV_NONFINITE; where it leaves the row's
+ * distribution undefined (NaN, +inf) the row's token is 0 and its lse NaN (a
+ * -inf logit only has probability 0).  temperature must be positive and finite
+ * (else PE_ERR_INVALID_ARG).
  */
 pe_status pe_sample_drafts(const pe_config *cfg, const float *logits, const float *u_draft, float temperature,
                            void *workspace, size_t workspace_bytes, int32_t *draft_tokens, float *lse,
