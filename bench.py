@@ -112,6 +112,37 @@ def round_cost(cfg, rnd) -> dict:
                 attn_flops=int(flops_attn))
 
 
+def stage_costs(cfg, rnd) -> dict:
+    """The same algorithmic bytes and flops as round_cost, split over the stages the library's
+    trace points bound (names as in stage_names): metadata to the rebuild, the input rows to
+    the row copy, each weight matrix, gain and KV stream to the stage that reads it, and the
+    drafts and target tokens to verification.  Maps stage name -> (bytes, flops)."""
+    eb = 2 if cfg.dtype == "bf16" else 4
+    K, B, d, hd = cfg.K, cfg.B, cfg.d, cfg.head_dim
+    n_b = rnd.num_accepted.astype(np.int64) + K
+    n_valid = int(n_b.sum())
+    P = rnd.prefix_len.astype(np.int64)
+    ctx = 0
+    for b in range(B):
+        ctx += int((P[b] + np.arange(n_b[b]) + 1).sum())
+    kv_read = int((P + n_b).sum() * cfg.n_kv * hd * 2 * eb)
+    out = {"prepare": (B * (K + 1) * 4 * 4 + B * 2 * K * 32, 0), "scatter": (n_valid * d * eb * 2, 0),
+           "forward_init": (0, 0), "fc": (d * 2 * d * eb, 2 * n_valid * d * 2 * d)}
+    for l in range(cfg.n_layers):
+        out[f"l{l}.norm1"] = (d * eb, 0)
+        out[f"l{l}.qkv_rope_kv"] = (cfg.qkv_out * d * eb + n_valid * cfg.n_kv * hd * 2 * eb,
+                                     2 * n_valid * cfg.qkv_out * d)
+        out[f"l{l}.attention"] = (kv_read, 4 * cfg.n_q * hd * ctx)
+        out[f"l{l}.o_proj"] = (d * cfg.n_q * hd * eb, 2 * n_valid * d * cfg.n_q * hd)
+        out[f"l{l}.norm2"] = (d * eb, 0)
+        out[f"l{l}.gate_up_swiglu"] = (2 * cfg.ffn * d * eb, 2 * n_valid * 2 * cfg.ffn * d)
+        out[f"l{l}.down"] = (d * cfg.ffn * eb, 2 * n_valid * d * cfg.ffn)
+    out["final_norm"] = (d * eb, 0)
+    out["lm_head_argmax"] = (cfg.vocab * d * eb, 2 * B * K * cfg.vocab * d)
+    out["verify"] = (B * K * 4 + B * (K + 1) * 4, 0)
+    return out
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -467,6 +498,14 @@ def run_ours(args):
     round_roof["nominal"] = dict(hbm_gbs=NOMINAL_HBM_BPS / 1e9, bf16_tflops=NOMINAL_BF16_FLOPS / 1e12,
                                  roofline_us=t_nominal * 1e6, frac=t_nominal / (ms * 1e-3))
 
+    # every traced stage against its own roofline (bytes / HBM, flops / sustained bf16)
+    stages = {}
+    for name, (sb, sf) in stage_costs(cfg_np, rnd).items():
+        t_us = stages_us.get(name)
+        t_roof = max(sb / hbm, sf / tc_sus)
+        stages[name] = dict(us=t_us, bytes=int(sb), flops=int(sf),
+                            roofline_frac=(t_roof / (t_us * 1e-6)) if t_us else None)
+
     cpu = None if args.no_cpu_baseline else cpu_oracle_sample(cfg_np, w_np, rnd, args.cpu_seconds)
     value = whole_job_rate(world, cfg_np.B, cfg_np.K, ms)
     out = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
@@ -477,7 +516,7 @@ def run_ours(args):
                            l2="flushed between timed steps (512 MiB write outside the step events)",
                            replicas="one independent replica per rank" if world > 1 else "single GPU"),
                timed_as=mode, direct_us_per_round=direct_ms * 1e3, roofline=roof, round_roofline=round_roof,
-               stages_us=stages_us, gpu_launches=int(launches), launches_per_step=launches_per_step,
+               stages_us=stages_us, stages=stages, gpu_launches=int(launches), launches_per_step=launches_per_step,
                device_error_word=err,
                wall_s_timed_loop=wall, clocks=clocks, cpu_baseline=cpu, e2e=e2e, sampled=sampled)
     print(json.dumps(out), flush=True)

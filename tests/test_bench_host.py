@@ -87,3 +87,19 @@ def test_stage_names_match_trace_points():
     """One name per interval between the library's trace points (8 + 7 L boundaries)."""
     for L in (1, 2, 4):
         assert len(bench.stage_names(L)) == 8 + 7 * L - 1
+
+
+def test_stage_costs_split_the_round_cost():
+    """The per-stage bytes and flops add up to the round's (verification's few bytes of drafts
+    and target tokens aside), on every workload and for two layers."""
+    for cfg in [config(i) for i in range(4)] + [_tiny()]:
+        rnd = make_round(cfg, with_cache=False)
+        for L in sorted({cfg.n_layers, 2}):
+            c = dataclasses.replace(cfg, n_layers=L)
+            st = bench.stage_costs(c, rnd)
+            assert list(st) == bench.stage_names(L)
+            total = bench.round_cost(c, rnd)
+            b = sum(v[0] for k, v in st.items() if k != "verify")
+            f = sum(v[1] for v in st.values())
+            assert b == total["bytes"], (cfg.name, L)
+            assert f == total["flops"], (cfg.name, L)
