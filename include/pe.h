@@ -341,7 +341,8 @@ int32_t pe_trace_points(const pe_config *cfg);
 /* Number of kernels this library has launched since it was loaded (all threads). */
 uint64_t pe_kernel_launches(void);
 
-/* Workspace bytes needed by pe_draft_forward and pe_step for this config (0 if invalid). */
+/* Workspace bytes needed by pe_draft_forward, pe_step, pe_sample_drafts and
+ * pe_verify_sampled for this config (0 if invalid); one workspace serves them all. */
 size_t pe_workspace_bytes(const pe_config *cfg);
 
 /*
