@@ -312,7 +312,8 @@ pe_status pe_verify_sampled(const pe_config *cfg, const int32_t *draft_tokens, c
  * again after the caller refills target_hidden and target_tokens is the next
  * round (the multi-round drafting loop; the prefix grows by num_accepted + 1
  * positions per round, which the block table must cover).  No other output may
- * alias an input.
+ * overlap an input or another output: such a call returns PE_ERR_INVALID_ARG
+ * before anything is launched.
  */
 pe_status pe_step(const pe_config *cfg, const pe_weights *w, const pe_kv *kv, const int32_t *block_table,
                   const int32_t *prev_tokens, const int32_t *prev_pos, const int32_t *num_accepted,

@@ -414,6 +414,46 @@ pe_status check_kv(const pe_config& c, const pe_kv* kv) {
   return PE_OK;
 }
 
+// pe_step's outputs against its inputs: an output may be exactly its paired state input
+// (next_prev_tokens / prev_tokens, next_prev_pos / prev_pos, num_accepted_out /
+// num_accepted, bonus_out / bonus); otherwise no output may overlap an input or another
+// output.  Byte ranges from the config's shapes.
+struct Span {
+  uintptr_t lo, hi;
+};
+bool overlaps(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; }
+Span span_of(const void* p, size_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Span{lo, lo + bytes};
+}
+bool step_aliasing_ok(const pe_config& c, const int32_t* block_table, const int32_t* prev_tokens,
+                      const int32_t* prev_pos, const int32_t* num_accepted, const int32_t* bonus,
+                      const void* target_hidden, const int32_t* target_tokens, const int32_t* draft_tokens,
+                      const int32_t* num_accepted_out, const int32_t* bonus_out, const int32_t* next_prev_tokens,
+                      const int32_t* next_prev_pos, const float* logits_dbg) {
+  const size_t B = (size_t)c.B, K = (size_t)c.K;
+  const Span in[7] = {span_of(block_table, 4 * B * (size_t)c.max_pages_per_seq), span_of(prev_tokens, 4 * B * (K + 1)),
+                      span_of(prev_pos, 4 * B * (K + 1)), span_of(num_accepted, 4 * B), span_of(bonus, 4 * B),
+                      span_of(target_hidden, elem_bytes(c.dtype) * B * (K + 1) * (size_t)c.d),
+                      span_of(target_tokens, 4 * B * (K + 1))};
+  // outputs, each with the index of the input it may replace exactly (-1: none)
+  const Span out[6] = {span_of(draft_tokens, 4 * B * K), span_of(num_accepted_out, 4 * B),
+                       span_of(bonus_out, 4 * B), span_of(next_prev_tokens, 4 * B * (K + 1)),
+                       span_of(next_prev_pos, 4 * B * (K + 1)),
+                       span_of(logits_dbg, logits_dbg ? 4 * B * K * (size_t)c.vocab : 0)};
+  const int pair[6] = {-1, 3, 4, 1, 2, -1};
+  for (int o = 0; o < 6; ++o) {
+    for (int i = 0; i < 7; ++i) {
+      if (!overlaps(out[o], in[i])) continue;
+      if (i == pair[o] && out[o].lo == in[i].lo && out[o].hi == in[i].hi) continue;
+      return false;
+    }
+    for (int o2 = 0; o2 < o; ++o2)
+      if (overlaps(out[o], out[o2])) return false;
+  }
+  return true;
+}
+
 PrepArgs make_prep_args(const pe_config& c, const int32_t* prev_tokens, const int32_t* prev_pos,
                         const int32_t* num_accepted, const int32_t* bonus, const int32_t* block_table, int32_t num_pages,
                         int32_t* input_ids, int32_t* positions, int64_t* slot_mapping, uint8_t* is_rejected,
@@ -707,6 +747,9 @@ pe_status pe_step(const pe_config* cfg, const pe_weights* w, const pe_kv* kv, co
       !err_word)
     return PE_ERR_INVALID_ARG;
   if (!aligned16(target_hidden) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PE_ERR_INVALID_ARG;
+  if (!step_aliasing_ok(*cfg, block_table, prev_tokens, prev_pos, num_accepted, bonus, target_hidden, target_tokens,
+                        draft_tokens, num_accepted_out, bonus_out, next_prev_tokens, next_prev_pos, logits_dbg))
+    return PE_ERR_INVALID_ARG;
   const Plan p = make_plan(*cfg);
   if (workspace_bytes < p.total) return PE_ERR_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;

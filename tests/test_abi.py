@@ -95,3 +95,48 @@ def test_sampling_calls_validate_before_launch():
     st = L.pe_verify_sampled(ctypes.byref(cfg), null, null, null, ctypes.c_float(1.0), null, null, null, null, 0,
                              null, null, null, null)
     assert st == 1
+
+
+def test_step_rejects_overlapping_outputs_before_launch():
+    """pe_step: a state output may be exactly its paired input (rounds back to back in
+    place); any other overlap of an output with an input or another output is rejected
+    before anything is launched.  Every call here stops at a host check (the workspace size
+    is zero): the pointers are placeholders that are never dereferenced."""
+    L = pe.lib()
+    cfg = _cfg(B=2, K=3)
+    B, K = 2, 3
+    base = 1 << 40
+    nxt = iter(range(base, base + (1 << 36), 1 << 20))  # disjoint 1 MiB-spaced placeholders
+    P = lambda: next(nxt)
+    layer = (ctypes.c_void_p * cfg.n_layers)(*[P() for _ in range(cfg.n_layers)])
+    w = pe._Weights(P(), P(), P(), layer, layer, layer, layer, layer, layer, P(), P())
+    kv = pe._KV(layer, layer, 4)
+    ins = dict(block_table=P(), prev_tokens=P(), prev_pos=P(), num_accepted=P(), bonus=P(), target_hidden=P(),
+               target_tokens=P())
+    outs = dict(draft_tokens=P(), num_accepted_out=P(), bonus_out=P(), next_prev_tokens=P(), next_prev_pos=P())
+    ws, err = P(), P()
+
+    def call(**over):
+        a = {**ins, **outs, **over}
+        v = lambda k: ctypes.c_void_p(a[k])
+        return L.pe_step(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(kv), v("block_table"), v("prev_tokens"),
+                         v("prev_pos"), v("num_accepted"), v("bonus"), v("target_hidden"), v("target_tokens"),
+                         ctypes.c_void_p(ws), ctypes.c_size_t(0), v("draft_tokens"), v("num_accepted_out"),
+                         v("bonus_out"), v("next_prev_tokens"), v("next_prev_pos"), ctypes.c_void_p(None),
+                         ctypes.c_void_p(err), ctypes.c_void_p(None))
+
+    # control: disjoint buffers, and the state updated exactly in place, pass every argument
+    # check and stop at the (deliberately empty) workspace: PE_ERR_SHAPE, still no launch
+    assert call() == 2
+    assert call(next_prev_tokens=ins["prev_tokens"], next_prev_pos=ins["prev_pos"],
+                num_accepted_out=ins["num_accepted"], bonus_out=ins["bonus"]) == 2
+    # a state output shifted by one element into its paired input
+    assert call(next_prev_tokens=ins["prev_tokens"] + 4) == 1
+    # a state output equal to another input than its pair
+    assert call(next_prev_pos=ins["prev_tokens"]) == 1
+    assert call(bonus_out=ins["num_accepted"]) == 1
+    # the drafts written over the target tokens, or over another output
+    assert call(draft_tokens=ins["target_tokens"]) == 1
+    assert call(draft_tokens=outs["next_prev_tokens"] + 4 * (K + 1) * B - 4) == 1
+    # a block table running into the next verify batch
+    assert call(next_prev_pos=ins["block_table"] + 4) == 1
