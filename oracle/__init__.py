@@ -57,15 +57,23 @@ PAD_TOKEN = 0
 
 # ----------------------------------------------------------------------------- build / load
 
+SOURCE = os.path.join(_HERE, "pe_oracle.c")
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile a C oracle source to a shared library with gcc (IEEE semantics, no FMA contraction)."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                           "-fno-fast-math", "-pthread", "-o", tmp, src, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile the C part of the oracle with gcc (IEEE semantics, no FMA contraction)."""
-    src = os.path.join(_HERE, "pe_oracle.c")
+    """Compile the C part of the oracle (``pe_oracle.c``) in-tree."""
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-                               "-fno-fast-math", "-pthread", "-o", tmp, src, "-lm"])
-        os.replace(tmp, _LIB_PATH)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(SOURCE):
+        compile_source(SOURCE, _LIB_PATH)
     return _LIB_PATH
 
 
@@ -84,21 +92,25 @@ class _W(ctypes.Structure):
                 ("w_gate_up", ctypes.POINTER(ctypes.c_void_p)), ("w_down", ctypes.POINTER(ctypes.c_void_p))]
 
 
+def load_library(path: str):
+    """Load a compiled copy of ``pe_oracle.c`` and declare its functions' signatures."""
+    L = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    L.oc_linear.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, dp]
+    L.oc_rmsnorm.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_double, dp]
+    L.oc_rope.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_double]
+    L.oc_silu.argtypes = [ctypes.c_double]
+    L.oc_silu.restype = ctypes.c_double
+    L.oc_attend.argtypes = [dp, dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_double, dp]
+    L.oc_forward.restype = ctypes.c_int
+    L.oc_threads_used.restype = ctypes.c_int
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(_LIB_PATH)
-        dp = ctypes.POINTER(ctypes.c_double)
-        L.oc_linear.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, dp]
-        L.oc_rmsnorm.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_double, dp]
-        L.oc_rope.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_double]
-        L.oc_silu.argtypes = [ctypes.c_double]
-        L.oc_silu.restype = ctypes.c_double
-        L.oc_attend.argtypes = [dp, dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_double, dp]
-        L.oc_forward.restype = ctypes.c_int
-        L.oc_threads_used.restype = ctypes.c_int
-        _lib = L
+        _lib = load_library(build())
     return _lib
 
 

@@ -267,6 +267,101 @@ def test_forward_gqa_mapping_and_causal_bound():
         assert (x[r, 4:] == 0).all()
 
 
+def closed_form_pass_checks() -> dict:
+    """One row through the whole drafter pass with weights chosen so that every step has a
+    closed form (the drafter of "N transformer layers and an LM head", P-EAGLE: Parallel
+    Speculative Decoding in vLLM, step 2 "Parallel Drafting"; the layer is fc 2d -> d, then
+    pre-norm GQA attention with rotate-half RoPE over the paged cache, a pre-norm SwiGLU MLP,
+    a final norm and the LM head).  Returns check name -> (got, want) in float64.
+
+    d = 32, one q head and one kv head of hd = 8, F = 4, vocab = d, RoPE base 10^4 (pair i
+    turns by p * 10^(-i/2) radians: 1 rad per position for i = 0, 0.1 rad for i = 1).
+    The row sits at position p = 1 of a sequence whose cache holds position 0.
+
+    * fc = [I | 0] and X0 = [s e0 ; 0]: x = s e0; the attention RMSNorm (gains 1) gives
+      y1 = r e0 with r = s / sqrt(s^2 / d + eps).
+    * W_qkv reads y1[0] into q = alpha r e0 (q block), k = beta r e1 (k block), v = gamma r e0
+      (v block): the three blocks in the order q | k | v.
+    * k and q turn by their own position (k: pair 1 by 0.1 rad; q: pair 0 by 1 rad); v does
+      not turn.
+    * Scores: the cached key at position 0 is kappa e0, so s0 = alpha r kappa cos(1) / sqrt(hd);
+      q and k lie in different rotation planes, so s1 = 0.  The output is
+      w0 * mu e6 (cached value) + w1 * gamma r e0 (the row's own value, written before the
+      attention reads the cache), w0 = 1 / (1 + exp(-s0)).
+    * W_o copies the head output into x[8..15]; the MLP RMSNorm gives y2; W_gate row f reads
+      a_f y2[0], W_up row f reads b_f y2[0]; u_f = silu(gate_f) * up_f; W_down copies u into
+      x[16..19].
+    * The final norm (gains 1) of x, then the LM head = I: the logits are that normalised x.
+    """
+    d, hd, F, eps, theta, p = 32, 8, 4, 1e-6, 10000.0, 1
+    s, alpha, beta, gamma, kappa, mu = 3.0, 1.5, 0.75, 1.25, 2.0, 5.0  # exact in float32 storage
+    a = np.array([1.0, -0.5, 2.0, 0.375])
+    b = np.array([0.625, 1.5, -1.0, 2.5])
+    cfg = _tiny(B=1, K=1, d=d, n_q=1, n_kv=1, head_dim=hd, ffn=F, vocab=d, rope_theta=theta)
+    z = lambda *sh: np.zeros(sh, np.float32)
+    fc = z(d, 2 * d)
+    fc[np.arange(d), np.arange(d)] = 1.0
+    wqkv = z(3 * hd, d)
+    wqkv[0, 0], wqkv[hd + 1, 0], wqkv[2 * hd + 0, 0] = alpha, beta, gamma
+    wo = z(d, hd)
+    wo[8 + np.arange(hd), np.arange(hd)] = 1.0
+    wgu = z(2 * F, d)
+    wgu[np.arange(F), 0] = a
+    wgu[F + np.arange(F), 0] = b
+    wdown = z(d, F)
+    wdown[16 + np.arange(F), np.arange(F)] = 1.0
+    w = type("W", (), {})()
+    w.fc, w.norm_final, w.lm_head = fc, np.ones(d, np.float32), np.eye(d, dtype=np.float32)
+    w.norm_attn, w.norm_mlp, w.wqkv, w.wo = [np.ones(d, np.float32)], [np.ones(d, np.float32)], [wqkv], [wo]
+    w.w_gate_up, w.w_down = [wgu], [wdown]
+    kc = np.full((1, 16, 1, hd), 100.0, np.float32)   # every slot but position 0's: stale garbage
+    vc = np.full((1, 16, 1, hd), -100.0, np.float32)
+    kc[0, 0, 0, :] = 0.0
+    kc[0, 0, 0, 0] = kappa
+    vc[0, 0, 0, :] = 0.0
+    vc[0, 0, 0, 6] = mu
+    x0 = np.zeros((1, 2 * d))
+    x0[0, 0] = s
+    res = oracle.draft_forward(cfg, w, x0, [p], [p], [0], np.zeros((1, 1), np.int32), [kc], [vc], [0],
+                               want_kv=True, want_x=True)
+    r = s / math.sqrt(s * s / d + eps)
+    k_want = np.zeros(hd)
+    ang_k = p * theta ** (-2.0 * 1 / hd)
+    k_want[1], k_want[1 + hd // 2] = beta * r * math.cos(ang_k), beta * r * math.sin(ang_k)
+    v_want = np.zeros(hd)
+    v_want[0] = gamma * r
+    s0 = alpha * r * math.cos(p * 1.0) * kappa / math.sqrt(hd)
+    w0 = 1.0 / (1.0 + math.exp(-s0))
+    o = np.zeros(hd)
+    o[6] = w0 * mu
+    o[0] = (1.0 - w0) * gamma * r
+    x1 = np.zeros(d)
+    x1[0] = s
+    x1[8:16] = o
+    y2 = x1 / math.sqrt((x1 ** 2).mean() + eps)
+    g, up = a * y2[0], b * y2[0]
+    u = g / (1.0 + np.exp(-g)) * up
+    x2 = x1.copy()
+    x2[16:20] = u
+    logits = x2 / math.sqrt((x2 ** 2).mean() + eps)
+    return {"k_block_rope": (res["new_k"][0, 0], k_want), "v_block_unrotated": (res["new_v"][0, 0], v_want),
+            "attention_q_rope": (res["x"][0, 8:16], o), "swiglu_roles": (res["x"][0, 16:20], u),
+            "residual_stream": (res["x"][0], x2), "final_norm_lm_head": (res["logits"][0], logits)}
+
+
+def closed_form_failures(checks: dict, rtol=1e-12) -> list:
+    return [k for k, (got, want) in checks.items()
+            if not np.allclose(got, want, rtol=rtol, atol=rtol * max(1.0, float(np.abs(want).max())))]
+
+
+def test_forward_closed_form_every_step():
+    """Every step of the drafter pass against its closed form (q | k | v order, RoPE of q and k
+    at the row's own position, v not rotated, the row's write read by its own attention, the
+    SwiGLU gate and up roles, the residual adds, the final norm and LM head).  A planted
+    mistake in any of them fails this test (tests/test_oracle_mutants.py)."""
+    assert closed_form_failures(closed_form_pass_checks()) == []
+
+
 def _c0_like():
     return _tiny(B=3, K=4, n_layers=1, d=64, n_q=4, n_kv=2, head_dim=16, ffn=96, vocab=211)
 
