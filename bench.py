@@ -4,15 +4,20 @@
 
 Prints one JSON line.  A step is one pe_step call: batch rebuild, input-row
 scatter, drafter pass, LM head + argmax, greedy verification, over seeded
-synthetic inputs of the chosen workload (default: workload 1, the
-Qwen3-Coder-30B-shaped drafter at B=8, K=7).  Inputs are resident in HBM
-before timing; every timed step is bracketed by CUDA events on the launch
-stream and L2 is flushed (512 MiB write) between steps, outside the events.
-The headline times the pe_step call captured once in a CUDA graph and
-replayed (how a serving loop runs the drafting step); `direct_us_per_round`
-is the same call launched directly each step.
+synthetic inputs of the chosen workload (default: workload 3, the
+GPT-OSS-20B-shaped drafter at B=64, K=7, the largest single-GPU one).  Inputs
+are resident in HBM before timing; every timed step is bracketed by CUDA events
+on the launch stream and L2 is flushed (512 MiB write) between steps, outside
+the events.  The headline times the pe_step call captured once in a CUDA graph
+and replayed (how a serving loop runs the drafting step); `direct_us_per_round`
+is the same call launched directly each step.  The clock sampler runs from a
+soak of at least one second of back-to-back replays through the timed steps.
 `e2e` repeats the measurement through the same C-ABI call with the round's
 per-step inputs copied from pinned host memory and its results copied back.
+The same line carries `c2` (the GPT-OSS-20B-shaped drafter at B=1, K=7: the
+weight-read-bound regime) and `k_sweep` (the 2-layer drafter at B in {1, 8, 32}
+and K in {1, 8}: latency against K), each timed the same way (graph replay, L2
+flushed) with its own roofline fraction.
 Under torchrun each rank runs an independent replica (no collective on the
 data path); the max over ranks is reported.
 
@@ -48,7 +53,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1, help="workload index 0..3")
+    ap.add_argument("--config", type=int, default=3, help="workload index 0..3")
     ap.add_argument("--sweep", type=str, default=None, help="B,K of the 2-layer K x B sweep workload")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
@@ -56,6 +61,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of a graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-oracle sample time")
+    ap.add_argument("--no-extra", action="store_true", help="skip the c2 and k_sweep objects")
+    ap.add_argument("--soak-s", type=float, default=1.2, help="back-to-back replays before the timed steps")
     return ap.parse_args()
 
 
@@ -239,23 +246,41 @@ def recorded_traffic(kernel_key: str, workload_name: str):
 
 # ----------------------------------------------------------------------------- CPU oracle arms
 
-def cpu_oracle_sample(cfg, w, rnd, target_seconds: float):
-    """The oracle on whole sequences of the workload, round-robin, for about target_seconds."""
+def config_dict(cfg, rnd, world: int) -> dict:
+    """The workload description both arms print (identical keys and values for one workload)."""
+    cost = round_cost(cfg, rnd)
+    return dict(workload=cfg.name, B=cfg.B, K=cfg.K, n_layers=cfg.n_layers, d=cfg.d, vocab=cfg.vocab,
+                n_valid_rows=cost["n_valid"],
+                l2="flushed between timed steps (512 MiB write outside the step events)",
+                replicas="one independent replica per rank" if world > 1 else "single GPU")
+
+
+def _oracle_passes(cfg, w, rnd, target_seconds: float, n_threads: int):
     import oracle
 
-    oracle.build()
     tokens, elapsed, n, i = 0, 0.0, 0, 0
     while elapsed < target_seconds:
         t0 = time.perf_counter()
-        oracle.run_round(cfg, w, rnd, seqs=[i % cfg.B])
+        oracle.run_round(cfg, w, rnd, n_threads=n_threads, seqs=[i % cfg.B])
         elapsed += time.perf_counter() - t0
         tokens += cfg.K
         n += 1
         i += 1
-    return dict(value=tokens / elapsed, unit=UNIT, cores=oracle.threads_used(), kind="oracle",
-                sample=f"{n} single-sequence passes (round-robin over the {cfg.B} sequences) of {cfg.name}: "
-                       f"batch rebuild, input rows, fp64 drafter pass and LM head over the sequence's draft "
-                       f"rows; {elapsed:.1f} s")
+    return tokens / elapsed, n, elapsed, oracle.threads_used()
+
+
+def cpu_oracle_sample(cfg, w, rnd, target_seconds: float):
+    """The oracle on whole sequences of the workload, round-robin, for about target_seconds on all
+    host cores, then for about the same time on one core."""
+    import oracle
+
+    oracle.build()
+    v, n, el, cores = _oracle_passes(cfg, w, rnd, target_seconds, 0)
+    v1, n1, el1, _ = _oracle_passes(cfg, w, rnd, target_seconds, 1)
+    what = (f"single-sequence passes (round-robin over the {cfg.B} sequences) of {cfg.name}: batch rebuild, "
+            f"input rows, fp64 drafter pass and LM head over the sequence's draft rows")
+    return dict(value=v, unit=UNIT, cores=cores, kind="oracle", sample=f"{n} {what}; {el:.1f} s",
+                single_thread=dict(value=v1, unit=UNIT, cores=1, sample=f"{n1} such passes; {el1:.1f} s"))
 
 
 def run_reference(args):
@@ -279,10 +304,10 @@ def run_reference(args):
     out = dict(impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus, steps=args.steps,
                warmup=args.warmup, ms_per_step=1e3 * per, higher_is_better=True, scaling="weak",
                vs_baseline=None, dtype="f64", data="synthetic (seeded; shapes and value distributions of the workload)",
-               config=dict(workload=cfg.name, B=cfg.B, K=cfg.K, n_layers=cfg.n_layers,
-                           step="one sequence's share of the round (sequences round-robin)"),
+               config=config_dict(cfg, rnd, world),
                cpu_baseline=dict(kind="oracle", cores=oracle.threads_used(), value=value, unit=UNIT,
-                                 sample=f"{args.steps} single-sequence passes of {cfg.name}"),
+                                 sample=f"{args.steps} single-sequence passes of {cfg.name}, sequences round-robin "
+                                        f"(a step is one sequence's share of the round: K draft tokens)"),
                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(out), flush=True)
 
@@ -295,6 +320,117 @@ def stage_names(n_layers):
         names += [f"l{l}.norm1", f"l{l}.qkv_rope_kv", f"l{l}.attention", f"l{l}.o_proj", f"l{l}.norm2",
                   f"l{l}.gate_up_swiglu", f"l{l}.down"]
     return names + ["final_norm", "lm_head_argmax", "verify"]
+
+
+class Bench:
+    """One workload on the device: weights, round inputs, target tokens and its pe_step calls."""
+
+    def __init__(self, cfg_np, seed, dev, w_np=None):
+        import torch
+
+        import speculative_decoding_step_gb300 as pe
+        from pe_workload.device import round_to_device, weights_to_device
+
+        self.pe, self.torch, self.dev, self.cfg_np = pe, torch, dev, cfg_np
+        self.w_np = w_np if w_np is not None else make_weights(cfg_np, seed)
+        self.rnd = make_round(cfg_np, seed)
+        self.W, self.R = weights_to_device(self.w_np, dev), round_to_device(self.rnd, dev)
+        self.cfg = pe.Config.make(cfg_np.B, cfg_np.K, cfg_np.d, cfg_np.n_q, cfg_np.n_kv, cfg_np.head_dim,
+                                  cfg_np.ffn, cfg_np.vocab, cfg_np.n_layers, self.rnd.block_table.shape[1],
+                                  cfg_np.dtype, rms_eps=cfg_np.rms_eps, rope_theta=cfg_np.rope_theta)
+        self.rd = pe.Round(self.cfg, pe.DeviceWeights(**self.W), pe.DeviceKV(self.R["k_cache"], self.R["v_cache"]),
+                           self.R["block_table"], dev)
+        # target tokens of this round's verify batch: from one untimed pass's drafts
+        R = self.R
+        self.rd.prepare(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"])
+        self.rd.scatter(R["target_hidden"])
+        self.rd.forward()
+        torch.cuda.synchronize()
+        self.target = torch.from_numpy(make_targets(self.rd.draft_tokens.cpu().numpy(), self.rnd.target_u,
+                                                    self.rnd.target_r)).to(dev)
+        self.graph = None
+
+    def step(self):
+        R = self.R
+        self.rd.step(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"], R["target_hidden"], self.target)
+
+    def capture(self):
+        """The pe_step call captured once in a CUDA graph (after a direct call: launch attributes
+        are set on each kernel's first use)."""
+        torch = self.torch
+        self.step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step()
+        g.replay()
+        torch.cuda.synchronize()
+        self.graph = g
+        return g.replay
+
+
+def timed(torch, stream, flush, n, fn, traced=None, pe=None):
+    """n calls of fn, each bracketed by CUDA events on the launch stream, L2 flushed before each."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        if traced is not None:
+            pe.set_trace_events(traced[i])
+        evs[i][0].record(stream)
+        fn()
+        evs[i][1].record(stream)
+    if traced is not None:
+        pe.set_trace_events([])
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def traced_stage_us(torch, stream, flush, pe, b: Bench, n: int) -> dict:
+    """Per-stage device times of n direct pe_step calls with events recorded between the stages
+    (this breaks the overlap of programmatic dependent launch: not the headline)."""
+    npts = pe.trace_points(b.cfg)
+    tr = [[torch.cuda.Event(enable_timing=True) for _ in range(npts)] for _ in range(n)]
+    for row in tr:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    timed(torch, stream, flush, n, b.step, traced=tr, pe=pe)
+    names = stage_names(b.cfg_np.n_layers)
+    return {nm: round(1e3 * statistics.median(tr[i][j].elapsed_time(tr[i][j + 1]) for i in range(n)), 2)
+            for j, nm in enumerate(names)}
+
+
+def roofline_of(cfg_np, rnd, us_round, lm_us, peaks, src) -> dict:
+    """The round against max(bytes / HBM, flops / sustained bf16) and the LM head + argmax kernel
+    against its own bound."""
+    cost = round_cost(cfg_np, rnd)
+    hbm = peaks["hbm_gbs"] * 1e9
+    tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 1e12
+    t_round = max(cost["bytes"] / hbm, cost["flops"] / tc)
+    out = dict(us_per_round=us_round, roofline_us=t_round * 1e6, frac=t_round / (us_round * 1e-6),
+               bound="hbm" if cost["bytes"] / hbm >= cost["flops"] / tc else "tensor", peak_source=src)
+    if lm_us:
+        t_lm = max(cost["lm_bytes"] / hbm, cost["lm_flops"] / tc)
+        out.update(lm_head_us=lm_us, lm_head_frac=t_lm / (lm_us * 1e-6),
+                   lm_head_bound="hbm" if cost["lm_bytes"] / hbm >= cost["lm_flops"] / tc else "tensor")
+    return out
+
+
+def quick_workload(torch, stream, flush, pe, cfg_np, seed, dev, steps, peaks, src, w_np=None) -> dict:
+    """One extra workload: graph-replayed round time (L2 flushed) and the traced LM head."""
+    b = Bench(cfg_np, seed, dev, w_np)
+    run = b.capture()
+    for _ in range(3):
+        run()
+    us = 1e3 * statistics.mean(timed(torch, stream, flush, steps, run))
+    st = traced_stage_us(torch, stream, flush, pe, b, max(3, steps // 2))
+    err = int(b.rd.err.item())
+    out = roofline_of(cfg_np, b.rnd, us, st["lm_head_argmax"], peaks, src)
+    out.update(workload=cfg_np.name, B=cfg_np.B, K=cfg_np.K, n_layers=cfg_np.n_layers,
+               draft_tokens_per_s=cfg_np.B * cfg_np.K / (us * 1e-6), device_error_word=err)
+    del b
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -312,71 +448,37 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
 
     import speculative_decoding_step_gb300 as pe
-    from pe_workload.device import round_to_device, weights_to_device
 
     pe.build()
     cfg_np = workload(args)
     seed = replica_seed(cfg_np.seed, rank, world)
-    w_np, rnd = make_weights(cfg_np, seed), make_round(cfg_np, seed)
-    W, R = weights_to_device(w_np, dev), round_to_device(rnd, dev)
-    cfg = pe.Config.make(cfg_np.B, cfg_np.K, cfg_np.d, cfg_np.n_q, cfg_np.n_kv, cfg_np.head_dim, cfg_np.ffn,
-                         cfg_np.vocab, cfg_np.n_layers, rnd.block_table.shape[1], cfg_np.dtype,
-                         rms_eps=cfg_np.rms_eps, rope_theta=cfg_np.rope_theta)
-    rd = pe.Round(cfg, pe.DeviceWeights(**W), pe.DeviceKV(R["k_cache"], R["v_cache"]), R["block_table"], dev)
+    b = Bench(cfg_np, seed, dev)
+    w_np, rnd, R, rd = b.w_np, b.rnd, b.R, b.rd
     stream = torch.cuda.current_stream()
-
-    # target tokens of this round's verify batch: from one untimed pass's drafts
-    rd.prepare(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"])
-    rd.scatter(R["target_hidden"])
-    rd.forward()
-    torch.cuda.synchronize()
-    target = torch.from_numpy(make_targets(rd.draft_tokens.cpu().numpy(), rnd.target_u, rnd.target_r)).to(dev)
-
-    def step():
-        rd.step(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"], R["target_hidden"], target)
-
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-
-    def timed(n, fn, traced=None):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-        for i in range(n):
-            flush.zero_()
-            if traced is not None:
-                pe.set_trace_events(traced[i])
-            evs[i][0].record(stream)
-            fn()
-            evs[i][1].record(stream)
-        if traced is not None:
-            pe.set_trace_events([])
-        torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in evs]
+    peaks, src = load_peaks()
 
     for _ in range(max(3, args.warmup)):
-        step()
+        b.step()
     torch.cuda.synchronize()
     err = int(rd.err.item())
 
     # ---- direct pe_step launches (host launch path in the loop), device-resident inputs
     launches0 = pe.kernel_launches()
-    direct_ms = statistics.mean(timed(args.steps, step))
+    direct_ms = statistics.mean(timed(torch, stream, flush, args.steps, b.step))
     launches_per_step = (pe.kernel_launches() - launches0) / args.steps
 
     # ---- headline: the same pe_step captured once in a CUDA graph and replayed, as a
     # serving loop runs the drafting step (the library allocates nothing and never
     # synchronises, so the call is capturable); direct launches if capture fails
-    run, mode = step, "direct_launches"
+    run, mode = b.step, "direct_launches"
     try:
         if args.no_graph:
             raise RuntimeError("--no-graph")
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            step()
-        g.replay()
-        torch.cuda.synchronize()
-        run, mode = g.replay, "cuda_graph_replay"
+        run, mode = b.capture(), "cuda_graph_replay"
     except Exception as exc:  # noqa: BLE001 - reported in the JSON line
         mode = f"direct_launches (graph capture unavailable: {exc})"[:200]
-    for _ in range(3):
+    for _ in range(max(3, args.warmup)):
         run()
     torch.cuda.synchronize()
     sampler = ClockSampler(torch.cuda.current_device())
@@ -384,37 +486,42 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    time.sleep(0.3)
+    # soak: back-to-back rounds (L2 flushed between them, as in the timed steps) so that the
+    # clock sampler sees the GPU under this load before and while the timed steps run
+    t_soak = time.perf_counter()
+    n_soak = 0
+    while time.perf_counter() - t_soak < args.soak_s:
+        for _ in range(50):
+            flush.zero_()
+            run()
+        n_soak += 50
+        torch.cuda.synchronize()
+    soak = time.perf_counter() - t_soak
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    step_ms = timed(args.steps, run)
+    step_ms = timed(torch, stream, flush, args.steps, run)
     wall = time.perf_counter() - t_wall
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
+    if clocks is not None:
+        clocks["window"] = f"{soak:.2f} s soak ({n_soak} rounds) then the {args.steps} timed steps"
     ms = sum(step_ms) / len(step_ms)
     ms, direct_ms = max_over_ranks([ms, direct_ms], dist, dev)
     launches = launches_per_step * args.steps  # kernels of ours per round x timed rounds
 
     # ---- per-stage device times: a separate traced pass (events between kernels; not the headline)
-    npts = pe.trace_points(cfg)
-    tr = [[torch.cuda.Event(enable_timing=True) for _ in range(npts)] for _ in range(args.steps)]
-    for row in tr:
-        for e in row:
-            e.record()
-    torch.cuda.synchronize()
-    timed(args.steps, step, traced=tr)
-    names = stage_names(cfg_np.n_layers)
-    stage_ms = [statistics.median(tr[i][j].elapsed_time(tr[i][j + 1]) for i in range(args.steps))
-                for j in range(npts - 1)]
-    stages_us = {n: round(1e3 * t, 2) for n, t in zip(names, stage_ms)}
-    lm_ms = stage_ms[names.index("lm_head_argmax")]
+    stages_us = traced_stage_us(torch, stream, flush, pe, b, args.steps)
+    lm_ms = stages_us["lm_head_argmax"] * 1e-3
 
     # ---- end to end through the same C-ABI call with host buffers
     e2e = None
     if not args.no_e2e:
         host_in = {k: R[k].cpu().pin_memory() for k in ("prev_tokens", "prev_pos", "num_accepted", "bonus",
                                                        "target_hidden")}
-        host_in["target"] = target.cpu().pin_memory()
+        host_in["target"] = b.target.cpu().pin_memory()
         dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
         outs = ("draft_tokens", "num_accepted", "bonus")
         host_out = {k: torch.empty(rd.out[k].shape, dtype=rd.out[k].dtype).pin_memory() for k in outs}
@@ -431,7 +538,7 @@ def run_ours(args):
 
         for _ in range(3):
             e2e_step()
-        e_ms = statistics.mean(timed(args.steps, e2e_step))
+        e_ms = statistics.mean(timed(torch, stream, flush, args.steps, e2e_step))
         (e_ms,) = max_over_ranks([e_ms], dist, dev)
         e2e = dict(value=whole_job_rate(world, cfg_np.B, cfg_np.K, e_ms), unit=UNIT, h2d_bytes_per_step=int(h2d),
                    d2h_bytes_per_step=int(d2h), ms_per_step=e_ms)
@@ -458,9 +565,9 @@ def run_ours(args):
         for _ in range(3):
             sampled_round()
         torch.cuda.synchronize()
-        t_round = statistics.mean(timed(args.steps, sampled_round))
-        t_s = statistics.mean(timed(args.steps, lambda: rd.sample(u_d)))
-        t_v = statistics.mean(timed(args.steps, lambda: rd.verify_sampled(P, u_a, u_r)))
+        t_round = statistics.mean(timed(torch, stream, flush, args.steps, sampled_round))
+        t_s = statistics.mean(timed(torch, stream, flush, args.steps, lambda: rd.sample(u_d)))
+        t_v = statistics.mean(timed(torch, stream, flush, args.steps, lambda: rd.verify_sampled(P, u_a, u_r)))
         lbytes = cfg_np.B * cfg_np.K * cfg_np.vocab * 4
         sampled = dict(round_us=t_round * 1e3, sample_us=t_s * 1e3, verify_sampled_us=t_v * 1e3,
                        logits_bytes=lbytes, sample_gbs=lbytes / (t_s * 1e-3) / 1e9, temperature=1.0,
@@ -472,7 +579,6 @@ def run_ours(args):
         dist.destroy_process_group()
         return
 
-    peaks, src = load_peaks()
     cost = round_cost(cfg_np, rnd)
     hbm = peaks["hbm_gbs"] * 1e9
     tc_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 1e12
@@ -487,7 +593,8 @@ def run_ours(args):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic("lm_head_argmax", cfg_np.name)
     roof.update(kernel="gemm_tc_kernel<EPI_ARGMAX> (LM head + argmax)", algorithmic_bytes_per_launch=cost["lm_bytes"],
-                algorithmic_flops_per_launch=cost["lm_flops"], avg_launch_us=lm_ms * 1e3)
+                algorithmic_flops_per_launch=cost["lm_flops"], avg_launch_us=lm_ms * 1e3,
+                timed_as="CUDA events around the LM-head launch in a traced pass, on the launch stream")
     t_round = max(cost["bytes"] / hbm, cost["flops"] / tc_sus)
     round_roof = dict(bytes=cost["bytes"], flops=cost["flops"], roofline_us=t_round * 1e6, measured_us=ms * 1e3,
                       frac=t_round / (ms * 1e-3),
@@ -506,19 +613,37 @@ def run_ours(args):
         stages[name] = dict(us=t_us, bytes=int(sb), flops=int(sf),
                             roofline_frac=(t_roof / (t_us * 1e-6)) if t_us else None)
 
+    # ---- the other regimes, in the same line: B = 1 (weight-read bound) and latency against K
+    c2, k_sweep = None, None
+    if not args.no_extra and world == 1:
+        del b, rd, R
+        torch.cuda.empty_cache()
+        if cfg_np.name != config(2).name:
+            c2 = quick_workload(torch, stream, flush, pe, config(2), config(2).seed, dev, args.steps, peaks, src)
+        w_sweep = None
+        k_sweep = dict(drafter="GPT-OSS-20B-shaped, 2 layers", points=[])
+        for Bs in (1, 8, 32):
+            pts = {}
+            for Ks in (1, 8):
+                sc = sweep_config(Bs, Ks)
+                if w_sweep is None:
+                    w_sweep = make_weights(sc)  # the weights do not depend on B or K
+                q = quick_workload(torch, stream, flush, pe, sc, sc.seed, dev, args.steps, peaks, src, w_sweep)
+                k_sweep["points"].append(q)
+                pts[Ks] = q["us_per_round"]
+            k_sweep[f"B{Bs}_K8_over_K1"] = pts[8] / pts[1]
+
     cpu = None if args.no_cpu_baseline else cpu_oracle_sample(cfg_np, w_np, rnd, args.cpu_seconds)
     value = whole_job_rate(world, cfg_np.B, cfg_np.K, ms)
     out = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
                ms_per_step=ms, us_per_round=ms * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
                dtype=cfg_np.dtype, data="synthetic (seeded; shapes and value distributions of the workload)",
-               config=dict(workload=cfg_np.name, B=cfg_np.B, K=cfg_np.K, n_layers=cfg_np.n_layers, d=cfg_np.d,
-                           vocab=cfg_np.vocab, n_valid_rows=cost["n_valid"],
-                           l2="flushed between timed steps (512 MiB write outside the step events)",
-                           replicas="one independent replica per rank" if world > 1 else "single GPU"),
+               config=config_dict(cfg_np, rnd, world),
                timed_as=mode, direct_us_per_round=direct_ms * 1e3, roofline=roof, round_roofline=round_roof,
                stages_us=stages_us, stages=stages, gpu_launches=int(launches), launches_per_step=launches_per_step,
                device_error_word=err,
-               wall_s_timed_loop=wall, clocks=clocks, cpu_baseline=cpu, e2e=e2e, sampled=sampled)
+               wall_s_timed_loop=wall, clocks=clocks, cpu_baseline=cpu, e2e=e2e, sampled=sampled, c2=c2,
+               k_sweep=k_sweep)
     print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()

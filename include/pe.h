@@ -80,7 +80,7 @@ typedef enum {
 #define PE_DEV_BAD_ACCEPTED 0x0205 /* num_accepted outside [0, K] */
 #define PE_DEV_BAD_PAGE     0x0305 /* block-table entry outside [0, num_pages) */
 #define PE_DEV_BAD_POSITION 0x0405 /* position beyond the block table, or negative */
-#define PE_DEV_NONFINITE    0x0505 /* a logit was NaN or infinite */
+#define PE_DEV_NONFINITE    0x0505 /* LM head: a logit was NaN or infinite; draws: NaN or +inf */
 #define PE_DEV_BAD_ROW      0x0605 /* a row index outside the batch */
 #define PE_DEV_TIMEOUT      0x0106 /* a pipeline wait exceeded its time limit */
 
@@ -223,8 +223,9 @@ pe_status pe_draft_forward(const pe_config *cfg, const pe_weights *w, const pe_k
  * Arguments and results are those of pe_draft_forward, without the workspace.
  * A config whose pe_workspace_bytes(cfg) exceeds PE_NOALLOC_SCRATCH_BYTES is
  * rejected with PE_ERR_SHAPE before any launch.  The first call on a device
- * looks up the array's device address on the current device; make that first
- * call before any stream capture.  This call allocates nothing and calls no
+ * looks up the array's device address on the current device (and so does the
+ * first call after cudaDeviceReset gave the device a new context); make that
+ * first call before any stream capture.  This call allocates nothing and calls no
  * allocating routine.  Every call shares the one array, and the array keeps
  * whatever the last call left in it.  The pass zeroes every counter and
  * accumulator it needs at its start, so leftover contents do no harm.  Two
@@ -264,10 +265,11 @@ pe_status pe_verify(const pe_config *cfg, const int32_t *draft_tokens, const int
  * 256-byte aligned, >= pe_workspace_bytes(cfg) bytes (the same workspace as
  * pe_draft_forward may be passed; its contents are scratch).  Two launches:
  * statistics of every 512-entry step of every row, then one warp per row for the
- * draw.  A non-finite logit sets PE_DEV_NONFINITE; where it leaves the row's
- * distribution undefined (NaN, +inf) the row's token is 0 and its lse NaN (a
- * -inf logit only has probability 0).  temperature must be positive and finite
- * (else PE_ERR_INVALID_ARG).
+ * draw.  A -inf logit is a masked entry: probability 0, never drawn (a row may
+ * mask whole 512-entry steps).  A NaN or +inf logit sets PE_DEV_NONFINITE and
+ * leaves the row's distribution undefined: the row's token is 0 and its lse NaN;
+ * so does a row whose every logit is -inf.  temperature must be positive and
+ * finite (else PE_ERR_INVALID_ARG).
  */
 pe_status pe_sample_drafts(const pe_config *cfg, const float *logits, const float *u_draft, float temperature,
                            void *workspace, size_t workspace_bytes, int32_t *draft_tokens, float *lse,
@@ -312,8 +314,9 @@ pe_status pe_verify_sampled(const pe_config *cfg, const int32_t *draft_tokens, c
  * again after the caller refills target_hidden and target_tokens is the next
  * round (the multi-round drafting loop; the prefix grows by num_accepted + 1
  * positions per round, which the block table must cover).  No other output may
- * overlap an input or another output: such a call returns PE_ERR_INVALID_ARG
- * before anything is launched.
+ * overlap an input or another output (err_word and the first
+ * pe_workspace_bytes(cfg) bytes of the workspace count as outputs): such a call
+ * returns PE_ERR_INVALID_ARG before anything is launched.
  */
 pe_status pe_step(const pe_config *cfg, const pe_weights *w, const pe_kv *kv, const int32_t *block_table,
                   const int32_t *prev_tokens, const int32_t *prev_pos, const int32_t *num_accepted,
@@ -341,6 +344,32 @@ int32_t pe_trace_points(const pe_config *cfg);
 
 /* Number of kernels this library has launched since it was loaded (all threads). */
 uint64_t pe_kernel_launches(void);
+
+/*
+ * Failure detection.  Inside a CTA the pipeline roles (copy issue, MMA issue,
+ * softmax, epilogue) wait on each other through shared-memory barriers; no CTA
+ * ever waits for another CTA.  Every such wait gives up after a time limit:
+ * it records PE_DEV_TIMEOUT in *err_word, raises the CTA's abort flag (the
+ * CTA's other roles stop waiting), waits for the CTA's own copies and MMAs in
+ * flight, frees its tensor memory and returns; the rest of the call's kernels
+ * still run (their results are then undefined) and the stream stays usable.
+ * pe_set_wait_limit_ns sets that limit, in nanoseconds, for the kernels
+ * launched afterwards by any thread (0 restores the default of one second; a
+ * round takes well under a millisecond, so only a lost arrival reaches it).
+ * Kernels captured into a CUDA graph keep the limit of the capture.
+ */
+pe_status pe_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test hook of the wait-expiry path above (for failure-detection tests only).
+ * The next tensor-core GEMM launch (bf16 configs), from any thread, leaves
+ * pipeline stage `stage` of its first CTA unarmed: no copy is issued into it
+ * and no byte count is expected on its barrier, so the MMA role's wait on it
+ * runs out after the wait limit.  One-shot: the launch that applies it clears
+ * it; -1 clears it beforehand.  PE_ERR_INVALID_ARG for stage < -1.  A stage
+ * beyond the CTA's pipeline leaves the launch unchanged.
+ */
+pe_status pe_test_skip_pipeline_stage(int32_t stage);
 
 /* Workspace bytes needed by pe_draft_forward, pe_step, pe_sample_drafts and
  * pe_verify_sampled for this config (0 if invalid); one workspace serves them all. */

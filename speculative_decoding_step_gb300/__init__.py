@@ -36,7 +36,8 @@ PE_DEV_TIMEOUT = 0x0106
 EXPORTED_SYMBOLS = ["pe_prepare_batch", "pe_scatter_hidden", "pe_draft_forward", "pe_verify", "pe_step",
                     "pe_sample_drafts", "pe_verify_sampled",
                     "pe_workspace_bytes", "pe_check_config", "pe_status_str", "pe_set_trace_events",
-                    "pe_trace_points", "pe_kernel_launches", "pe_draft_forward_noalloc"]
+                    "pe_trace_points", "pe_kernel_launches", "pe_draft_forward_noalloc", "pe_set_wait_limit_ns",
+                    "pe_test_skip_pipeline_stage"]
 
 # Size of the library-owned scratch used by pe_draft_forward_noalloc (PE_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 48 << 20
@@ -154,6 +155,8 @@ def lib():
         L.pe_trace_points.argtypes = [cp]
         L.pe_kernel_launches.restype = ctypes.c_uint64
         L.pe_kernel_launches.argtypes = []
+        L.pe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.pe_test_skip_pipeline_stage.argtypes = [i32]
         for name in EXPORTED_SYMBOLS:
             if name not in ("pe_status_str", "pe_workspace_bytes", "pe_kernel_launches"):
                 getattr(L, name).restype = ctypes.c_int
@@ -190,6 +193,17 @@ def trace_points(cfg: Config) -> int:
 def kernel_launches() -> int:
     """Kernels launched by the library so far in this process."""
     return int(lib().pe_kernel_launches())
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of every bounded pipeline wait in kernels launched from now on (0: the default, 1 s)."""
+    _check(lib().pe_set_wait_limit_ns(int(ns)), "pe_set_wait_limit_ns")
+
+
+def skip_pipeline_stage_for_test(stage: int) -> None:
+    """Failure-detection test hook: the next tensor-core GEMM launch leaves this pipeline stage of
+    its first CTA unarmed, so a wait on it runs out (-1 clears it)."""
+    _check(lib().pe_test_skip_pipeline_stage(int(stage)), "pe_test_skip_pipeline_stage")
 
 
 def check_config(cfg: Config) -> int:

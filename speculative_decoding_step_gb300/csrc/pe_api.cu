@@ -26,6 +26,14 @@ bool pdl_enabled() {
   return on;
 }
 
+static std::atomic<uint64_t> g_wait_ns{0};    // 0: the kernels' default limit
+static std::atomic<int> g_drop_stage{-1};
+uint64_t wait_limit_ns() {
+  const uint64_t v = g_wait_ns.load(std::memory_order_relaxed);
+  return v == 0 ? kDefaultWaitNs : v;
+}
+int take_drop_stage() { return g_drop_stage.exchange(-1, std::memory_order_relaxed); }
+
 namespace {
 
 // Caller-created events recorded at stage boundaries (tracing).
@@ -373,6 +381,8 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   a.acc_stride = g.acc_stride;
   a.tmem_cols = g.tmem_cols;
   a.n_tok_min = call.n_tok_dev != nullptr ? std::min(call.n_tok, c.B * c.K) : call.n_tok;
+  a.wait_ns = wait_limit_ns();
+  a.drop_stage = take_drop_stage();
   if (g.k_splits > 1 || g.balanced) a.partial = at<float>(ws, p.split_part);
   if (g.balanced) a.tile_cnt = at<int32_t>(ws, p.done) + 1 + c.n_layers;
   CUtensorMap tw, tx;
@@ -417,7 +427,8 @@ pe_status check_kv(const pe_config& c, const pe_kv* kv) {
 // pe_step's outputs against its inputs: an output may be exactly its paired state input
 // (next_prev_tokens / prev_tokens, next_prev_pos / prev_pos, num_accepted_out /
 // num_accepted, bonus_out / bonus); otherwise no output may overlap an input or another
-// output.  Byte ranges from the config's shapes.
+// output.  The error word and the part of the workspace the round uses count as outputs.
+// Byte ranges from the config's shapes.
 struct Span {
   uintptr_t lo, hi;
 };
@@ -430,19 +441,21 @@ bool step_aliasing_ok(const pe_config& c, const int32_t* block_table, const int3
                       const int32_t* prev_pos, const int32_t* num_accepted, const int32_t* bonus,
                       const void* target_hidden, const int32_t* target_tokens, const int32_t* draft_tokens,
                       const int32_t* num_accepted_out, const int32_t* bonus_out, const int32_t* next_prev_tokens,
-                      const int32_t* next_prev_pos, const float* logits_dbg) {
+                      const int32_t* next_prev_pos, const float* logits_dbg, const int32_t* err_word,
+                      const void* workspace, size_t workspace_used) {
   const size_t B = (size_t)c.B, K = (size_t)c.K;
   const Span in[7] = {span_of(block_table, 4 * B * (size_t)c.max_pages_per_seq), span_of(prev_tokens, 4 * B * (K + 1)),
                       span_of(prev_pos, 4 * B * (K + 1)), span_of(num_accepted, 4 * B), span_of(bonus, 4 * B),
                       span_of(target_hidden, elem_bytes(c.dtype) * B * (K + 1) * (size_t)c.d),
                       span_of(target_tokens, 4 * B * (K + 1))};
   // outputs, each with the index of the input it may replace exactly (-1: none)
-  const Span out[6] = {span_of(draft_tokens, 4 * B * K), span_of(num_accepted_out, 4 * B),
+  const Span out[8] = {span_of(draft_tokens, 4 * B * K), span_of(num_accepted_out, 4 * B),
                        span_of(bonus_out, 4 * B), span_of(next_prev_tokens, 4 * B * (K + 1)),
                        span_of(next_prev_pos, 4 * B * (K + 1)),
-                       span_of(logits_dbg, logits_dbg ? 4 * B * K * (size_t)c.vocab : 0)};
-  const int pair[6] = {-1, 3, 4, 1, 2, -1};
-  for (int o = 0; o < 6; ++o) {
+                       span_of(logits_dbg, logits_dbg ? 4 * B * K * (size_t)c.vocab : 0), span_of(err_word, 4),
+                       span_of(workspace, workspace_used)};
+  const int pair[8] = {-1, 3, 4, 1, 2, -1, -1, -1};
+  for (int o = 0; o < 8; ++o) {
     for (int i = 0; i < 7; ++i) {
       if (!overlaps(out[o], in[i])) continue;
       if (i == pair[o] && out[o].lo == in[i].lo && out[o].hi == in[i].hi) continue;
@@ -556,7 +569,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   at_.part_m = bf16 ? at<float>(ws, p.part_m) : nullptr;
   at_.part_l = bf16 ? at<float>(ws, p.part_l) : nullptr;
   at_.part_o = bf16 ? at<float>(ws, p.part_o) : nullptr;
-  at_.out = ao; at_.n_rows = p.R; at_.err = err;
+  at_.out = ao; at_.n_rows = p.R; at_.err = err; at_.wait_ns = wait_limit_ns();
 
   for (int l = 0; l < c.n_layers; ++l) {
     const int tp = 5 + 7 * l;
@@ -747,10 +760,12 @@ pe_status pe_step(const pe_config* cfg, const pe_weights* w, const pe_kv* kv, co
       !err_word)
     return PE_ERR_INVALID_ARG;
   if (!aligned16(target_hidden) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PE_ERR_INVALID_ARG;
-  if (!step_aliasing_ok(*cfg, block_table, prev_tokens, prev_pos, num_accepted, bonus, target_hidden, target_tokens,
-                        draft_tokens, num_accepted_out, bonus_out, next_prev_tokens, next_prev_pos, logits_dbg))
-    return PE_ERR_INVALID_ARG;
   const Plan p = make_plan(*cfg);
+  // the workspace bytes this round would use (a workspace that is too short fails below)
+  if (!step_aliasing_ok(*cfg, block_table, prev_tokens, prev_pos, num_accepted, bonus, target_hidden, target_tokens,
+                        draft_tokens, num_accepted_out, bonus_out, next_prev_tokens, next_prev_pos, logits_dbg,
+                        err_word, workspace, std::min(workspace_bytes, p.total)))
+    return PE_ERR_INVALID_ARG;
   if (workspace_bytes < p.total) return PE_ERR_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
   void* ws = workspace;
@@ -845,5 +860,16 @@ int32_t pe_trace_points(const pe_config* cfg) {
 }
 
 uint64_t pe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+pe_status pe_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns.store(ns, std::memory_order_relaxed);
+  return PE_OK;
+}
+
+pe_status pe_test_skip_pipeline_stage(int32_t stage) {
+  if (stage < -1) return PE_ERR_INVALID_ARG;
+  g_drop_stage.store(stage, std::memory_order_relaxed);
+  return PE_OK;
+}
 
 }  // extern "C"

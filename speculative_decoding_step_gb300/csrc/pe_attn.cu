@@ -104,9 +104,9 @@ static_assert(sizeof(AttnCtrl) <= 256, "attention control block");
 
 // Consumer side of the item ring: the index of this CTA's ii-th item (-1: done),
 // or -2 when the wait gave up (the kernel is unwinding).
-PE_DEV int attn_next_item(AttnCtrl* ctl, int ii, int32_t* err, volatile int* abort_flag) {
+PE_DEV int attn_next_item(AttnCtrl* ctl, int ii, int32_t* err, volatile int* abort_flag, uint64_t wait_ns) {
   const int k = ii % kAttnItemRing;
-  if (!mbar_wait(smem_u32(&ctl->item_full[k]), (uint32_t)(ii / kAttnItemRing) & 1u, err, abort_flag)) return -2;
+  if (!mbar_wait(smem_u32(&ctl->item_full[k]), (uint32_t)(ii / kAttnItemRing) & 1u, err, abort_flag, wait_ns)) return -2;
   const int it = *reinterpret_cast<volatile int*>(&ctl->item[k]);
   mbar_arrive(smem_u32(&ctl->item_empty[k]));
   return it;
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         bool ok = true;
         if (ii >= kAttnItemRing)
           ok = mbar_wait(smem_u32(&ctl->item_empty[k]), ((uint32_t)(ii / kAttnItemRing) & 1u) ^ 1u, a.err,
-                         abort_flag);
+                         abort_flag, a.wait_ns);
         if (!ok) it = -2;
         else {
           ctl->item[k] = it;
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           const int s = gi % S;
           bool ok = true;
           if (lane == 0 && gi >= S)
-            ok = mbar_wait(smem_u32(&ctl->empty[s]), ((uint32_t)(gi / S) & 1u) ^ 1u, a.err, abort_flag);
+            ok = mbar_wait(smem_u32(&ctl->empty[s]), ((uint32_t)(gi / S) & 1u) ^ 1u, a.err, abort_flag, a.wait_ns);
           if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
             stop = true;
             break;
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     if (stop && lane == 0) {
       // leave no bulk copy in flight into this CTA's shared memory
       for (int i = (gi > S ? gi - S : 0); i < gi; ++i)
-        mbar_wait(smem_u32(&ctl->full[i % S]), (uint32_t)(i / S) & 1u, a.err, nullptr);
+        mbar_wait(smem_u32(&ctl->full[i % S]), (uint32_t)(i / S) & 1u, a.err, nullptr, a.wait_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -253,14 +253,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const uint32_t id_s = idesc_bf16(kAttnRows, kAttnBlk);                 // S = Q K^T: N = positions
     const uint32_t id_o = idesc_bf16(kAttnRows, HD) | kIdescTransposeB;   // O += P V: V is MN-major
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
-      const bool ok = mbar_wait(bar, parity, a.err, abort_flag);
+      const bool ok = mbar_wait(bar, parity, a.err, abort_flag, a.wait_ns);
       return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
     };
     int gi = 0, ii = 0;
     bool stop = false;
     for (;; ++ii) {
       int it = 0;
-      if (elect_one()) it = attn_next_item(ctl, ii, a.err, abort_flag);
+      if (elect_one()) it = attn_next_item(ctl, ii, a.err, abort_flag, a.wait_ns);
       it = __shfl_sync(0xFFFFFFFFu, it, 0);
       if (it < 0) break;
       const int4 item = a.items[it];
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     // TMEM is freed only after every MMA issued here has completed
     if (elect_one()) tc_commit(smem_u32(&ctl->drain));
     __syncwarp();
-    mbar_wait(smem_u32(&ctl->drain), 0, a.err, nullptr);
+    mbar_wait(smem_u32(&ctl->drain), 0, a.err, nullptr, a.wait_ns);
   } else {
     // ------------------------------------------------------------------ softmax + epilogue (warps 2..5)
     const int et = tid - 64;                        // 0..127
@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     };
     int gi = 0, ii = 0;
     bool stop = false;
-    int it = attn_next_item(ctl, 0, a.err, abort_flag), it_next = -1;
+    int it = attn_next_item(ctl, 0, a.err, abort_flag, a.wait_ns), it_next = -1;
     if (it >= 0) stage_q(it);
     for (; it >= 0 && !stop; it = it_next, ++ii) {
       it_next = -1;
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       float m_ref = -INFINITY, l = 0.f;  // reference maximum (log2 units, scaled) and row sum
       for (int j = 0; j < nblk; ++j) {
         const int x = gi + j;
-        if (!warp_ok(mbar_wait(smem_u32(&ctl->s_full[x & 1]), (uint32_t)(x >> 1) & 1u, a.err, abort_flag))) {
+        if (!warp_ok(mbar_wait(smem_u32(&ctl->s_full[x & 1]), (uint32_t)(x >> 1) & 1u, a.err, abort_flag, a.wait_ns))) {
           stop = true;
           break;
         }
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           const bool need = !fresh && bm > m_ref + kAttnRescaleLog2;
           if (__any_sync(0xFFFFFFFFu, need)) {
             // O holds the PV products of blocks before j of this item (j >= 1 since m_ref is finite)
-            if (!warp_ok(mbar_wait(smem_u32(&ctl->pv_done), (uint32_t)(x - 1) & 1u, a.err, abort_flag))) {
+            if (!warp_ok(mbar_wait(smem_u32(&ctl->pv_done), (uint32_t)(x - 1) & 1u, a.err, abort_flag, a.wait_ns))) {
               stop = true;
             } else {
               tc_fence_after();
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       }
       if (stop) break;
       // every S product of this item has completed: the next item's query tile may go in
-      it_next = attn_next_item(ctl, ii + 1, a.err, abort_flag);
+      it_next = attn_next_item(ctl, ii + 1, a.err, abort_flag, a.wait_ns);
       if (it_next == -2) break;
       if (it_next >= 0) stage_q(it_next);
 
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       // the PV of the block before it is issued after the last S product, so pv_done
       // may still be a phase short of that block, and a parity wait cannot tell a
       // barrier two phases behind from one that is done.)
-      if (!warp_ok(mbar_wait(smem_u32(&ctl->pv_item), (uint32_t)ii & 1u, a.err, abort_flag))) break;
+      if (!warp_ok(mbar_wait(smem_u32(&ctl->pv_item), (uint32_t)ii & 1u, a.err, abort_flag, a.wait_ns))) break;
       tc_fence_after();
       if (nc == 1) {
         // the item covers the whole range: normalise and write the output row directly

@@ -69,14 +69,16 @@ PE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Upper bound on any single pipeline wait.  Kernels here finish in well under
-// a millisecond; a wait this long means a lost arrival, so give up and report.
+// Default upper bound on any single pipeline wait.  Kernels here finish in well
+// under a millisecond; a wait this long means a lost arrival, so give up and report.
+// The host may set another limit per launch (pe_set_wait_limit_ns).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // Wait for phase `parity` of an mbarrier.  Returns false (after flagging
-// PE_DEV_TIMEOUT and raising *abort) when the limit expires, or at once when
+// PE_DEV_TIMEOUT and raising *abort) when `limit_ns` expires, or at once when
 // another role of the CTA already raised *abort.
-PE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err, volatile int* abort) {
+PE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err, volatile int* abort,
+                      uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
@@ -84,7 +86,7 @@ PE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err, volatile int*
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       set_err(err, PE_DEV_TIMEOUT);
       if (abort != nullptr) *abort = 1;
       return false;

@@ -445,6 +445,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_trigger();
+  int issued = 0;  // k-block stages the producer issued (its drain after an abort)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -453,6 +454,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // phase advance incrementally: no division per k block.
     const uint64_t pol_w = l2_policy_evict_first();  // weights: read once
     const uint64_t pol_x = l2_policy_evict_last();   // activations: re-read by every weight tile
+    // wait-expiry test: CTA 0 never arms this stage, so the MMA warp's wait on it runs out
+    const int drop = blockIdx.x == 0 ? a.drop_stage : -1;
     // the weights do not depend on earlier kernels: start the first stages now
     int npre = 0;
     if (BAL) {  // the first S k blocks of the range, across pieces
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       Unit w;
       while (npre < S && sched_next<EPI>(a, s0, 1, w))
         for (int kb = w.kb0; kb < w.kb1 && npre < S; ++kb, ++npre)
-          if (elect_one()) {
+          if (npre != drop && elect_one()) {
             const uint32_t sa = smem_u32(smem + (size_t)npre * a.stage_bytes);
             mbar_expect_tx(smem_u32(full + npre), a.stage_bytes);
             issue_w<EPI>(&tmW, a, sa, smem_u32(full + npre), kb * a.ka, w.tile_f, pol_w);
@@ -470,6 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       npre = min(S, w.kb1 - w.kb0);
       if (elect_one())
         for (int i = 0; i < npre; ++i) {
+          if (i == drop) continue;
           const uint32_t sa = smem_u32(smem + (size_t)i * a.stage_bytes);
           mbar_expect_tx(smem_u32(full + i), a.stage_bytes);
           issue_w<EPI>(&tmW, a, sa, smem_u32(full + i), (w.kb0 + i) * a.ka, w.tile_f, pol_w);
@@ -489,13 +493,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
         const uint32_t fb = smem_u32(full + s);
         if (it >= npre && it >= S) {
-          const bool ok = mbar_wait(smem_u32(empty + s), ph ^ 1u, a.err, abort_flag);
+          const bool ok = mbar_wait(smem_u32(empty + s), ph ^ 1u, a.err, abort_flag, a.wait_ns);
           if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
             stop = true;
             break;
           }
         }
-        if (elect_one()) {
+        if (it != drop && elect_one()) {
           if (it >= npre) {
             mbar_expect_tx(fb, a.stage_bytes);
             issue_w<EPI>(&tmW, a, sa, fb, kb * a.ka, w.tile_f, pol_w);
@@ -509,12 +513,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-    if (stop || *abort_flag) {
-      // leave no bulk copy in flight into this CTA's shared memory
-      const int lo = it > S ? it - S : 0;
-      for (int i = lo; i < it; ++i)
-        mbar_wait(smem_u32(full + (i % S)), (uint32_t)(i / S) & 1u, a.err, nullptr);
-    }
+    issued = it;
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     // Converged warp; the elected lane issues every MMA and commit.
@@ -530,13 +529,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     while (!stop && sched_next<EPI>(a, sc, ntl, w)) {
       const int buf = i % a.nbuf;
       if (i >= a.nbuf) {
-        const bool ok = mbar_wait(smem_u32(tempty + buf), (uint32_t)((i / a.nbuf) - 1) & 1u, a.err, abort_flag);
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+        const bool ok =
+            mbar_wait(smem_u32(tempty + buf), (uint32_t)((i / a.nbuf) - 1) & 1u, a.err, abort_flag, a.wait_ns);
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+          stop = true;
+          break;
+        }
       }
       tc_fence_after();
       const uint32_t d = tmem + (uint32_t)(buf * a.acc_stride);
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
-        const bool ok = mbar_wait(smem_u32(full + s), ph, a.err, abort_flag);
+        const bool ok = mbar_wait(smem_u32(full + s), ph, a.err, abort_flag, a.wait_ns);
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
           stop = true;
           break;
@@ -570,6 +573,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       ++i;
     }
+    // After a wait gave up: every MMA issued so far completes before the tensor memory is
+    // freed (the last commit tracks all of them).
+    if (stop && i > 0) {
+      const int lb = (i - 1) % a.nbuf;
+      mbar_wait(smem_u32(tfull + lb), (uint32_t)((i - 1) / a.nbuf) & 1u, a.err, nullptr, a.wait_ns);
+    }
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2..5)
     pdl_wait();
@@ -583,7 +592,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     Unit w;
     while (sched_next<EPI>(a, sc, ntl, w)) {
       const int buf = i % a.nbuf;
-      const bool ok = mbar_wait(smem_u32(tfull + buf), (uint32_t)(i / a.nbuf) & 1u, a.err, abort_flag);
+      // after an abort the accumulator may be incomplete: skip its epilogue
+      const bool ok =
+          mbar_wait(smem_u32(tfull + buf), (uint32_t)(i / a.nbuf) & 1u, a.err, abort_flag, a.wait_ns) && !*abort_flag;
       tc_fence_after();
       const int unit = w.tile_f * kTcBM + r;
       const uint32_t tl = tmem + (uint32_t)(buf * a.acc_stride) + ((uint32_t)(q * 32) << 16);
@@ -671,6 +682,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
+  __syncthreads();
+  // After a wait gave up (every role has left its loop, so the flag is final): leave no bulk
+  // copy in flight into this CTA's shared memory.  The stages still in the ring are the last
+  // S issued; each wait is bounded.
+  if (warp == 0 && *abort_flag) {
+    const int drop = blockIdx.x == 0 ? a.drop_stage : -1;
+    for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+      if (i != drop) mbar_wait(smem_u32(full + (i % S)), (uint32_t)(i / S) & 1u, a.err, nullptr, a.wait_ns);
+    __syncwarp();
+  }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

@@ -17,6 +17,13 @@ void count_launch(int n = 1);
 // Programmatic dependent launch on (default on; PE_PDL=0 in the environment turns it off).
 bool pdl_enabled();
 
+// Limit of every bounded pipeline wait in the kernels launched from now on (pe_set_wait_limit_ns).
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
+uint64_t wait_limit_ns();
+// The pipeline stage the next tensor-core GEMM launch leaves unarmed in CTA 0, then -1 again
+// (pe_test_skip_pipeline_stage); -1: none.
+int take_drop_stage();
+
 // Launch with the programmatic-stream-serialization attribute so the kernel's
 // prologue may overlap the previous kernel's tail (see pdl_wait / pdl_trigger).
 template <typename... KArgs, typename... Args>
@@ -224,6 +231,8 @@ struct GemmArgs {
   int32_t* draft_out;        // LM head: argmax per token
   VerifyArgs verify;         // LM head: greedy verification of the drafts by the finishing CTA
   int has_verify;            //   (pe_step); 0: none
+  uint64_t wait_ns;          // limit of every pipeline wait (wait_limit_ns())
+  int drop_stage;            // test of the wait-expiry path: CTA 0 leaves this pipeline stage unarmed (-1: none)
   int32_t* err;
 };
 
@@ -261,6 +270,7 @@ struct AttnArgs {
   int32_t* work_counter;     // items handed out so far (zero before the launch)
   void* out;                 // [rows][n_q*hd]
   int n_rows;                // host upper bound on rows
+  uint64_t wait_ns;          // limit of every pipeline wait (wait_limit_ns())
   int32_t* err;
 };
 constexpr int kAttnRows = 128;    // query rows (row x GQA head) per work item

@@ -15,16 +15,38 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[PE_NOALLOC_SCRATCH_BY
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {nullptr};
+CUcontext g_ctx[kMaxDevices] = {nullptr};  // the context each cached address belongs to
 
-// Device address of the array on the current device (looked up once per device).
+// The calling thread's current context (the driver call found through the runtime, so the
+// library links against the runtime alone); nullptr when none is current.
+CUcontext current_context() {
+  using Fn = CUresult (*)(CUcontext*);
+  static Fn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (Fn) nullptr;
+    return reinterpret_cast<Fn>(p);
+  }();
+  CUcontext c = nullptr;
+  if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Device address of the array on the current device.  Looked up once per device, and again
+// when the device's context is no longer the one the address was taken in (after
+// cudaDeviceReset the array lives at a new address in a new context).
 pe_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PE_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_addr[dev] == nullptr) {
+  const CUcontext ctx = current_context();
+  if (g_addr[dev] == nullptr || ctx == nullptr || ctx != g_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PE_ERR_CUDA;
     g_addr[dev] = p;
+    g_ctx[dev] = current_context();  // the lookup made the device's context current if none was
   }
   *out = g_addr[dev];
   return PE_OK;

@@ -100,11 +100,14 @@ PE_DEV float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// 2^(z2 - m2) of a lane's logits (zero past n)
+// 2^(z2 - m2) of a lane's logits (zero past n).  m2 is the maximum of a range that holds
+// these entries; when it is -inf every entry is -inf (a masked range) and every weight 0
+// (not 2^(-inf + inf), which is NaN).
 PE_DEV Lane16 exp16(const Lane16& x, int v0, int n, float inv_t2, float m2) {
   Lane16 r;
+  const bool empty = m2 == -INFINITY;
 #pragma unroll
-  for (int q = 0; q < kSampPerLane; ++q) r.v[q] = v0 + q < n ? ex2(x.v[q] * inv_t2 - m2) : 0.f;
+  for (int q = 0; q < kSampPerLane; ++q) r.v[q] = v0 + q < n && !empty ? ex2(x.v[q] * inv_t2 - m2) : 0.f;
   return r;
 }
 // max(0, p - q) of a lane's entries (zero past n), q = 2^(z2 - lse2)
@@ -181,11 +184,11 @@ __global__ void __launch_bounds__(kSampAThreads, kSampCtasPerSm) sample_stats_ke
         for (int q = 0; q < kSampPerLane; ++q) {
           if (v0 + q < V) {
             const float z = x[j].v[q] * a.inv_t2;
-            bad |= !isfinite(z);
+            bad |= z != z || z == INFINITY;  // NaN or +inf; a -inf logit is a masked entry
             lm = fmaxf(lm, z);
           }
         }
-        const float m = samp_warp_max(lm);
+        const float m = samp_warp_max(lm);  // -inf: the whole step is masked, its sum 0
         const float sm = samp_warp_sum(sum16(exp16(x[j], v0, V, a.inv_t2, m)));
         if (lane == 0) st[s0 + j] = make_float2(m, sm);
       }
@@ -327,7 +330,7 @@ __global__ void __launch_bounds__(32 * kSampBWarps) sample_draw_kernel(const Sam
   int x = -1;
   if (isfinite(m))
     x = warp_draw(
-        steps, a.u[row], [&](int s) { const float2 v = st[s]; return v.y * ex2(v.x - m); },
+        steps, a.u[row], [&](int s) { const float2 v = st[s]; return v.x == -INFINITY ? 0.f : v.y * ex2(v.x - m); },
         [&](int v0) { return exp16(ld16(l, v0, V, vec), v0, V, a.inv_t2, m); }, &tot);
   if (lane == 0) {
     if (x < 0) {

@@ -116,12 +116,12 @@ def test_step_rejects_overlapping_outputs_before_launch():
     outs = dict(draft_tokens=P(), num_accepted_out=P(), bonus_out=P(), next_prev_tokens=P(), next_prev_pos=P())
     ws, err = P(), P()
 
-    def call(**over):
+    def call(ws=ws, ws_bytes=0, err=err, **over):
         a = {**ins, **outs, **over}
         v = lambda k: ctypes.c_void_p(a[k])
         return L.pe_step(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(kv), v("block_table"), v("prev_tokens"),
                          v("prev_pos"), v("num_accepted"), v("bonus"), v("target_hidden"), v("target_tokens"),
-                         ctypes.c_void_p(ws), ctypes.c_size_t(0), v("draft_tokens"), v("num_accepted_out"),
+                         ctypes.c_void_p(ws), ctypes.c_size_t(ws_bytes), v("draft_tokens"), v("num_accepted_out"),
                          v("bonus_out"), v("next_prev_tokens"), v("next_prev_pos"), ctypes.c_void_p(None),
                          ctypes.c_void_p(err), ctypes.c_void_p(None))
 
@@ -140,3 +140,21 @@ def test_step_rejects_overlapping_outputs_before_launch():
     assert call(draft_tokens=outs["next_prev_tokens"] + 4 * (K + 1) * B - 4) == 1
     # a block table running into the next verify batch
     assert call(next_prev_pos=ins["block_table"] + 4) == 1
+    # the error word inside an output or an input
+    assert call(err=outs["draft_tokens"] + 4) == 1
+    assert call(err=ins["target_tokens"]) == 1
+    # a workspace (of sufficient size) that runs into an input or holds the error word: only the
+    # rejected calls get a usable size, so no call here reaches a launch
+    need = pe.workspace_bytes(cfg)
+    assert need > 0
+    assert call(ws=ins["target_hidden"] - 256, ws_bytes=need) == 1
+    assert call(ws=err - 4096 // 256 * 256, ws_bytes=need) == 1
+
+
+def test_wait_limit_and_stage_hook_host_checks():
+    """The wait limit and the wait-expiry test hook are host settings: no launch, no GPU."""
+    L = pe.lib()
+    assert L.pe_test_skip_pipeline_stage(-2) == 1
+    assert L.pe_test_skip_pipeline_stage(-1) == 0
+    assert L.pe_set_wait_limit_ns(1000) == 0
+    assert L.pe_set_wait_limit_ns(0) == 0

@@ -103,3 +103,11 @@ def test_stage_costs_split_the_round_cost():
             f = sum(v[1] for v in st.values())
             assert b == total["bytes"], (cfg.name, L)
             assert f == total["flops"], (cfg.name, L)
+
+
+def test_both_arms_describe_the_workload_identically():
+    """The reference arm and the GPU arm print the same config object for one workload."""
+    cfg = _tiny()
+    rnd = make_round(cfg)
+    a, b = bench.config_dict(cfg, rnd, 1), bench.config_dict(cfg, make_round(cfg), 1)
+    assert a == b and a["workload"] == cfg.name and a["n_valid_rows"] == int(rnd.num_accepted.sum()) + cfg.B * cfg.K

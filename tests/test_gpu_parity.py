@@ -270,6 +270,87 @@ def test_step_equals_stages_and_next_batch():
         assert np.array_equal(npos[b], c.r_np.prev_pos[b][a] + 1 + np.arange(cfg_np.K + 1))
 
 
+# ----------------------------------------------------------------------------- the timed path at full size
+
+def _sampled_seqs(r_np):
+    """Sequences the oracle checks at B > 8: the shortest and longest prefix, two fully rejected
+    ones where present, and the one with the most accepted drafts."""
+    if len(r_np.prefix_len) <= 8:
+        return list(range(len(r_np.prefix_len)))
+    P, a = r_np.prefix_len, r_np.num_accepted
+    return sorted({int(np.argmin(P)), int(np.argmax(P)), int(np.argmax(a))} | set(np.nonzero(a == 0)[0][:2].tolist()))
+
+
+@pytest.mark.parametrize("which", ["c1", "c2", "c3", "sweep-B64-K8"])
+def test_step_graph_full_size(which):
+    """The path the benchmark times: pe_step without debug logits, captured once in a CUDA graph
+    and replayed, at full size.  Drafts agree with the oracle on the checked sequences (exactly
+    where the oracle's top-1/top-2 gap is clear, otherwise the picked token's oracle logit is
+    within twice the tolerance of the top one); accepted counts, bonus tokens and the next
+    verify batch are bit-exact for every sequence; the KV entries the checked sequences write
+    match the oracle's post-RoPE k / v, and no other cache entry changes; two more replays give
+    bit-identical drafts and outputs."""
+    cfg_np = {"c1": config(1), "c2": config(2), "c3": config(3), "sweep-B64-K8": sweep_config(64, 8)}[which]
+    c = setup(cfg_np)
+    B, K, L = cfg_np.B, cfg_np.K, cfg_np.n_layers
+    R = c.Rd
+    target = torch.zeros((B, K + 1), dtype=torch.int32, device="cuda")
+    step = lambda: c.rd.step(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"], R["target_hidden"],
+                             target)
+    step()                                  # launch attributes are set on each kernel's first use
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(c.rd.err.item()) == 0
+    drafts = c.rd.draft_tokens.cpu().numpy()
+    tgt = make_targets(drafts, c.r_np.target_u, c.r_np.target_r)
+    target.copy_(torch.from_numpy(tgt))
+    outs = []
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(c.rd.err.item()) == 0
+        outs.append({k: v.cpu().numpy().copy() for k, v in c.rd.out.items()})
+    for k in outs[0]:
+        assert np.array_equal(outs[0][k], outs[1][k]), k
+    out = outs[0]
+    assert np.array_equal(out["draft_tokens"], drafts)
+    # verification and the next verify batch, for every sequence, on the GPU's own drafts
+    acc, bon = oracle.verify(drafts, tgt)
+    assert np.array_equal(out["num_accepted"], acc) and np.array_equal(out["bonus"], bon)
+    nt, npos = oracle.next_verify_batch(c.r_np.prev_pos, c.r_np.num_accepted, c.r_np.bonus, drafts)
+    assert np.array_equal(out["next_prev_tokens"], nt) and np.array_equal(out["next_prev_pos"], npos)
+    # drafts of the checked sequences against the oracle
+    seqs = _sampled_seqs(c.r_np)
+    ref = oracle_round(c, seqs=seqs, want_kv=True)
+    tol = LOGIT_TOL[cfg_np.dtype]
+    lg = ref["logits"].reshape(len(seqs), K, -1)
+    got = drafts[seqs]
+    picked = np.take_along_axis(lg, got[..., None].astype(np.int64), axis=2)[..., 0]
+    assert (picked >= lg.max(axis=2) - 2 * tol).all()
+    sure = (oracle.top2_gap(ref["logits"]) > GAP).reshape(len(seqs), K)
+    assert sure.any()
+    assert np.array_equal(got[sure], ref["drafts"][sure])
+    # cache: the checked sequences' entries, then no entry outside the round's slots changed
+    meta = ref["meta"]
+    kvd = cfg_np.n_kv * cfg_np.head_dim
+    slots_all = torch.from_numpy(meta["slot_mapping"][meta["row_list"]]).cuda()
+    slots_chk = meta["slot_mapping"][ref["rows"]]
+    for l in range(L):
+        for nm, dev, before, new in (("k", c.kv.k_cache[l], c.k_before[l], ref["new_k"][l]),
+                                     ("v", c.kv.v_cache[l], c.v_before[l], ref["new_v"][l])):
+            a2, b2 = dev.view(-1, kvd), before.view(-1, kvd)
+            changed = (a2 != b2).any(dim=1)
+            changed[slots_all] = False
+            assert int(changed.sum().item()) == 0, f"{nm} cache layer {l}: stray write"
+            gotv = a2[torch.from_numpy(slots_chk).cuda()].float().cpu().numpy().astype(np.float64)
+            diff = np.abs(gotv - new) / np.maximum(1.0, np.abs(new))
+            assert diff.max() <= KV_TOL[cfg_np.dtype], f"{nm} cache layer {l}: rel diff {diff.max():.3g}"
+
+
 # ----------------------------------------------------------------------------- rounds back to back
 
 @pytest.mark.parametrize("name", ["f32-L2", "bf16-hd64", "bf16-L2-long"])

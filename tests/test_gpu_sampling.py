@@ -88,6 +88,56 @@ def test_sample_drafts_frequencies():
     assert np.abs(freq - q).max() <= 1.0 / N + CDF_EPS
 
 
+@pytest.mark.parametrize("V", [2048, 4099])
+def test_sample_drafts_masked_logits(V):
+    """-inf logits are masked entries: probability 0, never drawn, no error.  Rows with a whole
+    512-entry step masked, a partial step masked, all but three entries masked, and none."""
+    B, K = 2, 2
+    rng, logits = _seeded(B, K, V, seed=V)
+    logits[0, 512:1024] = -np.inf                   # a whole step
+    logits[1, 100:300] = -np.inf                    # part of a step
+    keep = [7, 1500, V - 1]
+    row2 = np.full(V, -np.inf, np.float32)
+    row2[keep] = logits[2, keep]
+    logits[2] = row2                                # every step but three entries masked
+    u = rng.random((B, K)).astype(np.float32).astype(np.float64)
+    _, drafts, lse = _gpu_sample(_cfg(B, K, V), logits, u, 1.0)
+    g = drafts.cpu().numpy().reshape(-1)
+    want, want_lse = oracle.sample_drafts(logits, u, 1.0)
+    gl = lse.cpu().numpy()
+    assert np.isfinite(gl).all()
+    assert np.abs(gl - want_lse.reshape(-1)).max() <= 1e-4 * max(1.0, np.abs(want_lse).max())
+    for r in range(B * K):
+        assert np.isfinite(logits[r, g[r]]), r
+        if g[r] != want.reshape(-1)[r]:
+            q, _ = oracle.drafter_distribution(logits[r], 1.0)
+            assert _in_band(q, int(g[r]), u.reshape(-1)[r], CDF_EPS), r
+    assert g[2] in keep
+
+
+def test_sample_drafts_fully_masked_row_is_flagged():
+    """A row whose every logit is -inf has no distribution: token 0, lse NaN, PE_DEV_NONFINITE;
+    the other rows draw normally."""
+    B, K, V = 1, 2, 1000
+    rng, logits = _seeded(B, K, V, seed=5)
+    logits[1] = -np.inf
+    u = rng.random((B, K))
+    cfg = _cfg(B, K, V)
+    lg = torch.from_numpy(logits).cuda()
+    drafts = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    lse = torch.empty(B * K, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pe.sample_drafts(cfg, lg, torch.from_numpy(u.astype(np.float32)).cuda(), 1.0, pe.alloc_workspace(cfg), drafts,
+                     lse, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pe.PE_DEV_NONFINITE
+    g, gl = drafts.cpu().numpy().reshape(-1), lse.cpu().numpy()
+    assert g[1] == 0 and np.isnan(gl[1])
+    q, want_lse = oracle.drafter_distribution(logits[0], 1.0)
+    assert abs(gl[0] - want_lse) <= 1e-4 * max(1.0, abs(want_lse))
+    assert q[g[0]] > 0
+
+
 def _targets(rng, drafts, B, K, V, boost=3.0):
     """Seeded target distributions: normalised exp of N(0, 2) draws, with the draft token
     raised at about 60 % of positions so that drafts get accepted."""
