@@ -64,6 +64,20 @@ int num_sms() {
   return cached[dev];
 }
 
+// Clusters of two GEMM CTAs (about 200 KB of shared memory each, one per SM) that fit on
+// the GPU at once: fewer than half the SMs when a GPU processing cluster has an odd number
+// of SMs.  Without a device (host-only use of the plan): half the SMs.
+int max_pairs(int sms) {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return sms / 2;
+  if (cached[dev] == 0) {
+    const int n = gemm_tc_max_pairs(EPI_ADD_F32, (size_t)kTcSmemOptIn);
+    cached[dev] = n > 0 ? std::min(n, sms / 2) : sms / 2;
+  }
+  return cached[dev];
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 size_t elem_bytes(pe_dtype dt) { return dt == PE_BF16 ? 2 : 4; }
@@ -73,6 +87,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct GemmPlan {
   int epi = 0, bn = 16, n_t = 1, n_f = 1, k_splits = 1, kb_total = 1, stages = 2, grid = 1;
+  int cg = 1;  // CTAs per MMA: 2 = CTA pairs (M = 256), each taking in half the token operand
   int nbuf = 1, acc_stride = 16;
   int balanced = 0;
   int ka = 1;  // 64-wide k atoms per stage
@@ -86,27 +101,40 @@ struct GemmPlan {
 // With fewer tiles than SMs, split K so that nearly every SM streams weights:
 // every CTA owns exactly one unit and leaves an fp32 partial tile for the
 // consumer to sum; each split keeps at least four 64-wide k blocks.
-GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
+//
+// Many token rows (more than one 256-row tile), or an LM head whose token tile is at
+// least 128 rows: CTA pairs (cg = 2).  The GEMM is then bound by how fast each SM takes
+// in its operands (measured: about 95 GB/s per SM from L2 with 32 KB boxes), not by the
+// tensor pipe: a pair's MMA of 256 weight rows has each CTA take in 128 weight rows and
+// half of the token tile, a quarter less per flop at 128 tokens than one CTA's 128 x 128
+// tile.  Layer GEMMs then use 128-token tiles (64 rows per CTA), which keeps enough units
+// to fill the GPU at B = 64.  `max_pairs`: clusters of two that fit on the GPU at once.
+GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms, int max_pairs) {
   GemmPlan g;
   g.epi = epi;
   const bool paired = (epi == EPI_SWIGLU || epi == EPI_QKV_ROPE);
   if (n_tok <= 256 || epi == EPI_ARGMAX) {  // one token tile, or the LM head (vocabulary tiles are plenty)
     g.n_t = (n_tok + 255) / 256;
     g.bn = round_up((n_tok + g.n_t - 1) / g.n_t, 16);
+    g.cg = (epi == EPI_ARGMAX && g.bn >= 128) ? 2 : 1;
   } else {  // many rows: 128-row token tiles give enough units to fill the GPU without split K
     g.bn = 128;
     g.n_t = (n_tok + g.bn - 1) / g.bn;
+    g.cg = 2;
   }
+  const int slots = g.cg == 2 ? std::max(1, max_pairs) : sms;  // units that run at once
   g.n_f = n_f_tiles;
   g.tiles = g.n_f * g.n_t;
+  const int unit_tiles = ((g.n_f + g.cg - 1) / g.cg) * g.n_t;  // work units per k split
   // epilogue scratch after the ring, in 8-byte words: the LM head's per-warp keys, or the
   // QKV epilogue's token positions and slots (two buffers of bn x 12 bytes)
   const int red = epi == EPI_ARGMAX ? 4 * g.n_t * g.bn : (epi == EPI_QKV_ROPE ? 3 * g.bn : 0);
   const long long avail = kTcSmemOptIn - 1024 - kTcCtrlBytes - (long long)red * 8;
   // Two k atoms per stage (one TMA box of both per operand: half the boxes per byte, half
   // the barrier round trips per MMA) while the ring still holds kMinStagesKa2 stages.
+  const int bnl = g.bn / g.cg;  // token rows a CTA loads
   auto stage_bytes = [&](int ka) {
-    return (uint32_t)ka * ((paired ? 2u : 1u) * kTcBM * kTcBK * 2 + (uint32_t)g.bn * kTcBK * 2);
+    return (uint32_t)ka * ((paired ? 2u : 1u) * kTcBM * kTcBK * 2 + (uint32_t)bnl * kTcBK * 2);
   };
   g.ka = avail / stage_bytes(2) >= kMinStagesKa2 ? 2 : 1;
   const int atoms = (k_dim + kTcBK - 1) / kTcBK;
@@ -114,14 +142,15 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   g.stage_bytes = stage_bytes(g.ka);
   g.stages = (int)std::min<long long>(kTcMaxStages, avail / g.stage_bytes);
   g.smem = gemm_tc_smem_bytes(g.stages, g.stage_bytes, red);
-  if (epi != EPI_ARGMAX && g.tiles < sms)
-    g.k_splits = std::max(1, std::min(kMaxSplits, std::min(sms / g.tiles, g.kb_total * g.ka / 4)));
+  if (epi != EPI_ARGMAX && unit_tiles < slots)
+    g.k_splits = std::max(1, std::min(kMaxSplits, std::min(slots / unit_tiles, g.kb_total * g.ka / 4)));
   const int acc_cols = (paired ? 2 : 1) * g.bn;
   g.nbuf = 2 * acc_cols <= 512 ? 2 : 1;
   g.acc_stride = acc_cols;
   const int need = g.nbuf * acc_cols;
   g.tmem_cols = need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
-  g.grid = g.k_splits > 1 ? g.tiles * g.k_splits : std::min(g.tiles, sms);
+  const int units = unit_tiles * g.k_splits;
+  g.grid = g.cg * (g.k_splits > 1 ? units : std::min(units, slots));
   // LM head with one token tile: equal k-block ranges per CTA when the last wave of
   // vocabulary tiles is at most three quarters full (a range then spans more than a
   // tile).  One SM streams at most about 53 GB/s (measured), little above its
@@ -129,7 +158,8 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms) {
   // the HBM rate; a nearly full last wave costs less than exchanging the partial
   // sums of the cut tiles.
   const int last_wave = g.tiles % sms;
-  if (epi == EPI_ARGMAX && g.n_t == 1 && g.tiles > sms && last_wave != 0 && 4 * last_wave <= 3 * sms) g.balanced = 1;
+  if (epi == EPI_ARGMAX && g.cg == 1 && g.n_t == 1 && g.tiles > sms && last_wave != 0 && 4 * last_wave <= 3 * sms)
+    g.balanced = 1;
   return g;
 }
 
@@ -153,12 +183,13 @@ Plan make_plan(const pe_config& c) {
   const int half = c.head_dim / 2;
   const int heads = c.n_q + 2 * c.n_kv;
   const int hpt = kTcBM / half;
-  p.fc = plan_gemm(EPI_STORE_F32, (c.d + kTcBM - 1) / kTcBM, p.R, 2 * c.d, p.sms);
-  p.qkv = plan_gemm(EPI_QKV_ROPE, (heads + hpt - 1) / hpt, p.R, c.d, p.sms);
-  p.o = plan_gemm(EPI_ADD_F32, (c.d + kTcBM - 1) / kTcBM, p.R, c.n_q * c.head_dim, p.sms);
-  p.gu = plan_gemm(EPI_SWIGLU, (c.ffn + kTcBM - 1) / kTcBM, p.R, c.d, p.sms);
-  p.down = plan_gemm(EPI_ADD_F32, (c.d + kTcBM - 1) / kTcBM, p.R, c.ffn, p.sms);
-  p.lm = plan_gemm(EPI_ARGMAX, (c.vocab + kTcBM - 1) / kTcBM, p.T, c.d, p.sms);
+  const int mp = c.dtype == PE_BF16 ? max_pairs(p.sms) : 0;
+  p.fc = plan_gemm(EPI_STORE_F32, (c.d + kTcBM - 1) / kTcBM, p.R, 2 * c.d, p.sms, mp);
+  p.qkv = plan_gemm(EPI_QKV_ROPE, (heads + hpt - 1) / hpt, p.R, c.d, p.sms, mp);
+  p.o = plan_gemm(EPI_ADD_F32, (c.d + kTcBM - 1) / kTcBM, p.R, c.n_q * c.head_dim, p.sms, mp);
+  p.gu = plan_gemm(EPI_SWIGLU, (c.ffn + kTcBM - 1) / kTcBM, p.R, c.d, p.sms, mp);
+  p.down = plan_gemm(EPI_ADD_F32, (c.d + kTcBM - 1) / kTcBM, p.R, c.ffn, p.sms, mp);
+  p.lm = plan_gemm(EPI_ARGMAX, (c.vocab + kTcBM - 1) / kTcBM, p.T, c.d, p.sms, mp);
   // attention items: the work list aims at attn_target items; rounding adds at
   // most one per (sequence, kv head), and no (sequence, kv head) can have more
   // chunks than its longest possible range holds minimum chunks
@@ -196,11 +227,11 @@ Plan make_plan(const pe_config& c) {
   p.ao = take(eb * (size_t)p.R * c.n_q * c.head_dim);
   p.u = take(eb * (size_t)p.R * c.ffn);
   p.yl = take(eb * (size_t)p.T * c.d);
-  size_t split_bytes = 0;  // fp32 partial tiles of the largest split-K launch
+  size_t split_bytes = 0;  // fp32 partial tiles of the largest split-K launch (one per unit)
   for (const GemmPlan* g : {&p.fc, &p.qkv, &p.o, &p.gu, &p.down})
     if (g->k_splits > 1) {
       const bool paired = g->epi == EPI_SWIGLU || g->epi == EPI_QKV_ROPE;
-      split_bytes = std::max(split_bytes, (size_t)g->grid * (paired ? 2 : 1) * g->bn * kTcBM * 4);
+      split_bytes = std::max(split_bytes, (size_t)g->n_f * g->n_t * g->k_splits * (paired ? 2 : 1) * g->bn * kTcBM * 4);
     }
   if (p.lm.balanced) split_bytes = std::max(split_bytes, (size_t)p.lm.grid * 2 * p.lm.bn * kTcBM * 4);
   p.split_part = c.dtype == PE_BF16 && split_bytes > 0 ? take(split_bytes) : 0;
@@ -391,9 +422,9 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   else if (call.w_kind == 2)
     ok = tmap_qkv(&tw, call.W, (uint64_t)(c.n_q + 2 * c.n_kv), (uint64_t)c.head_dim, (uint64_t)c.d, g.ka);
   else ok = tmap_matrix(&tw, call.W, call.w_rows, (uint64_t)call.k_dim, (uint32_t)kTcBM, g.ka);
-  ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)g.bn, g.ka);
+  ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)(g.bn / g.cg), g.ka);
   if (!ok) return PE_ERR_CUDA;
-  PE_TRY_CUDA(launch_gemm_tc(g.balanced ? EPI_ARGMAX_BAL : call.epi, tw, tx, a, g.grid, g.smem, s));
+  PE_TRY_CUDA(launch_gemm_tc(g.balanced ? EPI_ARGMAX_BAL : call.epi, g.cg, tw, tx, a, g.grid, g.smem, s));
   if (g.k_splits > 1 && (call.epi == EPI_QKV_ROPE || call.epi == EPI_SWIGLU))
     PE_TRY_CUDA(launch_splitk_finish(call.epi, a, p.sms, s));
   return PE_OK;

@@ -231,7 +231,9 @@ PE_DEV Unit decode_unit(const GemmArgs& a, int u, int n_t_live) {
   return w;
 }
 
-// A CTA's work.  Default: units blockIdx.x, blockIdx.x + gridDim.x, ...
+// A CTA's work.  Default: units blockIdx.x, blockIdx.x + gridDim.x, ...; a CTA pair
+// (CG = 2) takes units p, p + pairs, ... with p = blockIdx.x / 2, a unit's weight tile
+// then being 256 rows (1-CTA tiles 2 * tile_f and 2 * tile_f + 1, one per CTA).
 // Balanced LM head (EPI_ARGMAX_BAL: one token tile, more vocabulary tiles than
 // CTAs): the n_f * kb_total k blocks, tile after tile, are cut into gridDim.x
 // contiguous ranges of equal length, so every CTA streams the same number of
@@ -242,7 +244,7 @@ struct Sched {
   int cur, end;
 };
 
-template <int EPI>
+template <int EPI, int CG>
 PE_DEV Sched sched_begin(const GemmArgs& a, int n_t_live) {
   Sched sc;
   if (EPI == EPI_ARGMAX_BAL) {
@@ -250,13 +252,13 @@ PE_DEV Sched sched_begin(const GemmArgs& a, int n_t_live) {
     sc.cur = (int)(W * blockIdx.x / gridDim.x);
     sc.end = (int)(W * (blockIdx.x + 1) / gridDim.x);
   } else {
-    sc.cur = blockIdx.x;
-    sc.end = n_t_live * a.n_f * a.k_splits;
+    sc.cur = blockIdx.x / CG;
+    sc.end = n_t_live * ((a.n_f + CG - 1) / CG) * a.k_splits;
   }
   return sc;
 }
 
-template <int EPI>
+template <int EPI, int CG>
 PE_DEV bool sched_next(const GemmArgs& a, Sched& sc, int n_t_live, Unit& w) {
   if (sc.cur >= sc.end) return false;
   if (EPI == EPI_ARGMAX_BAL) {
@@ -272,7 +274,7 @@ PE_DEV bool sched_next(const GemmArgs& a, Sched& sc, int n_t_live, Unit& w) {
     sc.cur += w.kb1 - w.kb0;
   } else {
     w = decode_unit(a, sc.cur, n_t_live);
-    sc.cur += gridDim.x;
+    sc.cur += gridDim.x / CG;
   }
   return true;
 }
@@ -284,16 +286,20 @@ PE_DEV bool sched_next(const GemmArgs& a, Sched& sc, int n_t_live, Unit& w) {
 // 46 GB/s with 16 KB boxes, 95 GB/s with 32 KB boxes).
 // Paired operands (gate/up, the heads' first/second halves) come in the same box and
 // land per atom as two consecutive 128-row tiles: [ka][2][128][64].
-template <int EPI>
+// CG = 2: the copy completes on the leader CTA's barrier (fb is a cluster address).
+template <int EPI, int CG>
 PE_DEV void issue_w(const CUtensorMap* tmW, const GemmArgs& a, uint32_t sa, uint32_t fb, int ka0, int tile_f,
                     uint64_t pol) {
   if (EPI == EPI_SWIGLU) {  // W viewed as [K/64][2][F][64]
-    tma_load_4d(sa, tmW, fb, 0, tile_f * kTcBM, 0, ka0, pol);
+    if (CG == 2) tma_load_4d_pair(sa, tmW, fb, 0, tile_f * kTcBM, 0, ka0, pol);
+    else tma_load_4d(sa, tmW, fb, 0, tile_f * kTcBM, 0, ka0, pol);
   } else if (EPI == EPI_QKV_ROPE) {  // W viewed as [K/64][2][heads][hd/2][64]
     const int hpt = kTcBM / (a.head_dim >> 1);
-    tma_load_5d(sa, tmW, fb, 0, 0, tile_f * hpt, 0, ka0, pol);
+    if (CG == 2) tma_load_5d_pair(sa, tmW, fb, 0, 0, tile_f * hpt, 0, ka0, pol);
+    else tma_load_5d(sa, tmW, fb, 0, 0, tile_f * hpt, 0, ka0, pol);
   } else {
-    tma_load_3d(sa, tmW, fb, 0, tile_f * kTcBM, ka0, pol);
+    if (CG == 2) tma_load_3d_pair(sa, tmW, fb, 0, tile_f * kTcBM, ka0, pol);
+    else tma_load_3d(sa, tmW, fb, 0, tile_f * kTcBM, ka0, pol);
   }
 }
 
@@ -391,20 +397,32 @@ PE_DEV void argmax_piece(const GemmArgs& a, const Unit& w, uint32_t tl, int unit
   if (lane == 0) *cnt = 0;
 }
 
-template <int EPI>
+// CG = 2 (a CTA pair per unit, M = 256): the weight tile of a unit is 256 rows, 128 per
+// CTA, and its BN token columns are split in halves, BN / 2 rows loaded by each CTA; the
+// leader (rank 0) issues every MMA, whose D rows land in the tensor memory of the CTA that
+// holds them, so each CTA's epilogue handles its own 128 weight rows over all BN tokens.
+// Each CTA takes in half the token operand per unit that a single CTA does.  Both CTAs'
+// copies of a stage complete on the leader's barrier (armed for both); the leader's commits
+// free the stage and publish the accumulator in both CTAs; the epilogue warps of both
+// return an accumulator to the leader.
+template <int EPI, int CG>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmArgs a) {
   constexpr bool PAIRED = (EPI == EPI_SWIGLU || EPI == EPI_QKV_ROPE);
   constexpr bool ARGMAX = (EPI == EPI_ARGMAX || EPI == EPI_ARGMAX_BAL);
   constexpr bool BAL = (EPI == EPI_ARGMAX_BAL);
+  static_assert(CG == 1 || (CG == 2 && !BAL), "CTA pairs: every epilogue but the balanced LM head");
   constexpr uint32_t A_ATOM = kTcBM * kTcBK * 2;  // one 64-wide k atom of 128 weight rows
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int BN = a.bn;
-  const int U = a.n_t * a.n_f * a.k_splits;  // units of the largest row count
+  const int BN = a.bn;         // MMA N: token columns of a unit
+  const int BNL = BN / CG;     // token rows this CTA loads per unit
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int U = a.n_t * ((a.n_f + CG - 1) / CG) * a.k_splits;  // units of the largest row count
   const int S = a.stages;
   const int NT = a.n_t * BN;  // argmax keys per warp
   uint8_t* ctrl = smem + (size_t)S * a.stage_bytes;
@@ -427,7 +445,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(tfull + b), 1);
-      mbar_init(smem_u32(tempty + b), 4);  // one arrival per epilogue warp
+      mbar_init(smem_u32(tempty + b), 4 * CG);  // one arrival per epilogue warp (of both CTAs)
     }
 
     *abort_flag = 0;
@@ -437,13 +455,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (ARGMAX)
     for (int j = threadIdx.x; j < 4 * NT; j += blockDim.x) red[j] = 0ull;
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
-    tmem_relinquish();
+    if (CG == 2) {
+      tmem_alloc_cg2(smem_u32(tmem_slot), a.tmem_cols);
+      tmem_relinquish_cg2();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
+      tmem_relinquish();
+    }
     tc_fence_before();
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (CG == 2) cluster_sync();  // both CTAs' barriers are initialised before any arrival crosses over
   pdl_trigger();
   int issued = 0;  // k-block stages the producer issued (its drain after an abort)
 
@@ -456,27 +480,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t pol_x = l2_policy_evict_last();   // activations: re-read by every weight tile
     // wait-expiry test: CTA 0 never arms this stage, so the MMA warp's wait on it runs out
     const int drop = blockIdx.x == 0 ? a.drop_stage : -1;
+    const uint32_t tx = (uint32_t)CG * a.stage_bytes;  // the leader's barrier counts both CTAs' copies
+    auto fbar = [&](int st) { return CG == 2 ? mapa_shared(smem_u32(full + st), 0) : smem_u32(full + st); };
     // the weights do not depend on earlier kernels: start the first stages now
     int npre = 0;
     if (BAL) {  // the first S k blocks of the range, across pieces
-      Sched s0 = sched_begin<EPI>(a, 1);
+      Sched s0 = sched_begin<EPI, CG>(a, 1);
       Unit w;
-      while (npre < S && sched_next<EPI>(a, s0, 1, w))
+      while (npre < S && sched_next<EPI, CG>(a, s0, 1, w))
         for (int kb = w.kb0; kb < w.kb1 && npre < S; ++kb, ++npre)
           if (npre != drop && elect_one()) {
             const uint32_t sa = smem_u32(smem + (size_t)npre * a.stage_bytes);
             mbar_expect_tx(smem_u32(full + npre), a.stage_bytes);
-            issue_w<EPI>(&tmW, a, sa, smem_u32(full + npre), kb * a.ka, w.tile_f, pol_w);
+            issue_w<EPI, CG>(&tmW, a, sa, smem_u32(full + npre), kb * a.ka, w.tile_f, pol_w);
           }
-    } else if (a.n_t == 1 && (int)blockIdx.x < U) {  // unit numbering does not depend on the row count
-      const Unit w = decode_unit(a, blockIdx.x, 1);
+    } else if (a.n_t == 1 && (int)blockIdx.x / CG < U) {  // unit numbering does not depend on the row count
+      const Unit w = decode_unit(a, (int)blockIdx.x / CG, 1);
       npre = min(S, w.kb1 - w.kb0);
       if (elect_one())
         for (int i = 0; i < npre; ++i) {
           if (i == drop) continue;
           const uint32_t sa = smem_u32(smem + (size_t)i * a.stage_bytes);
-          mbar_expect_tx(smem_u32(full + i), a.stage_bytes);
-          issue_w<EPI>(&tmW, a, sa, smem_u32(full + i), (w.kb0 + i) * a.ka, w.tile_f, pol_w);
+          if (leader) mbar_expect_tx(smem_u32(full + i), tx);
+          issue_w<EPI, CG>(&tmW, a, sa, fbar(i), (w.kb0 + i) * a.ka, CG * w.tile_f + (int)rank, pol_w);
         }
     }
     __syncwarp();
@@ -486,12 +512,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int it = 0, s = 0;
     uint32_t ph = 0;  // (it / S) & 1
     bool stop = false;
-    Sched sc = sched_begin<EPI>(a, ntl);
+    Sched sc = sched_begin<EPI, CG>(a, ntl);
     Unit w;
-    while (!stop && sched_next<EPI>(a, sc, ntl, w)) {
+    while (!stop && sched_next<EPI, CG>(a, sc, ntl, w)) {
       for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
         const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
-        const uint32_t fb = smem_u32(full + s);
         if (it >= npre && it >= S) {
           const bool ok = mbar_wait(smem_u32(empty + s), ph ^ 1u, a.err, abort_flag, a.wait_ns);
           if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
@@ -500,11 +525,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (it != drop && elect_one()) {
+          const uint32_t fb = fbar(s);
           if (it >= npre) {
-            mbar_expect_tx(fb, a.stage_bytes);
-            issue_w<EPI>(&tmW, a, sa, fb, kb * a.ka, w.tile_f, pol_w);
+            if (leader) mbar_expect_tx(smem_u32(full + s), tx);
+            issue_w<EPI, CG>(&tmW, a, sa, fb, kb * a.ka, CG * w.tile_f + (int)rank, pol_w);
           }
-          tma_load_3d(sa + b_off, &tmX, fb, 0, w.tile_t * BN, kb * a.ka, pol_x);
+          if (CG == 2)
+            tma_load_3d_pair(sa + b_off, &tmX, fb, 0, w.tile_t * BN + (int)rank * BNL, kb * a.ka, pol_x);
+          else
+            tma_load_3d(sa + b_off, &tmX, fb, 0, w.tile_t * BN, kb * a.ka, pol_x);
         }
         __syncwarp();
         if (++s == S) {
@@ -515,69 +544,80 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     issued = it;
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ MMA issuer (the leader of a pair)
     // Converged warp; the elected lane issues every MMA and commit.
-    pdl_wait();
-    const int n_tok = effective_ntok(a);
-    const int ntl = live_token_tiles(a, n_tok);
-    const uint32_t idesc = idesc_bf16(kTcBM, BN);
-    int i = 0, s = 0;
-    uint32_t ph = 0;  // (it / S) & 1 over this CTA's k blocks
-    bool stop = false;
-    Sched sc = sched_begin<EPI>(a, ntl);
-    Unit w;
-    while (!stop && sched_next<EPI>(a, sc, ntl, w)) {
-      const int buf = i % a.nbuf;
-      if (i >= a.nbuf) {
-        const bool ok =
-            mbar_wait(smem_u32(tempty + buf), (uint32_t)((i / a.nbuf) - 1) & 1u, a.err, abort_flag, a.wait_ns);
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
-          stop = true;
-          break;
-        }
-      }
-      tc_fence_after();
-      const uint32_t d = tmem + (uint32_t)(buf * a.acc_stride);
-      for (int kb = w.kb0; kb < w.kb1; ++kb) {
-        const bool ok = mbar_wait(smem_u32(full + s), ph, a.err, abort_flag, a.wait_ns);
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
-          stop = true;
-          break;
+    if (CG == 1 || leader) {
+      pdl_wait();
+      const int n_tok = effective_ntok(a);
+      const int ntl = live_token_tiles(a, n_tok);
+      const uint32_t idesc = idesc_bf16(kTcBM * CG, BN);
+      int i = 0, s = 0;
+      uint32_t ph = 0;  // (it / S) & 1 over this CTA's k blocks
+      bool stop = false;
+      Sched sc = sched_begin<EPI, CG>(a, ntl);
+      Unit w;
+      while (!stop && sched_next<EPI, CG>(a, sc, ntl, w)) {
+        const int buf = i % a.nbuf;
+        if (i >= a.nbuf) {
+          const bool ok =
+              mbar_wait(smem_u32(tempty + buf), (uint32_t)((i / a.nbuf) - 1) & 1u, a.err, abort_flag, a.wait_ns);
+          if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+            stop = true;
+            break;
+          }
         }
         tc_fence_after();
-        if (elect_one()) {
-          const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
+        const uint32_t d = tmem + (uint32_t)(buf * a.acc_stride);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          const bool ok = mbar_wait(smem_u32(full + s), ph, a.err, abort_flag, a.wait_ns);
+          if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t sa = smem_u32(smem + (size_t)s * a.stage_bytes);
 #pragma unroll
-          for (int at = 0; at < 2; ++at) {  // the stage's k atoms (a.ka of them)
-            if (at < a.ka) {
-              const uint64_t da = sdesc_k_sw128(sa + (uint32_t)(PAIRED ? 2 * at : at) * A_ATOM);
-              const uint64_t da2 = sdesc_k_sw128(sa + (uint32_t)(2 * at + 1) * A_ATOM);
-              const uint64_t db = sdesc_k_sw128(sa + b_off + (uint32_t)(at * BN * kTcBK * 2));
+            for (int at = 0; at < 2; ++at) {  // the stage's k atoms (a.ka of them)
+              if (at < a.ka) {
+                const uint64_t da = sdesc_k_sw128(sa + (uint32_t)(PAIRED ? 2 * at : at) * A_ATOM);
+                const uint64_t da2 = sdesc_k_sw128(sa + (uint32_t)(2 * at + 1) * A_ATOM);
+                const uint64_t db = sdesc_k_sw128(sa + b_off + (uint32_t)(at * BNL * kTcBK * 2));
 #pragma unroll
-              for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                const uint32_t accum = (kb > w.kb0 || at > 0 || kk > 0) ? 1u : 0u;
-                tc_mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accum);
-                if (PAIRED) tc_mma_bf16(d + (uint32_t)BN, da2 + 2 * kk, db + 2 * kk, idesc, accum);
+                for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                  const uint32_t accum = (kb > w.kb0 || at > 0 || kk > 0) ? 1u : 0u;
+                  if (CG == 2) {
+                    tc_mma_bf16_pair(d, da + 2 * kk, db + 2 * kk, idesc, accum);
+                    if (PAIRED) tc_mma_bf16_pair(d + (uint32_t)BN, da2 + 2 * kk, db + 2 * kk, idesc, accum);
+                  } else {
+                    tc_mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accum);
+                    if (PAIRED) tc_mma_bf16(d + (uint32_t)BN, da2 + 2 * kk, db + 2 * kk, idesc, accum);
+                  }
+                }
               }
             }
+            if (CG == 2) tc_commit_pair(smem_u32(empty + s));
+            else tc_commit(smem_u32(empty + s));
           }
-          tc_commit(smem_u32(empty + s));
+          __syncwarp();
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (elect_one()) {
+          if (CG == 2) tc_commit_pair(smem_u32(tfull + buf));
+          else tc_commit(smem_u32(tfull + buf));
         }
         __syncwarp();
-        if (++s == S) {
-          s = 0;
-          ph ^= 1u;
-        }
+        ++i;
       }
-      if (elect_one()) tc_commit(smem_u32(tfull + buf));
-      __syncwarp();
-      ++i;
-    }
-    // After a wait gave up: every MMA issued so far completes before the tensor memory is
-    // freed (the last commit tracks all of them).
-    if (stop && i > 0) {
-      const int lb = (i - 1) % a.nbuf;
-      mbar_wait(smem_u32(tfull + lb), (uint32_t)((i - 1) / a.nbuf) & 1u, a.err, nullptr, a.wait_ns);
+      // After a wait gave up: every MMA issued so far completes before the tensor memory is
+      // freed (the last commit tracks all of them).
+      if (stop && i > 0) {
+        const int lb = (i - 1) % a.nbuf;
+        mbar_wait(smem_u32(tfull + lb), (uint32_t)((i - 1) / a.nbuf) & 1u, a.err, nullptr, a.wait_ns);
+      }
     }
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2..5)
@@ -588,15 +628,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned long long* red_w = red + (size_t)(warp - 2) * NT;
     const int ntl = live_token_tiles(a, n_tok);
     int i = 0;
-    Sched sc = sched_begin<EPI>(a, ntl);
+    Sched sc = sched_begin<EPI, CG>(a, ntl);
     Unit w;
-    while (sched_next<EPI>(a, sc, ntl, w)) {
+    while (sched_next<EPI, CG>(a, sc, ntl, w)) {
       const int buf = i % a.nbuf;
       // after an abort the accumulator may be incomplete: skip its epilogue
       const bool ok =
           mbar_wait(smem_u32(tfull + buf), (uint32_t)(i / a.nbuf) & 1u, a.err, abort_flag, a.wait_ns) && !*abort_flag;
       tc_fence_after();
-      const int unit = w.tile_f * kTcBM + r;
+      const int tf = CG * w.tile_f + (int)rank;  // this CTA's 128-row weight tile
+      const int unit = tf * kTcBM + r;
       const uint32_t tl = tmem + (uint32_t)(buf * a.acc_stride) + ((uint32_t)(q * 32) << 16);
       const int tbase = w.tile_t * BN;
       // QKV: the tile's token positions and KV slots, loaded once per unit by the four
@@ -618,7 +659,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (BAL && ok && w.bnd >= 0) {
         argmax_piece(a, w, tl, unit, n_tok, red_w, r, lane);
       } else if (ok && a.k_splits == 1) {
-        const float2 tf = (EPI == EPI_QKV_ROPE) ? rope_tf(a, unit) : make_float2(0.f, 0.f);
+        const float2 tf2 = (EPI == EPI_QKV_ROPE) ? rope_tf(a, unit) : make_float2(0.f, 0.f);
         for (int c = 0; c < BN / 16; ++c) {
           float v[16], v2[16];
           tmem_load16(tl + (uint32_t)(c * 16), v);
@@ -626,13 +667,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (ARGMAX)
             argmax16(a, unit, tbase + c * 16, n_tok, v, red_w + tbase + c * 16, lane);
           else
-            apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, tf, pos_s + c * 16, slot_s + c * 16);
+            apply16<EPI>(a, unit, tbase + c * 16, n_tok, v, v2, tf2, pos_s + c * 16, slot_s + c * 16);
         }
-      } else if (ok) {
+      } else if (ok && tf < a.n_f) {
         // split K (one unit per CTA): this split's fp32 partial tile straight from TMEM to
         // the workspace, column-major ([plane][token column][128 rows]: a warp's stores of
-        // one column are 128 contiguous bytes).  The next kernel sums the splits.
-        float* P = a.partial + (size_t)blockIdx.x * (PAIRED ? 2 : 1) * BN * kTcBM + r;
+        // one column are 128 contiguous bytes), at the unit's index over the live token
+        // tiles.  The next kernel sums the splits.
+        const size_t pu = ((size_t)tf * ntl + w.tile_t) * a.k_splits + w.split;
+        float* P = a.partial + pu * (PAIRED ? 2 : 1) * BN * kTcBM + r;
         const int cend = (PAIRED ? 2 : 1) * BN;
         for (int c = 0; c < cend;) {  // 64-column TMEM loads only at 64-aligned columns
           if ((c & 63) == 0 && c + 64 <= cend) {
@@ -652,7 +695,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(tempty + buf));  // accumulator free for a later unit
+      if (lane == 0) {  // accumulator free for a later unit
+        if (CG == 2) mbar_arrive_cluster(mapa_shared(smem_u32(tempty + buf), 0));
+        else mbar_arrive(smem_u32(tempty + buf));
+      }
       ++i;
     }
     if (ARGMAX) {
@@ -685,55 +731,130 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   // After a wait gave up (every role has left its loop, so the flag is final): leave no bulk
   // copy in flight into this CTA's shared memory.  The stages still in the ring are the last
-  // S issued; each wait is bounded.
-  if (warp == 0 && *abort_flag) {
+  // S issued; each wait is bounded.  In a pair the leader's barriers count both CTAs' copies,
+  // so the leader drains for both (the peer stops issuing when a wait of its own gives up,
+  // at least one wait limit after its last copy was issued).
+  if (warp == 0 && *abort_flag && leader) {
     const int drop = blockIdx.x == 0 ? a.drop_stage : -1;
     for (int i = issued > S ? issued - S : 0; i < issued; ++i)
       if (i != drop) mbar_wait(smem_u32(full + (i % S)), (uint32_t)(i / S) & 1u, a.err, nullptr, a.wait_ns);
     __syncwarp();
   }
   __syncthreads();
+  if (CG == 2) cluster_sync();  // neither CTA frees its tensor memory or exits while the pair works
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, a.tmem_cols);
+    if (CG == 2) tmem_dealloc_cg2(tmem, a.tmem_cols);
+    else tmem_dealloc(tmem, a.tmem_cols);
   }
 }
 
 // Opt every GEMM variant into the largest dynamic shared memory once per
 // device (an upper bound only; each launch passes its own size).
-template <int EPI>
+template <int EPI, int CG>
 static cudaError_t ensure_smem_attr() {
   static bool done[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemOptIn);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_kernel<EPI, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemOptIn);
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
   return cudaSuccess;
 }
 
-template <int EPI>
+template <int EPI, int CG>
 static cudaError_t launch_tc_typed(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
                                    size_t smem, cudaStream_t s) {
-  const cudaError_t e = ensure_smem_attr<EPI>();
+  const cudaError_t e = ensure_smem_attr<EPI, CG>();
   if (e != cudaSuccess) return e;
-  return launch_pdl(gemm_tc_kernel<EPI>, dim3(grid), dim3(kTcThreads), smem, s, tmW, tmX, a);
+  if constexpr (CG == 1) {
+    return launch_pdl(gemm_tc_kernel<EPI, 1>, dim3(grid), dim3(kTcThreads), smem, s, tmW, tmX, a);
+  } else {
+  // a pair per cluster, with programmatic dependent launch
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, 2>, tmW, tmX, a);
+  }
 }
 
-cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
-                           size_t smem, cudaStream_t s) {
+cudaError_t launch_gemm_tc(int epi, int cg, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a,
+                           int grid, size_t smem, cudaStream_t s) {
+  if (cg == 2) {
+    if (grid % 2 != 0) return cudaErrorInvalidValue;
+    switch (epi) {
+      case EPI_STORE_F32: return launch_tc_typed<EPI_STORE_F32, 2>(tmW, tmX, a, grid, smem, s);
+      case EPI_ADD_F32: return launch_tc_typed<EPI_ADD_F32, 2>(tmW, tmX, a, grid, smem, s);
+      case EPI_SWIGLU: return launch_tc_typed<EPI_SWIGLU, 2>(tmW, tmX, a, grid, smem, s);
+      case EPI_QKV_ROPE: return launch_tc_typed<EPI_QKV_ROPE, 2>(tmW, tmX, a, grid, smem, s);
+      case EPI_ARGMAX: return launch_tc_typed<EPI_ARGMAX, 2>(tmW, tmX, a, grid, smem, s);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (epi) {
-    case EPI_STORE_F32: return launch_tc_typed<EPI_STORE_F32>(tmW, tmX, a, grid, smem, s);
-    case EPI_ADD_F32: return launch_tc_typed<EPI_ADD_F32>(tmW, tmX, a, grid, smem, s);
-    case EPI_SWIGLU: return launch_tc_typed<EPI_SWIGLU>(tmW, tmX, a, grid, smem, s);
-    case EPI_QKV_ROPE: return launch_tc_typed<EPI_QKV_ROPE>(tmW, tmX, a, grid, smem, s);
-    case EPI_ARGMAX: return launch_tc_typed<EPI_ARGMAX>(tmW, tmX, a, grid, smem, s);
-    case EPI_ARGMAX_BAL: return launch_tc_typed<EPI_ARGMAX_BAL>(tmW, tmX, a, grid, smem, s);
+    case EPI_STORE_F32: return launch_tc_typed<EPI_STORE_F32, 1>(tmW, tmX, a, grid, smem, s);
+    case EPI_ADD_F32: return launch_tc_typed<EPI_ADD_F32, 1>(tmW, tmX, a, grid, smem, s);
+    case EPI_SWIGLU: return launch_tc_typed<EPI_SWIGLU, 1>(tmW, tmX, a, grid, smem, s);
+    case EPI_QKV_ROPE: return launch_tc_typed<EPI_QKV_ROPE, 1>(tmW, tmX, a, grid, smem, s);
+    case EPI_ARGMAX: return launch_tc_typed<EPI_ARGMAX, 1>(tmW, tmX, a, grid, smem, s);
+    case EPI_ARGMAX_BAL: return launch_tc_typed<EPI_ARGMAX_BAL, 1>(tmW, tmX, a, grid, smem, s);
   }
   return cudaErrorInvalidValue;
+}
+
+// Clusters of two CTAs of this GEMM that fit on the GPU at once (0 if the query fails).
+int gemm_tc_max_pairs(int epi, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (epi) {
+    case EPI_STORE_F32:
+      if (ensure_smem_attr<EPI_STORE_F32, 2>() == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI_STORE_F32, 2>, &cfg);
+      break;
+    case EPI_ADD_F32:
+      if (ensure_smem_attr<EPI_ADD_F32, 2>() == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI_ADD_F32, 2>, &cfg);
+      break;
+    case EPI_SWIGLU:
+      if (ensure_smem_attr<EPI_SWIGLU, 2>() == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI_SWIGLU, 2>, &cfg);
+      break;
+    case EPI_QKV_ROPE:
+      if (ensure_smem_attr<EPI_QKV_ROPE, 2>() == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI_QKV_ROPE, 2>, &cfg);
+      break;
+    case EPI_ARGMAX:
+      if (ensure_smem_attr<EPI_ARGMAX, 2>() == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI_ARGMAX, 2>, &cfg);
+      break;
+  }
+  return e == cudaSuccess ? n : 0;
 }
 
 // ============================================================================= split-K finish

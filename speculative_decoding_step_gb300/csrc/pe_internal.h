@@ -238,10 +238,15 @@ struct GemmArgs {
 
 // Tensor-core GEMM (tcgen05 + TMA): D[f][t] = W[f][:] . X[t][:], weights on the MMA M side.
 // Persistent: `grid` CTAs (at most one per SM) stride over the work units.  With
-// k_splits > 1 every CTA owns exactly one unit and writes its fp32 partial tile to
+// k_splits > 1 every CTA (pair) owns exactly one unit and writes its fp32 partial tile to
 // `partial`; the consumer sums the splits (RMSNorm, or launch_splitk_finish).
-cudaError_t launch_gemm_tc(int epi, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
-                           size_t smem_bytes, cudaStream_t s);
+// cg = 2: clusters of two CTAs, each unit one MMA of M = 256 over the pair (grid even;
+// the token operand's tensor map has boxes of bn / 2 rows); not for EPI_ARGMAX_BAL.
+cudaError_t launch_gemm_tc(int epi, int cg, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a,
+                           int grid, size_t smem_bytes, cudaStream_t s);
+// Clusters of two CTAs of this GEMM epilogue with this much shared memory that fit on the
+// GPU at once (0 if the query fails).
+int gemm_tc_max_pairs(int epi, size_t smem_bytes);
 // Sum of a split-K QKV or gate/up GEMM's partials and its epilogue (the same GemmArgs).
 cudaError_t launch_splitk_finish(int epi, const GemmArgs& a, int sms, cudaStream_t s);
 // fp32 CUDA-core GEMM for fp32 configurations (same epilogues).

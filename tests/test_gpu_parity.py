@@ -45,6 +45,15 @@ SMALL = {
     "bf16-odd-atoms": _small(B=3, K=5, d=320, ffn=448, seed=13),
     # a deeper drafter: four layers, each its own weights and KV cache
     "bf16-L4": _small(B=2, K=6, n_layers=4, prefix_args=(100, 700), seed=14),
+    # more than 256 rows and an LM head of 160 rows: every GEMM runs on CTA pairs (M = 256
+    # over two SMs); three weight tiles (an odd count: the last pair's second tile is past
+    # the end), split K in fc / o-proj / down, and a ragged nine-tile vocabulary
+    "bf16-pairs": _small(B=20, K=8, d=320, ffn=448, vocab=1037, seed=15),
+    # contractions short enough that no GEMM splits K (every epilogue writes final values and
+    # every RMSNorm reads the residual as it is), on single CTAs over two layers, and on CTA
+    # pairs
+    "bf16-fold": _small(B=6, K=8, d=192, n_q=4, n_kv=2, ffn=384, vocab=1037, n_layers=2, seed=16),
+    "bf16-fold-pairs": _small(B=20, K=8, d=192, n_q=4, n_kv=2, ffn=384, vocab=1037, seed=17),
     "f32-c0": config(0),
     "f32-L2": _small(dtype="f32", n_layers=2, seed=11),
 }
