@@ -18,6 +18,9 @@
  *   pe_verify_sampled  rejection-sampling verification against the target's
  *                      distributions
  *
+ * The DFlash-style variant: pe_inject_kv projects the verifier's hidden states
+ * straight into the drafter's KV cache.
+ *
  * Conventions shared by every entry point:
  *
  * - Memory.  Unless stated otherwise a pointer argument is a DEVICE pointer to
@@ -252,6 +255,33 @@ pe_status pe_verify(const pe_config *cfg, const int32_t *draft_tokens, const int
                     int32_t *num_accepted_out, int32_t *bonus_out, pe_stream_t stream);
 
 /*
+ * DFlash-style KV injection (vLLM Speculators: parallel drafting for speculative
+ * decoding, "DFlash": the verifier's hidden states are projected and injected
+ * straight into the drafter's KV cache, so that the drafter attends to the
+ * verifier's state without more input rows).  The page gives no formula; here the
+ * projected state stands where a row's residual stream would, so each layer turns
+ * it into k and v exactly as it does for its own rows.
+ *
+ * For sequence b and element j <= num_accepted[b] of its previous verify batch
+ * (the accepted drafts and the bonus token's position), with
+ * h = target_hidden[b*(K+1) + j] and p = prev_pos[b][j]:
+ *   x = W_inj . h                          (w_inj [d][d], nn.Linear layout, no bias)
+ *   per layer l: y = rms(x) * norm_attn[l]; k = RoPE(W_k[l] . y, p); v = W_v[l] . y
+ * (W_k, W_v: the k and v head blocks of wqkv[l]) are written to layer l's cache
+ * at slot(p) = block_table[b][p/16]*16 + p%16.  Elements j > num_accepted[b] are
+ * not written.  Only w->norm_attn and w->wqkv are read from w.  prev_pos,
+ * num_accepted, target_hidden are pe_step's / pe_prepare_batch's arrays of the
+ * same names; workspace as for pe_draft_forward.  Device checks: an accepted
+ * count outside [0, K] (PE_DEV_BAD_ACCEPTED: nothing of that sequence is
+ * written), a position outside the block table (PE_DEV_BAD_POSITION), a page id
+ * outside [0, num_pages) (PE_DEV_BAD_PAGE).
+ */
+pe_status pe_inject_kv(const pe_config *cfg, const pe_weights *w, const void *w_inj, const pe_kv *kv,
+                       const int32_t *block_table, const int32_t *prev_pos, const int32_t *num_accepted,
+                       const void *target_hidden, void *workspace, size_t workspace_bytes, int32_t *err_word,
+                       pe_stream_t stream);
+
+/*
  * Non-greedy drafting (vLLM Speculators: parallel drafting for speculative
  * decoding, "Production integration in vLLM": verification by rejection
  * sampling keeps the target's output distribution).  Draft row r = b*K + k
@@ -371,8 +401,9 @@ pe_status pe_set_wait_limit_ns(uint64_t ns);
  */
 pe_status pe_test_skip_pipeline_stage(int32_t stage);
 
-/* Workspace bytes needed by pe_draft_forward, pe_step, pe_sample_drafts and
- * pe_verify_sampled for this config (0 if invalid); one workspace serves them all. */
+/* Workspace bytes needed by pe_draft_forward, pe_step, pe_sample_drafts,
+ * pe_verify_sampled and pe_inject_kv for this config (0 if invalid); one workspace
+ * serves them all. */
 size_t pe_workspace_bytes(const pe_config *cfg);
 
 /*

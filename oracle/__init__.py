@@ -24,6 +24,9 @@ Functions (each a plain restatement; pure Python loops where sizes are small):
 * ``verify``         (R4) greedy verification.
 * ``next_verify_batch`` the verify batch the target checks after a round (the
   next round's previous batch): the bonus token, then the K drafts.
+* ``inject_kv`` (R6) the DFlash-style variant: the verifier's hidden states
+  projected into the drafter's KV cache (vLLM Speculators: parallel drafting
+  for speculative decoding, "DFlash").
 * ``inverse_cdf``, ``drafter_distribution``, ``sample_drafts``,
   ``verify_sampled`` (R5) non-greedy drafting and verification by rejection
   sampling (speculative sampling): drafts drawn from the drafter's
@@ -361,6 +364,51 @@ def next_verify_batch(prev_pos, num_accepted, bonus, drafts) -> tuple[np.ndarray
         for j in range(K + 1):
             positions[b][j] = p0 + j
     return tokens, positions
+
+
+# ----------------------------------------------------------------------------- R6: DFlash-style KV injection
+# vLLM Speculators: parallel drafting for speculative decoding, "DFlash": the verifier's
+# hidden states are projected and injected straight into the drafter's KV cache, so the
+# drafter attends to the verifier's state without extra input rows.  The page gives that
+# one sentence; the reading here: the projected state x = W_inj h stands where a row's
+# residual stream would, so each layer turns it into k and v exactly as it does for its
+# own rows (attention RMSNorm, the k and v blocks of W_qkv, RoPE on k at the position),
+# and writes them at the position's cache slot.
+
+def inject_kv(cfg, weights, w_inj, target_hidden, prev_pos, num_accepted, block_table, page_size: int = 16) -> dict:
+    """KV entries injected from the verifier's hidden states of the previous verify batch.
+
+    Sequence b, verify element j <= num_accepted[b] (the accepted drafts' positions and the
+    bonus token's position; rejected ones are not written): h = target_hidden[b*(K+1) + j],
+    p = prev_pos[b][j], x = W_inj h (W_inj [d][d], no bias); per layer l:
+    y = rms(x) * g_attn[l], k = RoPE(W_k[l] y, p), v = W_v[l] y.
+    Returns slots [n] (int64, the written cache slots in (b, j) order) and new_k / new_v
+    [L][n][n_kv * head_dim] (float64, post-RoPE k)."""
+    K = cfg.K
+    B = len(num_accepted)
+    hd, nq, nkv = cfg.head_dim, cfg.n_q, cfg.n_kv
+    H = widen(np.asarray(target_hidden))
+    rows, slots, pos = [], [], []
+    for b in range(B):
+        for j in range(int(num_accepted[b]) + 1):
+            p = int(prev_pos[b][j])
+            rows.append(b * (K + 1) + j)
+            pos.append(p)
+            slots.append(int(block_table[b][p // page_size]) * page_size + p % page_size)
+    X = linear(H[rows], np.asarray(w_inj))
+    L = cfg.n_layers
+    new_k = np.zeros((L, len(rows), nkv * hd))
+    new_v = np.zeros((L, len(rows), nkv * hd))
+    for l in range(L):
+        Y = rmsnorm(X, weights.norm_attn[l], cfg.rms_eps)
+        wkv = np.asarray(weights.wqkv[l])[nq * hd:]            # the k heads, then the v heads
+        KV = linear(Y, wkv)
+        for i in range(len(rows)):
+            for g in range(nkv):
+                new_k[l, i, g * hd:(g + 1) * hd] = rope(KV[i, g * hd:(g + 1) * hd], pos[i], cfg.rope_theta)
+            new_v[l, i] = KV[i, nkv * hd:]
+    return dict(slots=np.array(slots, dtype=np.int64), rows=np.array(rows, dtype=np.int32), new_k=new_k,
+                new_v=new_v, positions=np.array(pos, dtype=np.int32))
 
 
 # ----------------------------------------------------------------------------- R5: sampled drafting and verification

@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = ["pe_prepare_batch", "pe_scatter_hidden", "pe_draft_forward",
                     "pe_sample_drafts", "pe_verify_sampled",
                     "pe_workspace_bytes", "pe_check_config", "pe_status_str", "pe_set_trace_events",
                     "pe_trace_points", "pe_kernel_launches", "pe_draft_forward_noalloc", "pe_set_wait_limit_ns",
-                    "pe_test_skip_pipeline_stage"]
+                    "pe_test_skip_pipeline_stage", "pe_inject_kv"]
 
 # Size of the library-owned scratch used by pe_draft_forward_noalloc (PE_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 48 << 20
@@ -156,6 +156,8 @@ def lib():
         L.pe_kernel_launches.restype = ctypes.c_uint64
         L.pe_kernel_launches.argtypes = []
         L.pe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.pe_inject_kv.argtypes = [cp, ctypes.POINTER(_Weights), vp, ctypes.POINTER(_KV), vp, vp, vp, vp, vp,
+                                   ctypes.c_size_t, vp, vp]
         L.pe_test_skip_pipeline_stage.argtypes = [i32]
         for name in EXPORTED_SYMBOLS:
             if name not in ("pe_status_str", "pe_workspace_bytes", "pe_kernel_launches"):
@@ -281,6 +283,18 @@ def verify_sampled(cfg, draft_tokens, logits, lse, temperature, target_probs, u_
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _ptr(num_accepted_out), _ptr(bonus_out), _ptr(err), _stream(stream))
     _check(st, "pe_verify_sampled")
+
+
+def inject_kv(cfg, weights: DeviceWeights, w_inj, kv: DeviceKV, block_table, prev_pos, num_accepted, target_hidden,
+              workspace, err, stream=None):
+    """DFlash-style KV injection: the verifier's hidden states of the previous verify batch,
+    projected by w_inj [d][d], written as k / v into every layer's cache at the accepted
+    positions (see pe.h)."""
+    st = lib().pe_inject_kv(ctypes.byref(cfg), ctypes.byref(weights.struct), _ptr(w_inj), ctypes.byref(kv.struct),
+                            _ptr(block_table), _ptr(prev_pos), _ptr(num_accepted), _ptr(target_hidden),
+                            _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
+                            _stream(stream))
+    _check(st, "pe_inject_kv")
 
 
 def step(cfg, weights: DeviceWeights, kv: DeviceKV, block_table, prev_tokens, prev_pos, num_accepted, bonus,

@@ -166,6 +166,7 @@ GemmPlan plan_gemm(int epi, int n_f_tiles, int n_tok, int k_dim, int sms, int ma
 struct Plan {
   int R = 0, T = 0, S = 0, sms = 0, max_items = 0, attn_grid = 0, attn_target = 0, n_counters = 0;
   GemmPlan fc, qkv, o, gu, down, lm;
+  GemmPlan inj, injkv;  // KV injection: W_inj over the verify batch's hidden rows, then the k | v heads
   // workspace offsets
   size_t tok_pos, tok_seq, tok_slot, seq_start, seq_len, seq_maxpos, item_base, n_chunks, n_items, items;
   size_t done, keys, x, y, q, ao, u, yl, part_m, part_l, part_o, split_part;
@@ -190,6 +191,9 @@ Plan make_plan(const pe_config& c) {
   p.gu = plan_gemm(EPI_SWIGLU, (c.ffn + kTcBM - 1) / kTcBM, p.R, c.d, p.sms, mp);
   p.down = plan_gemm(EPI_ADD_F32, (c.d + kTcBM - 1) / kTcBM, p.R, c.ffn, p.sms, mp);
   p.lm = plan_gemm(EPI_ARGMAX, (c.vocab + kTcBM - 1) / kTcBM, p.T, c.d, p.sms, mp);
+  const int n_inj = c.B * (c.K + 1);
+  p.inj = plan_gemm(EPI_STORE_F32, (c.d + kTcBM - 1) / kTcBM, n_inj, c.d, p.sms, mp);
+  p.injkv = plan_gemm(EPI_QKV_ROPE, (2 * c.n_kv + hpt - 1) / hpt, n_inj, c.d, p.sms, mp);
   // attention items: the work list aims at attn_target items; rounding adds at
   // most one per (sequence, kv head), and no (sequence, kv head) can have more
   // chunks than its longest possible range holds minimum chunks
@@ -228,7 +232,7 @@ Plan make_plan(const pe_config& c) {
   p.u = take(eb * (size_t)p.R * c.ffn);
   p.yl = take(eb * (size_t)p.T * c.d);
   size_t split_bytes = 0;  // fp32 partial tiles of the largest split-K launch (one per unit)
-  for (const GemmPlan* g : {&p.fc, &p.qkv, &p.o, &p.gu, &p.down})
+  for (const GemmPlan* g : {&p.fc, &p.qkv, &p.o, &p.gu, &p.down, &p.inj, &p.injkv})
     if (g->k_splits > 1) {
       const bool paired = g->epi == EPI_SWIGLU || g->epi == EPI_QKV_ROPE;
       split_bytes = std::max(split_bytes, (size_t)g->n_f * g->n_t * g->k_splits * (paired ? 2 : 1) * g->bn * kTcBM * 4);
@@ -419,8 +423,9 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   CUtensorMap tw, tx;
   bool ok;
   if (call.w_kind == 1) ok = tmap_gate_up(&tw, call.W, (uint64_t)c.ffn, (uint64_t)c.d, g.ka);
-  else if (call.w_kind == 2)
-    ok = tmap_qkv(&tw, call.W, (uint64_t)(c.n_q + 2 * c.n_kv), (uint64_t)c.head_dim, (uint64_t)c.d, g.ka);
+  else if (call.w_kind == 2)  // w_rows: heads of W (0: all of q | k | v)
+    ok = tmap_qkv(&tw, call.W, call.w_rows ? call.w_rows : (uint64_t)(c.n_q + 2 * c.n_kv), (uint64_t)c.head_dim,
+                  (uint64_t)c.d, g.ka);
   else ok = tmap_matrix(&tw, call.W, call.w_rows, (uint64_t)call.k_dim, (uint32_t)kTcBM, g.ka);
   ok = ok && tmap_matrix(&tx, call.X, (uint64_t)call.n_tok, (uint64_t)call.k_dim, (uint32_t)(g.bn / g.cg), g.ka);
   if (!ok) return PE_ERR_CUDA;
@@ -874,6 +879,68 @@ pe_status pe_verify_sampled(const pe_config* cfg, const int32_t* draft_tokens, c
   a.acc_ws = at<int32_t>(workspace, p.samp_acc);
   a.acc_out = num_accepted_out; a.bonus_out = bonus_out; a.err = err_word;
   PE_TRY_CUDA(launch_verify_sampled(a, p.sms, (cudaStream_t)stream));
+  return PE_OK;
+}
+
+pe_status pe_inject_kv(const pe_config* cfg, const pe_weights* w, const void* w_inj, const pe_kv* kv,
+                       const int32_t* block_table, const int32_t* prev_pos, const int32_t* num_accepted,
+                       const void* target_hidden, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                       pe_stream_t stream) {
+  pe_status st = check_cfg(cfg);
+  if (st != PE_OK) return st;
+  const pe_config& c = *cfg;
+  if (w == nullptr || w->norm_attn == nullptr || w->wqkv == nullptr) return PE_ERR_INVALID_ARG;
+  for (int l = 0; l < c.n_layers; ++l)
+    if (!w->norm_attn[l] || !w->wqkv[l] || !aligned16(w->norm_attn[l]) || !aligned16(w->wqkv[l]))
+      return PE_ERR_INVALID_ARG;
+  if ((st = check_kv(c, kv)) != PE_OK) return st;
+  if (!w_inj || !block_table || !prev_pos || !num_accepted || !target_hidden || !workspace || !err_word)
+    return PE_ERR_INVALID_ARG;
+  if (!aligned16(w_inj) || !aligned16(target_hidden) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PE_ERR_INVALID_ARG;
+  const Plan p = make_plan(c);
+  if (workspace_bytes < p.total) return PE_ERR_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* ws = workspace;
+  const bool bf16 = c.dtype == PE_BF16;
+  const int NI = c.B * (c.K + 1);
+  const int hd = c.head_dim;
+  InjectArgs ia{};
+  ia.B = c.B; ia.K = c.K; ia.max_pages = c.max_pages_per_seq; ia.num_pages = kv->num_pages;
+  ia.page_size = c.page_size; ia.prev_pos = prev_pos; ia.num_accepted = num_accepted; ia.block_table = block_table;
+  ia.tok_pos = at<int32_t>(ws, p.tok_pos); ia.tok_slot = at<int64_t>(ws, p.tok_slot); ia.err = err_word;
+  PE_TRY_CUDA(launch_inject_init(ia, s));
+
+  GemmArgs base{};
+  base.n_q = c.n_q; base.n_kv = c.n_kv; base.head_dim = hd; set_rope_table(base, c.rope_theta, hd);
+  base.tok_pos = ia.tok_pos; base.tok_slot = ia.tok_slot; base.err = err_word;
+  float* x = at<float>(ws, p.x);
+  void* y = at<uint8_t>(ws, p.y);
+  // x = H . W_inj^T over every element of the verify batch (the rejected ones are computed but
+  // never written: their slot is -1)
+  {
+    GemmArgs a = base;
+    a.out_f32 = x; a.ld_out = c.d;
+    GemmCall call{EPI_STORE_F32, &p.inj, w_inj, target_hidden, c.d, c.d, NI, nullptr, 0, (uint64_t)c.d};
+    if ((st = run_gemm(c, p, ws, call, a, s)) != PE_OK) return st;
+  }
+  for (int l = 0; l < c.n_layers; ++l) {
+    NormArgs n{};
+    n.x = x; n.d = c.d; n.row_map = nullptr; n.n_rows = NI; n.n_rows_dev = nullptr; n.src_rows = NI;
+    n.g = w->norm_attn[l]; n.eps = c.rms_eps; n.y = y; n.err = err_word;
+    if (bf16 && p.inj.k_splits > 1 && l == 0) {  // the first norm also sums W_inj's split-K partials
+      n.part = at<float>(ws, p.split_part); n.n_splits = p.inj.k_splits; n.bn = p.inj.bn; n.n_t = p.inj.n_t;
+      n.g_ntok = NI; n.g_ntok_dev = nullptr; n.g_ntok_min = NI; n.x = nullptr; n.x_out = x;
+    }
+    PE_TRY_CUDA(launch_rmsnorm(n, c.dtype, s));
+    GemmArgs a = base;
+    a.out_act = at<uint8_t>(ws, p.q); a.ld_out = c.n_q * hd;  // no q heads here: never written
+    a.k_cache = kv->k_cache[l]; a.v_cache = kv->v_cache[l];
+    a.head0 = c.n_q;
+    const void* wkv = static_cast<const uint8_t*>(w->wqkv[l]) + (size_t)c.n_q * hd * c.d * elem_bytes(c.dtype);
+    GemmCall call{EPI_QKV_ROPE, &p.injkv, wkv, y, c.d, c.n_kv * hd, NI, nullptr, 2, (uint64_t)(2 * c.n_kv)};
+    if ((st = run_gemm(c, p, ws, call, a, s)) != PE_OK) return st;
+  }
   return PE_OK;
 }
 

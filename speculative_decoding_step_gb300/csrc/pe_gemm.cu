@@ -48,7 +48,7 @@ PE_DEV void rope_pair(float x1, float x2, int pos, float2 tf, float& o1, float& 
 template <typename T>
 PE_DEV void qkv_store(const GemmArgs& a, int unit, int t, float x1, float x2, float2 tf, int pos, long long slot) {
   const int half = a.head_dim >> 1;
-  const int head = unit / half, i = unit - head * half;
+  const int head = unit / half + a.head0, i = unit - (unit / half) * half;
   if (head < a.n_q + a.n_kv) rope_pair(x1, x2, pos, tf, x1, x2);
   if (head < a.n_q) {
     T* q = static_cast<T*>(a.out_act) + (size_t)t * a.ld_out + (size_t)head * a.head_dim + i;
@@ -67,7 +67,7 @@ PE_DEV void qkv_store(const GemmArgs& a, int unit, int t, float x1, float x2, fl
 template <typename T>
 PE_DEV void epi_qkv(const GemmArgs& a, int unit, int t, float x1, float x2, float2 tf) {
   const int half = a.head_dim >> 1;
-  const int head = unit / half, i = unit - head * half;
+  const int head = unit / half + a.head0, i = unit - (unit / half) * half;
   if (head < a.n_q + a.n_kv) rope_pair(x1, x2, a.tok_pos[t], tf, x1, x2);
   if (head < a.n_q) {
     T* q = static_cast<T*>(a.out_act) + (size_t)t * a.ld_out + (size_t)head * a.head_dim + i;
@@ -127,7 +127,7 @@ PE_DEV void epi_chunk(const GemmArgs& a, int unit, int t0, int nv, const float (
       if (j < nv) o[(size_t)j * a.ld_out] = from_float<T>(silu(v[j]) * v2[j]);
   } else if (EPI == EPI_QKV_ROPE) {
     const int half = a.head_dim >> 1;
-    const int head = unit / half, i = unit - head * half;
+    const int head = unit / half + a.head0, i = unit - (unit / half) * half;
     const bool is_q = head < a.n_q, rotated = head < a.n_q + a.n_kv;
     int pos[16];
     long long slot[16];

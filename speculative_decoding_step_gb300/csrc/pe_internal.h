@@ -155,6 +155,16 @@ struct InitArgs {
   int32_t* err;
 };
 cudaError_t launch_forward_init(const InitArgs& a, cudaStream_t s);
+// DFlash-style KV injection: position and cache slot of every element of the previous verify
+// batch (hidden row i = b*(K+1) + j): slot -1 for j > num_accepted[b].
+struct InjectArgs {
+  int B, K, max_pages, num_pages, page_size;
+  const int32_t *prev_pos, *num_accepted, *block_table;
+  int32_t* tok_pos;
+  int64_t* tok_slot;
+  int32_t* err;
+};
+cudaError_t launch_inject_init(const InjectArgs& a, cudaStream_t s);
 // Input rows (ScatterArgs) and the forward prologue (InitArgs) in one launch.
 cudaError_t launch_scatter_init(const ScatterArgs& sa, const InitArgs& ia, cudaStream_t s);
 
@@ -216,6 +226,8 @@ struct GemmArgs {
   void* out_act;         // SwiGLU output / q buffer (bf16 or fp32 by config)
   int ld_out;
   int n_q, n_kv, head_dim;
+  int head0;             // QKV: heads of this GEMM start at head0 of the q | k | v concatenation (0; KV
+                         //   injection: n_q, the GEMM covering the k and v heads only)
   // RoPE: turns per position of pair index i, theta^(-2i/head_dim) / (2 pi), split into
   // a float and the float nearest its remainder (i < head_dim / 2 <= 64)
   float rope_tf_hi[64], rope_tf_lo[64];

@@ -145,6 +145,46 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   return launch_pdl(verify_kernel, dim3((a.B + threads - 1) / threads), dim3(threads), 0, s, a);
 }
 
+// ============================================================================= DFlash-style KV injection
+// vLLM Speculators: parallel drafting for speculative decoding, "DFlash": the verifier's
+// hidden states are projected into the drafter's KV cache.  Each element j of sequence b's
+// previous verify batch (hidden row b*(K+1) + j) is written at its position's slot when
+// j <= num_accepted[b] (the accepted drafts and the bonus token's position); a rejected
+// element gets slot -1 (no write).
+
+__global__ void inject_init_kernel(const InjectArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int S = a.K + 1;
+  if (i >= a.B * S) return;
+  const int b = i / S, j = i - b * S;
+  int acc = a.num_accepted[b];
+  if (acc < 0 || acc > a.K) {
+    set_err(a.err, PE_DEV_BAD_ACCEPTED);
+    acc = -1;  // nothing of this sequence is written
+  }
+  const int p = a.prev_pos[i];
+  long long slot = -1;
+  if (j <= acc) {
+    const int pi = p / a.page_size;
+    if (p < 0 || pi >= a.max_pages) {
+      set_err(a.err, PE_DEV_BAD_POSITION);
+    } else {
+      const int page = a.block_table[(size_t)b * a.max_pages + pi];
+      if (page < 0 || page >= a.num_pages) set_err(a.err, PE_DEV_BAD_PAGE);
+      else slot = (long long)page * a.page_size + p % a.page_size;
+    }
+  }
+  a.tok_pos[i] = p < 0 ? 0 : p;
+  a.tok_slot[i] = slot;
+}
+
+cudaError_t launch_inject_init(const InjectArgs& a, cudaStream_t s) {
+  const int n = a.B * (a.K + 1), threads = 256;
+  return launch_pdl(inject_init_kernel, dim3((n + threads - 1) / threads), dim3(threads), 0, s, a);
+}
+
 // ============================================================================= forward prologue
 
 constexpr int kInitThreads = 1024;

@@ -158,3 +158,24 @@ def test_wait_limit_and_stage_hook_host_checks():
     assert L.pe_test_skip_pipeline_stage(-1) == 0
     assert L.pe_set_wait_limit_ns(1000) == 0
     assert L.pe_set_wait_limit_ns(0) == 0
+
+
+def test_inject_kv_host_checks():
+    """pe_inject_kv rejects null or misaligned pointers and a short workspace before any launch
+    (placeholder pointers, never dereferenced)."""
+    L = pe.lib()
+    cfg = _cfg(B=2, K=3)
+    P = iter(range(1 << 40, (1 << 40) + (1 << 30), 1 << 20))
+    layer = (ctypes.c_void_p * cfg.n_layers)(*[next(P) for _ in range(cfg.n_layers)])
+    w = pe._Weights(next(P), next(P), next(P), layer, layer, layer, layer, layer, layer, next(P), next(P))
+    kv = pe._KV(layer, layer, 4)
+    v = lambda: ctypes.c_void_p(next(P))
+
+    def call(w_inj=None, ws_bytes=0, hidden=None):
+        return L.pe_inject_kv(ctypes.byref(cfg), ctypes.byref(w), w_inj if w_inj is not None else v(),
+                              ctypes.byref(kv), v(), v(), v(), hidden if hidden is not None else v(), v(),
+                              ctypes.c_size_t(ws_bytes), v(), ctypes.c_void_p(None))
+
+    assert call(w_inj=ctypes.c_void_p(None)) == 1          # null projection
+    assert call(hidden=ctypes.c_void_p((1 << 41) + 8)) == 1  # misaligned hidden states
+    assert call(ws_bytes=16) == 2                          # workspace too short: PE_ERR_SHAPE

@@ -606,3 +606,53 @@ def test_verify_sampled_preserves_target_distribution():
     assert np.abs(f1 - p[1]).max() <= 5 * np.sqrt(p[1] * (1 - p[1]) / n).max()
     # acceptance rate of the first draft: sum_v min(p_0, q_0)
     assert abs(sel.mean() - np.minimum(p[0], np.exp(lg_rows[0])).sum()) <= 5 * 0.0025
+
+
+# ----------------------------------------------------------------------------- R6: DFlash-style KV injection
+
+def test_inject_kv_closed_form_and_rejected_positions():
+    """The verifier's hidden state h of an accepted (or bonus) position goes through
+    x = W_inj h, the attention RMSNorm, the k and v blocks of W_qkv, and RoPE on k at the
+    position: with W_inj = I, h = s e0 and one-hot k / v rows the entries have closed forms
+    (k pair 1 turned by 0.1 rad per position at RoPE base 10^4; v unrotated).  Positions after
+    the accepted count are not written."""
+    d, hd, s_, beta, gamma = 32, 8, 3.0, 0.75, 1.25
+    cfg = _tiny(B=2, K=3, d=d, n_q=1, n_kv=1, head_dim=hd, ffn=8, vocab=d)
+    wqkv = np.zeros((3 * hd, d), np.float32)
+    wqkv[hd + 1, 0], wqkv[2 * hd, 0] = beta, gamma
+    w = type("W", (), {})()
+    w.norm_attn, w.wqkv = [np.ones(d, np.float32)], [wqkv]
+    H = np.zeros((2 * (cfg.K + 1), d), np.float32)
+    H[:, 0] = s_
+    prev_pos = np.array([[10, 11, 12, 13], [40, 41, 42, 43]])
+    bt = np.arange(2 * 4, dtype=np.int32).reshape(2, 4)
+    res = oracle.inject_kv(cfg, w, np.eye(d, dtype=np.float32), H, prev_pos, [2, 0], bt)
+    assert res["rows"].tolist() == [0, 1, 2, 4]          # (b=0, j=0..2), (b=1, j=0)
+    assert res["slots"].tolist() == [16 * 0 + 10, 11, 12, 16 * 6 + 40 % 16]
+    r = s_ / math.sqrt(s_ * s_ / d + cfg.rms_eps)
+    for i, p in enumerate(res["positions"]):
+        ang = p * 10000.0 ** (-2.0 / hd)
+        k = np.zeros(hd)
+        k[1], k[1 + hd // 2] = beta * r * math.cos(ang), beta * r * math.sin(ang)
+        np.testing.assert_allclose(res["new_k"][0, i], k, rtol=1e-12, atol=1e-12)
+        v = np.zeros(hd)
+        v[0] = gamma * r
+        np.testing.assert_allclose(res["new_v"][0, i], v, rtol=1e-12, atol=1e-12)
+
+
+def test_inject_kv_matches_the_drafter_layer_on_projected_rows():
+    """A drafter row whose fc output is W_inj h (fc = [0 | W_inj], so emb drops out) writes, in
+    the first layer, exactly the k and v that injection writes for h at the same position."""
+    cfg = _c0_like().replace(B=2, K=3, n_layers=2)
+    w, rnd = make_weights(cfg), make_round(cfg)
+    d = cfg.d
+    rng = np.random.default_rng(4)
+    w_inj = (rng.standard_normal((d, d)) * 0.05).astype(np.float32)
+    inj = oracle.inject_kv(cfg, w, w_inj, rnd.target_hidden, rnd.prev_pos, rnd.num_accepted, rnd.block_table)
+    w.fc = np.concatenate([np.zeros((d, d), np.float32), w_inj], axis=1)
+    x0 = np.concatenate([np.zeros((len(inj["rows"]), d)), oracle.widen(rnd.target_hidden)[inj["rows"]]], axis=1)
+    seqs = inj["rows"] // (cfg.K + 1)
+    out = oracle.draft_forward(cfg, w, x0, inj["positions"], inj["slots"], seqs, rnd.block_table, rnd.k_cache,
+                               rnd.v_cache, [0], want_kv=True)
+    np.testing.assert_allclose(out["new_k"][0], inj["new_k"][0], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(out["new_v"][0], inj["new_v"][0], rtol=1e-10, atol=1e-12)
