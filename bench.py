@@ -121,8 +121,8 @@ def round_cost(cfg, rnd) -> dict:
 
 def stage_costs(cfg, rnd) -> dict:
     """The same algorithmic bytes and flops as round_cost, split over the stages the library's
-    trace points bound (names as in stage_names): metadata to the rebuild, the input rows to
-    the row copy, each weight matrix, gain and KV stream to the stage that reads it, and the
+    trace points bound (names as in stage_names): metadata and the input rows to pe_step's
+    first launch, each weight matrix, gain and KV stream to the stage that reads it, and the
     drafts and target tokens to verification.  Maps stage name -> (bytes, flops)."""
     eb = 2 if cfg.dtype == "bf16" else 4
     K, B, d, hd = cfg.K, cfg.B, cfg.d, cfg.head_dim
@@ -133,8 +133,8 @@ def stage_costs(cfg, rnd) -> dict:
     for b in range(B):
         ctx += int((P[b] + np.arange(n_b[b]) + 1).sum())
     kv_read = int((P + n_b).sum() * cfg.n_kv * hd * 2 * eb)
-    out = {"prepare": (B * (K + 1) * 4 * 4 + B * 2 * K * 32, 0), "scatter": (n_valid * d * eb * 2, 0),
-           "forward_init": (0, 0), "fc": (d * 2 * d * eb, 2 * n_valid * d * 2 * d)}
+    out = {"rebuild_rows_prologue": (B * (K + 1) * 4 * 4 + B * 2 * K * 32 + n_valid * d * eb * 2, 0),
+           "fc": (d * 2 * d * eb, 2 * n_valid * d * 2 * d)}
     for l in range(cfg.n_layers):
         out[f"l{l}.norm1"] = (d * eb, 0)
         out[f"l{l}.qkv_rope_kv"] = (cfg.qkv_out * d * eb + n_valid * cfg.n_kv * hd * 2 * eb,
@@ -315,11 +315,19 @@ def run_reference(args):
 # ----------------------------------------------------------------------------- GPU arm
 
 def stage_names(n_layers):
-    names = ["prepare", "scatter", "forward_init", "fc"]
+    """The stages of a traced pe_step, in order.  The first spans trace points 0..3 (the
+    batch rebuild, the input rows and the forward prologue run in one launch); every later
+    stage is one interval between consecutive trace points (stage_points)."""
+    names = ["rebuild_rows_prologue", "fc"]
     for l in range(n_layers):
         names += [f"l{l}.norm1", f"l{l}.qkv_rope_kv", f"l{l}.attention", f"l{l}.o_proj", f"l{l}.norm2",
                   f"l{l}.gate_up_swiglu", f"l{l}.down"]
     return names + ["final_norm", "lm_head_argmax", "verify"]
+
+
+def stage_points(n_layers):
+    """(start, end) trace points of each stage of stage_names (8 + 7 L points in all)."""
+    return [(0, 3)] + [(j, j + 1) for j in range(3, 7 + 7 * n_layers)]
 
 
 class Bench:
@@ -395,9 +403,9 @@ def traced_stage_us(torch, stream, flush, pe, b: Bench, n: int) -> dict:
             e.record()
     torch.cuda.synchronize()
     timed(torch, stream, flush, n, b.step, traced=tr, pe=pe)
-    names = stage_names(b.cfg_np.n_layers)
-    return {nm: round(1e3 * statistics.median(tr[i][j].elapsed_time(tr[i][j + 1]) for i in range(n)), 2)
-            for j, nm in enumerate(names)}
+    L = b.cfg_np.n_layers
+    return {nm: round(1e3 * statistics.median(tr[i][p0].elapsed_time(tr[i][p1]) for i in range(n)), 2)
+            for nm, (p0, p1) in zip(stage_names(L), stage_points(L))}
 
 
 def roofline_of(cfg_np, rnd, us_round, lm_us, peaks, src) -> dict:

@@ -368,6 +368,8 @@ pe_status pe_step(const pe_config *cfg, const pe_weights *w, const pe_kv *kv, co
  * pe_trace_points(cfg) = 8 + 7*n_layers boundaries.  Events beyond n_events
  * are not recorded; n_events = 0 turns tracing off.  The event array is host
  * memory and is copied; the events themselves must outlive their recording.
+ * pe_step runs the rebuild, the input rows and the forward prologue in one
+ * launch: its points 1, 2 and 3 all follow that launch.
  */
 pe_status pe_set_trace_events(void *const *events, int32_t n_events);
 int32_t pe_trace_points(const pe_config *cfg);

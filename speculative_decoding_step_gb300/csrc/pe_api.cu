@@ -815,16 +815,15 @@ pe_status pe_step(const pe_config* cfg, const pe_weights* w, const pe_kv* kv, co
   int32_t* nval = at<int32_t>(ws, p.st_nvalid);
   int32_t* drows = at<int32_t>(ws, p.st_draft);
   void* x0 = at<uint8_t>(ws, p.st_x0);
-  trace(0, s);
-  st = pe_prepare_batch(cfg, prev_tokens, prev_pos, num_accepted, bonus, block_table, kv->num_pages, ids, pos, slot,
-                        rej, msk, hmap, rows, nval, drows, err_word, stream);
-  if (st != PE_OK) return st;
-  trace(1, s);
-  // input rows and the forward prologue in one launch (both read only the rebuild's outputs)
+  // the batch rebuild, the input rows and the forward prologue in one launch
   if (!w->emb || !w->h_shared || !aligned16(w->emb) || !aligned16(w->h_shared)) return PE_ERR_INVALID_ARG;
+  const PrepArgs pa = make_prep_args(*cfg, prev_tokens, prev_pos, num_accepted, bonus, block_table, kv->num_pages, ids,
+                                     pos, slot, rej, msk, hmap, rows, nval, drows, err_word);
   const ScatterArgs sa = make_scatter_args(*cfg, w, target_hidden, ids, msk, hmap, rows, nval, x0, err_word);
   const InitArgs ia = make_init_args(*cfg, p, ws, rows, nval, pos, slot, err_word);
-  PE_TRY_CUDA(launch_scatter_init(sa, ia, s));
+  trace(0, s);
+  PE_TRY_CUDA(launch_step_prologue(pa, sa, ia, s));
+  trace(1, s);
   trace(2, s);
   VerifyArgs va{};
   va.B = cfg->B; va.K = cfg->K; va.draft = draft_tokens; va.target = target_tokens; va.acc_out = num_accepted_out;

@@ -165,8 +165,9 @@ struct InjectArgs {
   int32_t* err;
 };
 cudaError_t launch_inject_init(const InjectArgs& a, cudaStream_t s);
-// Input rows (ScatterArgs) and the forward prologue (InitArgs) in one launch.
-cudaError_t launch_scatter_init(const ScatterArgs& sa, const InitArgs& ia, cudaStream_t s);
+// pe_step's first launch: the batch rebuild (PrepArgs), the input rows (ScatterArgs, every
+// CTA placing one sequence's rows itself) and the forward prologue (InitArgs).
+cudaError_t launch_step_prologue(const PrepArgs& pa, const ScatterArgs& sa, const InitArgs& ia, cudaStream_t s);
 
 // ----------------------------------------------------------------------------- RMSNorm
 

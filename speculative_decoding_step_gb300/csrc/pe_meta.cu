@@ -311,10 +311,61 @@ cudaError_t launch_forward_init(const InitArgs& a, cudaStream_t s) {
 
 constexpr int kScatterRowsPerCta = 4;
 
-// One CTA's rows (thread 0 issues every copy).
-PE_DEV void scatter_body(const ScatterArgs& a, int cta) {
+// Copies of up to RPC input rows by one thread (it issues every copy): row k goes to x0
+// row dst[k]; kind 1: concat(emb[tok], hidden[hmp]), kind 2: the MASK row
+// concat(emb(mask), h_shared), staged in shared memory once; kind 0: nothing.
+PE_DEV void copy_rows(const ScatterArgs& a, const int (&kind)[kScatterRowsPerCta], const int (&tok)[kScatterRowsPerCta],
+                      const int (&hmp)[kScatterRowsPerCta], const int (&dst)[kScatterRowsPerCta]) {
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar;
+  constexpr int RPC = kScatterRowsPerCta;
+  const uint32_t rb = (uint32_t)a.d * a.elem_bytes;  // bytes of one half row
+  const uint8_t* emb = static_cast<const uint8_t*>(a.emb);
+  const uint8_t* hid = static_cast<const uint8_t*>(a.hidden);
+  uint8_t* x0 = static_cast<uint8_t*>(a.x0);
+  const uint32_t base = smem_u32(sm);
+  const uint32_t mask_slot = base + (uint32_t)(2 * RPC) * rb;  // [emb(mask) | h_shared]
+  uint32_t bytes = 0;
+  bool any_mask = false;
+#pragma unroll
+  for (int k = 0; k < RPC; ++k) {
+    if (kind[k] == 1) bytes += 2 * rb;
+    if (kind[k] == 2) any_mask = true;
+  }
+  if (any_mask) bytes += 2 * rb;
+  if (bytes == 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  mbar_expect_tx(b, bytes);
+#pragma unroll
+  for (int k = 0; k < RPC; ++k) {
+    if (kind[k] != 1) continue;
+    bulk_g2s(base + (uint32_t)(2 * k) * rb, emb + (size_t)tok[k] * rb, rb, b);
+    bulk_g2s(base + (uint32_t)(2 * k + 1) * rb, hid + (size_t)hmp[k] * rb, rb, b);
+  }
+  if (any_mask) {
+    bulk_g2s(mask_slot, emb + (size_t)a.vocab * rb, rb, b);
+    bulk_g2s(mask_slot + rb, a.h_shared, rb, b);
+  }
+  if (!mbar_wait(b, 0, a.err, nullptr)) return;
+  fence_proxy_async_smem();
+#pragma unroll
+  for (int k = 0; k < RPC; ++k) {
+    uint8_t* d = x0 + (size_t)dst[k] * 2 * rb;
+    if (kind[k] == 1) {
+      bulk_s2g(d, base + (uint32_t)(2 * k) * rb, rb);
+      bulk_s2g(d + rb, base + (uint32_t)(2 * k + 1) * rb, rb);
+    } else if (kind[k] == 2) {
+      bulk_s2g(d, mask_slot, 2 * rb);
+    }
+  }
+  bulk_commit();
+  bulk_wait_all();
+}
+
+// One CTA's rows of the compacted list (pe_scatter_hidden): rows i0 .. i0 + RPC - 1.
+PE_DEV void scatter_body(const ScatterArgs& a, int cta) {
   constexpr int RPC = kScatterRowsPerCta;
   const int i0 = cta * RPC;
   // the row count and this CTA's rows in one round trip (rows past the count are -1
@@ -326,7 +377,7 @@ PE_DEV void scatter_body(const ScatterArgs& a, int cta) {
   n = n < 0 ? 0 : (n > a.R ? a.R : n);
   if (i0 >= n) return;
   const int i1 = i0 + RPC < n ? i0 + RPC : n;
-  int msk[RPC], tok[RPC], hmp[RPC];
+  int msk[RPC], tok[RPC], hmp[RPC], kind[RPC], dst[RPC];
 #pragma unroll
   for (int k = 0; k < RPC; ++k) {
     const int row = rows[k];
@@ -335,64 +386,48 @@ PE_DEV void scatter_body(const ScatterArgs& a, int cta) {
     tok[k] = ok ? a.input_ids[row] : 0;
     hmp[k] = ok ? a.hidden_map[row] : 0;
   }
-  const uint32_t rb = (uint32_t)a.d * a.elem_bytes;  // bytes of one half row
-  const uint8_t* emb = static_cast<const uint8_t*>(a.emb);
-  const uint8_t* hid = static_cast<const uint8_t*>(a.hidden);
-  uint8_t* x0 = static_cast<uint8_t*>(a.x0);
-  const uint32_t base = smem_u32(sm);
-  const uint32_t mask_slot = base + (uint32_t)(2 * RPC) * rb;  // [emb(mask) | h_shared]
-  const uint32_t b = smem_u32(&bar);
-  mbar_init(b, 1);
-  fence_mbar_init();
-
-  // which rows need what
-  int kind[RPC];      // 0 skip, 1 regular, 2 MASK
-  const uint8_t* src_e[RPC];
-  const uint8_t* src_h[RPC];
-  uint32_t bytes = 0;
-  bool any_mask = false;
 #pragma unroll
   for (int k = 0; k < RPC; ++k) {
     kind[k] = 0;
-    src_e[k] = src_h[k] = nullptr;
+    dst[k] = i0 + k;
     if (i0 + k >= i1) continue;
     const int row = rows[k];
     if (row < 0 || row >= a.R) { set_err(a.err, PE_DEV_BAD_ROW); continue; }
-    if (msk[k]) { kind[k] = 2; any_mask = true; continue; }
+    if (msk[k]) { kind[k] = 2; continue; }
     if (tok[k] < 0 || tok[k] > a.vocab) { set_err(a.err, PE_DEV_BAD_TOKEN); continue; }
     if (hmp[k] < 0 || hmp[k] >= a.n_hidden) { set_err(a.err, PE_DEV_BAD_ROW); continue; }
     kind[k] = 1;
-    src_e[k] = emb + (size_t)tok[k] * rb;
-    src_h[k] = hid + (size_t)hmp[k] * rb;
-    bytes += 2 * rb;
   }
-  if (any_mask) bytes += 2 * rb;
-  if (bytes == 0) return;
-  mbar_expect_tx(b, bytes);
-#pragma unroll
-  for (int k = 0; k < RPC; ++k) {  // kind is 0 past this CTA's rows
-    if (kind[k] != 1) continue;
-    bulk_g2s(base + (uint32_t)(2 * k) * rb, src_e[k], rb, b);
-    bulk_g2s(base + (uint32_t)(2 * k + 1) * rb, src_h[k], rb, b);
-  }
-  if (any_mask) {
-    bulk_g2s(mask_slot, emb + (size_t)a.vocab * rb, rb, b);
-    bulk_g2s(mask_slot + rb, a.h_shared, rb, b);
-  }
-  if (!mbar_wait(b, 0, a.err, nullptr)) return;
-  fence_proxy_async_smem();
+  copy_rows(a, kind, tok, hmp, dst);
+}
+
+// The input rows of sequence b straight from the previous verify batch (pe_step): the
+// sequence's valid rows are, in the rebuild's order, its copy slots 0..a (accepted
+// context rows, then the NTP row) and its K-1 MASK rows; they land at compacted rows
+// base + 0 .. base + a + K - 1, base = the valid rows of the sequences before b.  CTA
+// group `grp` copies the sequence's valid rows grp*RPC .. grp*RPC + RPC - 1.
+PE_DEV void scatter_seq_body(const PrepArgs& p, const ScatterArgs& a, int b, int grp, int base) {
+  constexpr int RPC = kScatterRowsPerCta;
+  const int K = p.K;
+  int acc = p.num_accepted[b];
+  acc = acc < 0 ? 0 : (acc > K ? K : acc);  // the rebuild reports a bad count and clamps it the same way
+  const int v0 = grp * RPC, nv = acc + K;
+  if (v0 >= nv) return;
+  int kind[RPC], tok[RPC], hmp[RPC], dst[RPC];
 #pragma unroll
   for (int k = 0; k < RPC; ++k) {
-    uint8_t* dst = x0 + (size_t)(i0 + k) * 2 * rb;
-    if (kind[k] == 1) {
-      bulk_s2g(dst, base + (uint32_t)(2 * k) * rb, rb);
-      bulk_s2g(dst + rb, base + (uint32_t)(2 * k + 1) * rb, rb);
-    } else if (kind[k] == 2) {
-      bulk_s2g(dst, mask_slot, 2 * rb);
-    }
+    const int v = v0 + k;
+    kind[k] = 0;
+    tok[k] = hmp[k] = 0;
+    dst[k] = base + v;
+    if (v >= nv) continue;
+    if (v > acc) { kind[k] = 2; continue; }  // MASK row m = v - acc
+    tok[k] = v < acc ? p.prev_tokens[(size_t)b * (K + 1) + v + 1] : p.bonus[b];
+    hmp[k] = b * (K + 1) + v;
+    if (tok[k] < 0 || tok[k] >= a.vocab) { set_err(a.err, PE_DEV_BAD_TOKEN); continue; }
+    kind[k] = 1;
   }
-  bulk_commit();
-  bulk_wait_all();
+  copy_rows(a, kind, tok, hmp, dst);
 }
 
 __global__ void __launch_bounds__(32) scatter_kernel(const ScatterArgs a) {
@@ -420,30 +455,55 @@ cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
   return launch_pdl(scatter_kernel, dim3(grid), dim3(32), smem, s, a);
 }
 
-// Input rows and the forward prologue in one launch (pe_step): both read only the
-// batch rebuild's outputs, so the last CTA runs the prologue while the others copy.
-constexpr int kScatterInitThreads = 256;
+// pe_step's first launch: the batch rebuild, the input rows and the forward prologue.  The
+// last CTA rebuilds the batch (metadata, compaction) and then builds the prologue from it;
+// every other CTA copies up to RPC input rows of one sequence, finding where they land from
+// the accepted counts alone (the rows of the sequences before it), so no CTA waits for the
+// rebuild.
+constexpr int kStepPrologueThreads = 512;
 
-__global__ void __launch_bounds__(kScatterInitThreads) scatter_init_kernel(const ScatterArgs sa, const InitArgs ia) {
+__global__ void __launch_bounds__(kStepPrologueThreads)
+    step_prologue_kernel(const PrepArgs pa, const ScatterArgs sa, const InitArgs ia, int groups) {
+  __shared__ int part_s[kStepPrologueThreads / 32];
   pdl_wait();
   pdl_trigger();
-  if (blockIdx.x == gridDim.x - 1) init_body(ia);
-  else if (threadIdx.x == 0) scatter_body(sa, blockIdx.x);
+  if (blockIdx.x == gridDim.x - 1) {
+    prepare_body(pa);
+    __syncthreads();  // the rebuild's outputs (global memory) are visible to the whole CTA
+    init_body(ia);
+    return;
+  }
+  const int b = blockIdx.x / groups, grp = blockIdx.x - b * groups;
+  int part = 0;  // valid rows of sequences 0 .. b-1, each a + K (a clamped to [0, K])
+  for (int bb = threadIdx.x; bb < b; bb += blockDim.x) {
+    const int x = pa.num_accepted[bb];
+    part += (x < 0 ? 0 : (x > pa.K ? pa.K : x)) + pa.K;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+  if ((threadIdx.x & 31) == 0) part_s[threadIdx.x >> 5] = part;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int base = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) base += part_s[w];
+    scatter_seq_body(pa, sa, b, grp, base);
+  }
 }
 
-cudaError_t launch_scatter_init(const ScatterArgs& sa, const InitArgs& ia, cudaStream_t s) {
+cudaError_t launch_step_prologue(const PrepArgs& pa, const ScatterArgs& sa, const InitArgs& ia, cudaStream_t s) {
   const size_t smem = scatter_smem_bytes(sa.d, sa.elem_bytes);
   static bool configured[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(scatter_init_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(step_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kScatterSmemMax);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int grid = (sa.R + kScatterRowsPerCta - 1) / kScatterRowsPerCta + 1;
-  return launch_pdl(scatter_init_kernel, dim3(grid), dim3(kScatterInitThreads), smem, s, sa, ia);
+  const int groups = (2 * pa.K + kScatterRowsPerCta - 1) / kScatterRowsPerCta;  // a + K <= 2K rows per sequence
+  const int grid = pa.B * groups + 1;
+  return launch_pdl(step_prologue_kernel, dim3(grid), dim3(kStepPrologueThreads), smem, s, pa, sa, ia, groups);
 }
 
 // ============================================================================= RMSNorm

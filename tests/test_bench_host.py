@@ -84,9 +84,13 @@ def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
 
 
 def test_stage_names_match_trace_points():
-    """One name per interval between the library's trace points (8 + 7 L boundaries)."""
+    """One name per stage: pe_step's first launch spans trace points 0..3, every later stage one
+    interval between consecutive points, the last ending at the final point (8 + 7 L points)."""
     for L in (1, 2, 4):
-        assert len(bench.stage_names(L)) == 8 + 7 * L - 1
+        pts = bench.stage_points(L)
+        assert len(bench.stage_names(L)) == len(pts)
+        assert pts[0] == (0, 3) and pts[-1][1] == 8 + 7 * L - 1
+        assert all(a[1] == b[0] for a, b in zip(pts, pts[1:]))
 
 
 def test_stage_costs_split_the_round_cost():
