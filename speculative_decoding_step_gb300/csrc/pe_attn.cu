@@ -535,10 +535,78 @@ static cudaError_t launch_attn_typed(const CUtensorMap& tk, const CUtensorMap& t
 }
 
 // Merge of the chunks of every (sequence, kv head) whose range took more than
-// one chunk: one warp per (sequence, kv head, query vector), lanes over
-// head_dim.  out = sum_c w_c O_c / sum_c w_c l_c with w_c = 2^(m_c - max_c m_c);
-// the weighted sum runs in chunk order (deterministic).
+// one chunk: one warp per (sequence, kv head, group of 32 / LPR query vectors),
+// LPR lanes per query vector holding 8 of its head_dim values each.
+// out = sum_c w_c O_c / sum_c w_c l_c with w_c = 2^(m_c - max_c m_c); every sum
+// runs in a fixed order (deterministic): the statistics lane by lane and then a
+// tree over the vector's lanes, the weighted outputs in chunk order.
 constexpr int kMergeThreads = 256;
+
+template <int HD>
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_rows_kernel(const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int LPR = HD / 8;      // lanes per query vector (8 values each)
+  constexpr int RPW = 32 / LPR;    // query vectors per warp
+  constexpr int GROUPS = kAttnRows / RPW;
+  const int G = a.n_q / a.n_kv, lane = threadIdx.x & 31, sub = lane % LPR, rw = lane / LPR;
+  const int ldq = a.n_q * HD;
+  const long long n_tasks = (long long)a.B * a.n_kv * GROUPS;
+  const long long warps = (long long)gridDim.x * (kMergeThreads / 32);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  for (long long task = ((long long)blockIdx.x * kMergeThreads + threadIdx.x) >> 5; task < n_tasks; task += warps) {
+    const int grp = (int)(task % GROUPS);
+    const int bg = (int)(task / GROUPS);
+    const int b = bg / a.n_kv, g = bg - (bg / a.n_kv) * a.n_kv;
+    // the sequence's metadata in one round trip
+    const int nc = a.n_chunks[b], len = a.seq_len[b], ibase = a.item_base[b], start = a.seq_start[b];
+    const int M = min(len * G, kAttnRows);
+    if (nc <= 1 || grp * RPW >= M) continue;  // the same for the whole warp
+    const int m = grp * RPW + rw;
+    const bool valid = m < M;
+    const size_t base = (size_t)(ibase + g * nc) * kAttnRows + m;  // partial row of chunk 0
+    float mx = -INFINITY;
+    if (valid)
+      for (int c = sub; c < nc; c += LPR) mx = fmaxf(mx, __ldcg(a.part_m + base + (size_t)c * kAttnRows));
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    float L = 0.f;
+    if (valid)
+      for (int c = sub; c < nc; c += LPR) {
+        const float mc = __ldcg(a.part_m + base + (size_t)c * kAttnRows);
+        L += (mc == -INFINITY ? 0.f : exp2f(mc - mx)) * __ldcg(a.part_l + base + (size_t)c * kAttnRows);
+      }
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+    if (!valid) continue;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < nc; ++c) {  // chunk order
+      const size_t pr = base + (size_t)c * kAttnRows;
+      const float mc = __ldcg(a.part_m + pr);
+      const float wk = mc == -INFINITY ? 0.f : exp2f(mc - mx);
+      const float4* src = reinterpret_cast<const float4*>(a.part_o + pr * HD + sub * 8);
+      const float4 u0 = __ldcg(src), u1 = __ldcg(src + 1);
+      acc[0] += wk * u0.x; acc[1] += wk * u0.y; acc[2] += wk * u0.z; acc[3] += wk * u0.w;
+      acc[4] += wk * u1.x; acc[5] += wk * u1.y; acc[6] += wk * u1.z; acc[7] += wk * u1.w;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16* dst = out + (size_t)(start + m / G) * ldq + (size_t)(g * G + m % G) * HD + (size_t)sub * 8;
+    uint4 pk;
+    pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    pk.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+    pk.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(dst) = pk;
+  }
+}
+
+// The same merge for few (sequence, kv head) pairs with many chunks each: one warp
+// per (sequence, kv head, query vector), lanes over head_dim, the chunk statistics
+// one chunk per lane and eight chunks' outputs in flight at once.  out = sum_c w_c O_c / sum_c w_c l_c with w_c = 2^(m_c - max_c m_c);
+// the weighted sum runs in chunk order (deterministic).
 
 template <int HD>
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnArgs a) {
@@ -622,12 +690,20 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnArg
   }
 }
 
+// Many (sequence, kv head) pairs (large batches, few chunks each): several query vectors
+// per warp, so that most warps do work; few pairs (small batches, many chunks each): a warp
+// per query vector with its chunks spread over the lanes.
+constexpr int kMergeRowsMinPairs = 128;
+
 template <int HD>
 static cudaError_t launch_merge_typed(const AttnArgs& a, int sms, cudaStream_t s) {
-  const long long warps = (long long)a.B * a.n_kv * kAttnRows;
+  const bool rows = (long long)a.B * a.n_kv >= kMergeRowsMinPairs;
+  const int per_warp = rows ? 32 / (HD / 8) : 1;
+  const long long warps = (long long)a.B * a.n_kv * (kAttnRows / per_warp);
   const long long need = (warps + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
-  const int grid = (int)std::min<long long>(need, 64LL * sms);  // about one task per warp: two round trips each
+  const int grid = (int)std::min<long long>(need, 64LL * sms);
   if (grid <= 0) return cudaSuccess;
+  if (rows) return launch_pdl(attn_merge_rows_kernel<HD>, dim3(grid), dim3(kMergeThreads), 0, s, a);
   return launch_pdl(attn_merge_kernel<HD>, dim3(grid), dim3(kMergeThreads), 0, s, a);
 }
 

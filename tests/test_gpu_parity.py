@@ -54,6 +54,10 @@ SMALL = {
     # pairs
     "bf16-fold": _small(B=6, K=8, d=192, n_q=4, n_kv=2, ffn=384, vocab=1037, n_layers=2, seed=16),
     "bf16-fold-pairs": _small(B=20, K=8, d=192, n_q=4, n_kv=2, ffn=384, vocab=1037, seed=17),
+    # 128 (sequence, kv head) pairs with several chunks each: the chunk merge that packs
+    # several query vectors into a warp
+    "bf16-many-pairs": _small(B=64, K=2, n_q=4, n_kv=2, d=128, ffn=128, vocab=500, prefix_args=(300, 900),
+                              seed=18),
     "f32-c0": config(0),
     "f32-L2": _small(dtype="f32", n_layers=2, seed=11),
 }
