@@ -549,6 +549,8 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_rows_kernel(const At
   constexpr int LPR = HD / 8;      // lanes per query vector (8 values each)
   constexpr int RPW = 32 / LPR;    // query vectors per warp
   constexpr int GROUPS = kAttnRows / RPW;
+  constexpr int CB = 2;            // chunks whose outputs are loaded with the statistics (CB <= LPR)
+  static_assert(CB <= LPR, "a prefetched chunk's weight is held by a lane of its vector");
   const int G = a.n_q / a.n_kv, lane = threadIdx.x & 31, sub = lane % LPR, rw = lane / LPR;
   const int ldq = a.n_q * HD;
   const long long n_tasks = (long long)a.B * a.n_kv * GROUPS;
@@ -565,25 +567,50 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_rows_kernel(const At
     const int m = grp * RPW + rw;
     const bool valid = m < M;
     const size_t base = (size_t)(ibase + g * nc) * kAttnRows + m;  // partial row of chunk 0
-    float mx = -INFINITY;
-    if (valid)
-      for (int c = sub; c < nc; c += LPR) mx = fmaxf(mx, __ldcg(a.part_m + base + (size_t)c * kAttnRows));
+    // one round trip for the data: the statistics of chunk `sub` (and of every LPR-th one
+    // after it) and the outputs of the first CB chunks are all in flight together
+    float mc_l = -INFINITY, lc_l = 0.f;
+    if (valid && sub < nc) {
+      mc_l = __ldcg(a.part_m + base + (size_t)sub * kAttnRows);
+      lc_l = __ldcg(a.part_l + base + (size_t)sub * kAttnRows);
+    }
+    float4 o[CB][2];
 #pragma unroll
-    for (int o = LPR / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    float L = 0.f;
+    for (int k = 0; k < CB; ++k)
+      if (valid && k < nc) {
+        const float4* src = reinterpret_cast<const float4*>(a.part_o + (base + (size_t)k * kAttnRows) * HD + sub * 8);
+        o[k][0] = __ldcg(src);
+        o[k][1] = __ldcg(src + 1);
+      }
+    float mx = mc_l;
     if (valid)
-      for (int c = sub; c < nc; c += LPR) {
+      for (int c = sub + LPR; c < nc; c += LPR) mx = fmaxf(mx, __ldcg(a.part_m + base + (size_t)c * kAttnRows));
+#pragma unroll
+    for (int o2 = LPR / 2; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o2));
+    const float w_l = mc_l == -INFINITY ? 0.f : exp2f(mc_l - mx);  // weight of chunk `sub`
+    float L = w_l * lc_l;
+    if (valid)
+      for (int c = sub + LPR; c < nc; c += LPR) {
         const float mc = __ldcg(a.part_m + base + (size_t)c * kAttnRows);
         L += (mc == -INFINITY ? 0.f : exp2f(mc - mx)) * __ldcg(a.part_l + base + (size_t)c * kAttnRows);
       }
 #pragma unroll
-    for (int o = LPR / 2; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
-    if (!valid) continue;
+    for (int o2 = LPR / 2; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o2);
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    const int lane0 = lane - sub;  // the vector's first lane
+#pragma unroll
+    for (int k = 0; k < CB; ++k) {  // chunk order; chunk k's weight lives in lane lane0 + k
+      const float wk = __shfl_sync(0xFFFFFFFFu, w_l, lane0 + k);
+      if (k < nc) {
+        acc[0] += wk * o[k][0].x; acc[1] += wk * o[k][0].y; acc[2] += wk * o[k][0].z; acc[3] += wk * o[k][0].w;
+        acc[4] += wk * o[k][1].x; acc[5] += wk * o[k][1].y; acc[6] += wk * o[k][1].z; acc[7] += wk * o[k][1].w;
+      }
+    }
+    if (!valid) continue;
 #pragma unroll 4
-    for (int c = 0; c < nc; ++c) {  // chunk order
+    for (int c = CB; c < nc; ++c) {  // long ranges: the rest, in chunk order
       const size_t pr = base + (size_t)c * kAttnRows;
       const float mc = __ldcg(a.part_m + pr);
       const float wk = mc == -INFINITY ? 0.f : exp2f(mc - mx);

@@ -455,22 +455,210 @@ cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
   return launch_pdl(scatter_kernel, dim3(grid), dim3(32), smem, s, a);
 }
 
+// Block-wide exclusive prefix sum of v in thread order (every thread of the CTA calls it);
+// `total` receives the sum over the CTA.  warp_s: 33 ints of shared memory.
+PE_DEV int block_exclusive_scan(int v, int* warp_s, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_s[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nw ? warp_s[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < nw) warp_s[lane] = wi - w;
+    if (lane == 31) warp_s[32] = wi;
+  }
+  __syncthreads();
+  const int r = warp_s[warp] + incl - v;
+  total = warp_s[32];
+  __syncthreads();  // warp_s may be reused
+  return r;
+}
+
+// pe_step's batch rebuild and forward prologue in one CTA, with the same results as the
+// rebuild followed by the prologue (prepare_body, init_body), in fewer memory round trips:
+// a sequence's valid rows are contiguous in the compacted list (its copy slots 0..a, then
+// its K-1 MASK rows), so the accepted counts alone give each sequence's offset (a prefix sum
+// of a + K over the sequences before it), its row count and, with its positions, its largest
+// position; every padded row then finds its compacted index directly and writes the
+// prologue's per-row metadata in the same pass.  Sequences are taken kStepSeqChunk at a time,
+// one thread each.
+constexpr int kStepPrologueThreads = 512;
+constexpr int kStepSeqChunk = kStepPrologueThreads;
+
+PE_DEV void step_meta_body(const PrepArgs& a, const InitArgs& ia) {
+  __shared__ int warp_s[33];
+  __shared__ int acc_s[kStepSeqChunk], base_s[kStepSeqChunk];
+  __shared__ long long len_s[kStepPrologueThreads / 32];
+  __shared__ int chunk_s;
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int K = a.K, S = 2 * K, R = a.B * S;
+  for (int i = tid; i < ia.n_counters; i += NT) ia.counters[i] = 0;
+  for (int i = tid; i < ia.T; i += NT) ia.keys[i] = 0ull;
+  int carry = 0;           // compacted rows of the sequences before the chunk (the same in every thread)
+  long long len_part = 0;  // this thread's share of the summed causal ranges
+  for (int c0 = 0; c0 < a.B; c0 += kStepSeqChunk) {
+    const int b = c0 + tid;
+    const bool own = tid < kStepSeqChunk && b < a.B;
+    int acc = 0;
+    if (own) {
+      acc = a.num_accepted[b];
+      if (acc < 0 || acc > K) {
+        set_err(a.err, PE_DEV_BAD_ACCEPTED);
+        acc = acc < 0 ? 0 : K;
+      }
+    }
+    int total = 0;
+    const int excl = block_exclusive_scan(own ? acc + K : 0, warp_s, total);
+    if (own) {
+      acc_s[tid] = acc;
+      base_s[tid] = carry + excl;
+      // the largest position of the sequence's valid rows: its context rows, and the last
+      // MASK row (the NTP row itself when K = 1)
+      const int32_t* pp = a.prev_pos + (size_t)b * (K + 1);
+      int mx = pp[acc] + K - 1;
+      for (int r = 0; r < acc; ++r) mx = max(mx, pp[r]);
+      ia.seq_start[b] = carry + excl;
+      ia.seq_len[b] = acc + K;
+      ia.seq_maxpos[b] = mx;
+      len_part += (long long)mx + 1;
+    }
+    __syncthreads();
+    const int r0 = c0 * S, r1 = min(a.B, c0 + kStepSeqChunk) * S;
+    for (int row = r0 + tid; row < r1; row += NT) {
+      const int bb = row / S, r = row - bb * S, li = bb - c0;
+      const int ac = acc_s[li];
+      const int32_t* pt = a.prev_tokens + (size_t)bb * (K + 1);
+      const int32_t* pp = a.prev_pos + (size_t)bb * (K + 1);
+      int tok, pos, hmap, rej = 0, msk = 0, draft_k = -1;
+      if (r < ac) {          // accepted context row: token at p+1, hidden state of p
+        tok = pt[r + 1];
+        pos = pp[r];
+        hmap = bb * (K + 1) + r;
+      } else if (r == ac) {  // NTP row: bonus token with h_context
+        tok = a.bonus[bb];
+        pos = pp[ac];
+        hmap = bb * (K + 1) + ac;
+        draft_k = 0;
+      } else if (r <= K) {   // rejected draft position
+        tok = 0;
+        pos = pp[r];
+        hmap = bb * (K + 1) + r;
+        rej = 1;
+      } else {               // MASK slot m = r - K
+        const int m = r - K;
+        tok = a.vocab;
+        pos = pp[ac] + m;
+        hmap = -1;
+        msk = 1;
+        draft_k = m;
+      }
+      if (!msk && (tok < 0 || tok >= a.vocab)) set_err(a.err, PE_DEV_BAD_TOKEN);
+      long long slot = -1;
+      if (!rej) {
+        const int pi = pos / a.page_size;
+        if (pos < 0 || pi >= a.max_pages) {
+          set_err(a.err, PE_DEV_BAD_POSITION);
+        } else {
+          const int page = a.block_table[(size_t)bb * a.max_pages + pi];
+          if (page < 0 || page >= a.num_pages) set_err(a.err, PE_DEV_BAD_PAGE);
+          else slot = (long long)page * a.page_size + pos % a.page_size;
+        }
+      }
+      a.input_ids[row] = tok;
+      a.positions[row] = pos;
+      a.slot_mapping[row] = slot;
+      a.is_rejected[row] = (uint8_t)rej;
+      a.is_mask[row] = (uint8_t)msk;
+      a.hidden_map[row] = hmap;
+      if (!rej) {
+        const int idx = base_s[li] + (r <= ac ? r : r - (K - ac));
+        a.row_list[idx] = row;
+        if (draft_k >= 0) a.draft_rows[bb * K + draft_k] = idx;
+        ia.tok_pos[idx] = pos;
+        ia.tok_slot[idx] = slot;
+        ia.tok_seq[idx] = bb;
+      }
+    }
+    carry += total;
+    __syncthreads();  // acc_s / base_s are refilled by the next chunk
+  }
+  if (tid == 0) *a.n_valid = carry;
+  for (int i = carry + tid; i < R; i += NT) {
+    a.row_list[i] = -1;
+    ia.tok_pos[i] = 0;
+    ia.tok_slot[i] = -1;
+    ia.tok_seq[i] = 0;
+  }
+  // attention work list, as the prologue builds it: the chunk length from the summed causal
+  // ranges, then per sequence its chunk count and item offset (a prefix sum in sequence order)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) len_part += __shfl_xor_sync(0xFFFFFFFFu, len_part, o);
+  if ((tid & 31) == 0) len_s[tid >> 5] = len_part;
+  __syncthreads();
+  if (tid == 0) {
+    long long tot = 0;
+    for (int w = 0; w < NT / 32; ++w) tot += len_s[w];
+    long long per = (tot * ia.n_kv + ia.target_items - 1) / ia.target_items;
+    per = ((per + 63) / 64) * 64;
+    chunk_s = (int)(per < ia.min_chunk ? ia.min_chunk : per);
+  }
+  __syncthreads();
+  const int chunk = chunk_s;
+  int items = 0;
+  for (int c0 = 0; c0 < a.B; c0 += kStepSeqChunk) {
+    const int b = c0 + tid;
+    const bool own = tid < kStepSeqChunk && b < a.B;
+    const int nc = own ? (ia.seq_maxpos[b] + 1 + chunk - 1) / chunk : 0;  // written by this thread above
+    int total = 0;
+    const int excl = block_exclusive_scan(nc * ia.n_kv, warp_s, total);
+    if (own) {
+      ia.n_chunks[b] = nc;
+      ia.item_base[b] = items + excl;
+    }
+    items += total;
+  }
+  if (items > ia.max_items) {  // cannot happen with the host's sizing; keep the list in bounds
+    if (tid == 0) set_err(ia.err, PE_DEV_BAD_ROW);
+    items = 0;
+  }
+  if (tid == 0) *ia.n_items = items;
+  if (items == 0) return;
+  for (int b = tid; b < a.B; b += NT) {
+    const int L = ia.seq_maxpos[b] + 1;
+    const int nc = ia.n_chunks[b];
+    int it = ia.item_base[b];
+    for (int g = 0; g < ia.n_kv; ++g)
+      for (int c = 0; c < nc; ++c) {
+        const int c0 = c * chunk;
+        const int c1 = c0 + chunk < L ? c0 + chunk : L;
+        ia.items[it++] = make_int4(b, g, c0, c1);
+      }
+  }
+}
+
 // pe_step's first launch: the batch rebuild, the input rows and the forward prologue.  The
 // last CTA rebuilds the batch (metadata, compaction) and then builds the prologue from it;
 // every other CTA copies up to RPC input rows of one sequence, finding where they land from
 // the accepted counts alone (the rows of the sequences before it), so no CTA waits for the
 // rebuild.
-constexpr int kStepPrologueThreads = 512;
-
 __global__ void __launch_bounds__(kStepPrologueThreads)
     step_prologue_kernel(const PrepArgs pa, const ScatterArgs sa, const InitArgs ia, int groups) {
   __shared__ int part_s[kStepPrologueThreads / 32];
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == gridDim.x - 1) {
-    prepare_body(pa);
-    __syncthreads();  // the rebuild's outputs (global memory) are visible to the whole CTA
-    init_body(ia);
+    step_meta_body(pa, ia);
     return;
   }
   const int b = blockIdx.x / groups, grp = blockIdx.x - b * groups;
@@ -531,7 +719,11 @@ PE_DEV void store4<__nv_bfloat16>(__nv_bfloat16* y, float a, float b, float c, f
 
 constexpr int kNormMaxSplits = 16;  // split-K ways a GEMM may leave to the norm
 
-template <typename OutT, typename GT, int VPT>
+// SPLIT: the producing GEMM left split-K partials to sum (a.n_splits > 0).  A separate
+// instantiation without them keeps the register count low (the partial loads in flight
+// take 128 registers; without them several CTAs fit on an SM, and a many-row norm
+// runs in one wave).
+template <typename OutT, typename GT, int VPT, bool SPLIT>
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a) {
   __shared__ float warp_ss[kNormThreads / 32];
   const int row = blockIdx.x, tid = threadIdx.x;
@@ -549,7 +741,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
   pdl_trigger();
   // every count / index this row needs, in one round trip
   const int dev_n = a.n_rows_dev != nullptr ? *a.n_rows_dev : a.n_rows;
-  const int dev_g = a.n_splits == 0 ? 0
+  const int dev_g = !SPLIT ? 0
                     : (a.g_ntok_dev == nullptr ? a.g_ntok
                        : (a.g_ntok_dev == a.n_rows_dev ? dev_n : *a.g_ntok_dev));
   const int mapped = a.row_map != nullptr ? a.row_map[row] : row;
@@ -562,7 +754,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
   }
   float4 v[VPT];
   float ss = 0.f;
-  if (a.n_splits > 0) {
+  if constexpr (SPLIT) {
     // x_new = x + the producing GEMM's split-K partials (split order).  Units are numbered
     // as the GEMM numbers them over its live token tiles: ((tile_f * ntl + tile_t) * splits + split).
     const int n_eff = min(a.g_ntok, max(dev_g, a.g_ntok_min));
@@ -633,22 +825,26 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
   }
 }
 
-template <typename OutT, typename GT>
+template <typename OutT, typename GT, bool SPLIT>
 static cudaError_t launch_norm_typed(const NormArgs& a, cudaStream_t s) {
   const int per = (a.d / 4 + kNormThreads - 1) / kNormThreads;  // float4 per thread
   const dim3 grid(a.n_rows), block(kNormThreads);
-  if (per <= 1) return launch_pdl(rmsnorm_kernel<OutT, GT, 1>, grid, block, 0, s, a);
-  if (per <= 2) return launch_pdl(rmsnorm_kernel<OutT, GT, 2>, grid, block, 0, s, a);
-  if (per <= 4) return launch_pdl(rmsnorm_kernel<OutT, GT, 4>, grid, block, 0, s, a);
-  if (per <= 8) return launch_pdl(rmsnorm_kernel<OutT, GT, 8>, grid, block, 0, s, a);
-  if (per <= 16) return launch_pdl(rmsnorm_kernel<OutT, GT, 16>, grid, block, 0, s, a);
+  if (per <= 1) return launch_pdl(rmsnorm_kernel<OutT, GT, 1, SPLIT>, grid, block, 0, s, a);
+  if (per <= 2) return launch_pdl(rmsnorm_kernel<OutT, GT, 2, SPLIT>, grid, block, 0, s, a);
+  if (per <= 4) return launch_pdl(rmsnorm_kernel<OutT, GT, 4, SPLIT>, grid, block, 0, s, a);
+  if (per <= 8) return launch_pdl(rmsnorm_kernel<OutT, GT, 8, SPLIT>, grid, block, 0, s, a);
+  if (per <= 16) return launch_pdl(rmsnorm_kernel<OutT, GT, 16, SPLIT>, grid, block, 0, s, a);
   return cudaErrorInvalidValue;  // d > 16384 is rejected by the config check
 }
 
 cudaError_t launch_rmsnorm(const NormArgs& a, pe_dtype dt, cudaStream_t s) {
   if (a.n_rows == 0) return cudaSuccess;
-  if (dt == PE_BF16) return launch_norm_typed<__nv_bfloat16, __nv_bfloat16>(a, s);
-  return launch_norm_typed<float, float>(a, s);
+  if (a.n_splits > 0) {
+    if (dt == PE_BF16) return launch_norm_typed<__nv_bfloat16, __nv_bfloat16, true>(a, s);
+    return launch_norm_typed<float, float, true>(a, s);
+  }
+  if (dt == PE_BF16) return launch_norm_typed<__nv_bfloat16, __nv_bfloat16, false>(a, s);
+  return launch_norm_typed<float, float, false>(a, s);
 }
 
 }  // namespace pe
