@@ -12,8 +12,10 @@
 // range zero-filled) into an mbarrier ring of 64-position blocks (5 stages
 // at head_dim 64, 2 at head_dim 128: two CTAs share an SM).
 // Warp 1 issues the 5th-generation tensor-core MMAs: S = Q K^T (M = 128 query
-// vectors, N = 64 positions) into one of two TMEM buffers, and O += P V with
-// P read from TMEM and V as an MN-major operand straight from the ring.
+// vectors, N = 64 positions) into one of three TMEM buffers (two at head_dim
+// 128), and O += P V with P read from TMEM and V as an MN-major operand straight
+// from the ring; it issues each S as soon as its keys have landed and each PV as
+// soon as its P is written, so S runs up to two blocks ahead of the softmax.
 // Warps 2..5 own one query vector each (its TMEM lane): mask, exponentiate
 // (log2 domain) and write P as bf16 over the first half of S's columns.  A
 // row's reference maximum only moves when a block exceeds it by 2^8, and then
@@ -60,12 +62,20 @@ __host__ __device__ constexpr int attn_stages() { return HD == 64 ? 5 : 2; }
 constexpr int kAttnMaxStages = 5;
 constexpr int kAttnThreads = 192;     // warp 0: TMA, warp 1: MMA, warps 2..5: softmax (thread = query row)
 constexpr int kAttnSoftmax = 128;     // softmax threads
-constexpr uint32_t kAttnTmemCols = 256;  // S double buffer (2 x 64 columns) + O (head_dim columns)
-constexpr uint32_t kAttnTmemO = 2 * kAttnBlk;
+constexpr uint32_t kAttnTmemCols = 256;  // S buffers (64 columns each) + O (head_dim columns)
+// S/P buffers in TMEM: three at head_dim 64 (S runs up to two blocks ahead of the softmax),
+// two at head_dim 128 (O takes 128 of the 256 columns)
+template <int HD>
+__host__ __device__ constexpr int attn_sbufs() { return HD == 64 ? 3 : 2; }
+constexpr int kAttnMaxSbufs = 3;
+template <int HD>
+__host__ __device__ constexpr uint32_t attn_tmem_o() { return (uint32_t)(attn_sbufs<HD>() * kAttnBlk); }
 constexpr int kAttnItemRing = 4;      // item indices the producer may publish ahead
 // Lazy rescaling: a row keeps its reference maximum until a block's maximum
 // exceeds it by more than this (log2 units), so P <= 2^8 and O is rescaled rarely.
 constexpr float kAttnRescaleLog2 = 8.f;
+// Longest sleep of the MMA warp on one input while another may arrive first (ns).
+constexpr uint32_t kAttnPollNs = 100;
 
 // Shared-memory tile [HD/64 halves][ROWS][64 bf16]: 128-byte rows with the
 // 128-byte swizzle that TMA applies (16-byte unit c of row r sits at c ^ (r % 8)).
@@ -87,9 +97,8 @@ struct AttnLayout {
 struct AttnCtrl {
   uint64_t full[kAttnMaxStages], empty[kAttnMaxStages];
   uint64_t q_full;      // softmax threads staged the item's query tile
-  uint64_t s_full[2];   // S of a block is in TMEM buffer (block & 1)
-  uint64_t p_full[2];   // P of a block is in TMEM (over its S), O rescaled where needed
-  uint64_t pv_done;     // one phase per PV product (waited on only while the next PV cannot start)
+  uint64_t s_full[kAttnMaxSbufs];  // S of a block is in its TMEM buffer (block % sbufs)
+  uint64_t p_full[kAttnMaxSbufs];  // P of a block is in TMEM (over its S), O rescaled where needed
   uint64_t pv_item;     // one phase per item: its last PV product has completed
   uint64_t o_free;      // softmax threads read O of the item
   uint64_t drain;       // every MMA issued has completed
@@ -119,6 +128,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   using Lay = AttnLayout<HD>;
   constexpr int CH = HD / 8;  // 16-byte units per row
   constexpr int S = attn_stages<HD>();
+  constexpr int NB = attn_sbufs<HD>();
+  constexpr uint32_t TO = attn_tmem_o<HD>();  // first TMEM column of O
+  static_assert(TO + HD <= kAttnTmemCols, "S buffers and O fit the allocation");
+  static_assert(S >= NB - 1, "a stage's release orders the PV product a rescale waits for");
   extern __shared__ uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(sm);
@@ -136,11 +149,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
     mbar_init(smem_u32(&ctl->q_full), kAttnSoftmax);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NB; ++b) {
       mbar_init(smem_u32(&ctl->s_full[b]), 1);
       mbar_init(smem_u32(&ctl->p_full[b]), kAttnSoftmax);
     }
-    mbar_init(smem_u32(&ctl->pv_done), 1);
     mbar_init(smem_u32(&ctl->pv_item), 1);
     mbar_init(smem_u32(&ctl->o_free), kAttnSoftmax);
     mbar_init(smem_u32(&ctl->drain), 1);
@@ -267,53 +279,95 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       const int nblk = (item.w - item.z + kAttnBlk - 1) / kAttnBlk;
       if (!wait_all(smem_u32(&ctl->q_full), (uint32_t)ii & 1u)) break;
       tc_fence_after();
-      // S of block j is issued one block ahead of the PV product of block j - 1
-      for (int j = 0; j <= nblk; ++j) {
-        if (j < nblk) {
-          const int x = gi + j, s = x % S;
-          if (!wait_all(smem_u32(&ctl->full[s]), (uint32_t)(x / S) & 1u)) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
-          if (elect_one()) {
-            const uint32_t kbase = sRing + (uint32_t)s * Lay::STAGE;
-            const uint32_t d = tmem + (uint32_t)((x & 1) * kAttnBlk);
+      // Two streams, issued as their inputs arrive: S of block ns once its K has landed and
+      // its TMEM buffer is free (the PV of block ns - NB is issued: ns <= np + NB - 1), and the PV
+      // of block np once its P is written (and, for an item's first PV, which overwrites
+      // O, once the softmax threads have read the previous item's O).  Neither waits for
+      // the other's input: a PV is never held back by the next block's K still loading.
+      int ns = 0, np = 0;
+      bool o_ok = ii == 0;
+      uint64_t t_idle = 0;
+      uint32_t n_idle = 0;
+      while (np < nblk) {
+        bool prog = false;
+        if (ns < nblk && ns <= np + NB - 1) {
+          const int x = gi + ns, s = x % S;
+          if (__shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&ctl->full[s]), (uint32_t)(x / S) & 1u) ? 1 : 0, 0)) {
+            tc_fence_after();
+            if (elect_one()) {
+              const uint32_t kbase = sRing + (uint32_t)s * Lay::STAGE;
+              const uint32_t d = tmem + (uint32_t)((x % NB) * kAttnBlk);
 #pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) {
-              const uint64_t ad = sdesc_k_sw128(sQ + (uint32_t)((kk >> 2) * kAttnRows * 128)) + 2 * (kk & 3);
-              const uint64_t bd = sdesc_k_sw128(kbase + (uint32_t)((kk >> 2) * kAttnBlk * 128)) + 2 * (kk & 3);
-              tc_mma_bf16(d, ad, bd, id_s, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint64_t ad = sdesc_k_sw128(sQ + (uint32_t)((kk >> 2) * kAttnRows * 128)) + 2 * (kk & 3);
+                const uint64_t bd = sdesc_k_sw128(kbase + (uint32_t)((kk >> 2) * kAttnBlk * 128)) + 2 * (kk & 3);
+                tc_mma_bf16(d, ad, bd, id_s, kk > 0 ? 1u : 0u);
+              }
+              tc_commit(smem_u32(&ctl->s_full[x % NB]));
             }
-            tc_commit(smem_u32(&ctl->s_full[x & 1]));
+            __syncwarp();
+            ++ns;
+            prog = true;
           }
-          __syncwarp();
         }
-        if (j >= 1) {
-          const int x = gi + j - 1, s = x % S;
-          if (j == 1 && ii > 0 && !wait_all(smem_u32(&ctl->o_free), (uint32_t)(ii - 1) & 1u)) {
-            stop = true;
-            break;
-          }
-          if (!wait_all(smem_u32(&ctl->p_full[x & 1]), (uint32_t)(x >> 1) & 1u)) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
-          if (elect_one()) {
-            const uint32_t vbase = sRing + (uint32_t)s * Lay::STAGE + Lay::KV;
-            const uint32_t pa = tmem + (uint32_t)((x & 1) * kAttnBlk);
+        if (np < ns) {
+          const int x = gi + np, s = x % S;
+          if (!o_ok)
+            o_ok = __shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&ctl->o_free), (uint32_t)(ii - 1) & 1u) ? 1 : 0, 0);
+          if (o_ok &&
+              __shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&ctl->p_full[x % NB]), (uint32_t)(x / NB) & 1u) ? 1 : 0, 0)) {
+            tc_fence_after();
+            if (elect_one()) {
+              const uint32_t vbase = sRing + (uint32_t)s * Lay::STAGE + Lay::KV;
+              const uint32_t pa = tmem + (uint32_t)((x % NB) * kAttnBlk);
 #pragma unroll
-            for (int kk = 0; kk < kAttnBlk / 16; ++kk)
-              tc_mma_bf16_tmem_a(tmem + kAttnTmemO, pa + 8u * kk,
-                                 sdesc_mn_sw128(vbase + (uint32_t)kk * 2048u, kAttnBlk * 128), id_o,
-                                 (j > 1 || kk > 0) ? 1u : 0u);
-            tc_commit(smem_u32(&ctl->pv_done));
-            if (j == nblk) tc_commit(smem_u32(&ctl->pv_item));
-            tc_commit(smem_u32(&ctl->empty[s]));
+              for (int kk = 0; kk < kAttnBlk / 16; ++kk)
+                tc_mma_bf16_tmem_a(tmem + TO, pa + 8u * kk,
+                                   sdesc_mn_sw128(vbase + (uint32_t)kk * 2048u, kAttnBlk * 128), id_o,
+                                   (np > 0 || kk > 0) ? 1u : 0u);
+              if (np == nblk - 1) tc_commit(smem_u32(&ctl->pv_item));
+              tc_commit(smem_u32(&ctl->empty[s]));
+            }
+            __syncwarp();
+            ++np;
+            prog = true;
           }
-          __syncwarp();
         }
+        if (prog) {
+          n_idle = 0;
+          continue;
+        }
+        if ((n_idle++ & 7) == 0) {
+          // the same bounded wait as mbar_wait (checked every 8th idle turn): give up when
+          // another role did, or after the limit
+          if (*abort_flag) {
+            stop = true;
+            break;
+          }
+          const uint64_t now = global_timer_ns();
+          if (n_idle == 1) {
+            t_idle = now;
+          } else if (now - t_idle > a.wait_ns) {
+            if (elect_one()) {
+              set_err(a.err, PE_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+            __syncwarp();
+            stop = true;
+            break;
+          }
+        }
+        // Sleep on the input most likely to come next, for a short while (a hot loop of
+        // tests would take issue slots from the softmax warps): a pending P, else the
+        // next block's K.
+        if (np < ns) {
+          const int x = gi + np;
+          mbar_try_wait_for(smem_u32(&ctl->p_full[x % NB]), (uint32_t)(x / NB) & 1u, kAttnPollNs);
+        } else if (ns < nblk) {
+          const int x = gi + ns;
+          mbar_try_wait_for(smem_u32(&ctl->full[x % S]), (uint32_t)(x / S) & 1u, kAttnPollNs);
+        }
+        __syncwarp();
       }
       if (stop) break;
       gi += nblk;
@@ -386,12 +440,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       float m_ref = -INFINITY, l = 0.f;  // reference maximum (log2 units, scaled) and row sum
       for (int j = 0; j < nblk; ++j) {
         const int x = gi + j;
-        if (!warp_ok(mbar_wait(smem_u32(&ctl->s_full[x & 1]), (uint32_t)(x >> 1) & 1u, a.err, abort_flag, a.wait_ns))) {
+        if (!warp_ok(mbar_wait(smem_u32(&ctl->s_full[x % NB]), (uint32_t)(x / NB) & 1u, a.err, abort_flag, a.wait_ns))) {
           stop = true;
           break;
         }
         tc_fence_after();
-        const uint32_t sbuf = tmem + lane_base + (uint32_t)((x & 1) * kAttnBlk);
+        const uint32_t sbuf = tmem + lane_base + (uint32_t)((x % NB) * kAttnBlk);
         if (warp_any) {
           float sc[kAttnBlk];
           tmem_load64(sbuf, sc);
@@ -412,7 +466,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           const bool need = !fresh && bm > m_ref + kAttnRescaleLog2;
           if (__any_sync(0xFFFFFFFFu, need)) {
             // O holds the PV products of blocks before j of this item (j >= 1 since m_ref is finite)
-            if (!warp_ok(mbar_wait(smem_u32(&ctl->pv_done), (uint32_t)(x - 1) & 1u, a.err, abort_flag, a.wait_ns))) {
+            // (the release of block x-1's ring stage is committed after its PV product; the
+            // stage is at most one phase short of it: S(x) completing implies every PV up to
+            // block x-NB has completed, and S >= NB - 1)
+            const int xp = x - 1;
+            if (!warp_ok(mbar_wait(smem_u32(&ctl->empty[xp % S]), (uint32_t)(xp / S) & 1u, a.err, abort_flag,
+                                   a.wait_ns))) {
               stop = true;
             } else {
               tc_fence_after();
@@ -420,10 +479,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 #pragma unroll 1
               for (int c = 0; c < HD; c += 16) {
                 float ov[16];
-                tmem_load16(tmem + lane_base + kAttnTmemO + (uint32_t)c, ov);
+                tmem_load16(tmem + lane_base + TO + (uint32_t)c, ov);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) ov[e] *= f;
-                tmem_store16(tmem + lane_base + kAttnTmemO + (uint32_t)c, ov);
+                tmem_store16(tmem + lane_base + TO + (uint32_t)c, ov);
               }
               if (need) {
                 l *= f;
@@ -450,7 +509,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           tmem_store32(sbuf, pk);  // P over the first half of S's columns
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&ctl->p_full[x & 1]));
+        mbar_arrive(smem_u32(&ctl->p_full[x % NB]));
         if (stop) break;
       }
       if (stop) break;
@@ -460,10 +519,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       if (it_next >= 0) stage_q(it_next);
 
       gi += nblk;
-      // The item's PV products are complete.  (Not pv_done at the last block's parity:
-      // the PV of the block before it is issued after the last S product, so pv_done
-      // may still be a phase short of that block, and a parity wait cannot tell a
-      // barrier two phases behind from one that is done.)
+      // The item's PV products are complete (a barrier of its own, committed after the
+      // item's last PV: a parity wait cannot tell a barrier two phases behind from one
+      // that is done, so no per-block barrier serves here).
       if (!warp_ok(mbar_wait(smem_u32(&ctl->pv_item), (uint32_t)ii & 1u, a.err, abort_flag, a.wait_ns))) break;
       tc_fence_after();
       if (nc == 1) {
@@ -474,7 +532,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 #pragma unroll 1
           for (int c = 0; c < HD; c += 16) {
             float ov[16];
-            tmem_load16(tmem + lane_base + kAttnTmemO + (uint32_t)c, ov);
+            tmem_load16(tmem + lane_base + TO + (uint32_t)c, ov);
             if (valid) {
               uint4 w0, w1;
               w0.x = pack_bf16(ov[0] * inv, ov[1] * inv);   w0.y = pack_bf16(ov[2] * inv, ov[3] * inv);
@@ -495,7 +553,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 #pragma unroll 1
         for (int c = 0; c < HD; c += 16) {
           float ov[16];
-          tmem_load16(tmem + lane_base + kAttnTmemO + (uint32_t)c, ov);
+          tmem_load16(tmem + lane_base + TO + (uint32_t)c, ov);
           if (valid) {
             float4* dst = reinterpret_cast<float4*>(a.part_o + (ib + r) * HD + c);
 #pragma unroll
