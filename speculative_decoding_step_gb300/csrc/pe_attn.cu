@@ -7,10 +7,11 @@
 // bf16: one work item = (sequence b, kv head g, position chunk [c0, c1)).
 // The query tile packs every valid row of the sequence times the n_q/n_kv
 // query heads of g (<= 128 query vectors), so each KV page is read once per
-// (sequence, kv head).  Warp 0 streams the chunk's K and V pages with 3-D TMA
-// loads (one 16-position page per load, 128-byte swizzle, pages past the
-// range zero-filled) into an mbarrier ring of 64-position blocks (5 stages
-// at head_dim 64, 2 at head_dim 128: two CTAs share an SM).
+// (sequence, kv head).  Warps 0 and 6 stream the chunk's K and V pages with
+// 3-D TMA loads (one 16-position page per load, 128-byte swizzle, pages past
+// the range zero-filled) into two mbarrier rings of 64-position blocks (5
+// stages at head_dim 64, 2 at head_dim 128: two CTAs share an SM); a block's
+// keys are released when its S product completes, its values after its PV.
 // Warp 1 issues the 5th-generation tensor-core MMAs: S = Q K^T (M = 128 query
 // vectors, N = 64 positions) into one of three TMEM buffers (two at head_dim
 // 128), and O += P V with P read from TMEM and V as an MN-major operand straight
@@ -60,7 +61,7 @@ constexpr int kAttnBlk = 64;          // kv positions per pipeline stage (4 page
 template <int HD>
 __host__ __device__ constexpr int attn_stages() { return HD == 64 ? 5 : 2; }
 constexpr int kAttnMaxStages = 5;
-constexpr int kAttnThreads = 192;     // warp 0: TMA, warp 1: MMA, warps 2..5: softmax (thread = query row)
+constexpr int kAttnThreads = 224;     // warp 0: K loads, warp 1: MMA, warps 2..5: softmax (thread = query row), warp 6: V loads
 constexpr int kAttnSoftmax = 128;     // softmax threads
 constexpr uint32_t kAttnTmemCols = 256;  // S buffers (64 columns each) + O (head_dim columns)
 // S/P buffers in TMEM: three at head_dim 64 (S runs up to two blocks ahead of the softmax),
@@ -90,12 +91,15 @@ struct AttnLayout {
   static constexpr uint32_t KV = kAttnBlk * HD * 2;      // K (or V) of one stage
   static constexpr uint32_t STAGE = 2 * KV;
   static constexpr uint32_t BARS = Q + attn_stages<HD>() * STAGE;
-  static constexpr uint32_t TOTAL = 1024 + BARS + 256;   // + alignment slack
+  static constexpr uint32_t TOTAL = 1024 + BARS + 512;   // + alignment slack
 };
 
 // Barriers and flags after the tiles.
+// K and V of a stage are separate rings: a stage's keys are released once its S product
+// has completed, its values once its PV product has.
 struct AttnCtrl {
-  uint64_t full[kAttnMaxStages], empty[kAttnMaxStages];
+  uint64_t kfull[kAttnMaxStages], kempty[kAttnMaxStages];
+  uint64_t vfull[kAttnMaxStages], vempty[kAttnMaxStages];
   uint64_t q_full;      // softmax threads staged the item's query tile
   uint64_t s_full[kAttnMaxSbufs];  // S of a block is in its TMEM buffer (block % sbufs)
   uint64_t p_full[kAttnMaxSbufs];  // P of a block is in TMEM (over its S), O rescaled where needed
@@ -103,13 +107,13 @@ struct AttnCtrl {
   uint64_t o_free;      // softmax threads read O of the item
   uint64_t drain;       // every MMA issued has completed
   uint64_t item_full[kAttnItemRing];   // the producer published the next item index
-  uint64_t item_empty[kAttnItemRing];  // the MMA thread and every softmax thread read it
+  uint64_t item_empty[kAttnItemRing];  // the V loader, the MMA thread and every softmax thread read it
   int item[kAttnItemRing];  // item index, -1: no more work
   uint32_t tmem;
   int abort;
 };
 
-static_assert(sizeof(AttnCtrl) <= 256, "attention control block");
+static_assert(sizeof(AttnCtrl) <= 512, "attention control block");
 
 // Consumer side of the item ring: the index of this CTA's ii-th item (-1: done),
 // or -2 when the wait gave up (the kernel is unwinding).
@@ -145,8 +149,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl->kfull[s]), 1);
+      mbar_init(smem_u32(&ctl->kempty[s]), 1);
+      mbar_init(smem_u32(&ctl->vfull[s]), 1);
+      mbar_init(smem_u32(&ctl->vempty[s]), 1);
     }
     mbar_init(smem_u32(&ctl->q_full), kAttnSoftmax);
     for (int b = 0; b < NB; ++b) {
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     mbar_init(smem_u32(&ctl->drain), 1);
     for (int k = 0; k < kAttnItemRing; ++k) {
       mbar_init(smem_u32(&ctl->item_full[k]), 1);
-      mbar_init(smem_u32(&ctl->item_empty[k]), 1 + kAttnSoftmax);
+      mbar_init(smem_u32(&ctl->item_empty[k]), 2 + kAttnSoftmax);
     }
     ctl->abort = 0;
     fence_mbar_init();
@@ -175,11 +181,19 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   pdl_trigger();
   const int n_items = *a.n_items;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer (whole warp)
-    // The warp reads the page ids of 8 blocks (32 pages) at once, one per lane;
-    // lane 0 then issues the TMA loads.  Reading them one at a time would put an
-    // L2 round trip in front of every page.
+  if (warp == 0 || warp == 6) {
+    // ------------------------------------------------------------------ TMA loaders (whole warps)
+    // Warp 0 streams the keys and warp 6 the values of the same blocks, each into its own
+    // ring: a key stage is reused as soon as its S product has completed, without waiting
+    // for the block's PV product.  Warp 0 also takes the items (dynamic: long and short
+    // ranges even out across SMs) and publishes them through the item ring; warp 6 reads
+    // them from it like the other roles.  A warp reads the page ids of 8 blocks (32 pages)
+    // at once, one per lane; lane 0 then issues the TMA loads.
+    const bool is_v = warp == 6;
+    const CUtensorMap* tm = is_v ? &tmV : &tmK;
+    uint64_t* fullb = is_v ? ctl->vfull : ctl->kfull;
+    uint64_t* emptyb = is_v ? ctl->vempty : ctl->kempty;
+    const uint32_t half = is_v ? Lay::KV : 0u;  // offset of the K or V half in a stage
     const uint64_t pol = l2_policy_evict_first();  // the prefix is read once per round
     const int oob = a.num_pages * a.page_size;     // a row past the pool: TMA fills zeros
     constexpr int kPagesPerBlk = kAttnBlk / 16;
@@ -187,21 +201,23 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     int gi = 0;
     bool stop = false;
     for (int ii = 0; !stop; ++ii) {
-      // the next item for this CTA (dynamic: long and short ranges even out across SMs),
-      // published to the MMA and softmax warps through the item ring
       int it = 0;
       if (lane == 0) {
-        it = atomicAdd(a.work_counter, 1);
-        if (it >= n_items) it = -1;
-        const int k = ii % kAttnItemRing;
-        bool ok = true;
-        if (ii >= kAttnItemRing)
-          ok = mbar_wait(smem_u32(&ctl->item_empty[k]), ((uint32_t)(ii / kAttnItemRing) & 1u) ^ 1u, a.err,
-                         abort_flag, a.wait_ns);
-        if (!ok) it = -2;
-        else {
-          ctl->item[k] = it;
-          mbar_arrive(smem_u32(&ctl->item_full[k]));  // release: the index is visible to the waiters
+        if (is_v) {
+          it = attn_next_item(ctl, ii, a.err, abort_flag, a.wait_ns);
+        } else {
+          it = atomicAdd(a.work_counter, 1);
+          if (it >= n_items) it = -1;
+          const int k = ii % kAttnItemRing;
+          bool ok = true;
+          if (ii >= kAttnItemRing)
+            ok = mbar_wait(smem_u32(&ctl->item_empty[k]), ((uint32_t)(ii / kAttnItemRing) & 1u) ^ 1u, a.err,
+                           abort_flag, a.wait_ns);
+          if (!ok) it = -2;
+          else {
+            ctl->item[k] = it;
+            mbar_arrive(smem_u32(&ctl->item_full[k]));  // release: the index is visible to the waiters
+          }
         }
       }
       it = __shfl_sync(0xFFFFFFFFu, it, 0);
@@ -230,24 +246,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           const int s = gi % S;
           bool ok = true;
           if (lane == 0 && gi >= S)
-            ok = mbar_wait(smem_u32(&ctl->empty[s]), ((uint32_t)(gi / S) & 1u) ^ 1u, a.err, abort_flag, a.wait_ns);
+            ok = mbar_wait(smem_u32(&emptyb[s]), ((uint32_t)(gi / S) & 1u) ^ 1u, a.err, abort_flag, a.wait_ns);
           if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
             stop = true;
             break;
           }
-          const uint32_t fb = smem_u32(&ctl->full[s]);
-          const uint32_t kdst = sRing + (uint32_t)s * Lay::STAGE;
-          if (lane == 0) mbar_expect_tx(fb, Lay::STAGE);
+          const uint32_t fb = smem_u32(&fullb[s]);
+          const uint32_t dst = sRing + (uint32_t)s * Lay::STAGE + half;
+          if (lane == 0) mbar_expect_tx(fb, Lay::KV);
 #pragma unroll
           for (int p = 0; p < kPagesPerBlk; ++p) {
             const int yp = __shfl_sync(0xFFFFFFFFu, y, bb * kPagesPerBlk + p);
             if (lane == 0) {
 #pragma unroll
-              for (int h = 0; h < HD / 64; ++h) {
-                const uint32_t off = (uint32_t)(h * kAttnBlk * 128 + p * 16 * 128);
-                tma_load_3d(kdst + off, &tmK, fb, h * 64, g, yp, pol);
-                tma_load_3d(kdst + Lay::KV + off, &tmV, fb, h * 64, g, yp, pol);
-              }
+              for (int h = 0; h < HD / 64; ++h)
+                tma_load_3d(dst + (uint32_t)(h * kAttnBlk * 128 + p * 16 * 128), tm, fb, h * 64, g, yp, pol);
             }
           }
         }
@@ -256,7 +269,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     if (stop && lane == 0) {
       // leave no bulk copy in flight into this CTA's shared memory
       for (int i = (gi > S ? gi - S : 0); i < gi; ++i)
-        mbar_wait(smem_u32(&ctl->full[i % S]), (uint32_t)(i / S) & 1u, a.err, nullptr, a.wait_ns);
+        mbar_wait(smem_u32(&fullb[i % S]), (uint32_t)(i / S) & 1u, a.err, nullptr, a.wait_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -292,7 +305,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         bool prog = false;
         if (ns < nblk && ns <= np + NB - 1) {
           const int x = gi + ns, s = x % S;
-          if (__shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&ctl->full[s]), (uint32_t)(x / S) & 1u) ? 1 : 0, 0)) {
+          if (__shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&ctl->kfull[s]), (uint32_t)(x / S) & 1u) ? 1 : 0, 0)) {
             tc_fence_after();
             if (elect_one()) {
               const uint32_t kbase = sRing + (uint32_t)s * Lay::STAGE;
@@ -304,6 +317,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                 tc_mma_bf16(d, ad, bd, id_s, kk > 0 ? 1u : 0u);
               }
               tc_commit(smem_u32(&ctl->s_full[x % NB]));
+              tc_commit(smem_u32(&ctl->kempty[s]));  // the stage's keys are read
             }
             __syncwarp();
             ++ns;
@@ -315,7 +329,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           if (!o_ok)
             o_ok = __shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&ctl->o_free), (uint32_t)(ii - 1) & 1u) ? 1 : 0, 0);
           if (o_ok &&
-              __shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&ctl->p_full[x % NB]), (uint32_t)(x / NB) & 1u) ? 1 : 0, 0)) {
+              __shfl_sync(0xFFFFFFFFu,
+                          (mbar_test_wait(smem_u32(&ctl->p_full[x % NB]), (uint32_t)(x / NB) & 1u) &&
+                           mbar_test_wait(smem_u32(&ctl->vfull[s]), (uint32_t)(x / S) & 1u))
+                              ? 1
+                              : 0,
+                          0)) {
             tc_fence_after();
             if (elect_one()) {
               const uint32_t vbase = sRing + (uint32_t)s * Lay::STAGE + Lay::KV;
@@ -326,7 +345,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                                    sdesc_mn_sw128(vbase + (uint32_t)kk * 2048u, kAttnBlk * 128), id_o,
                                    (np > 0 || kk > 0) ? 1u : 0u);
               if (np == nblk - 1) tc_commit(smem_u32(&ctl->pv_item));
-              tc_commit(smem_u32(&ctl->empty[s]));
+              tc_commit(smem_u32(&ctl->vempty[s]));
             }
             __syncwarp();
             ++np;
@@ -365,7 +384,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           mbar_try_wait_for(smem_u32(&ctl->p_full[x % NB]), (uint32_t)(x / NB) & 1u, kAttnPollNs);
         } else if (ns < nblk) {
           const int x = gi + ns;
-          mbar_try_wait_for(smem_u32(&ctl->full[x % S]), (uint32_t)(x / S) & 1u, kAttnPollNs);
+          mbar_try_wait_for(smem_u32(&ctl->kfull[x % S]), (uint32_t)(x / S) & 1u, kAttnPollNs);
         }
         __syncwarp();
       }
@@ -466,11 +485,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           const bool need = !fresh && bm > m_ref + kAttnRescaleLog2;
           if (__any_sync(0xFFFFFFFFu, need)) {
             // O holds the PV products of blocks before j of this item (j >= 1 since m_ref is finite)
-            // (the release of block x-1's ring stage is committed after its PV product; the
-            // stage is at most one phase short of it: S(x) completing implies every PV up to
-            // block x-NB has completed, and S >= NB - 1)
+            // (the release of block x-1's values is committed after its PV product; that
+            // barrier is at most one phase short of it: S(x) completing implies every PV up
+            // to block x-NB has completed, and S >= NB - 1)
             const int xp = x - 1;
-            if (!warp_ok(mbar_wait(smem_u32(&ctl->empty[xp % S]), (uint32_t)(xp / S) & 1u, a.err, abort_flag,
+            if (!warp_ok(mbar_wait(smem_u32(&ctl->vempty[xp % S]), (uint32_t)(xp / S) & 1u, a.err, abort_flag,
                                    a.wait_ns))) {
               stop = true;
             } else {
