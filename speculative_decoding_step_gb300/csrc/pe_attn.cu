@@ -57,9 +57,13 @@ PE_DEV bool warp_ok(bool ok) { return __all_sync(0xFFFFFFFFu, ok); }
 }  // namespace
 
 constexpr int kAttnBlk = 64;          // kv positions per pipeline stage (4 pages) = MMA N of S
-// stages in flight: 5 x 16 KB (head_dim 64) or 2 x 32 KB (head_dim 128), so two CTAs fit per SM
+// key and value stages in flight: 5 + 5 x 8 KB (head_dim 64) or 2 + 2 x 16 KB (head_dim 128), so
+// two CTAs fit per SM
+// (a deeper value ring and a shallower key ring, 6 + 4 or 7 + 3, measured no faster)
 template <int HD>
-__host__ __device__ constexpr int attn_stages() { return HD == 64 ? 5 : 2; }
+__host__ __device__ constexpr int attn_kstages() { return HD == 64 ? 5 : 2; }
+template <int HD>
+__host__ __device__ constexpr int attn_vstages() { return HD == 64 ? 5 : 2; }
 constexpr int kAttnMaxStages = 5;
 constexpr int kAttnThreads = 224;     // warp 0: K loads, warp 1: MMA, warps 2..5: softmax (thread = query row), warp 6: V loads
 constexpr int kAttnSoftmax = 128;     // softmax threads
@@ -89,8 +93,8 @@ template <int HD>
 struct AttnLayout {
   static constexpr uint32_t Q = kAttnRows * HD * 2;      // query tile
   static constexpr uint32_t KV = kAttnBlk * HD * 2;      // K (or V) of one stage
-  static constexpr uint32_t STAGE = 2 * KV;
-  static constexpr uint32_t BARS = Q + attn_stages<HD>() * STAGE;
+  static constexpr uint32_t VRING = Q + attn_kstages<HD>() * KV;  // the value ring follows the key ring
+  static constexpr uint32_t BARS = VRING + attn_vstages<HD>() * KV;
   static constexpr uint32_t TOTAL = 1024 + BARS + 512;   // + alignment slack
 };
 
@@ -131,15 +135,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                      const AttnArgs a) {
   using Lay = AttnLayout<HD>;
   constexpr int CH = HD / 8;  // 16-byte units per row
-  constexpr int S = attn_stages<HD>();
+  constexpr int SK = attn_kstages<HD>(), SV = attn_vstages<HD>();
   constexpr int NB = attn_sbufs<HD>();
   constexpr uint32_t TO = attn_tmem_o<HD>();  // first TMEM column of O
   static_assert(TO + HD <= kAttnTmemCols, "S buffers and O fit the allocation");
-  static_assert(S >= NB - 1, "a stage's release orders the PV product a rescale waits for");
+  static_assert(SV >= NB - 1, "a value stage's release orders the PV product a rescale waits for");
   extern __shared__ uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(sm);
-  const uint32_t sRing = sQ + Lay::Q;
   AttnCtrl* ctl = reinterpret_cast<AttnCtrl*>(sm + Lay::BARS);
   volatile int* abort_flag = &ctl->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -148,9 +151,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   if (tid == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SK; ++s) {
       mbar_init(smem_u32(&ctl->kfull[s]), 1);
       mbar_init(smem_u32(&ctl->kempty[s]), 1);
+    }
+    for (int s = 0; s < SV; ++s) {
       mbar_init(smem_u32(&ctl->vfull[s]), 1);
       mbar_init(smem_u32(&ctl->vempty[s]), 1);
     }
@@ -193,7 +198,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const CUtensorMap* tm = is_v ? &tmV : &tmK;
     uint64_t* fullb = is_v ? ctl->vfull : ctl->kfull;
     uint64_t* emptyb = is_v ? ctl->vempty : ctl->kempty;
-    const uint32_t half = is_v ? Lay::KV : 0u;  // offset of the K or V half in a stage
+    const uint32_t ring = sQ + (is_v ? Lay::VRING : Lay::Q);
+    const int S = is_v ? SV : SK;
     const uint64_t pol = l2_policy_evict_first();  // the prefix is read once per round
     const int oob = a.num_pages * a.page_size;     // a row past the pool: TMA fills zeros
     constexpr int kPagesPerBlk = kAttnBlk / 16;
@@ -252,7 +258,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             break;
           }
           const uint32_t fb = smem_u32(&fullb[s]);
-          const uint32_t dst = sRing + (uint32_t)s * Lay::STAGE + half;
+          const uint32_t dst = ring + (uint32_t)s * Lay::KV;
           if (lane == 0) mbar_expect_tx(fb, Lay::KV);
 #pragma unroll
           for (int p = 0; p < kPagesPerBlk; ++p) {
@@ -304,11 +310,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       while (np < nblk) {
         bool prog = false;
         if (ns < nblk && ns <= np + NB - 1) {
-          const int x = gi + ns, s = x % S;
-          if (__shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&ctl->kfull[s]), (uint32_t)(x / S) & 1u) ? 1 : 0, 0)) {
+          const int x = gi + ns, s = x % SK;
+          if (__shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&ctl->kfull[s]), (uint32_t)(x / SK) & 1u) ? 1 : 0, 0)) {
             tc_fence_after();
             if (elect_one()) {
-              const uint32_t kbase = sRing + (uint32_t)s * Lay::STAGE;
+              const uint32_t kbase = sQ + Lay::Q + (uint32_t)s * Lay::KV;
               const uint32_t d = tmem + (uint32_t)((x % NB) * kAttnBlk);
 #pragma unroll
               for (int kk = 0; kk < HD / 16; ++kk) {
@@ -325,19 +331,19 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           }
         }
         if (np < ns) {
-          const int x = gi + np, s = x % S;
+          const int x = gi + np, s = x % SV;
           if (!o_ok)
             o_ok = __shfl_sync(0xFFFFFFFFu, mbar_test_wait(smem_u32(&ctl->o_free), (uint32_t)(ii - 1) & 1u) ? 1 : 0, 0);
           if (o_ok &&
               __shfl_sync(0xFFFFFFFFu,
                           (mbar_test_wait(smem_u32(&ctl->p_full[x % NB]), (uint32_t)(x / NB) & 1u) &&
-                           mbar_test_wait(smem_u32(&ctl->vfull[s]), (uint32_t)(x / S) & 1u))
+                           mbar_test_wait(smem_u32(&ctl->vfull[s]), (uint32_t)(x / SV) & 1u))
                               ? 1
                               : 0,
                           0)) {
             tc_fence_after();
             if (elect_one()) {
-              const uint32_t vbase = sRing + (uint32_t)s * Lay::STAGE + Lay::KV;
+              const uint32_t vbase = sQ + Lay::VRING + (uint32_t)s * Lay::KV;
               const uint32_t pa = tmem + (uint32_t)((x % NB) * kAttnBlk);
 #pragma unroll
               for (int kk = 0; kk < kAttnBlk / 16; ++kk)
@@ -384,7 +390,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           mbar_try_wait_for(smem_u32(&ctl->p_full[x % NB]), (uint32_t)(x / NB) & 1u, kAttnPollNs);
         } else if (ns < nblk) {
           const int x = gi + ns;
-          mbar_try_wait_for(smem_u32(&ctl->kfull[x % S]), (uint32_t)(x / S) & 1u, kAttnPollNs);
+          mbar_try_wait_for(smem_u32(&ctl->kfull[x % SK]), (uint32_t)(x / SK) & 1u, kAttnPollNs);
         }
         __syncwarp();
       }
@@ -487,9 +493,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             // O holds the PV products of blocks before j of this item (j >= 1 since m_ref is finite)
             // (the release of block x-1's values is committed after its PV product; that
             // barrier is at most one phase short of it: S(x) completing implies every PV up
-            // to block x-NB has completed, and S >= NB - 1)
+            // to block x-NB has completed, and SV >= NB - 1)
             const int xp = x - 1;
-            if (!warp_ok(mbar_wait(smem_u32(&ctl->vempty[xp % S]), (uint32_t)(xp / S) & 1u, a.err, abort_flag,
+            if (!warp_ok(mbar_wait(smem_u32(&ctl->vempty[xp % SV]), (uint32_t)(xp / SV) & 1u, a.err, abort_flag,
                                    a.wait_ns))) {
               stop = true;
             } else {
