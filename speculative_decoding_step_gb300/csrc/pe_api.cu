@@ -222,7 +222,7 @@ Plan make_plan(const pe_config& c) {
   p.items = take(16 * (size_t)p.max_items);
   // LM-head completion counter, one attention work counter per layer, then the
   // balanced LM head's arrival counters (4 per CTA)
-  p.n_counters = 1 + c.n_layers + 4 * p.sms;
+  p.n_counters = 1 + c.n_layers + kTcEpiWarps * p.sms;
   p.done = take(4 * (size_t)p.n_counters);
   p.keys = take(8 * (size_t)p.T);
   p.x = take(4 * (size_t)p.R * c.d);

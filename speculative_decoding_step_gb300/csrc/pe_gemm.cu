@@ -362,16 +362,17 @@ PE_DEV void argmax16(const GemmArgs& a, int unit, int t0, int n_tok, const float
 
 // Epilogue of one piece of a vocabulary tile cut by a schedule boundary (balanced
 // LM head).  Each epilogue warp stores its 32 rows of the piece's fp32
-// accumulator ([boundary][side][token column][128 rows]); the warp whose piece
-// arrives second adds the other piece and takes the argmax of the full sums.
+// accumulator over its half of the column chunks ([boundary][side][token column][128
+// rows]); of the two warps (one per piece) that hold the same rows and columns, the one
+// that arrives second adds the other piece and takes the argmax of the full sums.
 // fp32 addition is commutative, so the sum is the same whichever piece is first.
 PE_DEV void argmax_piece(const GemmArgs& a, const Unit& w, uint32_t tl, int unit, int n_tok,
-                         unsigned long long* red_w, int r, int lane) {
+                         unsigned long long* red_w, int r, int lane, int h, int hs) {
   const int BN = a.bn;
   const size_t plane = (size_t)BN * kTcBM;
   float* mine = a.partial + (size_t)(2 * w.bnd + w.side) * plane + r;
   const float* other = a.partial + (size_t)(2 * w.bnd + 1 - w.side) * plane + r;
-  for (int c = 0; c < BN / 16; ++c) {
+  for (int c = h; c < BN / 16; c += hs) {
     float v[16];
     tmem_load16(tl + (uint32_t)(c * 16), v);
 #pragma unroll
@@ -379,13 +380,13 @@ PE_DEV void argmax_piece(const GemmArgs& a, const Unit& w, uint32_t tl, int unit
   }
   __threadfence();
   __syncwarp();
-  int* cnt = a.tile_cnt + 4 * w.bnd + (r >> 5);
+  int* cnt = a.tile_cnt + kTcEpiWarps * w.bnd + 2 * (r >> 5) + h;
   int old = 0;
   if (lane == 0) old = atomicAdd(cnt, 1);
   old = __shfl_sync(0xFFFFFFFFu, old, 0);
   if (old == 0) return;  // the other piece finishes this tile
   __threadfence();
-  for (int c = 0; c < BN / 16; ++c) {
+  for (int c = h; c < BN / 16; c += hs) {
     float v[16], o[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) o[j] = __ldcg(other + (size_t)(c * 16 + j) * kTcBM);
@@ -418,6 +419,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int EW = (int)(blockDim.x >> 5) - 2;  // epilogue warps: 4 or 8 (gemm_tc_threads)
   const int BN = a.bn;         // MMA N: token columns of a unit
   const int BNL = BN / CG;     // token rows this CTA loads per unit
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(tfull + b), 1);
-      mbar_init(smem_u32(tempty + b), 4 * CG);  // one arrival per epilogue warp (of both CTAs)
+      mbar_init(smem_u32(tempty + b), EW * CG);  // one arrival per epilogue warp (of both CTAs)
     }
 
     *abort_flag = 0;
@@ -620,12 +622,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------------ epilogue (warps 2..9)
+    // Two warps per TMEM lane quarter: each takes every other 16-column chunk of the
+    // accumulator, so that an epilogue (argmax over a 224-token tile: ~10 us with one warp
+    // per quarter, as long as the next unit's MMAs) stays hidden behind the next unit.
     pdl_wait();
     const int n_tok = effective_ntok(a);
     const int q = warp & 3;                // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;         // which half of the column chunks (0 with four warps)
+    const int hs = EW >> 2;                // chunk stride: the number of halves
     const int r = q * 32 + lane;           // row of the tile = TMEM lane
-    unsigned long long* red_w = red + (size_t)(warp - 2) * NT;
+    unsigned long long* red_w = red + (size_t)q * NT;  // per quarter; the halves' columns are disjoint
     const int ntl = live_token_tiles(a, n_tok);
     int i = 0;
     Sched sc = sched_begin<EPI, CG>(a, ntl);
@@ -649,18 +656,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (EPI == EPI_QKV_ROPE && a.k_splits == 1) {
         slot_s = reinterpret_cast<long long*>(red) + (size_t)(i & 1) * BN;
         pos_s = reinterpret_cast<int*>(reinterpret_cast<long long*>(red) + 2 * (size_t)BN) + (size_t)(i & 1) * BN;
-        for (int t = threadIdx.x - 64; t < BN; t += 128) {
+        for (int t = threadIdx.x - 64; t < BN; t += 32 * EW) {
           const int tok = tbase + t;
           pos_s[t] = tok < n_tok ? a.tok_pos[tok] : 0;
           slot_s[t] = tok < n_tok ? a.tok_slot[tok] : -1;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, 32 * EW);
       }
       if (BAL && ok && w.bnd >= 0) {
-        argmax_piece(a, w, tl, unit, n_tok, red_w, r, lane);
+        argmax_piece(a, w, tl, unit, n_tok, red_w, r, lane, h, hs);
       } else if (ok && a.k_splits == 1) {
         const float2 tf2 = (EPI == EPI_QKV_ROPE) ? rope_tf(a, unit) : make_float2(0.f, 0.f);
-        for (int c = 0; c < BN / 16; ++c) {
+        for (int c = h; c < BN / 16; c += hs) {
           float v[16], v2[16];
           tmem_load16(tl + (uint32_t)(c * 16), v);
           if (PAIRED) tmem_load16(tl + (uint32_t)(BN + c * 16), v2);
@@ -677,18 +684,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const size_t pu = ((size_t)tf * ntl + w.tile_t) * a.k_splits + w.split;
         float* P = a.partial + pu * (PAIRED ? 2 : 1) * BN * kTcBM + r;
         const int cend = (PAIRED ? 2 : 1) * BN;
-        for (int c = 0; c < cend;) {  // 64-column TMEM loads only at 64-aligned columns
+        // 64-column TMEM loads at 64-aligned columns; the halves take alternate loads
+        for (int c = 0; c < cend;) {
           if ((c & 63) == 0 && c + 64 <= cend) {
-            float v[64];
-            tmem_load64(tl + (uint32_t)c, v);
+            if (((c >> 6) & (hs - 1)) == h) {
+              float v[64];
+              tmem_load64(tl + (uint32_t)c, v);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) P[(size_t)(c + j) * kTcBM] = v[j];
+              for (int j = 0; j < 64; ++j) P[(size_t)(c + j) * kTcBM] = v[j];
+            }
             c += 64;
           } else {
-            float v[16];
-            tmem_load16(tl + (uint32_t)c, v);
+            if (((c >> 4) & (hs - 1)) == h) {
+              float v[16];
+              tmem_load16(tl + (uint32_t)c, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) P[(size_t)(c + j) * kTcBM] = v[j];
+              for (int j = 0; j < 16; ++j) P[(size_t)(c + j) * kTcBM] = v[j];
+            }
             c += 16;
           }
         }
@@ -702,27 +714,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ++i;
     }
     if (ARGMAX) {
-      named_bar_sync(1, 128);
+      const int ET = 32 * EW;  // epilogue threads
+      named_bar_sync(1, ET);
       const int ethread = threadIdx.x - 64;
-      for (int j = ethread; j < NT; j += 128) {  // key index = token = tile_t * BN + column
+      for (int j = ethread; j < NT; j += ET) {  // key index = token = tile_t * BN + column
         const unsigned long long k =
             umax64(umax64(red[j], red[NT + j]), umax64(red[2 * NT + j], red[3 * NT + j]));
         if (j < n_tok && k != 0ull) atomicMax(a.keys + j, k);
       }
       __threadfence();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, ET);
       if (ethread == 0) {
         const int old = atomicAdd(a.done_counter, 1);
         *last_flag = (old == (int)gridDim.x - 1) ? 1 : 0;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, ET);
       if (*last_flag) {
         __threadfence();
-        argmax_finish(a, n_tok, ethread, 128);
+        argmax_finish(a, n_tok, ethread, ET);
         if (ethread == 0) *a.done_counter = 0;
         if (a.has_verify) {  // every draft token is known: verify them here
-          named_bar_sync(1, 128);
-          for (int b = ethread; b < a.verify.B; b += 128) verify_seq(a.verify, b);
+          named_bar_sync(1, ET);
+          for (int b = ethread; b < a.verify.B; b += ET) verify_seq(a.verify, b);
         }
       }
     }
@@ -771,12 +784,12 @@ static cudaError_t launch_tc_typed(const CUtensorMap& tmW, const CUtensorMap& tm
   const cudaError_t e = ensure_smem_attr<EPI, CG>();
   if (e != cudaSuccess) return e;
   if constexpr (CG == 1) {
-    return launch_pdl(gemm_tc_kernel<EPI, 1>, dim3(grid), dim3(kTcThreads), smem, s, tmW, tmX, a);
+    return launch_pdl(gemm_tc_kernel<EPI, 1>, dim3(grid), dim3(gemm_tc_threads(a.bn)), smem, s, tmW, tmX, a);
   } else {
   // a pair per cluster, with programmatic dependent launch
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(gemm_tc_threads(a.bn));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];

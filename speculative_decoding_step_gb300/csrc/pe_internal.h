@@ -239,7 +239,7 @@ struct GemmArgs {
   float* logits_dbg;         // nullable [tokens][n_out]
   int32_t* done_counter;     // LM head: CTAs finished (zero before the launch)
   float* partial;            // split K: [grid][planes][bn][128] fp32 partial tiles (column-major per plane)
-  int32_t* tile_cnt;         // EPI_ARGMAX_BAL: [grid][4] arrivals per cut tile and epilogue warp (zero
+  int32_t* tile_cnt;         // EPI_ARGMAX_BAL: [grid][8] arrivals per cut tile and epilogue warp (zero
                              //   before the launch); the pieces' partials go to `partial` as [grid][2][bn][128]
   int32_t* draft_out;        // LM head: argmax per token
   VerifyArgs verify;         // LM head: greedy verification of the drafts by the finishing CTA
@@ -265,7 +265,11 @@ cudaError_t launch_splitk_finish(int epi, const GemmArgs& a, int sms, cudaStream
 // fp32 CUDA-core GEMM for fp32 configurations (same epilogues).
 cudaError_t launch_gemm_f32(int epi, const GemmArgs& a, cudaStream_t s);
 
-constexpr int kTcThreads = 192;        // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+constexpr int kTcEpiWarps = 8;         // at most: two per TMEM lane quarter, each taking half of the token columns
+constexpr int kTcThreads = 64 + 32 * kTcEpiWarps;  // warp 0: TMA, warp 1: MMA, warps 2-9: epilogue
+// Threads of a tensor-core GEMM launch: eight epilogue warps for token tiles of at least 64
+// columns, four (one per lane quarter) for narrower ones, whose epilogue is a chunk or two.
+constexpr int gemm_tc_threads(int bn) { return bn >= 64 ? kTcThreads : 64 + 32 * 4; }
 constexpr int kTcBM = 128;             // weight rows per tile
 constexpr int kTcBK = 64;              // k per atom (one 128-byte swizzle row); a stage holds 1 or 2 atoms
 constexpr int kTcCtrlBytes = 1024;     // barriers + TMEM slot + flags
