@@ -58,6 +58,10 @@ SMALL = {
     # several query vectors into a warp
     "bf16-many-pairs": _small(B=64, K=2, n_q=4, n_kv=2, d=128, ffn=128, vocab=500, prefix_args=(300, 900),
                               seed=18),
+    # LM heads on CTA pairs over more units than pairs (161 vocabulary tiles, the last
+    # ragged: 81 units of two), with one token tile of 160 rows and with two of 160
+    "bf16-pairs-many-units": _small(B=20, K=8, d=320, ffn=448, vocab=160 * 128 + 37, seed=19),
+    "bf16-pairs-many-units-2t": _small(B=40, K=8, d=320, ffn=448, vocab=160 * 128 + 37, seed=20),
     "f32-c0": config(0),
     "f32-L2": _small(dtype="f32", n_layers=2, seed=11),
 }
