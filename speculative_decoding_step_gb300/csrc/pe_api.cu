@@ -416,6 +416,10 @@ pe_status run_gemm(const pe_config& c, const Plan& p, void* ws, const GemmCall& 
   a.acc_stride = g.acc_stride;
   a.tmem_cols = g.tmem_cols;
   a.n_tok_min = call.n_tok_dev != nullptr ? std::min(call.n_tok, c.B * c.K) : call.n_tok;
+  // many-row GEMMs on pairs that (at the usual row counts) run one wave: weight tile fastest,
+  // so that every CTA prefetches its first weight stages before the dependency wait; the
+  // multi-wave gate/up and the LM head keep a weight tile's token tiles side by side (L2 reuse)
+  a.tok_major = (g.cg == 2 && g.n_t > 1 && call.epi != EPI_SWIGLU && call.epi != EPI_ARGMAX) ? 1 : 0;
   a.wait_ns = wait_limit_ns();
   a.drop_stage = take_drop_stage();
   if (g.k_splits > 1 || g.balanced) a.partial = at<float>(ws, p.split_part);

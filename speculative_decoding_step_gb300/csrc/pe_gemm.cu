@@ -218,12 +218,18 @@ PE_DEV int live_token_tiles(const GemmArgs& a, int n_tok) {
   return min(a.n_t, (n_tok + a.bn - 1) / a.bn);
 }
 
-PE_DEV Unit decode_unit(const GemmArgs& a, int u, int n_t_live) {
+// nfp: weight tiles of a unit's kind (pair tiles on CTA pairs).
+PE_DEV Unit decode_unit(const GemmArgs& a, int u, int n_t_live, int nfp) {
   Unit w;
   w.split = u % a.k_splits;  // splits of a tile are consecutive (one arrival counter per tile)
   const int r = u / a.k_splits;
-  w.tile_t = r % n_t_live;   // token tiles of a weight tile run side by side (L2 reuse)
-  w.tile_f = r / n_t_live;
+  if (a.tok_major) {         // weight tile fastest: unit r's weight tile does not depend on the rows
+    w.tile_f = r % nfp;
+    w.tile_t = r / nfp;
+  } else {
+    w.tile_t = r % n_t_live;   // token tiles of a weight tile run side by side (L2 reuse)
+    w.tile_f = r / n_t_live;
+  }
   w.kb0 = (int)((long long)w.split * a.kb_total / a.k_splits);
   w.kb1 = (int)((long long)(w.split + 1) * a.kb_total / a.k_splits);
   w.bnd = -1;
@@ -273,7 +279,7 @@ PE_DEV bool sched_next(const GemmArgs& a, Sched& sc, int n_t_live, Unit& w) {
     w.side = w.kb0 > 0 ? 1 : 0;
     sc.cur += w.kb1 - w.kb0;
   } else {
-    w = decode_unit(a, sc.cur, n_t_live);
+    w = decode_unit(a, sc.cur, n_t_live, (a.n_f + CG - 1) / CG);
     sc.cur += gridDim.x / CG;
   }
   return true;
@@ -496,8 +502,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_expect_tx(smem_u32(full + npre), a.stage_bytes);
             issue_w<EPI, CG>(&tmW, a, sa, smem_u32(full + npre), kb * a.ka, w.tile_f, pol_w);
           }
-    } else if (a.n_t == 1 && (int)blockIdx.x / CG < U) {  // unit numbering does not depend on the row count
-      const Unit w = decode_unit(a, (int)blockIdx.x / CG, 1);
+    } else if ((a.n_t == 1 || a.tok_major) &&
+               (int)blockIdx.x / CG < U / a.n_t * min(a.n_t, (a.n_tok_min + BN - 1) / BN)) {
+      // the CTA's first unit exists whatever the row count (it lies within the token tiles of
+      // the rows that certainly exist), and its weight tile does not depend on the count
+      const Unit w = decode_unit(a, (int)blockIdx.x / CG, 1, (a.n_f + CG - 1) / CG);
       npre = min(S, w.kb1 - w.kb0);
       if (elect_one())
         for (int i = 0; i < npre; ++i) {

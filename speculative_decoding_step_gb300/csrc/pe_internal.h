@@ -212,6 +212,8 @@ struct GemmArgs {
   int bn;                // token columns per tile (MMA N)
   int n_t, n_f;          // token tiles, weight tiles; work units = n_t * n_f * k_splits
   int n_tok_min;         // token rows that certainly exist (every tile below it is computed)
+  int tok_major;         // units numbered token tile after token tile (weight tile fastest): a CTA's
+                         // first weight tile is then known before the row count, and prefetched
   int kb_total, k_splits, stages;  // k stages over the whole K (each ka 64-wide atoms)
   int ka;                          // 64-wide k atoms per pipeline stage (1 or 2)
   uint32_t stage_bytes;
