@@ -179,18 +179,36 @@ __global__ void __launch_bounds__(kSampAThreads, kSampCtasPerSm) sample_stats_ke
     for (int j = 0; j < kSampBatch; ++j) {
       if (s0 + j < s_hi) {
         const int v0 = (s0 + j) * kSampStep + kSampPerLane * lane;
-        float lm = -INFINITY;
+        if ((s0 + j + 1) * kSampStep <= V) {
+          // a step inside the row: no bounds per entry, and the non-finite check once on
+          // the sum (a NaN logit makes its weight NaN, a +inf one makes the maximum +inf
+          // and its weight 2^(inf - inf) = NaN), with the same values as the general path
+          float lm = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < kSampPerLane; ++q) {
-          if (v0 + q < V) {
-            const float z = x[j].v[q] * a.inv_t2;
-            bad |= z != z || z == INFINITY;  // NaN or +inf; a -inf logit is a masked entry
-            lm = fmaxf(lm, z);
+          for (int q = 0; q < kSampPerLane; ++q) lm = fmaxf(lm, x[j].v[q] * a.inv_t2);
+          const float m = samp_warp_max(lm);
+          float t = 0.f;
+          if (m != -INFINITY) {
+#pragma unroll
+            for (int q = 0; q < kSampPerLane; ++q) t += ex2(x[j].v[q] * a.inv_t2 - m);
           }
+          const float sm = samp_warp_sum(t);
+          bad |= sm != sm;
+          if (lane == 0) st[s0 + j] = make_float2(m, sm);
+        } else {
+          float lm = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < kSampPerLane; ++q) {
+            if (v0 + q < V) {
+              const float z = x[j].v[q] * a.inv_t2;
+              bad |= z != z || z == INFINITY;  // NaN or +inf; a -inf logit is a masked entry
+              lm = fmaxf(lm, z);
+            }
+          }
+          const float m = samp_warp_max(lm);  // -inf: the whole step is masked, its sum 0
+          const float sm = samp_warp_sum(sum16(exp16(x[j], v0, V, a.inv_t2, m)));
+          if (lane == 0) st[s0 + j] = make_float2(m, sm);
         }
-        const float m = samp_warp_max(lm);  // -inf: the whole step is masked, its sum 0
-        const float sm = samp_warp_sum(sum16(exp16(x[j], v0, V, a.inv_t2, m)));
-        if (lane == 0) st[s0 + j] = make_float2(m, sm);
       }
     }
   }
