@@ -115,6 +115,35 @@ def test_sample_drafts_masked_logits(V):
     assert g[2] in keep
 
 
+@pytest.mark.parametrize("where", ["full-step-nan", "full-step-posinf", "last-step-nan", "none"])
+def test_sample_drafts_nonfinite_logit_is_flagged(where):
+    """A NaN or +inf logit, in a step inside the row (the statistics' fast path) or in the
+    ragged last step, leaves that row without a distribution and sets PE_DEV_NONFINITE; the
+    error word stays clear without one."""
+    B, K, V = 2, 2, 4099
+    rng, logits = _seeded(B, K, V, seed=23)
+    if where == "full-step-nan":
+        logits[1, 1500] = np.nan
+    elif where == "full-step-posinf":
+        logits[2, 700] = np.inf
+    elif where == "last-step-nan":
+        logits[3, V - 2] = np.nan
+    u = rng.random((B, K))
+    cfg = _cfg(B, K, V)
+    lg = torch.from_numpy(logits).cuda()
+    drafts = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    lse = torch.empty(B * K, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pe.sample_drafts(cfg, lg, torch.from_numpy(u.astype(np.float32)).cuda(), 1.0, pe.alloc_workspace(cfg), drafts,
+                     lse, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == (0 if where == "none" else pe.PE_DEV_NONFINITE)
+    gl = lse.cpu().numpy()
+    bad_row = {"full-step-nan": 1, "full-step-posinf": 2, "last-step-nan": 3}.get(where)
+    for r in range(B * K):
+        assert np.isfinite(gl[r]) == (r != bad_row), r
+
+
 def test_sample_drafts_fully_masked_row_is_flagged():
     """A row whose every logit is -inf has no distribution: token 0, lse NaN, PE_DEV_NONFINITE;
     the other rows draw normally."""
