@@ -168,7 +168,7 @@ struct Plan {
   GemmPlan fc, qkv, o, gu, down, lm;
   GemmPlan inj, injkv;  // KV injection: W_inj over the verify batch's hidden rows, then the k | v heads
   // workspace offsets
-  size_t tok_pos, tok_seq, tok_slot, seq_start, seq_len, seq_maxpos, item_base, n_chunks, n_items, items;
+  size_t tok_pos, tok_seq, tok_slot, seq_start, seq_len, seq_maxpos, seq_minpos, item_base, n_chunks, n_items, items;
   size_t done, keys, x, y, q, ao, u, yl, part_m, part_l, part_o, split_part;
   size_t st_ids, st_pos, st_slot, st_rej, st_mask, st_hmap, st_rows, st_nvalid, st_draft, st_x0;
   size_t samp, samp_acc;
@@ -216,6 +216,7 @@ Plan make_plan(const pe_config& c) {
   p.seq_start = take(4 * (size_t)c.B);
   p.seq_len = take(4 * (size_t)c.B);
   p.seq_maxpos = take(4 * (size_t)c.B);
+  p.seq_minpos = take(4 * (size_t)c.B);
   p.item_base = take(4 * (size_t)c.B);
   p.n_chunks = take(4 * (size_t)c.B);
   p.n_items = take(4);
@@ -541,6 +542,7 @@ InitArgs make_init_args(const pe_config& c, const Plan& p, void* ws, const int32
   ia.tok_slot = at<int64_t>(ws, p.tok_slot);
   ia.seq_start = at<int32_t>(ws, p.seq_start); ia.seq_len = at<int32_t>(ws, p.seq_len);
   ia.seq_maxpos = at<int32_t>(ws, p.seq_maxpos);
+  ia.seq_minpos = at<int32_t>(ws, p.seq_minpos);
   ia.target_items = p.attn_target; ia.max_items = p.max_items; ia.min_chunk = kAttnMinChunk;
   ia.items = at<int4>(ws, p.items); ia.n_items = at<int32_t>(ws, p.n_items);
   ia.item_base = at<int32_t>(ws, p.item_base); ia.n_chunks = at<int32_t>(ws, p.n_chunks);
@@ -605,6 +607,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   at_.page_size = c.page_size; at_.num_pages = kv->num_pages; at_.scale = 1.0f / sqrtf((float)hd);
   at_.q = qb; at_.block_table = block_table; at_.tok_pos = ia.tok_pos; at_.tok_seq = ia.tok_seq;
   at_.seq_start = ia.seq_start; at_.seq_len = ia.seq_len; at_.n_valid = n_valid; at_.items = ia.items;
+  at_.seq_minpos = ia.seq_minpos;
   at_.n_items = ia.n_items; at_.item_base = ia.item_base; at_.n_chunks = ia.n_chunks;
   at_.part_m = bf16 ? at<float>(ws, p.part_m) : nullptr;
   at_.part_l = bf16 ? at<float>(ws, p.part_l) : nullptr;

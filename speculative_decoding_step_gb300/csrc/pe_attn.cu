@@ -182,9 +182,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
-  pdl_wait();
+  // Until a role's dependency wait (pdl_wait) it reads only what kernels before the previous
+  // one wrote, all complete once this kernel has started: the work list, the sequences'
+  // metadata, and cache pages wholly below the sequence's smallest position of this round.
+  // The queries, the new rows' k / v and the outputs come after the wait (L2 loads before it).
   pdl_trigger();
-  const int n_items = *a.n_items;
+  const int n_items = __ldcg(a.n_items);
 
   if (warp == 0 || warp == 6) {
     // ------------------------------------------------------------------ TMA loaders (whole warps)
@@ -205,14 +208,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     constexpr int kPagesPerBlk = kAttnBlk / 16;
     constexpr int kBlkPerBatch = 32 / kPagesPerBlk;
     int gi = 0;
-    bool stop = false;
+    bool stop = false, waited = false;
     for (int ii = 0; !stop; ++ii) {
       int it = 0;
       if (lane == 0) {
         if (is_v) {
           it = attn_next_item(ctl, ii, a.err, abort_flag, a.wait_ns);
         } else {
-          it = atomicAdd(a.work_counter, 1);
+          // CTA x's first item is item x (no round trip before the first loads); the
+          // counter hands out the rest
+          it = ii == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.work_counter, 1);
           if (it >= n_items) it = -1;
           const int k = ii % kAttnItemRing;
           bool ok = true;
@@ -231,9 +236,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         stop = it == -2;
         break;
       }
-      const int4 item = a.items[it];
+      const int4 item = __ldcg(a.items + it);
       const int b = item.x, g = item.y, c0 = item.z, c1 = item.w;
       const int nblk = (c1 - c0 + kAttnBlk - 1) / kAttnBlk;
+      const int first_new = __ldcg(a.seq_minpos + b);  // no k / v of this round lies below it
       for (int blk0 = 0; blk0 < nblk && !stop; blk0 += kBlkPerBatch) {
         const int pos0 = c0 + (blk0 * kPagesPerBlk + lane) * 16;
         int y = oob;
@@ -249,6 +255,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         }
         const int nb = min(kBlkPerBatch, nblk - blk0);
         for (int bb = 0; bb < nb; ++bb, ++gi) {
+          if (!waited && c0 + (blk0 + bb + 1) * kAttnBlk > first_new) {  // the block's pages may hold new rows
+            pdl_wait();
+            waited = true;
+          }
           const int s = gi % S;
           bool ok = true;
           if (lane == 0 && gi >= S)
@@ -294,7 +304,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       if (elect_one()) it = attn_next_item(ctl, ii, a.err, abort_flag, a.wait_ns);
       it = __shfl_sync(0xFFFFFFFFu, it, 0);
       if (it < 0) break;
-      const int4 item = a.items[it];
+      const int4 item = __ldcg(a.items + it);
       const int nblk = (item.w - item.z + kAttnBlk - 1) / kAttnBlk;
       if (!wait_all(smem_u32(&ctl->q_full), (uint32_t)ii & 1u)) break;
       tc_fence_after();
@@ -412,11 +422,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const int ldq = a.n_q * HD;
 
     // query tile: row m = (row m / G of the sequence, head g*G + m % G); zeros past the valid rows
+    bool waited = false;
     auto stage_q = [&](int it) {
-      const int4 item = a.items[it];
+      const int4 item = __ldcg(a.items + it);
       const int b = item.x, g = item.y;
-      const int start = a.seq_start[b];
-      const int M = min(a.seq_len[b] * G, kAttnRows);
+      const int start = __ldcg(a.seq_start + b);
+      const int M = min(__ldcg(a.seq_len + b) * G, kAttnRows);
+      if (!waited) {  // the queries come from the previous kernel
+        pdl_wait();
+        waited = true;
+      }
       // every load of this thread first (one round trip), then the shared-memory stores
       constexpr int PER = kAttnRows * CH / kAttnSoftmax;
       uint4 val[PER];
@@ -594,6 +609,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       mbar_arrive(smem_u32(&ctl->o_free));
     }
   }
+  pdl_wait();  // no CTA completes before the previous kernel has (later kernels rely on the chain)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

@@ -146,6 +146,7 @@ struct InitArgs {
   int32_t *tok_pos, *tok_seq;
   int64_t* tok_slot;
   int32_t *seq_start, *seq_len, *seq_maxpos;
+  int32_t* seq_minpos;       // smallest position of the sequence's valid rows (INT_MAX: none)
   int target_items, max_items, min_chunk;
   int4* items;
   int32_t *n_items, *item_base, *n_chunks;
@@ -288,6 +289,10 @@ struct AttnArgs {
   const void *k_cache, *v_cache;
   const int32_t* block_table;
   const int32_t *tok_pos, *tok_seq, *seq_start, *seq_len, *n_valid;
+  // smallest position of each sequence's rows: every k / v this round writes for the
+  // sequence lies at or after it, so cache pages wholly below it may be read before the
+  // kernel that writes the new rows has finished
+  const int32_t* seq_minpos;
   const int4* items;         // (b, g, c0, c1)
   const int32_t *n_items, *item_base, *n_chunks;
   float *part_m, *part_l, *part_o;  // [items][128], [items][128], [items][128][hd]

@@ -203,6 +203,7 @@ PE_DEV void init_body(const InitArgs& a) {
     a.seq_start[b] = INT_MAX;
     a.seq_len[b] = 0;
     a.seq_maxpos[b] = -1;
+    a.seq_minpos[b] = INT_MAX;
   }
   __syncthreads();
   for (int t = tid; t < a.R; t += blockDim.x) {
@@ -223,6 +224,7 @@ PE_DEV void init_body(const InitArgs& a) {
       atomicMin(&a.seq_start[b], t);
       atomicAdd(&a.seq_len[b], 1);
       atomicMax(&a.seq_maxpos[b], pos);
+      atomicMin(&a.seq_minpos[b], pos);
     } else {
       a.tok_pos[t] = 0;
       a.tok_slot[t] = -1;
@@ -526,11 +528,15 @@ PE_DEV void step_meta_body(const PrepArgs& a, const InitArgs& ia) {
       // the largest position of the sequence's valid rows: its context rows, and the last
       // MASK row (the NTP row itself when K = 1)
       const int32_t* pp = a.prev_pos + (size_t)b * (K + 1);
-      int mx = pp[acc] + K - 1;
-      for (int r = 0; r < acc; ++r) mx = max(mx, pp[r]);
+      int mx = pp[acc] + K - 1, mn = pp[acc];
+      for (int r = 0; r < acc; ++r) {
+        mx = max(mx, pp[r]);
+        mn = min(mn, pp[r]);
+      }
       ia.seq_start[b] = carry + excl;
       ia.seq_len[b] = acc + K;
       ia.seq_maxpos[b] = mx;
+      ia.seq_minpos[b] = mn;
       len_part += (long long)mx + 1;
     }
     __syncthreads();
