@@ -795,13 +795,27 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnArg
         for (int e = 0; e < VPL; ++e) acc[e] += wk * v[k][e];
       }
     }
-    for (int c = CB; c < nc; ++c) {  // long ranges: the rest, one chunk at a time
-      const size_t pr = base + (size_t)c * kAttnRows;
-      const float mc = __ldcg(a.part_m + pr);
-      const float wk = mc == -INFINITY ? 0.f : exp2f(mc - mx);
-      const float* src = a.part_o + pr * HD + lane * VPL;
+    for (int c0 = CB; c0 < nc; c0 += CB) {  // long ranges: the rest, CB chunks' loads at a time
 #pragma unroll
-      for (int e = 0; e < VPL; ++e) acc[e] += wk * __ldcg(src + e);
+      for (int k = 0; k < CB; ++k) {
+        const int c = c0 + k;
+        if (c < nc) {
+          const float* src = a.part_o + (base + (size_t)c * kAttnRows) * HD + lane * VPL;
+#pragma unroll
+          for (int e = 0; e < VPL; ++e) v[k][e] = __ldcg(src + e);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < CB; ++k) {  // chunk order
+        const int c = c0 + k;
+        const float wk = __shfl_sync(0xFFFFFFFFu, w_l, c & 31);  // lane c holds chunk c's weight for c < 32
+        const float mc = (c >= 32 && c < nc) ? __ldcg(a.part_m + base + (size_t)c * kAttnRows) : 0.f;
+        const float w = c < 32 ? wk : (mc == -INFINITY ? 0.f : exp2f(mc - mx));
+        if (c < nc) {
+#pragma unroll
+          for (int e = 0; e < VPL; ++e) acc[e] += w * v[k][e];
+        }
+      }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     __nv_bfloat16* dst = out + (size_t)(start + m / G) * ldq + (size_t)(g * G + m % G) * HD + (size_t)lane * VPL;

@@ -498,106 +498,164 @@ PE_DEV int block_exclusive_scan(int v, int* warp_s, int& total) {
 constexpr int kStepPrologueThreads = 512;
 constexpr int kStepSeqChunk = kStepPrologueThreads;
 
+// Inputs of one padded row that do not depend on the accepted counts (loaded before the
+// counts are known, so that they share a round trip with them).
+struct StepRowIn {
+  int tok_ctx, pos_own, bonus;
+};
+
+PE_DEV StepRowIn step_row_inputs(const PrepArgs& a, int row, int r1, int K, int S) {
+  StepRowIn in{0, 0, 0};
+  if (row >= r1) return in;
+  const int bb = row / S, r = row - bb * S;
+  if (r < K) in.tok_ctx = a.prev_tokens[(size_t)bb * (K + 1) + r + 1];
+  if (r <= K) {
+    in.pos_own = a.prev_pos[(size_t)bb * (K + 1) + r];
+    in.bonus = a.bonus[bb];
+  }
+  return in;
+}
+
+// One padded row of the rebuilt batch and, for a valid row, its compacted entry and the
+// prologue's per-row metadata.  acc_s / base_s / ppac_s: the row's sequence's accepted
+// count, first compacted row and NTP position (index bb - c0).
+PE_DEV void step_write_row(const PrepArgs& a, const InitArgs& ia, int row, const StepRowIn& in, int c0,
+                           const int* acc_s, const int* base_s, const int* ppac_s) {
+  const int K = a.K, S = 2 * K;
+  const int bb = row / S, r = row - bb * S, li = bb - c0;
+  const int ac = acc_s[li];
+  int tok, pos, hmap, rej = 0, msk = 0, draft_k = -1;
+  if (r < ac) {          // accepted context row: token at p+1, hidden state of p
+    tok = in.tok_ctx;
+    pos = in.pos_own;
+    hmap = bb * (K + 1) + r;
+  } else if (r == ac) {  // NTP row: bonus token with h_context
+    tok = in.bonus;
+    pos = in.pos_own;
+    hmap = bb * (K + 1) + ac;
+    draft_k = 0;
+  } else if (r <= K) {   // rejected draft position
+    tok = 0;
+    pos = in.pos_own;
+    hmap = bb * (K + 1) + r;
+    rej = 1;
+  } else {               // MASK slot m = r - K
+    const int m = r - K;
+    tok = a.vocab;
+    pos = ppac_s[li] + m;
+    hmap = -1;
+    msk = 1;
+    draft_k = m;
+  }
+  if (!msk && (tok < 0 || tok >= a.vocab)) set_err(a.err, PE_DEV_BAD_TOKEN);
+  long long slot = -1;
+  if (!rej) {
+    const int pi = pos / a.page_size;
+    if (pos < 0 || pi >= a.max_pages) {
+      set_err(a.err, PE_DEV_BAD_POSITION);
+    } else {
+      const int page = a.block_table[(size_t)bb * a.max_pages + pi];
+      if (page < 0 || page >= a.num_pages) set_err(a.err, PE_DEV_BAD_PAGE);
+      else slot = (long long)page * a.page_size + pos % a.page_size;
+    }
+  }
+  a.input_ids[row] = tok;
+  a.positions[row] = pos;
+  a.slot_mapping[row] = slot;
+  a.is_rejected[row] = (uint8_t)rej;
+  a.is_mask[row] = (uint8_t)msk;
+  a.hidden_map[row] = hmap;
+  if (!rej) {
+    const int idx = base_s[li] + (r <= ac ? r : r - (K - ac));
+    a.row_list[idx] = row;
+    if (draft_k >= 0) a.draft_rows[bb * K + draft_k] = idx;
+    ia.tok_pos[idx] = pos;
+    ia.tok_slot[idx] = slot;
+    ia.tok_seq[idx] = bb;
+  }
+}
+
+constexpr int kStepRowsPf = 2;  // rows per thread whose inputs are loaded with the accepted counts
+
 PE_DEV void step_meta_body(const PrepArgs& a, const InitArgs& ia) {
   __shared__ int warp_s[33];
-  __shared__ int acc_s[kStepSeqChunk], base_s[kStepSeqChunk];
+  __shared__ int acc_s[kStepSeqChunk], base_s[kStepSeqChunk], ppac_s[kStepSeqChunk];
+  __shared__ int ib_s[kStepSeqChunk], nc_s[kStepSeqChunk], rng_s[kStepSeqChunk];
   __shared__ long long len_s[kStepPrologueThreads / 32];
   __shared__ int chunk_s;
   const int tid = threadIdx.x, NT = blockDim.x;
   const int K = a.K, S = 2 * K, R = a.B * S;
+  const bool one_chunk = a.B <= kStepSeqChunk;  // every sequence has a thread of its own
   for (int i = tid; i < ia.n_counters; i += NT) ia.counters[i] = 0;
   for (int i = tid; i < ia.T; i += NT) ia.keys[i] = 0ull;
   int carry = 0;           // compacted rows of the sequences before the chunk (the same in every thread)
   long long len_part = 0;  // this thread's share of the summed causal ranges
+  int my_range = 0;        // (one chunk) the causal range of this thread's sequence: largest position + 1
   for (int c0 = 0; c0 < a.B; c0 += kStepSeqChunk) {
     const int b = c0 + tid;
     const bool own = tid < kStepSeqChunk && b < a.B;
-    int acc = 0;
-    if (own) {
-      acc = a.num_accepted[b];
-      if (acc < 0 || acc > K) {
-        set_err(a.err, PE_DEV_BAD_ACCEPTED);
-        acc = acc < 0 ? 0 : K;
-      }
+    const int r0 = c0 * S, r1 = min(a.B, c0 + kStepSeqChunk) * S;
+    // one round trip for everything that does not depend on the accepted counts: the
+    // sequence's count and first eight positions, and the inputs of this thread's first rows
+    const int32_t* pp = a.prev_pos + (size_t)b * (K + 1);
+    int acc = own ? a.num_accepted[b] : 0;
+    int pv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pv[k] = (own && k <= K) ? pp[k] : 0;
+    StepRowIn rin[kStepRowsPf];
+#pragma unroll
+    for (int j = 0; j < kStepRowsPf; ++j) rin[j] = step_row_inputs(a, r0 + tid + j * NT, r1, K, S);
+    if (own && (acc < 0 || acc > K)) {
+      set_err(a.err, PE_DEV_BAD_ACCEPTED);
+      acc = acc < 0 ? 0 : K;
     }
     int total = 0;
     const int excl = block_exclusive_scan(own ? acc + K : 0, warp_s, total);
     if (own) {
+      // the largest and smallest positions of the sequence's valid rows: its context rows
+      // (0..a-1), its NTP row (a) and the MASK rows after it (the last at NTP + K - 1)
+      int ppa = pv[0], mx = INT_MIN, mn = INT_MAX;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k == acc) ppa = pv[k];
+        if (k < acc) {
+          mx = max(mx, pv[k]);
+          mn = min(mn, pv[k]);
+        }
+      }
+      if (acc >= 8) ppa = pp[acc];
+      for (int r8 = 8; r8 < acc; r8 += 8) {  // more than eight context rows (K > 8)
+        int v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = r8 + k < acc ? pp[r8 + k] : ppa;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          mx = max(mx, v[k]);
+          mn = min(mn, v[k]);
+        }
+      }
+      mx = max(mx, ppa + K - 1);
+      mn = min(mn, ppa);
       acc_s[tid] = acc;
       base_s[tid] = carry + excl;
-      // the largest position of the sequence's valid rows: its context rows, and the last
-      // MASK row (the NTP row itself when K = 1)
-      const int32_t* pp = a.prev_pos + (size_t)b * (K + 1);
-      int mx = pp[acc] + K - 1, mn = pp[acc];
-      for (int r = 0; r < acc; ++r) {
-        mx = max(mx, pp[r]);
-        mn = min(mn, pp[r]);
-      }
+      ppac_s[tid] = ppa;
       ia.seq_start[b] = carry + excl;
       ia.seq_len[b] = acc + K;
       ia.seq_maxpos[b] = mx;
       ia.seq_minpos[b] = mn;
       len_part += (long long)mx + 1;
+      my_range = mx + 1;
     }
     __syncthreads();
-    const int r0 = c0 * S, r1 = min(a.B, c0 + kStepSeqChunk) * S;
-    for (int row = r0 + tid; row < r1; row += NT) {
-      const int bb = row / S, r = row - bb * S, li = bb - c0;
-      const int ac = acc_s[li];
-      const int32_t* pt = a.prev_tokens + (size_t)bb * (K + 1);
-      const int32_t* pp = a.prev_pos + (size_t)bb * (K + 1);
-      int tok, pos, hmap, rej = 0, msk = 0, draft_k = -1;
-      if (r < ac) {          // accepted context row: token at p+1, hidden state of p
-        tok = pt[r + 1];
-        pos = pp[r];
-        hmap = bb * (K + 1) + r;
-      } else if (r == ac) {  // NTP row: bonus token with h_context
-        tok = a.bonus[bb];
-        pos = pp[ac];
-        hmap = bb * (K + 1) + ac;
-        draft_k = 0;
-      } else if (r <= K) {   // rejected draft position
-        tok = 0;
-        pos = pp[r];
-        hmap = bb * (K + 1) + r;
-        rej = 1;
-      } else {               // MASK slot m = r - K
-        const int m = r - K;
-        tok = a.vocab;
-        pos = pp[ac] + m;
-        hmap = -1;
-        msk = 1;
-        draft_k = m;
-      }
-      if (!msk && (tok < 0 || tok >= a.vocab)) set_err(a.err, PE_DEV_BAD_TOKEN);
-      long long slot = -1;
-      if (!rej) {
-        const int pi = pos / a.page_size;
-        if (pos < 0 || pi >= a.max_pages) {
-          set_err(a.err, PE_DEV_BAD_POSITION);
-        } else {
-          const int page = a.block_table[(size_t)bb * a.max_pages + pi];
-          if (page < 0 || page >= a.num_pages) set_err(a.err, PE_DEV_BAD_PAGE);
-          else slot = (long long)page * a.page_size + pos % a.page_size;
-        }
-      }
-      a.input_ids[row] = tok;
-      a.positions[row] = pos;
-      a.slot_mapping[row] = slot;
-      a.is_rejected[row] = (uint8_t)rej;
-      a.is_mask[row] = (uint8_t)msk;
-      a.hidden_map[row] = hmap;
-      if (!rej) {
-        const int idx = base_s[li] + (r <= ac ? r : r - (K - ac));
-        a.row_list[idx] = row;
-        if (draft_k >= 0) a.draft_rows[bb * K + draft_k] = idx;
-        ia.tok_pos[idx] = pos;
-        ia.tok_slot[idx] = slot;
-        ia.tok_seq[idx] = bb;
-      }
+#pragma unroll
+    for (int j = 0; j < kStepRowsPf; ++j) {
+      const int row = r0 + tid + j * NT;
+      if (row < r1) step_write_row(a, ia, row, rin[j], c0, acc_s, base_s, ppac_s);
     }
+    for (int row = r0 + tid + kStepRowsPf * NT; row < r1; row += NT)
+      step_write_row(a, ia, row, step_row_inputs(a, row, r1, K, S), c0, acc_s, base_s, ppac_s);
     carry += total;
-    __syncthreads();  // acc_s / base_s are refilled by the next chunk
+    __syncthreads();  // acc_s / base_s / ppac_s are refilled by the next chunk
   }
   if (tid == 0) *a.n_valid = carry;
   for (int i = carry + tid; i < R; i += NT) {
@@ -625,12 +683,16 @@ PE_DEV void step_meta_body(const PrepArgs& a, const InitArgs& ia) {
   for (int c0 = 0; c0 < a.B; c0 += kStepSeqChunk) {
     const int b = c0 + tid;
     const bool own = tid < kStepSeqChunk && b < a.B;
-    const int nc = own ? (ia.seq_maxpos[b] + 1 + chunk - 1) / chunk : 0;  // written by this thread above
+    const int range = own ? (one_chunk ? my_range : ia.seq_maxpos[b] + 1) : 0;
+    const int nc = (range + chunk - 1) / chunk;
     int total = 0;
     const int excl = block_exclusive_scan(nc * ia.n_kv, warp_s, total);
     if (own) {
       ia.n_chunks[b] = nc;
       ia.item_base[b] = items + excl;
+      ib_s[tid] = excl;  // read only with one chunk (items is then 0 here)
+      nc_s[tid] = nc;
+      rng_s[tid] = range;
     }
     items += total;
   }
@@ -640,6 +702,24 @@ PE_DEV void step_meta_body(const PrepArgs& a, const InitArgs& ia) {
   }
   if (tid == 0) *ia.n_items = items;
   if (items == 0) return;
+  if (one_chunk) {
+    // every thread writes items: item i belongs to the last sequence whose first item is at
+    // most i (every sequence has at least n_kv items, so the first items increase)
+    __syncthreads();
+    for (int i = tid; i < items; i += NT) {
+      int lo = 0, hi = a.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ib_s[mid] <= i) lo = mid;
+        else hi = mid - 1;
+      }
+      const int k = i - ib_s[lo], nc = nc_s[lo];
+      const int g = k / nc, c = k - g * nc;
+      const int c0 = c * chunk;
+      ia.items[i] = make_int4(lo, g, c0, min(c0 + chunk, rng_s[lo]));
+    }
+    return;
+  }
   for (int b = tid; b < a.B; b += NT) {
     const int L = ia.seq_maxpos[b] + 1;
     const int nc = ia.n_chunks[b];
@@ -725,12 +805,14 @@ PE_DEV void store4<__nv_bfloat16>(__nv_bfloat16* y, float a, float b, float c, f
 
 constexpr int kNormMaxSplits = 16;  // split-K ways a GEMM may leave to the norm
 
-// SPLIT: the producing GEMM left split-K partials to sum (a.n_splits > 0).  A separate
-// instantiation without them keeps the register count low (the partial loads in flight
-// take 128 registers; without them several CTAs fit on an SM, and a many-row norm
-// runs in one wave).
-template <typename OutT, typename GT, int VPT, bool SPLIT>
+// MS: the most split-K partials the producing GEMM may have left to sum (8 or 16; 0: none).
+// The partial loads in flight take KC * MS float4 registers (128 registers): with at most 8
+// splits a thread's four float4 groups load in one round trip instead of two.  The
+// instantiation without partials keeps the register count low (several CTAs fit on an SM,
+// and a many-row norm runs in one wave).
+template <typename OutT, typename GT, int VPT, int MS>
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a) {
+  constexpr bool SPLIT = MS > 0;
   __shared__ float warp_ss[kNormThreads / 32];
   const int row = blockIdx.x, tid = threadIdx.x;
   const int nv = a.d / 4;
@@ -767,10 +849,11 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
     const int ntl = min(a.n_t, (n_eff + a.bn - 1) / a.bn);
     const int tile_t = src / a.bn, tt = src - tile_t * a.bn;
     const size_t tile_floats = (size_t)a.bn * 128;
-    constexpr int KC = VPT < 2 ? VPT : 2;  // groups of four features whose loads are in flight together
+    constexpr int KC0 = MS <= 8 ? 4 : 2;
+    constexpr int KC = VPT < KC0 ? VPT : KC0;  // groups of four features whose loads are in flight together
 #pragma unroll
     for (int k0 = 0; k0 < VPT; k0 += KC) {
-      float4 q[KC][kNormMaxSplits];
+      float4 q[KC][MS > 0 ? MS : 1];
 #pragma unroll
       for (int kc = 0; kc < KC; ++kc) {
         const int k = k0 + kc, j = tid + k * kNormThreads;
@@ -781,7 +864,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
           const float* p = a.part + ((size_t)(tile_f * ntl + tile_t) * a.n_splits) * tile_floats +
                            (size_t)tt * 128 + (f & 127);
 #pragma unroll
-          for (int sp = 0; sp < kNormMaxSplits; ++sp)
+          for (int sp = 0; sp < MS; ++sp)
             if (sp < a.n_splits) q[kc][sp] = __ldcg(reinterpret_cast<const float4*>(p + (size_t)sp * tile_floats));
         }
       }
@@ -790,7 +873,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
         const int k = k0 + kc, j = tid + k * kNormThreads;
         if (j < nv) {
 #pragma unroll
-          for (int sp = 0; sp < kNormMaxSplits; ++sp)  // split order
+          for (int sp = 0; sp < MS; ++sp)  // split order
             if (sp < a.n_splits) {
               v[k].x += q[kc][sp].x; v[k].y += q[kc][sp].y; v[k].z += q[kc][sp].z; v[k].w += q[kc][sp].w;
             }
@@ -831,7 +914,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
   }
 }
 
-template <typename OutT, typename GT, bool SPLIT>
+template <typename OutT, typename GT, int SPLIT>
 static cudaError_t launch_norm_typed(const NormArgs& a, cudaStream_t s) {
   const int per = (a.d / 4 + kNormThreads - 1) / kNormThreads;  // float4 per thread
   const dim3 grid(a.n_rows), block(kNormThreads);
@@ -845,12 +928,17 @@ static cudaError_t launch_norm_typed(const NormArgs& a, cudaStream_t s) {
 
 cudaError_t launch_rmsnorm(const NormArgs& a, pe_dtype dt, cudaStream_t s) {
   if (a.n_rows == 0) return cudaSuccess;
-  if (a.n_splits > 0) {
-    if (dt == PE_BF16) return launch_norm_typed<__nv_bfloat16, __nv_bfloat16, true>(a, s);
-    return launch_norm_typed<float, float, true>(a, s);
+  if (a.n_splits > kNormMaxSplits) return cudaErrorInvalidValue;
+  if (a.n_splits > 8) {
+    if (dt == PE_BF16) return launch_norm_typed<__nv_bfloat16, __nv_bfloat16, kNormMaxSplits>(a, s);
+    return launch_norm_typed<float, float, kNormMaxSplits>(a, s);
   }
-  if (dt == PE_BF16) return launch_norm_typed<__nv_bfloat16, __nv_bfloat16, false>(a, s);
-  return launch_norm_typed<float, float, false>(a, s);
+  if (a.n_splits > 0) {
+    if (dt == PE_BF16) return launch_norm_typed<__nv_bfloat16, __nv_bfloat16, 8>(a, s);
+    return launch_norm_typed<float, float, 8>(a, s);
+  }
+  if (dt == PE_BF16) return launch_norm_typed<__nv_bfloat16, __nv_bfloat16, 0>(a, s);
+  return launch_norm_typed<float, float, 0>(a, s);
 }
 
 }  // namespace pe
