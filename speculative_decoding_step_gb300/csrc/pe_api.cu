@@ -551,6 +551,28 @@ InitArgs make_init_args(const pe_config& c, const Plan& p, void* ws, const int32
   return ia;
 }
 
+// The weight matrices the prologue warms (bf16 storage; fp32 configurations run the CUDA-core
+// path, which is not limited by the first loads).
+void set_warm_ranges(InitArgs& ia, const pe_config& c, const pe_weights* w) {
+  ia.warm_n = 0;
+  if (c.dtype != PE_BF16) return;
+  const long long d = c.d, hd = c.head_dim, F = c.ffn;
+  auto add = [&](const void* base, long long elems) {
+    if (ia.warm_n < kWarmRanges && base != nullptr) {
+      ia.warm_base[ia.warm_n] = static_cast<const uint8_t*>(base);
+      ia.warm_bytes[ia.warm_n++] = 2 * elems;
+    }
+  };
+  add(w->fc, 2 * d * d);
+  for (int l = 0; l < c.n_layers && l < (kWarmRanges - 2) / 4; ++l) {
+    add(w->wqkv[l], (long long)(c.n_q + 2 * c.n_kv) * hd * d);
+    add(w->wo[l], d * c.n_q * hd);
+    add(w->w_gate_up[l], 2 * F * d);
+    add(w->w_down[l], d * F);
+  }
+  add(w->lm_head, (long long)c.vocab * d);
+}
+
 pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv, const int32_t* block_table,
                        const void* x0, const int32_t* positions, const int64_t* slot_mapping,
                        const int32_t* row_list, const int32_t* n_valid, const int32_t* draft_rows, void* ws,
@@ -559,7 +581,8 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   const bool bf16 = c.dtype == PE_BF16;
   const int hd = c.head_dim;
   // prologue (already run by pe_step's fused batch-rebuild kernel when init_done)
-  const InitArgs ia = make_init_args(c, p, ws, row_list, n_valid, positions, slot_mapping, err);
+  InitArgs ia = make_init_args(c, p, ws, row_list, n_valid, positions, slot_mapping, err);
+  set_warm_ranges(ia, c, w);
   if (!init_done) PE_TRY_CUDA(launch_forward_init(ia, s));
   trace(3, s);
 
@@ -827,7 +850,8 @@ pe_status pe_step(const pe_config* cfg, const pe_weights* w, const pe_kv* kv, co
   const PrepArgs pa = make_prep_args(*cfg, prev_tokens, prev_pos, num_accepted, bonus, block_table, kv->num_pages, ids,
                                      pos, slot, rej, msk, hmap, rows, nval, drows, err_word);
   const ScatterArgs sa = make_scatter_args(*cfg, w, target_hidden, ids, msk, hmap, rows, nval, x0, err_word);
-  const InitArgs ia = make_init_args(*cfg, p, ws, rows, nval, pos, slot, err_word);
+  InitArgs ia = make_init_args(*cfg, p, ws, rows, nval, pos, slot, err_word);
+  set_warm_ranges(ia, *cfg, w);
   trace(0, s);
   PE_TRY_CUDA(launch_step_prologue(pa, sa, ia, s));
   trace(1, s);

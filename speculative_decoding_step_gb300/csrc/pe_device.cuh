@@ -134,6 +134,11 @@ PE_DEV uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// A prefetch of the line at p into L2 (a hint: nothing waits for it).
+PE_DEV void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 PE_DEV void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }

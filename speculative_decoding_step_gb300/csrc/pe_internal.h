@@ -139,6 +139,7 @@ size_t sample_stats_bytes(int rows, int vocab);
 
 // Forward prologue: per compacted row metadata, per sequence ranges, the
 // attention work list, and zeroing of the pass's counters and argmax keys.
+constexpr int kWarmRanges = 18;  // fc, LM head, and four matrices of each of the first four layers
 struct InitArgs {
   int B, K, R, T, n_kv;
   const int32_t *row_list, *n_valid, *positions;
@@ -154,6 +155,12 @@ struct InitArgs {
   int n_counters;
   unsigned long long* keys;
   int32_t* err;
+  // The round's weight matrices (fc, the first layers' four, the LM head): the prologue touches
+  // one line per 64 KB of each, so that their address translations are in place before the
+  // GEMMs stream them (the first touch of each page otherwise stalls every GEMM's first loads).
+  const uint8_t* warm_base[kWarmRanges];
+  long long warm_bytes[kWarmRanges];
+  int warm_n;
 };
 cudaError_t launch_forward_init(const InitArgs& a, cudaStream_t s);
 // DFlash-style KV injection: position and cache slot of every element of the previous verify
