@@ -293,11 +293,11 @@ PE_DEV void init_body(const InitArgs& a) {
   }
 }
 
-// One L2 prefetch per 64 KB of every warmed weight range, spread over all threads of the
-// launch; nothing waits for them.  The weights do not depend on earlier kernels.
-PE_DEV void warm_weight_translations(const InitArgs& a) {
+// One L2 prefetch per 64 KB of every warmed weight range, spread over the threads of CTAs
+// 0 .. n_cta - 1; nothing waits for them.  The weights do not depend on earlier kernels.
+PE_DEV void warm_weight_translations(const InitArgs& a, int n_cta) {
   constexpr long long kPiece = 64 << 10;
-  const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x, stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x, stride = (long long)n_cta * blockDim.x;
   for (int r = 0; r < a.warm_n; ++r) {
     const long long n = a.warm_bytes[r] / kPiece;
     for (long long i = i0; i < n; i += stride) prefetch_l2(a.warm_base[r] + i * kPiece);
@@ -305,7 +305,7 @@ PE_DEV void warm_weight_translations(const InitArgs& a) {
 }
 
 __global__ void __launch_bounds__(kInitThreads) forward_init_kernel(const InitArgs a) {
-  warm_weight_translations(a);
+  warm_weight_translations(a, gridDim.x);
   pdl_wait();
   pdl_trigger();
   init_body(a);
@@ -753,7 +753,9 @@ PE_DEV void step_meta_body(const PrepArgs& a, const InitArgs& ia) {
 __global__ void __launch_bounds__(kStepPrologueThreads)
     step_prologue_kernel(const PrepArgs pa, const ScatterArgs sa, const InitArgs ia, int groups) {
   __shared__ int part_s[kStepPrologueThreads / 32];
-  warm_weight_translations(ia);
+  // the input-row CTAs warm the weights' translations; the metadata CTA (the last) is the
+  // longest and leaves them out
+  if (blockIdx.x != gridDim.x - 1) warm_weight_translations(ia, gridDim.x - 1);
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == gridDim.x - 1) {
