@@ -156,7 +156,7 @@ struct InitArgs {
   unsigned long long* keys;
   int32_t* err;
   // The round's weight matrices (fc, the first layers' four, the LM head): the prologue touches
-  // one line per 64 KB of each, so that their address translations are in place before the
+  // one line per 2 MB of each, so that their address translations are in place before the
   // GEMMs stream them (the first touch of each page otherwise stalls every GEMM's first loads).
   const uint8_t* warm_base[kWarmRanges];
   long long warm_bytes[kWarmRanges];

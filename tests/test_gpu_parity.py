@@ -275,6 +275,39 @@ def test_deterministic_and_page_permutation_invariant():
     assert torch.equal(lg1, c2.rd.logits) and torch.equal(d1, c2.rd.draft_tokens)
 
 
+@pytest.mark.parametrize("path", ["stages", "step"])
+def test_context_positions_decreasing(path):
+    """Rows whose positions do not increase along the verify batch: the context rows of
+    sequence b sit at P + 2(K - r), the NTP row above them all, so the sequence's smallest
+    position this round is its last context row's (neither its first row's nor the NTP
+    row's).  The attention loads the cache pages wholly below that position before the
+    kernel writing the round's k / v has finished; logits, drafts and every cache entry match
+    the oracle."""
+    cfg_np = SMALL["bf16-L2-long"]
+    K = cfg_np.K
+    rnd = make_round(cfg_np, extra_positions=K + 2)
+    P, a = rnd.prefix_len, rnd.num_accepted
+    pp = np.empty_like(rnd.prev_pos)
+    for b in range(cfg_np.B):
+        for r in range(K + 1):
+            pp[b, r] = P[b] + 2 * (K - r) if r < a[b] else P[b] + 2 * K + 1 + (r - a[b])
+    rnd.prev_pos = pp.astype(np.int32)
+    assert (a > 1).any()  # some sequence has its smallest position at a context row past the first
+    c = setup(cfg_np, rnd=rnd)
+    if path == "stages":
+        assert run_stages(c) == 0
+    else:
+        drafts_target = np.zeros((cfg_np.B, K), dtype=np.int32)
+        R = c.Rd
+        c.rd.step(R["prev_tokens"], R["prev_pos"], R["num_accepted"], R["bonus"], R["target_hidden"],
+                  torch.from_numpy(drafts_target).cuda(), logits=True)
+        torch.cuda.synchronize()
+        assert int(c.rd.err.item()) == 0
+    ref = oracle_round(c, want_kv=True)
+    check_logits(c, ref)
+    check_kv_writes(c, ref)
+
+
 @pytest.mark.parametrize("idx", [1, 2])
 def test_repeat_runs_bit_identical_full_size(idx):
     """The full-size workloads run repeatedly give bit-identical logits and drafts: a
