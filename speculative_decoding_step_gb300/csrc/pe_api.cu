@@ -564,13 +564,14 @@ void set_warm_ranges(InitArgs& ia, const pe_config& c, const pe_weights* w) {
     }
   };
   add(w->fc, 2 * d * d);
-  for (int l = 0; l < c.n_layers && l < (kWarmRanges - 2) / 4; ++l) {
+  for (int l = 0; l < c.n_layers && l < (kWarmRanges - 1) / 4; ++l) {
     add(w->wqkv[l], (long long)(c.n_q + 2 * c.n_kv) * hd * d);
     add(w->wo[l], d * c.n_q * hd);
     add(w->w_gate_up[l], 2 * F * d);
     add(w->w_down[l], d * F);
   }
-  add(w->lm_head, (long long)c.vocab * d);
+  // not the LM head: it streams long enough for its own first touches to overlap, and its
+  // ~600 pages would make a prologue that finds every translation missing 10-20 us longer
 }
 
 pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv, const int32_t* block_table,

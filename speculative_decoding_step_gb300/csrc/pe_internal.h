@@ -139,7 +139,7 @@ size_t sample_stats_bytes(int rows, int vocab);
 
 // Forward prologue: per compacted row metadata, per sequence ranges, the
 // attention work list, and zeroing of the pass's counters and argmax keys.
-constexpr int kWarmRanges = 18;  // fc, LM head, and four matrices of each of the first four layers
+constexpr int kWarmRanges = 17;  // fc and the four matrices of each of the first four layers
 struct InitArgs {
   int B, K, R, T, n_kv;
   const int32_t *row_list, *n_valid, *positions;
@@ -155,7 +155,7 @@ struct InitArgs {
   int n_counters;
   unsigned long long* keys;
   int32_t* err;
-  // The round's weight matrices (fc, the first layers' four, the LM head): the prologue touches
+  // The round's layer weight matrices (fc, the first layers' four): the prologue touches
   // one line per 2 MB of each, so that their address translations are in place before the
   // GEMMs stream them (the first touch of each page otherwise stalls every GEMM's first loads).
   const uint8_t* warm_base[kWarmRanges];
