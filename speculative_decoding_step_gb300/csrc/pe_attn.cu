@@ -594,10 +594,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         for (int c = 0; c < HD; c += 16) {
           float ov[16];
           tmem_load16(tmem + lane_base + TO + (uint32_t)c, ov);
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(a.part_o + (ib + r) * HD + c);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dst[e] = make_float4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
+          if (valid) {  // two 32-byte stores (a partial row is 256-byte aligned)
+            float* dst = a.part_o + (ib + r) * HD + c;
+            st_global_v8(dst, ov);
+            st_global_v8(dst + 8, ov + 8);
           }
         }
         if (valid) {
