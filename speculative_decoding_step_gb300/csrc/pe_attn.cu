@@ -673,14 +673,10 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_rows_kernel(const At
       mc_l = __ldcg(a.part_m + base + (size_t)sub * kAttnRows);
       lc_l = __ldcg(a.part_l + base + (size_t)sub * kAttnRows);
     }
-    float4 o[CB][2];
+    float o[CB][8];
 #pragma unroll
     for (int k = 0; k < CB; ++k)
-      if (valid && k < nc) {
-        const float4* src = reinterpret_cast<const float4*>(a.part_o + (base + (size_t)k * kAttnRows) * HD + sub * 8);
-        o[k][0] = __ldcg(src);
-        o[k][1] = __ldcg(src + 1);
-      }
+      if (valid && k < nc) ldcg_v8(a.part_o + (base + (size_t)k * kAttnRows) * HD + sub * 8, o[k]);
     float mx = mc_l;
     if (valid)
       for (int c = sub + LPR; c < nc; c += LPR) mx = fmaxf(mx, __ldcg(a.part_m + base + (size_t)c * kAttnRows));
@@ -703,8 +699,8 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_rows_kernel(const At
     for (int k = 0; k < CB; ++k) {  // chunk order; chunk k's weight lives in lane lane0 + k
       const float wk = __shfl_sync(0xFFFFFFFFu, w_l, lane0 + k);
       if (k < nc) {
-        acc[0] += wk * o[k][0].x; acc[1] += wk * o[k][0].y; acc[2] += wk * o[k][0].z; acc[3] += wk * o[k][0].w;
-        acc[4] += wk * o[k][1].x; acc[5] += wk * o[k][1].y; acc[6] += wk * o[k][1].z; acc[7] += wk * o[k][1].w;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += wk * o[k][e];
       }
     }
     if (!valid) continue;
@@ -713,10 +709,10 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_rows_kernel(const At
       const size_t pr = base + (size_t)c * kAttnRows;
       const float mc = __ldcg(a.part_m + pr);
       const float wk = mc == -INFINITY ? 0.f : exp2f(mc - mx);
-      const float4* src = reinterpret_cast<const float4*>(a.part_o + pr * HD + sub * 8);
-      const float4 u0 = __ldcg(src), u1 = __ldcg(src + 1);
-      acc[0] += wk * u0.x; acc[1] += wk * u0.y; acc[2] += wk * u0.z; acc[3] += wk * u0.w;
-      acc[4] += wk * u1.x; acc[5] += wk * u1.y; acc[6] += wk * u1.z; acc[7] += wk * u1.w;
+      float u[8];
+      ldcg_v8(a.part_o + pr * HD + sub * 8, u);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += wk * u[e];
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     __nv_bfloat16* dst = out + (size_t)(start + m / G) * ldq + (size_t)(g * G + m % G) * HD + (size_t)sub * 8;

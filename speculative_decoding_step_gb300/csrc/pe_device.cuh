@@ -146,6 +146,13 @@ PE_DEV void st_global_v8(float* p, const float* v) {
                : "memory");
 }
 
+// One 32-byte load of eight floats through L2 (p 32-byte aligned).
+PE_DEV void ldcg_v8(const float* p, float* v) {
+  asm volatile("ld.global.cg.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+               : "l"(reinterpret_cast<uint64_t>(p)));
+}
+
 PE_DEV void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
