@@ -591,6 +591,11 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   GemmArgs base{};
   base.n_q = c.n_q; base.n_kv = c.n_kv; base.head_dim = hd; set_rope_table(base, c.rope_theta, hd);
   base.tok_pos = ia.tok_pos; base.tok_slot = ia.tok_slot; base.err = err;
+  // Every kernel from the first QKV GEMM on starts only after the prologue has completed (its
+  // predecessor triggers dependents after its own dependency wait, or the one before does), so
+  // it may read the prologue's row count and maps before its own wait; fc and the norm after it
+  // may start while the prologue still runs.
+  base.meta_ready = 1;
 
   float* x = at<float>(ws, p.x);
   void* y = at<uint8_t>(ws, p.y);
@@ -617,6 +622,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   {
     GemmArgs a = base;
     a.out_f32 = x; a.ld_out = c.d;
+    a.meta_ready = 0;
     GemmCall call{EPI_STORE_F32, &p.fc, w->fc, x0, 2 * c.d, c.d, p.R, n_valid, 0, (uint64_t)c.d};
     pe_status st = run_gemm(c, p, ws, call, a, s);
     if (st != PE_OK) return st;
@@ -641,6 +647,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   for (int l = 0; l < c.n_layers; ++l) {
     const int tp = 5 + 7 * l;
     na.g = w->norm_attn[l];
+    na.meta_ready = l == 0 ? 0 : 1;
     if (l == 0) norm_after(na, p.fc, false, true);
     else norm_after(na, p.down, true, true);
     PE_TRY_CUDA(launch_rmsnorm(na, c.dtype, s));
@@ -674,6 +681,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
     }
     trace(tp + 3, s);
     na.g = w->norm_mlp[l];
+    na.meta_ready = 1;
     norm_after(na, p.o, true, true);
     PE_TRY_CUDA(launch_rmsnorm(na, c.dtype, s));
     trace(tp + 4, s);
@@ -698,6 +706,7 @@ pe_status forward_impl(const pe_config& c, const pe_weights* w, const pe_kv* kv,
   // final norm of the draft rows (in draft order), then LM head + argmax
   NormArgs nf = na;
   nf.row_map = draft_rows; nf.n_rows = p.T; nf.n_rows_dev = nullptr; nf.src_rows = p.R; nf.g = w->norm_final;
+  nf.meta_ready = 1;
   nf.y = yl;
   norm_after(nf, p.down, true, false);  // the residual after the last layer is needed only here
   PE_TRY_CUDA(launch_rmsnorm(nf, c.dtype, s));

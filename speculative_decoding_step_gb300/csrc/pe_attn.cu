@@ -643,8 +643,9 @@ constexpr int kMergeThreads = 256;
 
 template <int HD>
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_rows_kernel(const AttnArgs a) {
-  pdl_wait();
-  pdl_trigger();
+  // the sequences' metadata come from the prologue, complete once this kernel has started:
+  // they are read before the dependency wait, the partials after it
+  bool waited = false;
   constexpr int LPR = HD / 8;      // lanes per query vector (8 values each)
   constexpr int RPW = 32 / LPR;    // query vectors per warp
   constexpr int GROUPS = kAttnRows / RPW;
@@ -660,9 +661,15 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_rows_kernel(const At
     const int bg = (int)(task / GROUPS);
     const int b = bg / a.n_kv, g = bg - (bg / a.n_kv) * a.n_kv;
     // the sequence's metadata in one round trip
-    const int nc = a.n_chunks[b], len = a.seq_len[b], ibase = a.item_base[b], start = a.seq_start[b];
+    const int nc = __ldcg(a.n_chunks + b), len = __ldcg(a.seq_len + b), ibase = __ldcg(a.item_base + b),
+              start = __ldcg(a.seq_start + b);
     const int M = min(len * G, kAttnRows);
     if (nc <= 1 || grp * RPW >= M) continue;  // the same for the whole warp
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
     const int m = grp * RPW + rw;
     const bool valid = m < M;
     const size_t base = (size_t)(ibase + g * nc) * kAttnRows + m;  // partial row of chunk 0
@@ -723,6 +730,10 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_rows_kernel(const At
     pk.w = pack_bf16(acc[6] * inv, acc[7] * inv);
     *reinterpret_cast<uint4*>(dst) = pk;
   }
+  if (!waited) {  // no CTA completes before the previous kernel has
+    pdl_wait();
+    pdl_trigger();
+  }
 }
 
 // The same merge for few (sequence, kv head) pairs with many chunks each: one warp
@@ -732,8 +743,7 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_rows_kernel(const At
 
 template <int HD>
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnArgs a) {
-  pdl_wait();
-  pdl_trigger();
+  bool waited = false;  // metadata before the dependency wait, partials after it (as above)
   constexpr int VPL = HD / 32;  // output values per lane
   constexpr int CB = 8;         // chunks whose outputs are in flight together
   const int G = a.n_q / a.n_kv, lane = threadIdx.x & 31;
@@ -746,8 +756,14 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnArg
     const int bg = (int)(task / kAttnRows);
     const int b = bg / a.n_kv, g = bg - (bg / a.n_kv) * a.n_kv;
     // the sequence's metadata in one round trip
-    const int nc = a.n_chunks[b], len = a.seq_len[b], ibase = a.item_base[b], start = a.seq_start[b];
+    const int nc = __ldcg(a.n_chunks + b), len = __ldcg(a.seq_len + b), ibase = __ldcg(a.item_base + b),
+              start = __ldcg(a.seq_start + b);
     if (nc <= 1 || m >= min(len * G, kAttnRows)) continue;
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
     const size_t base = (size_t)(ibase + g * nc) * kAttnRows + m;  // partial row of chunk 0
     // chunk statistics (one chunk per lane) and the first CB chunks' outputs, all in flight together
     float mc_l = -INFINITY, lc_l = 0.f;
@@ -823,6 +839,10 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnArg
     } else {
       *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
     }
+  }
+  if (!waited) {  // no CTA completes before the previous kernel has
+    pdl_wait();
+    pdl_trigger();
   }
 }
 

@@ -200,7 +200,7 @@ size_t gemm_tc_smem_bytes(int stages, uint32_t stage_bytes, int red_entries) {
 PE_DEV int effective_ntok(const GemmArgs& a) {
   int n = a.n_tok;
   if (a.n_tok_dev != nullptr) {
-    const int d = *a.n_tok_dev;
+    const int d = __ldcg(a.n_tok_dev);
     if (d < a.n_tok_min) set_err(a.err, PE_DEV_BAD_ROW);
     n = min(n, max(d, a.n_tok_min));
   }
@@ -517,8 +517,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     }
     __syncwarp();
+    const int n_tok_early = a.meta_ready ? effective_ntok(a) : 0;
     pdl_wait();
-    const int n_tok = effective_ntok(a);
+    const int n_tok = a.meta_ready ? n_tok_early : effective_ntok(a);
     const int ntl = live_token_tiles(a, n_tok);
     int it = 0, s = 0;
     uint32_t ph = 0;  // (it / S) & 1
@@ -558,8 +559,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------------------ MMA issuer (the leader of a pair)
     // Converged warp; the elected lane issues every MMA and commit.
     if (CG == 1 || leader) {
+      const int n_tok_early = a.meta_ready ? effective_ntok(a) : 0;
       pdl_wait();
-      const int n_tok = effective_ntok(a);
+      const int n_tok = a.meta_ready ? n_tok_early : effective_ntok(a);
       const int ntl = live_token_tiles(a, n_tok);
       const uint32_t idesc = idesc_bf16(kTcBM * CG, BN);
       int i = 0, s = 0;
@@ -635,8 +637,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Two warps per TMEM lane quarter: each takes every other 16-column chunk of the
     // accumulator, so that an epilogue (argmax over a 224-token tile: ~10 us with one warp
     // per quarter, as long as the next unit's MMAs) stays hidden behind the next unit.
+    const int n_tok_early = a.meta_ready ? effective_ntok(a) : 0;
     pdl_wait();
-    const int n_tok = effective_ntok(a);
+    const int n_tok = a.meta_ready ? n_tok_early : effective_ntok(a);
     const int q = warp & 3;                // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;         // which half of the column chunks (0 with four warps)
     const int hs = EW >> 2;                // chunk stride: the number of halves
@@ -892,9 +895,10 @@ constexpr int kFinishTok = 2;
 
 template <int EPI, int MAXS>  // MAXS >= k_splits: bounds the registers holding the loads
 __global__ void __launch_bounds__(kFinishThreads) splitk_finish_kernel(const GemmArgs a) {
+  const int n_tok_early = a.meta_ready ? effective_ntok(a) : 0;
   pdl_wait();
   pdl_trigger();
-  const int n_tok = effective_ntok(a);
+  const int n_tok = a.meta_ready ? n_tok_early : effective_ntok(a);
   const int ntl = live_token_tiles(a, n_tok);
   const int ns = a.k_splits, BN = a.bn;
   const size_t tile_floats = (size_t)2 * BN * kTcBM;  // both planes

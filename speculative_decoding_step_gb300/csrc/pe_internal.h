@@ -197,6 +197,8 @@ struct NormArgs {
   const int32_t* g_ntok_dev; // the GEMM's device row count (nullable)
   float* x_out;              // nullable: where x_new is written ([rows][d], may alias x)
   int32_t* err;
+  int meta_ready;            // the row counts and row map were written by a kernel that has completed
+                             //   when this one starts: read them before the dependency wait
 };
 cudaError_t launch_rmsnorm(const NormArgs& a, pe_dtype dt, cudaStream_t s);
 
@@ -257,6 +259,9 @@ struct GemmArgs {
   uint64_t wait_ns;          // limit of every pipeline wait (wait_limit_ns())
   int drop_stage;            // test of the wait-expiry path: CTA 0 leaves this pipeline stage unarmed (-1: none)
   int32_t* err;
+  int meta_ready;            // the row count was written by a kernel that has completed when this one
+                             //   starts (every kernel from the first QKV GEMM on): read it before the
+                             //   dependency wait
 };
 
 // Tensor-core GEMM (tcgen05 + TMA): D[f][t] = W[f][:] . X[t][:], weights on the MMA M side.

@@ -842,14 +842,16 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a)
 #pragma unroll
     for (int e = 0; e < 4; ++e) gn[k][e] = j < nv ? to_float<GT>(g[4 * j + e]) : 0.f;
   }
-  pdl_wait();
-  pdl_trigger();
-  // every count / index this row needs, in one round trip
-  const int dev_n = a.n_rows_dev != nullptr ? *a.n_rows_dev : a.n_rows;
+  // every count / index this row needs, in one round trip (before the dependency wait when
+  // the kernel that wrote them has completed by the time this one starts)
+  if (!a.meta_ready) pdl_wait();
+  const int dev_n = a.n_rows_dev != nullptr ? __ldcg(a.n_rows_dev) : a.n_rows;
   const int dev_g = !SPLIT ? 0
                     : (a.g_ntok_dev == nullptr ? a.g_ntok
-                       : (a.g_ntok_dev == a.n_rows_dev ? dev_n : *a.g_ntok_dev));
-  const int mapped = a.row_map != nullptr ? a.row_map[row] : row;
+                       : (a.g_ntok_dev == a.n_rows_dev ? dev_n : __ldcg(a.g_ntok_dev)));
+  const int mapped = a.row_map != nullptr ? __ldcg(a.row_map + row) : row;
+  if (a.meta_ready) pdl_wait();
+  pdl_trigger();
   const int n = min(a.n_rows, dev_n);
   if (row >= n) return;
   const int src = mapped;
