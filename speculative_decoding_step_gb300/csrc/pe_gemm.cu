@@ -651,18 +651,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     Unit w;
     while (sched_next<EPI, CG>(a, sc, ntl, w)) {
       const int buf = i % a.nbuf;
-      // after an abort the accumulator may be incomplete: skip its epilogue
-      const bool ok =
-          mbar_wait(smem_u32(tfull + buf), (uint32_t)(i / a.nbuf) & 1u, a.err, abort_flag, a.wait_ns) && !*abort_flag;
-      tc_fence_after();
-      const int tf = CG * w.tile_f + (int)rank;  // this CTA's 128-row weight tile
-      const int unit = tf * kTcBM + r;
-      const uint32_t tl = tmem + (uint32_t)(buf * a.acc_stride) + ((uint32_t)(q * 32) << 16);
       const int tbase = w.tile_t * BN;
-      // QKV: the tile's token positions and KV slots, loaded once per unit by the four
-      // epilogue warps into shared memory (two buffers by unit parity, so the next unit's
-      // loads never overwrite a buffer still being read) instead of a round trip per chunk.
-      // Every epilogue warp passes the barrier once per unit, whatever its wait returned.
+      // QKV: the tile's token positions and KV slots, loaded once per unit by the epilogue
+      // warps into shared memory (two buffers by unit parity, so the next unit's loads never
+      // overwrite a buffer still being read) instead of a round trip per chunk, while the
+      // unit's MMAs run.  Every epilogue warp passes the barrier once per unit.
       int* pos_s = nullptr;
       long long* slot_s = nullptr;
       if (EPI == EPI_QKV_ROPE && a.k_splits == 1) {
@@ -675,6 +668,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         named_bar_sync(1, 32 * EW);
       }
+      // after an abort the accumulator may be incomplete: skip its epilogue
+      const bool ok =
+          mbar_wait(smem_u32(tfull + buf), (uint32_t)(i / a.nbuf) & 1u, a.err, abort_flag, a.wait_ns) && !*abort_flag;
+      tc_fence_after();
+      const int tf = CG * w.tile_f + (int)rank;  // this CTA's 128-row weight tile
+      const int unit = tf * kTcBM + r;
+      const uint32_t tl = tmem + (uint32_t)(buf * a.acc_stride) + ((uint32_t)(q * 32) << 16);
       if (BAL && ok && w.bnd >= 0) {
         argmax_piece(a, w, tl, unit, n_tok, red_w, r, lane, h, hs);
       } else if (ok && a.k_splits == 1) {
